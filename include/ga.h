@@ -1,0 +1,253 @@
+/*
+ * ga.h -- C ABI of the paged split-KV GQA decode-attention library (libga.so)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is one decode step of Gemma-4-shaped attention over two KV
+ * families that keep their own head counts and cache shapes ("[Model] Gemma 4
+ * M1 12B", Description): a local sliding-window family at head_dim 256 with a
+ * 1024-token window and a global full-context family at head_dim 512 with
+ * fewer KV heads ("[Model] Gemma 4 M3 31B", Description; "visible-cx/Gemma-4-
+ * 31B-CoreAI", hybrid-pf64 numerics gate: 32 query heads over 4 global KV
+ * heads).  Each family has its own paged KV pools and page table.
+ *
+ * For every row b and query head h (kv head c = h / (Hq / Hkv), block GQA):
+ *     keys   j in [lo_b, L_b),  lo_b = max(0, L_b - window) (local) or 0 (global)
+ *     s_j    = scale * <q[b,h,:], K[page_table[b][j/P], c, j%P, :]>
+ *     out    = sum_j softmax(s)_j * V[page_table[b][j/P], c, j%P, :]
+ * where L_b = seq_lens[b] counts the token appended this step.
+ *
+ * Conventions shared by every entry point:
+ *   - Memory: the caller owns all buffers.  Pointer arguments named
+ *     *_host are host memory; every other pointer is device memory of the
+ *     current CUDA device.  The library never allocates, frees or
+ *     synchronises.  Work is enqueued on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and returns before it runs.
+ *   - Layouts are dense, row-major (C order):
+ *       q, out      [B, Hq, D]            bf16
+ *       k_new,v_new [B, Hkv, D]           bf16
+ *       pools       [num_pages, Hkv, P, D] bf16 (GA_KV_BF16) or OCP E4M3FN
+ *                   codes (GA_KV_E4M3), one page-head block of P*D elements
+ *                   contiguous
+ *       k_scale, v_scale [Hkv] fp32 (E4M3 pools only; value = code * scale)
+ *       page_table  [B, pt_stride] int32 physical page ids
+ *       seq_lens, positions [B] int32
+ *     q, out, pools, k_new, v_new and workspace must be 16-byte aligned.
+ *   - page_size must be 16.  Offsets are 64-bit; num_pages * Hkv * 16 must
+ *     stay below 2^31.
+ *   - Return value: GA_OK, or a GA_ERR_* code when the arguments are rejected
+ *     before anything is launched (fail closed, nothing enqueued), or
+ *     GA_ERR_CUDA when a launch fails.  ga_strerror() names a code.
+ *   - Device-side checks: values only the device sees (page ids, seq_lens,
+ *     positions) are checked by the kernels.  A violation is OR-ed into
+ *     *err_word as GA_DEVERR_* bits and the offending access is skipped (an
+ *     invalid page contributes no keys, an invalid length is treated as 0).
+ *     err_word may be NULL (no reporting; accesses are still skipped).  Read
+ *     it after the stream has completed; clear it to 0 yourself.
+ */
+#ifndef GA_H_
+#define GA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* ga_stream_t;   /* same type as cudaStream_t */
+
+/* ----------------------------------------------------------- status codes */
+enum {
+    GA_OK = 0,
+    GA_ERR_INVALID_ARG = 1,         /* null / misaligned pointer, bad size or shape */
+    GA_ERR_UNSUPPORTED = 2,         /* valid but not served: head_dim, page_size, dtype */
+    GA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < plan->workspace_bytes */
+    GA_ERR_CUDA = 4,                /* a CUDA runtime / driver call or launch failed */
+    GA_ERR_DEVICE_CHECK = 5         /* returned by ga_check_error_word for a nonzero word */
+};
+
+/* KV element types. */
+enum { GA_KV_BF16 = 0, GA_KV_E4M3 = 1 };
+
+/* Bits a kernel ORs into *err_word. */
+enum {
+    GA_DEVERR_PAGE_ID = 1,       /* a page id outside [0, num_pages) was met */
+    GA_DEVERR_SEQ_LEN = 2,       /* seq_len < 0 or > pt_stride * page_size */
+    GA_DEVERR_CAPACITY = 4,      /* seq_lens need more split chunks than the plan holds */
+    GA_DEVERR_Q_RANGE = 8,       /* E4M3 path: |q| beyond the f16 range it is staged in */
+    GA_DEVERR_TIMEOUT = 16,      /* a bounded wait for a bulk copy ran out */
+    GA_DEVERR_POSITION = 32      /* append: position / page_table[pos / P] invalid */
+};
+
+/* --------------------------------------------------------------- the plan */
+
+/* Split modes. */
+enum {
+    GA_SPLIT_NONE = 0,    /* one chunk per (row, kv head); output written directly */
+    GA_SPLIT_COUNT = 1,   /* each row's pages cut into `splits` near-equal chunks */
+    GA_SPLIT_CHUNK = 2    /* chunks of `chunk_pages` pages; a row's chunking depends
+                             only on its own length (batch-invariant) */
+};
+
+/* Plan flags. */
+enum {
+    GA_PLAN_TOUCH_LOG = 1,        /* decode records every physical page it reads (tests) */
+    GA_PLAN_EXTERNAL_COMBINE = 2  /* a split decode call leaves the partials in the
+                                     workspace; the caller runs ga_splitkv_combine */
+};
+
+/*
+ * Split-KV plan, filled by ga_plan_splits on the host and passed by pointer
+ * to the decode and combine calls (read on the host at call time only).
+ */
+typedef struct ga_plan {
+    int32_t mode;            /* GA_SPLIT_* */
+    int32_t splits;          /* GA_SPLIT_COUNT: chunks per row */
+    int32_t chunk_pages;     /* GA_SPLIT_CHUNK: pages per chunk */
+    int32_t batch;           /* B the plan was made for */
+    int32_t num_q_heads;     /* Hq */
+    int32_t num_kv_heads;    /* Hkv */
+    int32_t head_dim;        /* D */
+    int32_t window;          /* W (0 = global family) */
+    int32_t page_size;       /* P */
+    int32_t grid;            /* CTAs the decode launch uses */
+    int32_t flags;           /* GA_PLAN_* */
+    int32_t touch_stride;    /* touch-log entries per row-chunk (flag set) */
+    int64_t row_chunks;      /* (row, chunk) pairs the workspace holds */
+    int64_t units;           /* work units (row-chunk x kv head x head group) planned */
+    int64_t workspace_bytes; /* device workspace the decode call needs (0 if none) */
+    int64_t partial_o_offset;    /* byte offsets inside the workspace */
+    int64_t partial_lse_offset;
+    int64_t touch_log_offset;
+} ga_plan;
+
+/*
+ * ga_plan_splits -- choose how each row's attended pages are cut into split-KV
+ * chunks so that the decode launch fills all SMs ("[Model] Gemma 4 M3 31B",
+ * Proposed Plan: the split-KV chunk policy re-checked when the global
+ * family's head count changes; "visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa
+ * is mandatory here": flash-decode split factor 8).  Host only, no CUDA call.
+ *
+ *   seq_lens_host [batch] int32, host memory: the lengths (or upper bounds of
+ *       the lengths) the decode calls will see; the workspace is sized for them.
+ *   window: 0 for the global family, else the sliding window W.
+ *   num_sms: SMs of the device the decode runs on (>= 1).
+ *   requested_splits > 0: GA_SPLIT_COUNT with that many chunks per row
+ *       (1 = GA_SPLIT_NONE).  fixed_chunk_tokens > 0 (a multiple of
+ *       page_size): GA_SPLIT_CHUNK with that chunk size.  Both 0: automatic
+ *       (a cost model over candidate chunk sizes of the static round-robin
+ *       schedule; the result may depend on the whole batch).  Both > 0 is an
+ *       error.
+ *   flags: GA_PLAN_* bits.
+ * Returns GA_OK and fills *plan_out, or GA_ERR_INVALID_ARG / GA_ERR_UNSUPPORTED.
+ */
+int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_heads,
+                   int32_t num_kv_heads, int32_t head_dim, int32_t window, int32_t page_size,
+                   int32_t num_sms, int32_t requested_splits, int32_t fixed_chunk_tokens,
+                   int32_t flags, ga_plan* plan_out);
+
+/*
+ * ga_kv_append -- write this step's new K and V token of every row into its
+ * page slot: page page_table[b][positions[b] / P], slot positions[b] % P, for
+ * every kv head ("[Model] Gemma 4 M1 12B", Description: paged prefill and
+ * decode; "[Model] Gemma 4 M2 26B-A4B", Proposed Plan: opt-in FP8 KV pool for
+ * the sliding family, and page offsets through one checked helper).
+ *
+ *   k_new, v_new [batch, num_kv_heads, head_dim] bf16.
+ *   k_pool, v_pool written in place; kv_dtype GA_KV_BF16 copies the bits,
+ *       GA_KV_E4M3 stores E4M3FN(round-to-nearest-even, saturate to +-448)
+ *       of fp32(x) / scale[c] (IEEE division); k_scale, v_scale required for
+ *       E4M3 and ignored for bf16.
+ *   positions [batch] int32: slot index of the new token (= L_b - 1); rows
+ *       with a negative position are skipped.
+ *   head_dim 256 or 512.
+ * Device errors: GA_DEVERR_POSITION (row skipped).
+ */
+int ga_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                 int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                 const int32_t* page_table, int64_t pt_stride, const int32_t* positions,
+                 int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                 int64_t num_pages, int32_t* err_word, ga_stream_t stream);
+
+/*
+ * ga_decode_local_hd256 -- sliding-window paged decode, head_dim 256
+ * ("[Model] Gemma 4 M3 31B", Acceptance Criteria: window boundaries at 1023,
+ * 1024, 1025 with multiple-window continuation).  Only the pages holding keys
+ * [L_b - window, L_b) are read ("Gemma 4 31B on vLLM -- operating-point
+ * reference", Three load-bearing facts: sliding-window tile pruning).
+ *
+ *   q [batch, num_q_heads, 256] bf16; num_q_heads % num_kv_heads == 0.
+ *   kv_dtype GA_KV_BF16 or GA_KV_E4M3 (with k_scale, v_scale [Hkv] fp32;
+ *       with E4M3 the q operand is staged in f16, |q| <= 65504).
+ *   seq_lens [batch] int32 device; window >= 1.
+ *   scale: softmax scale (e.g. 1/sqrt(256), or 1.0 for the Gemma convention).
+ *   plan: from ga_plan_splits with the same batch, heads, head_dim, window
+ *       and page_size.  If plan->mode != GA_SPLIT_NONE the call needs
+ *       workspace (>= plan->workspace_bytes, 16-byte aligned) and runs the
+ *       decode kernel then ga_splitkv_combine's kernel on `stream` (the
+ *       latter is left to the caller when the plan has
+ *       GA_PLAN_EXTERNAL_COMBINE).
+ *   out [batch, num_q_heads, 256] bf16.
+ * Rows with L_b = 0 produce zeros.
+ */
+int ga_decode_local_hd256(const void* q, const void* k_pool, const void* v_pool,
+                          int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                          const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t window, int32_t page_size, int64_t num_pages, float scale,
+                          const ga_plan* plan, void* workspace, size_t workspace_bytes,
+                          void* out, int32_t* err_word, ga_stream_t stream);
+
+/*
+ * ga_decode_global_hd512 -- full-context paged decode, head_dim 512
+ * ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is mandatory here" and
+ * hybrid-pf64 numerics gate: S=1 decode over the whole cache, no causal mask,
+ * 32 query heads x 512 over 4 KV heads).  Arguments as for the local call
+ * without `window`; head_dim is 512.
+ */
+int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool,
+                           int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                           const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t page_size, int64_t num_pages, float scale,
+                           const ga_plan* plan, void* workspace, size_t workspace_bytes,
+                           void* out, int32_t* err_word, ga_stream_t stream);
+
+/*
+ * ga_splitkv_combine -- merge split-KV partials by log-sum-exp
+ * ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is mandatory here":
+ * flash-decode with split factor 8):
+ *     M = max_s lse_s,  out = sum_s e^{lse_s - M} o_s / sum_s e^{lse_s - M}
+ * with o_s normalised within its chunk and lse_s = ln sum_{j in chunk s} e^{s_j}
+ * (natural log; an empty chunk has lse_s = -inf and weighs nothing).
+ *
+ *   partial_o [plan->row_chunks, Hq, D] fp32 and partial_lse
+ *       [plan->row_chunks, Hq] fp32, device: row-chunk r of row b is
+ *       rc_b + j, rc_b = sum over rows b' < b of that row's chunk count, in
+ *       the chunking the plan defines for the device seq_lens.
+ *   seq_lens [plan->batch] int32 device and pt_stride: the same values the
+ *   decode call got (a length beyond pt_stride * page_size counts as 0).
+ *   Rows whose chunk count is 1 are left untouched (the decode call wrote
+ *   them).  out [plan->batch, Hq, D] bf16.
+ * The decode calls invoke this themselves when split; it is exported for
+ * testing and for callers that write their own partials.
+ */
+int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
+                       const int32_t* seq_lens, int64_t pt_stride, void* out,
+                       int32_t* err_word, ga_stream_t stream);
+
+/* Name of a GA_* status code (static string). */
+const char* ga_strerror(int status);
+
+/* GA_OK for a zero device error word, else GA_ERR_DEVICE_CHECK. */
+int ga_check_error_word(int32_t word);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t ga_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* GA_H_ */

@@ -1,0 +1,326 @@
+// ga_api.cu -- the exported C ABI: argument checks (fail closed before any
+// launch), the split-KV planner and the launch of the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <vector>
+
+#include "ga_internal.h"
+
+namespace ga {
+
+int launch_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                  int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                  const int32_t* page_table, int64_t pt_stride, const int32_t* positions,
+                  int32_t batch, int32_t num_kv_heads, int32_t head_dim, int64_t num_pages,
+                  int32_t* err_word, cudaStream_t stream);
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> cached{nullptr};
+    EncodeTiledFn f = cached.load();
+    if (f) return f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+        return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    cached.store(f);
+    return f;
+}
+
+int encode_pool_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_t rows,
+                    int32_t head_dim) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return GA_ERR_CUDA;
+    const int esz = kv_dtype == GA_KV_BF16 ? 2 : 1;
+    const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)head_dim * esz};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)kPageSize};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map,
+                           kv_dtype == GA_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                           2, const_cast<void*>(pool), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
+}
+
+int ensure_smem_attr(const void* func, int bytes, int slot) {
+    static std::atomic<uint64_t> done[8];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GA_ERR_CUDA;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done[slot].load() & bit) return GA_OK;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return GA_ERR_CUDA;
+    done[slot].fetch_or(bit);
+    return GA_OK;
+}
+
+// ------------------------------------------------------------------ planner
+
+namespace {
+
+struct PlanInput {
+    const int32_t* lens;
+    int32_t B, Hq, Hkv, D, W, num_sms;
+};
+
+// Row-chunk count and per-unit page counts of a candidate chunking.
+struct Candidate {
+    int32_t mode, splits, chunk_pages;
+    int64_t row_chunks = 0, units = 0;
+    int32_t max_cp = 0;
+    double cost = 0;
+};
+
+void evaluate(const PlanInput& in, Candidate& cand) {
+    const int32_t HG = head_groups(in.Hq / in.Hkv);
+    const int64_t per_rc = (int64_t)in.Hkv * HG;
+    std::vector<int32_t> rc_pages;
+    rc_pages.reserve(in.B * 4);
+    int64_t split_rows_rc = 0;
+    for (int32_t b = 0; b < in.B; ++b) {
+        const RowGeom g = row_geometry(in.lens[b], in.W, INT64_MAX / 64, cand.mode, cand.splits,
+                                       cand.chunk_pages);
+        cand.max_cp = std::max(cand.max_cp, std::min(g.cp, std::max(g.npages, 1)));
+        for (int32_t j = 0; j < g.chunks; ++j) {
+            int32_t p0, np;
+            chunk_pages_of(g, j, &p0, &np);
+            rc_pages.push_back(np);
+        }
+        if (g.chunks > 1) split_rows_rc += g.chunks;
+    }
+    cand.row_chunks = (int64_t)rc_pages.size();
+    cand.units = cand.row_chunks * per_rc;
+    // Static round-robin schedule of the persistent grid: unit u -> CTA u % G.
+    // Cost in "page loads per SM": each unit costs its pages plus a fixed
+    // overhead (warp merge, pipeline refill); a split adds the partial
+    // round trip spread over all SMs plus one extra launch.
+    const int64_t G = std::max<int64_t>(1, std::min<int64_t>(cand.units, in.num_sms));
+    const double unit_ovh = 2.0;
+    std::vector<double> load((size_t)G, 0.0);
+    for (int64_t u = 0; u < cand.units; ++u) {
+        const int64_t rc = u / per_rc;
+        load[(size_t)(u % G)] += rc_pages[(size_t)rc] + unit_ovh;
+    }
+    double makespan = 0;
+    for (double v : load) makespan = std::max(makespan, v);
+    double combine = 0;
+    if (split_rows_rc > 0) {
+        const double page_bytes = 2.0 * kPageSize * in.D * 2.0;   // K + V page-head, bf16
+        const double partial_bytes = 2.0 * (double)split_rows_rc * in.Hq * in.D * 4.0;
+        combine = partial_bytes / page_bytes / in.num_sms + 4.0;
+    }
+    cand.cost = makespan + combine;
+}
+
+}  // namespace
+
+}  // namespace ga
+
+using namespace ga;
+
+extern "C" {
+
+int32_t ga_version(void) { return 0x000100; }
+
+const char* ga_strerror(int status) {
+    switch (status) {
+        case GA_OK: return "GA_OK";
+        case GA_ERR_INVALID_ARG: return "GA_ERR_INVALID_ARG: invalid argument";
+        case GA_ERR_UNSUPPORTED: return "GA_ERR_UNSUPPORTED: unsupported configuration";
+        case GA_ERR_WORKSPACE_TOO_SMALL: return "GA_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+        case GA_ERR_CUDA: return "GA_ERR_CUDA: CUDA call or kernel launch failed";
+        case GA_ERR_DEVICE_CHECK: return "GA_ERR_DEVICE_CHECK: a kernel reported invalid device data";
+        default: return "unknown ga status";
+    }
+}
+
+int ga_check_error_word(int32_t word) { return word == 0 ? GA_OK : GA_ERR_DEVICE_CHECK; }
+
+int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_heads,
+                   int32_t num_kv_heads, int32_t head_dim, int32_t window, int32_t page_size,
+                   int32_t num_sms, int32_t requested_splits, int32_t fixed_chunk_tokens,
+                   int32_t flags, ga_plan* plan_out) {
+    if (plan_out == nullptr || batch < 0 || (batch > 0 && seq_lens_host == nullptr))
+        return GA_ERR_INVALID_ARG;
+    if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || window < 0 ||
+        num_sms < 1 || requested_splits < 0 || fixed_chunk_tokens < 0 ||
+        (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~(GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE)))
+        return GA_ERR_INVALID_ARG;
+    if (batch > kMaxBatch) return GA_ERR_UNSUPPORTED;
+    if (head_dim != 256 && head_dim != 512) return GA_ERR_UNSUPPORTED;
+    if (page_size != kPageSize) return GA_ERR_UNSUPPORTED;
+    if (fixed_chunk_tokens % page_size != 0) return GA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < batch; ++b)
+        if (seq_lens_host[b] < 0) return GA_ERR_INVALID_ARG;
+
+    PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, window, num_sms};
+    Candidate best;
+    if (requested_splits == 1) {
+        best = Candidate{kSplitNone, 0, 0};
+        evaluate(in, best);
+    } else if (requested_splits > 1) {
+        best = Candidate{kSplitCount, requested_splits, 0};
+        evaluate(in, best);
+    } else if (fixed_chunk_tokens > 0) {
+        best = Candidate{kSplitChunk, 0, fixed_chunk_tokens / page_size};
+        evaluate(in, best);
+    } else {
+        best = Candidate{kSplitNone, 0, 0};
+        evaluate(in, best);
+        int32_t max_np = 0;
+        for (int32_t b = 0; b < batch; ++b)
+            max_np = std::max(max_np,
+                              row_geometry(seq_lens_host[b], window, INT64_MAX / 64, kSplitNone,
+                                           0, 0).npages);
+        for (int32_t cp = 4; cp < max_np; cp *= 2) {
+            Candidate c{kSplitChunk, 0, cp};
+            evaluate(in, c);
+            if (c.cost < best.cost * 0.98) best = c;
+        }
+    }
+    ga_plan p{};
+    p.mode = best.mode;
+    p.splits = best.splits;
+    p.chunk_pages = best.chunk_pages;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.window = window;
+    p.page_size = page_size;
+    p.flags = flags;
+    p.row_chunks = best.row_chunks;
+    p.units = best.units;
+    p.grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(best.units, num_sms));
+    int64_t off = 0;
+    auto take = [&off](int64_t bytes) {
+        const int64_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    if (p.mode != kSplitNone) {
+        p.partial_o_offset = take(p.row_chunks * num_q_heads * (int64_t)head_dim * 4);
+        p.partial_lse_offset = take(p.row_chunks * num_q_heads * 4);
+    }
+    if (flags & GA_PLAN_TOUCH_LOG) {
+        p.touch_stride = std::max(best.max_cp, 1);
+        p.touch_log_offset = take(p.row_chunks * (int64_t)p.touch_stride * 4);
+    }
+    p.workspace_bytes = off;
+    *plan_out = p;
+    return GA_OK;
+}
+
+int ga_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                 int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                 const int32_t* page_table, int64_t pt_stride, const int32_t* positions,
+                 int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                 int64_t num_pages, int32_t* err_word, ga_stream_t stream) {
+    if (batch < 0 || num_kv_heads < 1 || pt_stride < 1 || num_pages < 1) return GA_ERR_INVALID_ARG;
+    if (kv_dtype != GA_KV_BF16 && kv_dtype != GA_KV_E4M3) return GA_ERR_UNSUPPORTED;
+    if (head_dim != 256 && head_dim != 512) return GA_ERR_UNSUPPORTED;
+    if (page_size != kPageSize) return GA_ERR_UNSUPPORTED;
+    if (batch == 0) return GA_OK;
+    if (!k_new || !v_new || !k_pool || !v_pool || !page_table || !positions)
+        return GA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return GA_ERR_INVALID_ARG;
+    if (kv_dtype == GA_KV_E4M3 && (!k_scale || !v_scale)) return GA_ERR_INVALID_ARG;
+    return launch_append(k_new, v_new, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table,
+                         pt_stride, positions, batch, num_kv_heads, head_dim, num_pages,
+                         err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static int decode_entry(const void* q, const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                        const float* k_scale, const float* v_scale, const int32_t* page_table,
+                        int64_t pt_stride, const int32_t* seq_lens, int32_t batch,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t window, int32_t page_size, int64_t num_pages, float scale,
+                        const ga_plan* plan, void* workspace, size_t workspace_bytes, void* out,
+                        int32_t* err_word, ga_stream_t stream) {
+    if (plan == nullptr || batch < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+        num_q_heads % num_kv_heads != 0 || pt_stride < 1 || num_pages < 1 ||
+        !std::isfinite(scale))
+        return GA_ERR_INVALID_ARG;
+    if (kv_dtype != GA_KV_BF16 && kv_dtype != GA_KV_E4M3) return GA_ERR_UNSUPPORTED;
+    if (page_size != kPageSize) return GA_ERR_UNSUPPORTED;
+    if (batch > kMaxBatch) return GA_ERR_UNSUPPORTED;
+    if (num_pages * num_kv_heads * (int64_t)kPageSize >= (int64_t(1) << 31))
+        return GA_ERR_UNSUPPORTED;
+    if (plan->batch != batch || plan->num_q_heads != num_q_heads ||
+        plan->num_kv_heads != num_kv_heads || plan->head_dim != head_dim ||
+        plan->window != window || plan->page_size != page_size)
+        return GA_ERR_INVALID_ARG;
+    if (batch == 0) return GA_OK;
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return GA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return GA_ERR_INVALID_ARG;
+    if (kv_dtype == GA_KV_E4M3 && (!k_scale || !v_scale)) return GA_ERR_INVALID_ARG;
+    if (plan->workspace_bytes > 0) {
+        if (!workspace || !aligned16(workspace)) return GA_ERR_INVALID_ARG;
+        if ((int64_t)workspace_bytes < plan->workspace_bytes) return GA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    DecodeArgs a{q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride, seq_lens,
+                 batch, num_q_heads, num_kv_heads, head_dim, window, num_pages, scale, plan,
+                 workspace, out, err_word, reinterpret_cast<cudaStream_t>(stream)};
+    return launch_decode(a);
+}
+
+int ga_decode_local_hd256(const void* q, const void* k_pool, const void* v_pool,
+                          int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                          const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t window, int32_t page_size, int64_t num_pages, float scale,
+                          const ga_plan* plan, void* workspace, size_t workspace_bytes,
+                          void* out, int32_t* err_word, ga_stream_t stream) {
+    if (window < 1) return GA_ERR_INVALID_ARG;
+    return decode_entry(q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride,
+                        seq_lens, batch, num_q_heads, num_kv_heads, 256, window, page_size,
+                        num_pages, scale, plan, workspace, workspace_bytes, out, err_word,
+                        stream);
+}
+
+int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool,
+                           int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                           const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t page_size, int64_t num_pages, float scale,
+                           const ga_plan* plan, void* workspace, size_t workspace_bytes,
+                           void* out, int32_t* err_word, ga_stream_t stream) {
+    return decode_entry(q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride,
+                        seq_lens, batch, num_q_heads, num_kv_heads, 512, 0, page_size,
+                        num_pages, scale, plan, workspace, workspace_bytes, out, err_word,
+                        stream);
+}
+
+int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
+                       const int32_t* seq_lens, int64_t pt_stride, void* out,
+                       int32_t* err_word, ga_stream_t stream) {
+    if (plan == nullptr || pt_stride < 1) return GA_ERR_INVALID_ARG;
+    if (plan->head_dim != 256 && plan->head_dim != 512) return GA_ERR_UNSUPPORTED;
+    if (plan->batch == 0 || plan->mode == GA_SPLIT_NONE) return GA_OK;
+    if (!partial_o || !partial_lse || !seq_lens || !out) return GA_ERR_INVALID_ARG;
+    if (!aligned16(partial_o) || !aligned16(out)) return GA_ERR_INVALID_ARG;
+    return launch_combine(partial_o, partial_lse, plan, seq_lens, out, err_word, pt_stride,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,658 @@
+// ga_decode.cu -- paged split-KV GQA decode attention for sm_103a.
+//
+// One templated kernel body serves both KV families (local hd256 window,
+// global hd512 full context) and both KV element types (bf16, E4M3), so the
+// hd512 path is never a hand-copied twin of the hd256 one ("[Model] Gemma 4
+// M2 26B-A4B", Proposed Plan: one home for the paged-KV launch bodies).
+//
+// Work decomposition.  A unit is (row-chunk, kv head, head group of <= 8
+// query heads).  A row's attended pages (only the window's pages for the
+// local family: "Gemma 4 31B on vLLM -- operating-point reference", Three
+// load-bearing facts, sliding-window tile pruning) are cut into chunks by the
+// split plan; each chunk of each kv head is one unit.  The grid is
+// persistent: CTA i takes units i, i + grid, ...
+//
+// Inside a CTA (NCW + 1 warps):
+//   * the producer warp reads page ids from the page table, checks them,
+//     and issues 2-D bulk tensor copies (TMA, 128-byte swizzle) of the K and V
+//     page-head blocks into a ring of NS shared-memory stages, each completing
+//     on that stage's "full" mbarrier;
+//   * NCW consumer warps take the unit's pages round-robin.  Per 16-key page a
+//     warp computes S^T = K Q^T with m16n8k16 tensor-core MMAs (16 keys x 8
+//     query heads), applies the window mask, runs the online softmax on
+//     fp32 scores (warp shuffles across the 8 lanes sharing a head column),
+//     transposes P with movmatrix and accumulates O^T += V^T P^T (V read with
+//     ldmatrix.trans).  The stage is then released on its "empty" mbarrier.
+//   * at the end of a unit the consumer warps merge their (m, l, O) in shared
+//     memory in a fixed order (deterministic) and write either the final bf16
+//     output (row in one chunk) or an fp32 partial plus its log-sum-exp.
+// The S=1 decode has no causal mask ("visible-cx/Gemma-4-31B-CoreAI",
+// "--metal-sdpa is mandatory here"); the window mask only touches the first
+// and last page of the attended range.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math_constants.h>
+
+#include "ga_device.cuh"
+#include "ga_internal.h"
+
+namespace ga {
+
+struct DecodeParams {
+    const __nv_bfloat16* q;       // [B, Hq, D]
+    const int32_t* page_table;    // [B, pt_stride]
+    const int32_t* seq_lens;      // [B]
+    const float* k_scale;         // [Hkv] (E4M3)
+    const float* v_scale;
+    __nv_bfloat16* out;           // [B, Hq, D]
+    float* partial_o;             // [rc_capacity, Hq, D]
+    float* partial_lse;           // [rc_capacity, Hq]
+    int32_t* touch_log;           // [rc_capacity, touch_stride] or null
+    int32_t* err_word;
+    int64_t pt_stride;
+    int64_t num_pages;
+    int64_t rc_capacity;
+    int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
+    float scale_log2;             // softmax scale * log2(e)
+};
+
+template <int D_, int KV_, int NCW_, int NS_>
+struct DecodeCfg {
+    static constexpr int D = D_;
+    static constexpr int KV = KV_;                  // GA_KV_BF16 / GA_KV_E4M3
+    static constexpr int NCW = NCW_;                // consumer warps
+    static constexpr int NS = NS_;                  // ring stages (one page each)
+    static constexpr int NCT = NCW * 32;            // consumer threads
+    static constexpr int NTHREADS = NCT + 32;
+    static constexpr int ESZ = KV == GA_KV_BF16 ? 2 : 1;
+    static constexpr int TILE_ELEMS = 128 / ESZ;    // elements per 128-byte box row
+    static constexpr int NTILES = D * ESZ / 128;    // boxes per page-head block
+    static constexpr int TILE_BYTES = kPageSize * 128;
+    static constexpr int BLOCK_BYTES = NTILES * TILE_BYTES;
+    static constexpr int STAGE_BYTES = 2 * BLOCK_BYTES;   // K block + V block
+    static constexpr int KSTEPS = D / 16;
+    static constexpr int MTILES = D / 16;
+    static constexpr bool Q_IN_REGS = (D <= 256);
+    static constexpr int MSTRIDE = D + 4;           // floats per head row of the merge buffer
+    // shared-memory map; every region starts on a 128-byte boundary (the
+    // mbarriers need 8, the float4 / uint2 accesses 16)
+    static constexpr int al(int x) { return (x + 127) / 128 * 128; }
+    static constexpr int OFF_RING = 0;
+    static constexpr int OFF_QF = al(OFF_RING + NS * STAGE_BYTES);
+    static constexpr int OFF_MERGE = al(OFF_QF + KSTEPS * 32 * 8);
+    static constexpr int OFF_ML = al(OFF_MERGE + NCW * kHeadTile * MSTRIDE * 4);
+    static constexpr int OFF_PREFIX = al(OFF_ML + 2 * NCW * kHeadTile * 4);
+    static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
+    static constexpr int OFF_BARS = al(OFF_FLAGS + NS * 4);
+    static constexpr int SMEM_USED = al(OFF_BARS + 2 * NS * 8);
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
+    static_assert(D % 64 == 0 && NTILES >= 1, "head_dim");
+    static_assert(OFF_BARS % 8 == 0 && OFF_QF % 16 == 0 && OFF_MERGE % 16 == 0, "alignment");
+    static_assert(STAGE_BYTES % 1024 == 0, "swizzle-128B boxes need 1024-byte aligned stages");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// Row owning row-chunk rc: largest b with pre[b] <= rc.
+__device__ __forceinline__ int find_row(const int32_t* pre, int B, int64_t rc) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)pre[mid] <= rc) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct UnitInfo {
+    int64_t rc;
+    int32_t b, c, hg, j, p0, np, h0, nvalid;
+    RowGeom g;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const DecodeParams& p, const int32_t* pre,
+                                              int64_t u) {
+    UnitInfo x;
+    unit_coords(u, p.Hkv, p.HG, &x.rc, &x.c, &x.hg);
+    x.b = find_row(pre, p.B, x.rc);
+    x.j = (int32_t)(x.rc - pre[x.b]);
+    x.g = row_geometry(__ldg(p.seq_lens + x.b), p.window, p.pt_stride, p.mode, p.splits,
+                       p.chunk_pages);
+    chunk_pages_of(x.g, x.j, &x.p0, &x.np);
+    x.h0 = x.c * p.group + x.hg * kHeadTile;
+    int nv = p.group - x.hg * kHeadTile;
+    x.nvalid = nv < kHeadTile ? nv : kHeadTile;
+    return x;
+}
+
+// ------------------------------------------------------------------ producer
+
+template <class C>
+__device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
+                         const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
+                         volatile uint32_t* flags, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t policy = l2_evict_first_policy();
+    uint32_t seq = 0;
+    int32_t issued_round[C::NS];
+#pragma unroll
+    for (int s = 0; s < C::NS; ++s) issued_round[s] = -1;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
+        const UnitInfo x = unit_info(p, pre, u);
+        const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride;
+        const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
+        for (int i0 = 0; i0 < x.np && !stop; i0 += 32) {
+            const int i = i0 + lane;
+            const int32_t id = (i < x.np) ? __ldg(tbl + x.p0 + i) : 0;
+            const int cnt = min(32, x.np - i0);
+            for (int k = 0; k < cnt; ++k) {
+                const int32_t pid = __shfl_sync(0xffffffffu, id, k);
+                if (lane == 0 && !stop) {
+                    const uint32_t slot = seq % C::NS;
+                    const uint32_t round = seq / C::NS;
+                    const uint32_t full = bars + 8 * slot;
+                    const uint32_t empty = bars + 8 * (C::NS + slot);
+                    if (*abort_flag || !mbar_wait(empty, (round & 1) ^ 1)) {
+                        report(p.err_word, kErrTimeout);
+                        *abort_flag = 1;
+                        stop = true;
+                    } else if (page_ok(pid, p.num_pages)) {
+                        flags[slot] = 0;
+                        mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                        const int32_t y = page_block_row(pid, x.c, p.Hkv);
+                        const uint32_t dst = ring + slot * C::STAGE_BYTES;
+#pragma unroll
+                        for (int t = 0; t < C::NTILES; ++t)
+                            tma_load_2d(dst + t * C::TILE_BYTES, tmK, full, t * C::TILE_ELEMS, y,
+                                        policy);
+#pragma unroll
+                        for (int t = 0; t < C::NTILES; ++t)
+                            tma_load_2d(dst + C::BLOCK_BYTES + t * C::TILE_BYTES, tmV, full,
+                                        t * C::TILE_ELEMS, y, policy);
+                        issued_round[slot] = (int32_t)round;
+                    } else {
+                        flags[slot] = 1;
+                        report(p.err_word, kErrPageId);
+                        mbar_arrive(full);
+                    }
+                    if (log && i0 + k < p.touch_stride)
+                        p.touch_log[x.rc * p.touch_stride + i0 + k] = pid;
+                }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+                ++seq;
+            }
+        }
+    }
+    // Never leave with a copy in flight into this CTA's shared memory.
+    if (lane == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            if (issued_round[s] >= 0 &&
+                !mbar_wait(bars + 8 * s, (uint32_t)issued_round[s] & 1)) {
+                report(p.err_word, kErrTimeout);
+                *abort_flag = 1;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ consumer
+
+// Builds the per-lane B fragments of Q^T for one unit in shared memory:
+// qf[ks][lane] = {b0, b1}.  bf16: b0 = q[n][16ks+2t .. +1], b1 = q[n][16ks+2t+8 .. +9]
+// with n = lane/4 the head column, t = lane%4.  E4M3: the four dims
+// 16ks+4t .. +3 in f16 (k order permuted to match the byte layout of the
+// E4M3 K fragments; the dot product does not depend on the order).
+template <class C>
+__device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInfo& x,
+                                            uint2* qf, int tid) {
+    for (int e = tid; e < C::KSTEPS * 32; e += C::NCT) {
+        const int ks = e >> 5, ln = e & 31, n = ln >> 2, t = ln & 3;
+        uint2 v = make_uint2(0u, 0u);
+        if (n < x.nvalid) {
+            const __nv_bfloat16* row = p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D;
+            if (C::KV == GA_KV_BF16) {
+                v.x = __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t));
+                v.y = __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t + 8));
+            } else {
+                const uint2 w = __ldg(reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t));
+                const float f0 = bf16_lo(w.x), f1 = bf16_hi(w.x);
+                const float f2 = bf16_lo(w.y), f3 = bf16_hi(w.y);
+                v.x = pack_f16x2(f0, f1);
+                v.y = pack_f16x2(f2, f3);
+                const __half2 h0 = *reinterpret_cast<__half2*>(&v.x);
+                const __half2 h1 = *reinterpret_cast<__half2*>(&v.y);
+                const bool big = (fabsf(f0) < CUDART_INF_F && __hisinf(__low2half(h0))) ||
+                                 (fabsf(f1) < CUDART_INF_F && __hisinf(__high2half(h0))) ||
+                                 (fabsf(f2) < CUDART_INF_F && __hisinf(__low2half(h1))) ||
+                                 (fabsf(f3) < CUDART_INF_F && __hisinf(__high2half(h1)));
+                if (big) report(p.err_word, kErrQRange);
+            }
+        }
+        qf[e] = v;
+    }
+}
+
+template <class C>
+__device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
+                         uint32_t ring, uint32_t bars, volatile uint32_t* flags,
+                         volatile int* abort_flag) {
+    const int tid = threadIdx.x;            // 0 .. NCT-1
+    const int w = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, t = lane & 3;
+    // ldmatrix row / 16-byte-chunk selectors of this lane
+    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8, khi = lane >> 4;
+    const int vrow = (lane & 7) + ((lane >> 4) & 1) * 8, vhi = (lane >> 3) & 1;
+    const uint32_t koff = krow * 128, kx = krow & 7;
+    const uint32_t voff = vrow * 128, vx = vrow & 7;
+
+    uint2* qf = reinterpret_cast<uint2*>(smem + C::OFF_QF);
+    float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
+    float* mlw = reinterpret_cast<float*>(smem + C::OFF_ML);   // [2][NCW][8]
+
+    uint32_t seq_base = 0;
+    for (int64_t u = blockIdx.x; u < U; u += gridDim.x) {
+        const UnitInfo x = unit_info(p, pre, u);
+        const bool single = (x.g.chunks == 1);
+        float kfac = p.scale_log2, vfac = 1.0f;
+        if (C::KV == GA_KV_E4M3) {
+            kfac *= __ldg(p.k_scale + x.c);
+            vfac = __ldg(p.v_scale + x.c);
+        }
+        fill_qfrags<C>(p, x, qf, tid);
+        named_barrier(1, C::NCT);
+
+        uint32_t qr[C::Q_IN_REGS ? C::KSTEPS : 1][2];
+        if constexpr (C::Q_IN_REGS) {
+#pragma unroll
+            for (int ks = 0; ks < C::KSTEPS; ++ks) {
+                const uint2 v = qf[ks * 32 + lane];
+                qr[ks][0] = v.x;
+                qr[ks][1] = v.y;
+            }
+        }
+
+        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+        float o[C::MTILES][4];
+#pragma unroll
+        for (int mt = 0; mt < C::MTILES; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+        for (int i = w; i < x.np; i += C::NCW) {
+            const uint32_t n = seq_base + (uint32_t)i;
+            const uint32_t slot = n % C::NS;
+            const uint32_t full = bars + 8 * slot;
+            bool ready = false;
+            if (!*abort_flag) {
+                ready = mbar_wait(full, (n / C::NS) & 1);
+                if (!ready) {
+                    if (lane == 0) report(p.err_word, kErrTimeout);
+                    *abort_flag = 1;
+                }
+            }
+            ready = __all_sync(0xffffffffu, ready);
+            if (ready && flags[slot] == 0) {
+                const uint32_t kb = ring + slot * C::STAGE_BYTES;
+                const uint32_t vb = kb + C::BLOCK_BYTES;
+                // ---- S^T = K Q^T (16 keys x 8 heads), 4 independent chains
+                float sa[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sa[r][0] = sa[r][1] = sa[r][2] = sa[r][3] = 0.f;
+                if constexpr (C::KV == GA_KV_BF16) {
+#pragma unroll
+                    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+                        uint32_t a[4];
+                        const uint32_t ch = (uint32_t)(((ks & 3) << 1) + khi);
+                        ldsm_x4(kb + (ks >> 2) * C::TILE_BYTES + koff + ((ch ^ kx) << 4), a);
+                        uint32_t b0, b1;
+                        if constexpr (C::Q_IN_REGS) {
+                            b0 = qr[ks][0];
+                            b1 = qr[ks][1];
+                        } else {
+                            const uint2 v = qf[ks * 32 + lane];
+                            b0 = v.x;
+                            b1 = v.y;
+                        }
+                        mma_bf16(sa[ks & 3], a, b0, b1);
+                    }
+                } else {
+#pragma unroll
+                    for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
+                        uint32_t r[4];
+                        const uint32_t ch = (uint32_t)(((kp & 3) << 1) + khi);
+                        ldsm_x4(kb + (kp >> 2) * C::TILE_BYTES + koff + ((ch ^ kx) << 4), r);
+#pragma unroll
+                        for (int hs = 0; hs < 2; ++hs) {
+                            const int ks = 2 * kp + hs;
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2(r[2 * hs] & 0xFFFFu);
+                            a[1] = e4m3x2_to_f16x2(r[2 * hs + 1] & 0xFFFFu);
+                            a[2] = e4m3x2_to_f16x2(r[2 * hs] >> 16);
+                            a[3] = e4m3x2_to_f16x2(r[2 * hs + 1] >> 16);
+                            uint32_t b0, b1;
+                            if constexpr (C::Q_IN_REGS) {
+                                b0 = qr[ks][0];
+                                b1 = qr[ks][1];
+                            } else {
+                                const uint2 v = qf[ks * 32 + lane];
+                                b0 = v.x;
+                                b1 = v.y;
+                            }
+                            mma_f16(sa[ks & 3], a, b0, b1);
+                        }
+                    }
+                }
+                float s[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    s[r] = ((sa[0][r] + sa[1][r]) + (sa[2][r] + sa[3][r])) * kfac;
+                // ---- window / length mask (first and last page of the range only)
+                const int32_t key0 = (x.p0 + i) * kPageSize;
+                const bool partial = key0 < x.g.lo || key0 + kPageSize > x.g.len;
+                uint32_t mk01 = 0xffffffffu, mk89 = 0xffffffffu;
+                if (partial) {
+                    const int32_t ka = key0 + gid, kb8 = key0 + gid + 8;
+                    const bool va = ka >= x.g.lo && ka < x.g.len;
+                    const bool vb = kb8 >= x.g.lo && kb8 < x.g.len;
+                    if (!va) { s[0] = -CUDART_INF_F; s[1] = -CUDART_INF_F; }
+                    if (!vb) { s[2] = -CUDART_INF_F; s[3] = -CUDART_INF_F; }
+                    auto valid = [&](int k) {
+                        const int32_t kk = key0 + k;
+                        return kk >= x.g.lo && kk < x.g.len;
+                    };
+                    mk01 = (valid(2 * t) ? 0x0000ffffu : 0u) | (valid(2 * t + 1) ? 0xffff0000u : 0u);
+                    mk89 = (valid(2 * t + 8) ? 0x0000ffffu : 0u) |
+                           (valid(2 * t + 9) ? 0xffff0000u : 0u);
+                }
+                // ---- online softmax (base 2) over this page, per head column
+                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float ms0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+                const float ms1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+                const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
+                const float p0 = exp2f(s[0] - ms0), p1 = exp2f(s[1] - ms1);
+                const float p2 = exp2f(s[2] - ms0), p3 = exp2f(s[3] - ms1);
+                m0 = mn0;
+                m1 = mn1;
+                l0 = l0 * al0 + (p0 + p2);
+                l1 = l1 * al1 + (p1 + p3);
+#pragma unroll
+                for (int mt = 0; mt < C::MTILES; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                }
+                // ---- P^T fragments: rows = keys, cols = heads -> transpose
+                uint32_t pb0, pb1;
+                if constexpr (C::KV == GA_KV_BF16) {
+                    pb0 = movmatrix_t(pack_bf16x2(p0, p1));
+                    pb1 = movmatrix_t(pack_bf16x2(p2, p3));
+                } else {
+                    pb0 = movmatrix_t(pack_f16x2(p0, p1));
+                    pb1 = movmatrix_t(pack_f16x2(p2, p3));
+                }
+                // ---- O^T += V^T P^T
+                if constexpr (C::KV == GA_KV_BF16) {
+#pragma unroll
+                    for (int mt = 0; mt < C::MTILES; ++mt) {
+                        uint32_t a[4];
+                        const uint32_t ch = (uint32_t)(((mt & 3) << 1) + vhi);
+                        ldsm_x4_t(vb + (mt >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), a);
+                        a[0] &= mk01;
+                        a[1] &= mk01;
+                        a[2] &= mk89;
+                        a[3] &= mk89;
+                        mma_bf16(o[mt], a, pb0, pb1);
+                    }
+                } else {
+#pragma unroll
+                    for (int mp = 0; mp < C::MTILES / 2; ++mp) {
+                        uint32_t r[4];
+                        const uint32_t ch = (uint32_t)(((mp & 3) << 1) + vhi);
+                        ldsm_x4_t(vb + (mp >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), r);
+                        uint32_t ev[4], od[4];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            ev[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0020u));
+                            od[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0031u));
+                        }
+                        ev[0] &= mk01; ev[1] &= mk01; ev[2] &= mk89; ev[3] &= mk89;
+                        od[0] &= mk01; od[1] &= mk01; od[2] &= mk89; od[3] &= mk89;
+                        mma_f16(o[2 * mp], ev, pb0, pb1);
+                        mma_f16(o[2 * mp + 1], od, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * (C::NS + slot));
+        }
+        seq_base += (uint32_t)x.np;
+
+        // ---- merge the warps' (m, l, O) in a fixed order
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        if (gid == 0) {
+            mlw[w * kHeadTile + 2 * t] = m0;
+            mlw[w * kHeadTile + 2 * t + 1] = m1;
+            mlw[C::NCW * kHeadTile + w * kHeadTile + 2 * t] = l0;
+            mlw[C::NCW * kHeadTile + w * kHeadTile + 2 * t + 1] = l1;
+        }
+        named_barrier(1, C::NCT);
+        float fac[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int col = 2 * t + e;
+            float M = -CUDART_INF_F;
+            for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, mlw[ww * kHeadTile + col]);
+            const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
+            float Lt = 0.f;
+            for (int ww = 0; ww < C::NCW; ++ww)
+                Lt += mlw[C::NCW * kHeadTile + ww * kHeadTile + col] *
+                      exp2f(mlw[ww * kHeadTile + col] - Ms);
+            const float mown = (e == 0) ? m0 : m1;
+            fac[e] = (Lt > 0.f) ? exp2f(mown - Ms) * (vfac / Lt) : 0.f;
+        }
+        float* mw = merge + w * kHeadTile * C::MSTRIDE;
+#pragma unroll
+        for (int mt = 0; mt < C::MTILES; ++mt) {
+            int d0, d1;
+            if constexpr (C::KV == GA_KV_BF16) {
+                d0 = 16 * mt + gid;
+                d1 = d0 + 8;
+            } else {   // E4M3 m-tile pairs hold even / odd dims of 32-dim groups
+                d0 = 32 * (mt >> 1) + 2 * gid + (mt & 1);
+                d1 = d0 + 16;
+            }
+            mw[(2 * t) * C::MSTRIDE + d0] = o[mt][0] * fac[0];
+            mw[(2 * t + 1) * C::MSTRIDE + d0] = o[mt][1] * fac[1];
+            mw[(2 * t) * C::MSTRIDE + d1] = o[mt][2] * fac[0];
+            mw[(2 * t + 1) * C::MSTRIDE + d1] = o[mt][3] * fac[1];
+        }
+        named_barrier(1, C::NCT);
+        constexpr int D8 = C::D / 8;
+        for (int e = tid; e < x.nvalid * D8; e += C::NCT) {
+            const int n = e / D8, d = (e % D8) * 8;
+            float acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+            for (int ww = 0; ww < C::NCW; ++ww) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(merge + (ww * kHeadTile + n) * C::MSTRIDE + d);
+                const float4 a = src[0], b = src[1];
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            }
+            const int h = x.h0 + n;
+            if (single) {
+                uint4 v;
+                v.x = pack_bf16x2(acc[0], acc[1]);
+                v.y = pack_bf16x2(acc[2], acc[3]);
+                v.z = pack_bf16x2(acc[4], acc[5]);
+                v.w = pack_bf16x2(acc[6], acc[7]);
+                *reinterpret_cast<uint4*>(p.out + ((int64_t)x.b * p.Hq + h) * C::D + d) = v;
+            } else {
+                float4* dst = reinterpret_cast<float4*>(
+                    p.partial_o + (x.rc * p.Hq + h) * (int64_t)C::D + d);
+                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+        }
+        if (!single && tid < x.nvalid) {
+            float M = -CUDART_INF_F;
+            for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, mlw[ww * kHeadTile + tid]);
+            const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
+            float Lt = 0.f;
+            for (int ww = 0; ww < C::NCW; ++ww)
+                Lt += mlw[C::NCW * kHeadTile + ww * kHeadTile + tid] *
+                      exp2f(mlw[ww * kHeadTile + tid] - Ms);
+            // natural-log LSE of the chunk's scaled scores
+            p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
+                (Lt > 0.f) ? (Ms + log2f(Lt)) * CUDART_LN2_F : -CUDART_INF_F;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <class C>
+__global__ void __launch_bounds__(C::NTHREADS, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int abort_flag;
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* pre = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
+    volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_FLAGS);
+    const uint32_t ring = smem_addr(smem + C::OFF_RING);
+    const uint32_t bars = smem_addr(smem + C::OFF_BARS);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bars + 8 * s, 1);
+            mbar_init(bars + 8 * (C::NS + s), 1);
+        }
+        mbar_init_fence();
+        abort_flag = 0;
+    }
+    if (warp == C::NCW && lane == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    // chunk count of every row, then an inclusive prefix: pre[b+1] = sum_{b'<=b}
+    int bad = 0;
+    for (int b = threadIdx.x; b < p.B; b += C::NTHREADS) {
+        const RowGeom g = row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride, p.mode,
+                                       p.splits, p.chunk_pages);
+        pre[b + 1] = g.chunks;
+        bad |= g.bad_len ? 1 : 0;
+    }
+    bad = __syncthreads_or(bad);
+    if (warp == 0) {
+        const int seg = (p.B + 31) / 32;
+        const int lo = min(p.B, lane * seg), hi = min(p.B, lo + seg);
+        int run = 0;
+        for (int b = lo; b < hi; ++b) {
+            run += pre[b + 1];
+            pre[b + 1] = run;
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const int excl = incl - run;
+        for (int b = lo; b < hi; ++b) pre[b + 1] += excl;
+        if (lane == 0) pre[0] = 0;
+    }
+    __syncthreads();
+    if (bad && blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrSeqLen);
+    const int64_t total_rc = pre[p.B];
+    if (p.mode != kSplitNone && total_rc > p.rc_capacity) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrCapacity);
+        return;
+    }
+    const int64_t U = total_rc * p.Hkv * p.HG;
+    if (warp == C::NCW)
+        producer<C>(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
+    else
+        consumer<C>(p, pre, U, smem, ring, bars, flags, &abort_flag);
+}
+
+// ------------------------------------------------------------------ host
+
+template <class C>
+static int run(const DecodeArgs& a, int slot) {
+    const void* fn = reinterpret_cast<const void*>(&decode_kernel<C>);
+    int rc = ensure_smem_attr(fn, C::SMEM_BYTES, slot);
+    if (rc != GA_OK) return rc;
+    const ga_plan& pl = *a.plan;
+    const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
+    CUtensorMap tmK, tmV;
+    rc = encode_pool_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim);
+    if (rc != GA_OK) return rc;
+    rc = encode_pool_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim);
+    if (rc != GA_OK) return rc;
+
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.page_table = a.page_table;
+    p.seq_lens = a.seq_lens;
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    const bool split = pl.mode != GA_SPLIT_NONE;
+    p.partial_o = split ? reinterpret_cast<float*>(ws + pl.partial_o_offset) : nullptr;
+    p.partial_lse = split ? reinterpret_cast<float*>(ws + pl.partial_lse_offset) : nullptr;
+    p.touch_log = (pl.flags & GA_PLAN_TOUCH_LOG)
+                      ? reinterpret_cast<int32_t*>(ws + pl.touch_log_offset)
+                      : nullptr;
+    p.err_word = a.err_word;
+    p.pt_stride = a.pt_stride;
+    p.num_pages = a.num_pages;
+    p.rc_capacity = pl.row_chunks;
+    p.B = a.batch;
+    p.Hq = a.num_q_heads;
+    p.Hkv = a.num_kv_heads;
+    p.group = a.num_q_heads / a.num_kv_heads;
+    p.HG = head_groups(p.group);
+    p.window = a.window;
+    p.mode = pl.mode;
+    p.splits = pl.splits;
+    p.chunk_pages = pl.chunk_pages;
+    p.touch_stride = pl.touch_stride;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const int grid = pl.grid > 0 ? pl.grid : 1;
+    decode_kernel<C><<<grid, C::NTHREADS, C::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
+    if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
+    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
+        return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
+                              a.pt_stride, a.stream);
+    return GA_OK;
+}
+
+// Tuned shapes: consumer warps x ring stages per (head_dim, KV type).
+using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, 4, 8>;
+using CfgLocalE4m3 = DecodeCfg<256, GA_KV_E4M3, 4, 12>;
+using CfgGlobalBf16 = DecodeCfg<512, GA_KV_BF16, 2, 5>;
+using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, 2, 8>;
+
+int launch_decode(const DecodeArgs& a) {
+    if (a.head_dim == 256)
+        return a.kv_dtype == GA_KV_BF16 ? run<CfgLocalBf16>(a, 0) : run<CfgLocalE4m3>(a, 1);
+    if (a.head_dim == 512)
+        return a.kv_dtype == GA_KV_BF16 ? run<CfgGlobalBf16>(a, 2) : run<CfgGlobalE4m3>(a, 3);
+    return GA_ERR_UNSUPPORTED;
+}
+
+}  // namespace ga

@@ -1,0 +1,99 @@
+// ga_geometry.h -- the one home of paged-KV index arithmetic, shared by the
+// host planner and every kernel (append, decode, combine).
+//
+// Page offsets go through these checked helpers only, never re-derived by
+// hand in a kernel ("[Model] Gemma 4 M2 26B-A4B", Proposed Plan: route the
+// hand-derived page offsets through the checked helper; give the paged-KV
+// launch bodies one home so the hd512 twin is not hand-copied).
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define GA_HD __host__ __device__ __forceinline__
+#else
+#define GA_HD inline
+#endif
+
+namespace ga {
+
+constexpr int kPageSize = 16;     // keys per page; one page = one 16-key MMA tile
+constexpr int kHeadTile = 8;      // query heads per unit (MMA N)
+constexpr int kMaxBatch = 2048;   // rows per call (decode keeps a row prefix in smem)
+
+enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
+
+// Geometry of one row for one call: which keys it attends, which logical
+// pages hold them, and how those pages are cut into split-KV chunks.
+struct RowGeom {
+    int32_t len;         // L (0 if the given length was invalid)
+    int32_t lo;          // first attended key: max(0, L - W) or 0
+    int32_t first_page;  // logical page of key lo
+    int32_t npages;      // logical pages holding keys [lo, L)
+    int32_t cp;          // pages per chunk for this row
+    int32_t chunks;      // chunks of this row (>= 1; an empty row has one empty chunk)
+    bool bad_len;        // L < 0 or L > pt_stride * P
+};
+
+GA_HD int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+GA_HD RowGeom row_geometry(int32_t L, int32_t window, int64_t pt_stride, int32_t mode,
+                           int32_t splits, int32_t chunk_pages) {
+    RowGeom g;
+    g.bad_len = (L < 0) || ((int64_t)L > pt_stride * kPageSize);
+    if (g.bad_len) L = 0;
+    g.len = L;
+    g.lo = (window > 0 && L > window) ? L - window : 0;
+    g.first_page = g.lo / kPageSize;
+    g.npages = L > 0 ? (L - 1) / kPageSize - g.first_page + 1 : 0;
+    int32_t cp;
+    if (mode == kSplitCount)
+        cp = g.npages > 0 ? ceil_div(g.npages, splits > 0 ? splits : 1) : 1;
+    else if (mode == kSplitChunk)
+        cp = chunk_pages > 0 ? chunk_pages : 1;
+    else
+        cp = g.npages > 0 ? g.npages : 1;
+    g.cp = cp;
+    g.chunks = g.npages > 0 ? ceil_div(g.npages, cp) : 1;
+    return g;
+}
+
+// Logical page range [*p0, *p0 + *np) of chunk j of a row.
+GA_HD void chunk_pages_of(const RowGeom& g, int32_t j, int32_t* p0, int32_t* np) {
+    int32_t a = j * g.cp;
+    int32_t b = a + g.cp;
+    if (b > g.npages) b = g.npages;
+    if (a > b) a = b;
+    *p0 = g.first_page + a;
+    *np = b - a;
+}
+
+// Head groups of kHeadTile query heads per kv head.
+GA_HD int32_t head_groups(int32_t group) { return ceil_div(group, kHeadTile); }
+
+// Work unit u -> (row-chunk rc, kv head c, head group hg); units are ordered
+// row-chunk major so that neighbouring CTAs share page-table lines.
+GA_HD void unit_coords(int64_t u, int32_t Hkv, int32_t HG, int64_t* rc, int32_t* c,
+                       int32_t* hg) {
+    *hg = (int32_t)(u % HG);
+    *c = (int32_t)((u / HG) % Hkv);
+    *rc = u / ((int64_t)HG * Hkv);
+}
+
+// Checked page-id test: true iff page is a valid physical page.
+GA_HD bool page_ok(int32_t page, int64_t num_pages) {
+    return page >= 0 && (int64_t)page < num_pages;
+}
+
+// Index of the first element of page-head block (page, c) in a pool
+// [num_pages, Hkv, P, D]; only call with page_ok(page).
+GA_HD int64_t page_block_elem(int32_t page, int32_t c, int32_t Hkv, int32_t D) {
+    return ((int64_t)page * Hkv + c) * (int64_t)kPageSize * D;
+}
+
+// Row of the 2-D [num_pages * Hkv * P, D] view a bulk tensor copy addresses.
+GA_HD int32_t page_block_row(int32_t page, int32_t c, int32_t Hkv) {
+    return (page * Hkv + c) * kPageSize;
+}
+
+}  // namespace ga

@@ -1,0 +1,52 @@
+// ga_internal.h -- host-side declarations shared by the library's translation
+// units (argument checks, tensor-map encoding, kernel launchers).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ga.h"
+#include "ga_geometry.h"
+
+namespace ga {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Everything one decode launch needs, already validated on the host.
+struct DecodeArgs {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    int32_t kv_dtype;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* page_table;
+    int64_t pt_stride;
+    const int32_t* seq_lens;
+    int32_t batch, num_q_heads, num_kv_heads, head_dim, window;
+    int64_t num_pages;
+    float scale;
+    const ga_plan* plan;
+    void* workspace;
+    void* out;
+    int32_t* err_word;
+    cudaStream_t stream;
+};
+
+// Builds a 2-D tensor map over a pool viewed as [num_pages * Hkv * P, D]
+// elements with 128-byte swizzled boxes of [P rows, 128 bytes].
+int encode_pool_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_t rows,
+                    int32_t head_dim);
+
+int launch_decode(const DecodeArgs& a);
+
+int launch_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
+                   const int32_t* seq_lens, void* out, int32_t* err_word, int64_t pt_stride,
+                   cudaStream_t stream);
+
+// Sets the dynamic shared-memory limit of `func` once per device.
+int ensure_smem_attr(const void* func, int bytes, int slot);
+
+}  // namespace ga

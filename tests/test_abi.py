@@ -1,0 +1,140 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import re
+import os
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ga():
+    from paged_split_kv_gqa_gb300 import _build
+    _build.build()
+    from paged_split_kv_gqa_gb300 import ga as mod
+    return mod
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "ga.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ga_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = _declared()
+    for n in ("ga_kv_append", "ga_decode_local_hd256", "ga_decode_global_hd512",
+              "ga_splitkv_combine", "ga_plan_splits"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(ga):
+    lib = ctypes.CDLL(ga._build.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_python_binding_has_same_names(ga):
+    for name in ("ga_kv_append", "ga_decode_local_hd256", "ga_decode_global_hd512",
+                 "ga_splitkv_combine", "ga_plan_splits", "ga_check_error_word", "ga_version"):
+        assert callable(getattr(ga, name)), name
+
+
+def test_strerror_and_version(ga):
+    assert ga.strerror(0) == "GA_OK"
+    assert "WORKSPACE" in ga.strerror(3)
+    assert "unknown" in ga.strerror(99)
+    assert ga.ga_version() == 0x000100
+    assert ga.ga_check_error_word(0) == ga.GA_OK
+    assert ga.ga_check_error_word(ga.GA_DEVERR_PAGE_ID) == ga.GA_ERR_DEVICE_CHECK
+
+
+def test_plan_struct_layout_matches_header(ga):
+    # 12 int32 then 6 int64, no padding surprises
+    assert ctypes.sizeof(ga.ga_plan) == 12 * 4 + 6 * 8
+
+
+# ------------------------------------------------------------------ host-side rejection
+# These calls must return before touching CUDA, so they run without a GPU.
+
+def _plan(ga, **kw):
+    args = dict(num_q_heads=4, num_kv_heads=2, head_dim=256, window=32, num_sms=8)
+    args.update(kw)
+    return ga.ga_plan_splits([40, 33], **args)
+
+
+FAKE = 0x100000          # aligned fake device addresses: never dereferenced
+MIS = 0x100001
+
+
+def _decode_local(ga, plan, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, ks=None, vs=None, pt=FAKE, pts=3, sl=FAKE, B=2, Hq=4,
+             Hkv=2, W=32, P=16, npg=9, scale=0.0625, ws=None, wsb=0, out=FAKE)
+    a.update(over)
+    return ga.lib.ga_decode_local_hd256(
+        a["q"], a["k"], a["v"], a["dt"], a["ks"], a["vs"], a["pt"], a["pts"], a["sl"], a["B"],
+        a["Hq"], a["Hkv"], a["W"], a["P"], a["npg"], a["scale"], ctypes.byref(plan), a["ws"],
+        a["wsb"], a["out"], None, None)
+
+
+def test_decode_rejects_before_launch(ga):
+    plan = _plan(ga)
+    assert _decode_local(ga, plan, P=8) == ga.GA_ERR_UNSUPPORTED
+    assert _decode_local(ga, plan, Hq=3) == ga.GA_ERR_INVALID_ARG          # not a multiple
+    assert _decode_local(ga, plan, W=0) == ga.GA_ERR_INVALID_ARG
+    assert _decode_local(ga, plan, W=64) == ga.GA_ERR_INVALID_ARG          # plan mismatch
+    assert _decode_local(ga, plan, q=MIS) == ga.GA_ERR_INVALID_ARG         # misaligned
+    assert _decode_local(ga, plan, out=None) == ga.GA_ERR_INVALID_ARG
+    assert _decode_local(ga, plan, dt=7) == ga.GA_ERR_UNSUPPORTED
+    assert _decode_local(ga, plan, dt=1) == ga.GA_ERR_INVALID_ARG          # E4M3 needs scales
+    assert _decode_local(ga, plan, scale=float("nan")) == ga.GA_ERR_INVALID_ARG
+    assert _decode_local(ga, plan, npg=1 << 27) == ga.GA_ERR_UNSUPPORTED   # 2^31 rows
+    split = _plan(ga, requested_splits=2)
+    assert split.workspace_bytes > 0
+    assert _decode_local(ga, split) == ga.GA_ERR_INVALID_ARG               # no workspace
+    assert _decode_local(ga, split, ws=FAKE, wsb=split.workspace_bytes - 1) == \
+        ga.GA_ERR_WORKSPACE_TOO_SMALL
+    assert _decode_local(ga, plan, B=0) == ga.GA_ERR_INVALID_ARG           # plan says B=2
+
+
+def test_append_rejects_before_launch(ga):
+    f = ga.lib.ga_kv_append
+    ok = [FAKE, FAKE, FAKE, FAKE, 0, None, None, FAKE, 3, FAKE, 2, 2, 256, 16, 9, None, None]
+
+    def call(**idx):
+        a = list(ok)
+        for k, v in idx.items():
+            a[int(k[1:])] = v
+        return f(*a)
+
+    assert call(a13=8) == ga.GA_ERR_UNSUPPORTED        # page size
+    assert call(a12=128) == ga.GA_ERR_UNSUPPORTED      # head dim
+    assert call(a4=1) == ga.GA_ERR_INVALID_ARG         # E4M3 without scales
+    assert call(a2=MIS) == ga.GA_ERR_INVALID_ARG
+    assert call(a0=None) == ga.GA_ERR_INVALID_ARG
+    assert call(a10=0) == ga.GA_OK                     # empty batch: nothing to do
+
+
+def test_combine_rejects_before_launch(ga):
+    plan = _plan(ga, requested_splits=2)
+    f = ga.lib.ga_splitkv_combine
+    assert f(FAKE, FAKE, None, FAKE, 3, FAKE, None, None) == ga.GA_ERR_INVALID_ARG
+    assert f(None, FAKE, ctypes.byref(plan), FAKE, 3, FAKE, None, None) == ga.GA_ERR_INVALID_ARG
+    assert f(MIS, FAKE, ctypes.byref(plan), FAKE, 3, FAKE, None, None) == ga.GA_ERR_INVALID_ARG
+    none = _plan(ga)
+    assert f(None, None, ctypes.byref(none), None, 3, None, None, None) == ga.GA_OK
+
+
+def test_oracle_and_library_share_no_code():
+    """The oracle sources never include or import the CUDA path and vice versa."""
+    orc = open(os.path.join(ROOT, "oracle", "ga_oracle.c")).read() + \
+        open(os.path.join(ROOT, "oracle", "oracle.py")).read()
+    assert "ga_geometry" not in orc and "ga_device" not in orc and "import ga" not in orc
+    assert "from paged_split_kv_gqa_gb300 import ga" not in orc
+    for fn in os.listdir(os.path.join(ROOT, "paged_split_kv_gqa_gb300")):
+        if fn.endswith(".py"):
+            src = open(os.path.join(ROOT, "paged_split_kv_gqa_gb300", fn)).read()
+            assert "oracle" not in src.replace("the oracle", "").replace("oracle's", ""), fn

@@ -127,13 +127,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def build_step(device, seed):
+def build_step(device, seed, rows=0):
     import torch
     from paged_split_kv_gqa_gb300 import ga
     from paged_split_kv_gqa_gb300 import metrics as M
     from paged_split_kv_gqa_gb300 import workloads as W
 
     wl = W.config(WORKLOAD_INDEX, seed=seed)
+    if rows:
+        wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
+                        wl.page_size, wl.local, wl.global_)
     fams = {}
     for fam in wl.families():
         fi = W.make_family_inputs(wl, fam, device=device, seed=seed,
@@ -282,7 +285,7 @@ def run_ga(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
         pg = dist
-    wl, fams, err = build_step(device, args.seed + rank)
+    wl, fams, err = build_step(device, args.seed + rank, args.rows)
     loc, glo = fams["local"], fams["global"]
     stream = torch.cuda.current_stream()
 
@@ -392,9 +395,10 @@ def run_ga(args):
             "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {
-                "workload": "31B-shaped decode: B64, L~U[8192,32768] seed 0, 32 q heads; local "
-                            "16 kv hd256 window 1024 (bf16); global 4 kv hd512 (bf16); "
-                            "page 16, shuffled page pool",
+                "workload": ("31B-shaped decode: B64, L~U[8192,32768] seed 0, 32 q heads; local "
+                             "16 kv hd256 window 1024 (bf16); global 4 kv hd512 (bf16); "
+                             "page 16, shuffled page pool")
+                            + (f" -- PROFILING SUBSET: first {args.rows} rows" if args.rows else ""),
                 "global_batch": wl.batch * world, "step": "append+decode(+combine), both families",
                 "l2": "inputs larger than L2 (global KV pools ~10.4 GB, local ~1.1 GB); no flush",
                 "plans": {n: plan_desc(f["plan"]) for n, f in fams.items()},
@@ -430,6 +434,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="profiling only: the first N rows of the batch (not a bench line)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

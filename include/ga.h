@@ -237,6 +237,38 @@ int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const g
                        const int32_t* seq_lens, int64_t pt_stride, void* out,
                        int32_t* err_word, ga_stream_t stream);
 
+/*
+ * ga_decode_global_hd512_noalloc -- the same decode as ga_decode_global_hd512,
+ * for callers that cannot allocate device memory when they decode (the pages
+ * have no counterpart; this is a library convenience).  Examples: a plain-C
+ * serving loop without a caching allocator, where cudaMalloc would
+ * synchronise the whole device in the middle of a decode step, or a host that
+ * has given all free device memory to its fixed KV pools.
+ *
+ * The split-KV scratch comes from a device array built into the library,
+ * GA_NOALLOC_SCRATCH_BYTES per GPU, held by every GPU that loads the library
+ * until the process exits.  The caller still passes q, the pools, the page
+ * table, seq_lens and out exactly as for ga_decode_global_hd512.
+ *   - plan->workspace_bytes > GA_NOALLOC_SCRATCH_BYTES is rejected with
+ *     GA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls whose kernels overlap on the GPU
+ *     (other streams, unordered threads) race on it and give wrong results.
+ *     The array keeps the last call's contents; nothing in it needs to start
+ *     at zero.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define GA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int ga_decode_global_hd512_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                   int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                                   const int32_t* page_table, int64_t pt_stride,
+                                   const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t page_size, int64_t num_pages,
+                                   float scale, const ga_plan* plan, void* out,
+                                   int32_t* err_word, ga_stream_t stream);
+
 /* Name of a GA_* status code (static string). */
 const char* ga_strerror(int status);
 

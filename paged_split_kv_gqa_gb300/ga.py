@@ -75,8 +75,11 @@ def _load():
     lib.ga_decode_global_hd512.argtypes = [p, p, p, i32, p, p, p, i64, p, i32, i32, i32, i32,
                                            i64, f32, P, p, sz, p, p, p]
     lib.ga_splitkv_combine.argtypes = [p, p, P, p, i64, p, p, p]
+    lib.ga_decode_global_hd512_noalloc.argtypes = [p, p, p, i32, p, p, p, i64, p, i32, i32, i32,
+                                                   i32, i64, f32, P, p, p, p]
     for fn in ("ga_plan_splits", "ga_kv_append", "ga_decode_local_hd256",
-               "ga_decode_global_hd512", "ga_splitkv_combine", "ga_check_error_word"):
+               "ga_decode_global_hd512", "ga_splitkv_combine", "ga_check_error_word",
+               "ga_decode_global_hd512_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.ga_check_error_word.argtypes = [i32]
     lib.ga_strerror.argtypes = [ctypes.c_int]
@@ -201,6 +204,25 @@ def ga_decode_global_hd512(q, k_pool, v_pool, page_table, seq_lens, *, scale, pl
                    page_table, seq_lens, window=None, scale=scale, plan=plan,
                    workspace=workspace, out=out, k_scale=k_scale, v_scale=v_scale,
                    err_word=err_word, stream=stream)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def ga_decode_global_hd512_noalloc(q, k_pool, v_pool, page_table, seq_lens, *, scale, plan,
+                                   out, k_scale=None, v_scale=None, err_word=None, stream=None):
+    """Global decode whose split-KV scratch is the library's built-in device
+    array (no workspace argument): for callers that cannot allocate device
+    memory at decode time.  Calls that overlap on the GPU share that array and
+    race; plans needing more than NOALLOC_SCRATCH_BYTES are rejected."""
+    B, Hq, D = q.shape
+    st = _lib.ga_decode_global_hd512_noalloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _kv_dtype(k_pool), _ptr(k_scale), _ptr(v_scale),
+        _ptr(page_table), page_table.shape[1], _ptr(seq_lens), B, Hq, k_pool.shape[1],
+        k_pool.shape[2], k_pool.shape[0], float(scale), ctypes.byref(plan), _ptr(out),
+        _ptr(err_word), _stream(stream))
+    _check(st, "ga_decode_global_hd512_noalloc")
+    return out
 
 
 def ga_splitkv_combine(partial_o, partial_lse, plan, seq_lens, pt_stride, out, *, err_word=None,

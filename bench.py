@@ -428,7 +428,7 @@ def run_ga(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ga", choices=["ga", "reference"])
     ap.add_argument("--seed", type=int, default=0)

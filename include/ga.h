@@ -77,7 +77,8 @@ enum {
     GA_DEVERR_CAPACITY = 4,      /* seq_lens need more split chunks than the plan holds */
     GA_DEVERR_Q_RANGE = 8,       /* E4M3 path: |q| beyond the f16 range it is staged in */
     GA_DEVERR_TIMEOUT = 16,      /* a bounded wait for a bulk copy ran out */
-    GA_DEVERR_POSITION = 32      /* append: position / page_table[pos / P] invalid */
+    GA_DEVERR_POSITION = 32,     /* append: position / page_table[pos / P] invalid */
+    GA_DEVERR_SELF_CHECK = 64    /* GA_CHECKED builds: an access outside its buffer was skipped */
 };
 
 /* --------------------------------------------------------------- the plan */

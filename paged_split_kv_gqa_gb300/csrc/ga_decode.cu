@@ -14,9 +14,10 @@
 //
 // Inside a CTA (NCW + 1 warps):
 //   * the producer warp reads page ids from the page table, checks them,
-//     and issues 2-D bulk tensor copies (TMA, 128-byte swizzle) of the K and V
-//     page-head blocks into a ring of NS shared-memory stages, each completing
-//     on that stage's "full" mbarrier;
+//     and issues one 3-D bulk tensor copy (TMA, 128-byte swizzle) per K and per
+//     V page-head block into a ring of NS shared-memory stages, each completing
+//     on that stage's "full" mbarrier (one instruction per block: small 2-D
+//     boxes issued from one thread capped the stream well below HBM speed);
 //   * NCW consumer warps take the unit's pages round-robin.  Per 16-key page a
 //     warp computes S^T = K Q^T with m16n8k16 tensor-core MMAs (16 keys x 8
 //     query heads), applies the window mask, runs the online softmax on
@@ -34,10 +35,16 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "ga_device.cuh"
 #include "ga_internal.h"
 
 namespace ga {
+
+// Slack (log2 units) by which a score may exceed the running max before the
+// max is raised and the accumulators rescaled.
+constexpr float kMaxSlack = 8.0f;
 
 struct DecodeParams {
     const __nv_bfloat16* q;       // [B, Hq, D]
@@ -55,7 +62,17 @@ struct DecodeParams {
     int64_t rc_capacity;
     int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
     float scale_log2;             // softmax scale * log2(e)
+    int64_t out_elems;            // B * Hq * D
+    int64_t pool_rows;            // num_pages * Hkv * P
 };
+
+// GA_CHECKED builds test every shared- and global-memory access of the decode
+// kernel against its buffer, record GA_DEVERR_SELF_CHECK and skip the access.
+#ifdef GA_CHECKED
+#define GA_CHK(cond) (cond)
+#else
+#define GA_CHK(cond) true
+#endif
 
 template <int D_, int KV_, int NCW_, int NS_>
 struct DecodeCfg {
@@ -63,6 +80,7 @@ struct DecodeCfg {
     static constexpr int KV = KV_;                  // GA_KV_BF16 / GA_KV_E4M3
     static constexpr int NCW = NCW_;                // consumer warps
     static constexpr int NS = NS_;                  // ring stages (one page each)
+
     static constexpr int NCT = NCW * 32;            // consumer threads
     static constexpr int NTHREADS = NCT + 32;
     static constexpr int ESZ = KV == GA_KV_BF16 ? 2 : 1;
@@ -81,7 +99,7 @@ struct DecodeCfg {
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_QF = al(OFF_RING + NS * STAGE_BYTES);
     static constexpr int OFF_MERGE = al(OFF_QF + KSTEPS * 32 * 8);
-    static constexpr int OFF_ML = al(OFF_MERGE + NCW * kHeadTile * MSTRIDE * 4);
+    static constexpr int OFF_ML = al(OFF_MERGE + kHeadTile * MSTRIDE * 4);
     static constexpr int OFF_PREFIX = al(OFF_ML + 2 * NCW * kHeadTile * 4);
     static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
     static constexpr int OFF_BARS = al(OFF_FLAGS + NS * 4);
@@ -90,6 +108,13 @@ struct DecodeCfg {
     static_assert(D % 64 == 0 && NTILES >= 1, "head_dim");
     static_assert(OFF_BARS % 8 == 0 && OFF_QF % 16 == 0 && OFF_MERGE % 16 == 0, "alignment");
     static_assert(STAGE_BYTES % 1024 == 0, "swizzle-128B boxes need 1024-byte aligned stages");
+    // Every ring slot must always be consumed by the same warp: page n sits in
+    // slot n % NS and, within a unit, goes to warp n % NCW (up to the unit's
+    // offset).  A warp waiting on round r of a slot has then consumed round r-1
+    // of that slot itself, so the parity wait cannot be satisfied by an older
+    // phase of the same parity; unit boundaries are ordered by the merge
+    // barrier.  With NS % NCW != 0 a fast warp could see a stale completion.
+    static_assert(NS % NCW == 0, "ring stages must be a multiple of consumer warps");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -141,12 +166,13 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
         const UnitInfo x = unit_info(p, pre, u);
         const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride;
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
+        // page ids of this unit, 32 at a time (the next batch loads one batch ahead)
+        int32_t id_cur = (lane < x.np) ? __ldg(tbl + x.p0 + lane) : -1;
+        int32_t id_nxt = (32 + lane < x.np) ? __ldg(tbl + x.p0 + 32 + lane) : -1;
         for (int i0 = 0; i0 < x.np && !stop; i0 += 32) {
-            const int i = i0 + lane;
-            const int32_t id = (i < x.np) ? __ldg(tbl + x.p0 + i) : 0;
             const int cnt = min(32, x.np - i0);
             for (int k = 0; k < cnt; ++k) {
-                const int32_t pid = __shfl_sync(0xffffffffu, id, k);
+                const int32_t pid = __shfl_sync(0xffffffffu, id_cur, k);
                 if (lane == 0 && !stop) {
                     const uint32_t slot = seq % C::NS;
                     const uint32_t round = seq / C::NS;
@@ -156,31 +182,31 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                         report(p.err_word, kErrTimeout);
                         *abort_flag = 1;
                         stop = true;
-                    } else if (page_ok(pid, p.num_pages)) {
+                    } else if (page_ok(pid, p.num_pages) &&
+                               GA_CHK(page_block_row(pid, x.c, p.Hkv) >= 0 &&
+                                      page_block_row(pid, x.c, p.Hkv) + kPageSize <= p.pool_rows &&
+                                      slot < (uint32_t)C::NS)) {
                         flags[slot] = 0;
                         mbar_arrive_expect_tx(full, C::STAGE_BYTES);
                         const int32_t y = page_block_row(pid, x.c, p.Hkv);
                         const uint32_t dst = ring + slot * C::STAGE_BYTES;
-#pragma unroll
-                        for (int t = 0; t < C::NTILES; ++t)
-                            tma_load_2d(dst + t * C::TILE_BYTES, tmK, full, t * C::TILE_ELEMS, y,
-                                        policy);
-#pragma unroll
-                        for (int t = 0; t < C::NTILES; ++t)
-                            tma_load_2d(dst + C::BLOCK_BYTES + t * C::TILE_BYTES, tmV, full,
-                                        t * C::TILE_ELEMS, y, policy);
+                        // one 3-D box per block: the whole page-head block of K, then V
+                        tma_load_3d(dst, tmK, full, 0, y, 0, policy);
+                        tma_load_3d(dst + C::BLOCK_BYTES, tmV, full, 0, y, 0, policy);
                         issued_round[slot] = (int32_t)round;
                     } else {
                         flags[slot] = 1;
-                        report(p.err_word, kErrPageId);
+                        report(p.err_word, page_ok(pid, p.num_pages) ? kErrSelfCheck : kErrPageId);
                         mbar_arrive(full);
                     }
-                    if (log && i0 + k < p.touch_stride)
+                    if (log && i0 + k < p.touch_stride && GA_CHK(x.rc < p.rc_capacity))
                         p.touch_log[x.rc * p.touch_stride + i0 + k] = pid;
                 }
                 stop = __shfl_sync(0xffffffffu, stop, 0);
                 ++seq;
             }
+            id_cur = id_nxt;
+            id_nxt = (i0 + 64 + lane < x.np) ? __ldg(tbl + x.p0 + i0 + 64 + lane) : -1;
         }
     }
     // Never leave with a copy in flight into this CTA's shared memory.
@@ -208,7 +234,9 @@ __device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInf
     for (int e = tid; e < C::KSTEPS * 32; e += C::NCT) {
         const int ks = e >> 5, ln = e & 31, n = ln >> 2, t = ln & 3;
         uint2 v = make_uint2(0u, 0u);
-        if (n < x.nvalid) {
+        if (n < x.nvalid && !GA_CHK(((int64_t)x.b * p.Hq + x.h0 + n + 1) * C::D <= p.out_elems)) {
+            report(p.err_word, kErrSelfCheck);
+        } else if (n < x.nvalid) {
             const __nv_bfloat16* row = p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D;
             if (C::KV == GA_KV_BF16) {
                 v.x = __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t));
@@ -362,30 +390,43 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                     mk89 = (valid(2 * t + 8) ? 0x0000ffffu : 0u) |
                            (valid(2 * t + 9) ? 0xffff0000u : 0u);
                 }
-                // ---- online softmax (base 2) over this page, per head column
-                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+                // ---- online softmax (base 2) over this page, per head column.
+                // The running max m is only raised when some score exceeds it by
+                // more than kMaxSlack, so p <= 2^kMaxSlack between updates; the
+                // common page needs one warp vote instead of a shuffle reduction
+                // and an O rescale.  m stays uniform across the 8 lanes of a
+                // column because it only changes on the warp-uniform slow path.
+                {
+                    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+                    const bool grow = (mx0 > m0 + kMaxSlack) || (mx1 > m1 + kMaxSlack);
+                    if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                        for (int off = 4; off < 32; off <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                        }
+                        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                        const float al0 = (m0 == -CUDART_INF_F) ? 0.f : exp2f(m0 - mn0);
+                        const float al1 = (m1 == -CUDART_INF_F) ? 0.f : exp2f(m1 - mn1);
+                        m0 = mn0;
+                        m1 = mn1;
+                        l0 *= al0;
+                        l1 *= al1;
+#pragma unroll
+                        for (int mt = 0; mt < C::MTILES; ++mt) {
+                            o[mt][0] *= al0;
+                            o[mt][1] *= al1;
+                            o[mt][2] *= al0;
+                            o[mt][3] *= al1;
+                        }
+                    }
                 }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float ms0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
-                const float ms1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
-                const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
+                const float ms0 = (m0 == -CUDART_INF_F) ? 0.f : m0;
+                const float ms1 = (m1 == -CUDART_INF_F) ? 0.f : m1;
                 const float p0 = exp2f(s[0] - ms0), p1 = exp2f(s[1] - ms1);
                 const float p2 = exp2f(s[2] - ms0), p3 = exp2f(s[3] - ms1);
-                m0 = mn0;
-                m1 = mn1;
-                l0 = l0 * al0 + (p0 + p2);
-                l1 = l1 * al1 + (p1 + p3);
-#pragma unroll
-                for (int mt = 0; mt < C::MTILES; ++mt) {
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
-                }
+                l0 += p0 + p2;
+                l1 += p1 + p3;
                 // ---- P^T fragments: rows = keys, cols = heads -> transpose
                 uint32_t pb0, pb1;
                 if constexpr (C::KV == GA_KV_BF16) {
@@ -395,37 +436,48 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                     pb0 = movmatrix_t(pack_f16x2(p0, p1));
                     pb1 = movmatrix_t(pack_f16x2(p2, p3));
                 }
-                // ---- O^T += V^T P^T
-                if constexpr (C::KV == GA_KV_BF16) {
+                // ---- O^T += V^T P^T (V rows of unattended slots zeroed on partial pages)
+                auto pv = [&](auto masked) {
+                    constexpr bool kMask = decltype(masked)::value;
+                    if constexpr (C::KV == GA_KV_BF16) {
 #pragma unroll
-                    for (int mt = 0; mt < C::MTILES; ++mt) {
-                        uint32_t a[4];
-                        const uint32_t ch = (uint32_t)(((mt & 3) << 1) + vhi);
-                        ldsm_x4_t(vb + (mt >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), a);
-                        a[0] &= mk01;
-                        a[1] &= mk01;
-                        a[2] &= mk89;
-                        a[3] &= mk89;
-                        mma_bf16(o[mt], a, pb0, pb1);
-                    }
-                } else {
-#pragma unroll
-                    for (int mp = 0; mp < C::MTILES / 2; ++mp) {
-                        uint32_t r[4];
-                        const uint32_t ch = (uint32_t)(((mp & 3) << 1) + vhi);
-                        ldsm_x4_t(vb + (mp >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), r);
-                        uint32_t ev[4], od[4];
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            ev[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0020u));
-                            od[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0031u));
+                        for (int mt = 0; mt < C::MTILES; ++mt) {
+                            uint32_t a[4];
+                            const uint32_t ch = (uint32_t)(((mt & 3) << 1) + vhi);
+                            ldsm_x4_t(vb + (mt >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), a);
+                            if constexpr (kMask) {
+                                a[0] &= mk01;
+                                a[1] &= mk01;
+                                a[2] &= mk89;
+                                a[3] &= mk89;
+                            }
+                            mma_bf16(o[mt], a, pb0, pb1);
                         }
-                        ev[0] &= mk01; ev[1] &= mk01; ev[2] &= mk89; ev[3] &= mk89;
-                        od[0] &= mk01; od[1] &= mk01; od[2] &= mk89; od[3] &= mk89;
-                        mma_f16(o[2 * mp], ev, pb0, pb1);
-                        mma_f16(o[2 * mp + 1], od, pb0, pb1);
+                    } else {
+#pragma unroll
+                        for (int mp = 0; mp < C::MTILES / 2; ++mp) {
+                            uint32_t r[4];
+                            const uint32_t ch = (uint32_t)(((mp & 3) << 1) + vhi);
+                            ldsm_x4_t(vb + (mp >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), r);
+                            uint32_t ev[4], od[4];
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                ev[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0020u));
+                                od[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0031u));
+                            }
+                            if constexpr (kMask) {
+                                ev[0] &= mk01; ev[1] &= mk01; ev[2] &= mk89; ev[3] &= mk89;
+                                od[0] &= mk01; od[1] &= mk01; od[2] &= mk89; od[3] &= mk89;
+                            }
+                            mma_f16(o[2 * mp], ev, pb0, pb1);
+                            mma_f16(o[2 * mp + 1], od, pb0, pb1);
+                        }
                     }
-                }
+                };
+                if (partial)
+                    pv(std::true_type{});
+                else
+                    pv(std::false_type{});
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bars + 8 * (C::NS + slot));
@@ -459,37 +511,47 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             const float mown = (e == 0) ? m0 : m1;
             fac[e] = (Lt > 0.f) ? exp2f(mown - Ms) * (vfac / Lt) : 0.f;
         }
-        float* mw = merge + w * kHeadTile * C::MSTRIDE;
+        // warps add their scaled O into one buffer in turn (fixed order:
+        // deterministic, so results do not depend on timing)
+        for (int ww = 0; ww < C::NCW; ++ww) {
+            if (w == ww) {
+                float* r0 = merge + (2 * t) * C::MSTRIDE;
+                float* r1 = r0 + C::MSTRIDE;
+                const bool c0 = 2 * t < x.nvalid, c1 = 2 * t + 1 < x.nvalid;
+                if (!GA_CHK(2 * t + 1 < kHeadTile)) report(p.err_word, kErrSelfCheck);
 #pragma unroll
-        for (int mt = 0; mt < C::MTILES; ++mt) {
-            int d0, d1;
-            if constexpr (C::KV == GA_KV_BF16) {
-                d0 = 16 * mt + gid;
-                d1 = d0 + 8;
-            } else {   // E4M3 m-tile pairs hold even / odd dims of 32-dim groups
-                d0 = 32 * (mt >> 1) + 2 * gid + (mt & 1);
-                d1 = d0 + 16;
+                for (int mt = 0; mt < C::MTILES; ++mt) {
+                    int d0, d1;
+                    if constexpr (C::KV == GA_KV_BF16) {
+                        d0 = 16 * mt + gid;
+                        d1 = d0 + 8;
+                    } else {   // E4M3 m-tile pairs hold even / odd dims of 32-dim groups
+                        d0 = 32 * (mt >> 1) + 2 * gid + (mt & 1);
+                        d1 = d0 + 16;
+                    }
+                    if (ww == 0) {
+                        if (c0) { r0[d0] = o[mt][0] * fac[0]; r0[d1] = o[mt][2] * fac[0]; }
+                        if (c1) { r1[d0] = o[mt][1] * fac[1]; r1[d1] = o[mt][3] * fac[1]; }
+                    } else {
+                        if (c0) { r0[d0] += o[mt][0] * fac[0]; r0[d1] += o[mt][2] * fac[0]; }
+                        if (c1) { r1[d0] += o[mt][1] * fac[1]; r1[d1] += o[mt][3] * fac[1]; }
+                    }
+                }
             }
-            mw[(2 * t) * C::MSTRIDE + d0] = o[mt][0] * fac[0];
-            mw[(2 * t + 1) * C::MSTRIDE + d0] = o[mt][1] * fac[1];
-            mw[(2 * t) * C::MSTRIDE + d1] = o[mt][2] * fac[0];
-            mw[(2 * t + 1) * C::MSTRIDE + d1] = o[mt][3] * fac[1];
+            named_barrier(1, C::NCT);
         }
-        named_barrier(1, C::NCT);
         constexpr int D8 = C::D / 8;
         for (int e = tid; e < x.nvalid * D8; e += C::NCT) {
             const int n = e / D8, d = (e % D8) * 8;
-            float acc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-            for (int ww = 0; ww < C::NCW; ++ww) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(merge + (ww * kHeadTile + n) * C::MSTRIDE + d);
-                const float4 a = src[0], b = src[1];
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-            }
+            const float4* src = reinterpret_cast<const float4*>(merge + n * C::MSTRIDE + d);
+            const float4 a = src[0], b = src[1];
+            const float acc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             const int h = x.h0 + n;
+            if (!GA_CHK(((int64_t)x.b * p.Hq + h) * C::D + d + 8 <= p.out_elems &&
+                        (single || (x.rc < p.rc_capacity && p.partial_o != nullptr)))) {
+                report(p.err_word, kErrSelfCheck);
+                continue;
+            }
             if (single) {
                 uint4 v;
                 v.x = pack_bf16x2(acc[0], acc[1]);
@@ -504,7 +566,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                 dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
             }
         }
-        if (!single && tid < x.nvalid) {
+        if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity)) {
             float M = -CUDART_INF_F;
             for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, mlw[ww * kHeadTile + tid]);
             const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
@@ -632,6 +694,8 @@ static int run(const DecodeArgs& a, int slot) {
     p.chunk_pages = pl.chunk_pages;
     p.touch_stride = pl.touch_stride;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.pool_rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
+    p.out_elems = (int64_t)a.batch * a.num_q_heads * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
     decode_kernel<C><<<grid, C::NTHREADS, C::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
@@ -641,11 +705,28 @@ static int run(const DecodeArgs& a, int slot) {
     return GA_OK;
 }
 
-// Tuned shapes: consumer warps x ring stages per (head_dim, KV type).
-using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, 4, 8>;
-using CfgLocalE4m3 = DecodeCfg<256, GA_KV_E4M3, 4, 12>;
-using CfgGlobalBf16 = DecodeCfg<512, GA_KV_BF16, 2, 5>;
-using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, 2, 8>;
+// Tuned shapes per (head_dim, KV type): consumer warps, ring stages (a
+// multiple of the warps).  The macros let a build sweep them.
+#ifndef GA_LB_NCW
+#define GA_LB_NCW 2
+#define GA_LB_NS 12
+#endif
+#ifndef GA_LE_NCW
+#define GA_LE_NCW 4
+#define GA_LE_NS 24
+#endif
+#ifndef GA_GB_NCW
+#define GA_GB_NCW 2
+#define GA_GB_NS 6
+#endif
+#ifndef GA_GE_NCW
+#define GA_GE_NCW 2
+#define GA_GE_NS 12
+#endif
+using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, GA_LB_NCW, GA_LB_NS>;
+using CfgLocalE4m3 = DecodeCfg<256, GA_KV_E4M3, GA_LE_NCW, GA_LE_NS>;
+using CfgGlobalBf16 = DecodeCfg<512, GA_KV_BF16, GA_GB_NCW, GA_GB_NS>;
+using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, GA_GE_NS>;
 
 int launch_decode(const DecodeArgs& a) {
     if (a.head_dim == 256)

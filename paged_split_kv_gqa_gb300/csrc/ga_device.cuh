@@ -21,7 +21,7 @@ constexpr long long kWaitBudgetCycles = 4000000000LL;
 // Device error bits (mirror GA_DEVERR_* of the public header).
 enum : int32_t {
     kErrPageId = 1, kErrSeqLen = 2, kErrCapacity = 4, kErrQRange = 8, kErrTimeout = 16,
-    kErrPosition = 32
+    kErrPosition = 32, kErrSelfCheck = 64
 };
 
 __device__ __forceinline__ void report(int32_t* err_word, int32_t bits) {
@@ -90,6 +90,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// 3-D tiled bulk tensor copy global -> shared, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
 }
 

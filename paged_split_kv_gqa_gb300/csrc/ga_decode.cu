@@ -712,7 +712,7 @@ static int run(const DecodeArgs& a, int slot) {
 #define GA_LB_NS 12
 #endif
 #ifndef GA_LE_NCW
-#define GA_LE_NCW 4
+#define GA_LE_NCW 3
 #define GA_LE_NS 24
 #endif
 #ifndef GA_GB_NCW
@@ -720,7 +720,7 @@ static int run(const DecodeArgs& a, int slot) {
 #define GA_GB_NS 6
 #endif
 #ifndef GA_GE_NCW
-#define GA_GE_NCW 2
+#define GA_GE_NCW 4
 #define GA_GE_NS 12
 #endif
 using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, GA_LB_NCW, GA_LB_NS>;

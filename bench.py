@@ -1,16 +1,17 @@
 """Decode-attention benchmark: one step = the whole hot path over one batch.
 
-A step on the 31B-shaped decode batch (B 64, L ~ U[8192, 32768], 32 query
-heads; local 16 KV heads hd256 window 1024; global 4 KV heads hd512) is:
-KV append (local) -> local decode (+ split-KV combine if planned) -> KV
-append (global) -> global decode -> split-KV combine.  All of it runs in
-libga's CUDA kernels through the C ABI.
+A step on the 31B-shaped decode batch (the default workload: B 64, L ~
+U[8192, 32768], 32 query heads; local 16 KV heads hd256 window 1024; global 4
+KV heads hd512) is: KV append (local) -> local decode (+ split-KV combine if
+planned) -> KV append (global) -> global decode -> split-KV combine.  All of
+it runs in libga's CUDA kernels through the C ABI.  --workload ragged runs
+the 50-local (fp8) + 10-global layer sweep instead.
 
 Printed: one JSON line with the metric (algorithmic HBM GB/s of the step),
 the roofline of the dominant kernel (global decode), the end-to-end figure
 through host buffers, the CPU oracle baseline and the SM clocks seen.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload W]
 """
 from __future__ import annotations
 
@@ -32,7 +33,6 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("decode-attention HBM GB/s and % of GB300 peak; attended KV-tokens/sec per layer")
 NOMINAL_HBM_GBS = 8000.0
-WORKLOAD_INDEX = 3          # the 31B-shaped decode batch
 
 
 def measured_peak_gbs():
@@ -127,43 +127,64 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def build_step(device, seed, rows=0):
+WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
+
+
+def make_layer(device, wl, fam, seed, layer):
     import torch
     from paged_split_kv_gqa_gb300 import ga
     from paged_split_kv_gqa_gb300 import metrics as M
     from paged_split_kv_gqa_gb300 import workloads as W
 
-    wl = W.config(WORKLOAD_INDEX, seed=seed)
+    fi = W.make_family_inputs(wl, fam, device=device, seed=seed, layer=layer,
+                              release_old=(fam.window > 0))
+    plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                             num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
+                             window=fam.window, flags=ga.GA_PLAN_EXTERNAL_COMBINE)
+    ws = ga.workspace_for(plan, device)
+    po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
+    esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
+    return dict(
+        fam=fam, fi=fi, plan=plan, ws=ws, po=po, plse=plse,
+        out=torch.empty_like(fi.q), pos=(fi.seq_lens - 1).contiguous(),
+        scale=1.0 / math.sqrt(fam.head_dim),
+        bytes=M.decode_bytes(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                             num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
+                             window=fam.window, page_size=wl.page_size, kv_bytes_per_elem=esz),
+        append_bytes=M.append_bytes(wl.batch, num_kv_heads=fam.num_kv_heads,
+                                    head_dim=fam.head_dim, kv_bytes_per_elem=esz),
+        keys=int(M.attended_keys(wl.seq_lens, fam.window).sum()))
+
+
+def build_step(device, seed, workload="31b", rows=0, pools=4):
+    """The layers one step launches, in order.  31b / 12b / long: one local and
+    one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
+    layers of a family rotating over `pools` distinct KV pools (each > L2)."""
+    import torch
+    from paged_split_kv_gqa_gb300 import workloads as W
+
+    wl = W.config(WORKLOADS[workload], seed=seed)
     if rows:
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
-                        wl.page_size, wl.local, wl.global_)
-    fams = {}
-    for fam in wl.families():
-        fi = W.make_family_inputs(wl, fam, device=device, seed=seed,
-                                  release_old=(fam.window > 0))
-        plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
-                                 num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
-                                 window=fam.window, flags=ga.GA_PLAN_EXTERNAL_COMBINE)
-        ws = ga.workspace_for(plan, device)
-        po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
-        esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
-        fams[fam.name] = dict(
-            fam=fam, fi=fi, plan=plan, ws=ws, po=po, plse=plse,
-            out=torch.empty_like(fi.q), pos=(fi.seq_lens - 1).contiguous(),
-            scale=1.0 / math.sqrt(fam.head_dim),
-            bytes=M.decode_bytes(wl.seq_lens, num_q_heads=fam.num_q_heads,
-                                 num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
-                                 window=fam.window, page_size=wl.page_size,
-                                 kv_bytes_per_elem=esz),
-            append_bytes=M.append_bytes(wl.batch, num_kv_heads=fam.num_kv_heads,
-                                        head_dim=fam.head_dim, kv_bytes_per_elem=esz),
-            keys=int(M.attended_keys(wl.seq_lens, fam.window).sum()))
+                        wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
+    npool = pools if workload == "ragged" else 1
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i) for i in range(npool)]
+            for fam in wl.families()}
+    if workload == "ragged":
+        schedule, nl, ng = [], 0, 0
+        per = wl.local_layers // wl.global_layers           # 5 local, then 1 global
+        for _ in range(wl.global_layers):
+            for _ in range(per):
+                schedule.append(sets["local"][nl % npool]); nl += 1
+            schedule.append(sets["global"][ng % npool]); ng += 1
+    else:
+        schedule = [sets["local"][0], sets["global"][0]]
     err = torch.zeros(1, dtype=torch.int32, device=device)
-    return wl, fams, err
+    return wl, schedule, sets, err
 
 
-def launch_family(ga, f, err, events=None):
-    """append + decode (+ combine) of one family on the current stream.
+def launch_layer(ga, f, err, events=None):
+    """append + decode (+ combine) of one layer on the current stream.
     Returns the number of kernels launched."""
     fi, fam, plan = f["fi"], f["fam"], f["plan"]
     ga.ga_kv_append(fi.k_new, fi.v_new, fi.k_pool, fi.v_pool, fi.page_table, f["pos"],
@@ -189,55 +210,79 @@ def launch_family(ga, f, err, events=None):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(fams_cpu, rows, nthreads=0):
-    """Run the oracle on the sampled rows of both families; returns seconds."""
+def oracle_sample(fams_cpu):
+    """Run the oracle on every row of the sampled inputs; returns seconds."""
     from oracle import oracle as O
     t0 = time.perf_counter()
     for f in fams_cpu:
         O.decode(f.q, f.k_pool, f.v_pool, f.page_table, f.seq_lens,
                  num_kv_heads=f.family.num_kv_heads, window=f.family.window,
                  scale=1.0 / math.sqrt(f.family.head_dim), kv_dtype=f.family.kv_dtype,
-                 k_scale=f.k_scale, v_scale=f.v_scale, rows=rows, nthreads=nthreads)
+                 k_scale=f.k_scale, v_scale=f.v_scale)
     return time.perf_counter() - t0
 
 
-def cpu_sample_inputs(seed, nrows):
-    """CPU copies of a bounded sample of the same workload: the first nrows
-    rows of the batch (same lengths), drawn on the host."""
+def cpu_sample_inputs(seed, nrows, workload):
+    """CPU copies of a bounded sample of the same workload: its first nrows
+    rows (same lengths), one layer per family, drawn on the host."""
     from paged_split_kv_gqa_gb300 import metrics as M
     from paged_split_kv_gqa_gb300 import workloads as W
-    wl = W.config(WORKLOAD_INDEX, seed=seed)
+    wl = W.config(WORKLOADS[workload], seed=seed)
     sub = W.Workload(wl.name, wl.seq_lens[:nrows].copy(), wl.page_size, wl.local, wl.global_)
     fams = [W.make_family_inputs(sub, fam, device="cpu", seed=seed,
                                  release_old=(fam.window > 0)) for fam in sub.families()]
     nbytes = sum(M.decode_bytes(sub.seq_lens, num_q_heads=f.num_q_heads,
                                 num_kv_heads=f.num_kv_heads, head_dim=f.head_dim,
                                 window=f.window, page_size=sub.page_size,
-                                kv_bytes_per_elem=2) for f in sub.families())
-    keys = {f.name: int(M.attended_keys(sub.seq_lens, f.window).sum()) for f in sub.families()}
-    return fams, nbytes, keys
+                                kv_bytes_per_elem=1 if f.kv_dtype == W.KV_E4M3 else 2)
+                 for f in sub.families())
+    return fams, nbytes
 
 
-def cpu_cores():
-    try:
-        return len(os.sched_getaffinity(0))
-    except Exception:
-        return os.cpu_count() or 1
+def gather_rows_to_host(layer, nrows):
+    """Host copies of the first nrows rows of a device layer: only the pages
+    those rows reference, renumbered, plus their q, table and lengths."""
+    import numpy as np
+    import torch
+    from paged_split_kv_gqa_gb300 import workloads as W
+    fi = layer["fi"]
+    table = fi.page_table[:nrows].cpu().numpy()
+    used = np.unique(table[table >= 0])
+    remap = np.full(max(int(fi.num_pages), 1), -1, dtype=np.int64)
+    remap[used] = np.arange(len(used))
+    sub = np.where(table >= 0, remap[np.maximum(table, 0)], -1).astype(np.int32)
+    idx = torch.as_tensor(used, device=fi.k_pool.device)
+    return W.FamilyInputs(fi.family, fi.q[:nrows].cpu(), fi.k_pool.index_select(0, idx).cpu(),
+                          fi.v_pool.index_select(0, idx).cpu(),
+                          None if fi.k_scale is None else fi.k_scale.cpu(),
+                          None if fi.v_scale is None else fi.v_scale.cpu(),
+                          torch.from_numpy(sub), fi.seq_lens[:nrows].cpu(), None, None,
+                          len(used))
 
 
-def run_cpu_baseline(seed, target_s=12.0):
+def run_cpu_baseline(sets, batch, target_s=10.0):
+    """The oracle as it stands on the host cores, on the first rows of the
+    bench's own inputs (one layer per family), the sample grown toward about
+    target_s / 2 .. target_s of work or the whole batch."""
     from oracle import oracle as O
-    nrows = 2
-    fams, nbytes, _ = cpu_sample_inputs(seed, nrows)
-    t = oracle_sample(fams, None)
-    # grow the sample toward ~target_s of CPU work (bounded)
-    while t < target_s / 4 and nrows < 16:
-        nrows = min(16, nrows * 2)
-        fams, nbytes, _ = cpu_sample_inputs(seed, nrows)
-        t = oracle_sample(fams, None)
+    from paged_split_kv_gqa_gb300 import metrics as M
+    from paged_split_kv_gqa_gb300 import workloads as W
+    nrows = min(batch, 4)
+    while True:
+        fams = [gather_rows_to_host(layers[0], nrows) for layers in sets.values()]
+        t = oracle_sample(fams)
+        if t >= target_s / 2 or nrows >= batch:
+            break
+        nrows = min(batch, max(nrows + 1, int(nrows * min(8.0, 0.75 * target_s / max(t, 1e-3)))))
+    lens = fams[0].seq_lens.numpy()
+    nbytes = sum(M.decode_bytes(lens, num_q_heads=f.family.num_q_heads,
+                                num_kv_heads=f.family.num_kv_heads, head_dim=f.family.head_dim,
+                                window=f.family.window, page_size=16,
+                                kv_bytes_per_elem=1 if f.family.kv_dtype == W.KV_E4M3 else 2)
+                 for f in fams)
     return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": O.max_threads(), "kind": "oracle",
-            "sample": f"first {nrows} rows of the 31B-shaped batch, both families, fp64 C "
-                      f"oracle with OpenMP, {t:.2f} s"}
+            "sample": f"first {nrows} of {batch} rows of the bench batch, one layer per family, "
+                      f"fp64 C oracle with OpenMP on all cores, {t:.2f} s"}
 
 
 # ------------------------------------------------------------------ arms
@@ -254,23 +299,37 @@ def run_reference(args):
         return
     from oracle import oracle as O
     nrows = 2
-    fams, nbytes, keys = cpu_sample_inputs(args.seed, nrows)
+    fams, nbytes = cpu_sample_inputs(args.seed, nrows, args.workload)
     for _ in range(args.warmup):
-        oracle_sample(fams, None)
-    times = [oracle_sample(fams, None) for _ in range(args.steps)]
+        oracle_sample(fams)
+    times = [oracle_sample(fams) for _ in range(args.steps)]
     t = sum(times) / len(times)
     value = nbytes / t / 1e9
     cb = {"value": value, "unit": "GB/s", "cores": O.max_threads(), "kind": "oracle",
-          "sample": f"first {nrows} rows of the 31B-shaped batch per step, both families"}
+          "sample": f"first {nrows} rows of the {args.workload} batch per step, one layer per "
+                    f"family"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "31B-shaped decode, sampled rows", "batch": nrows},
+            "config": {"workload": f"{args.workload} decode, sampled rows", "batch": nrows},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+WORKLOAD_TEXT = {
+    "31b": "31B-shaped decode: B64, L~U[8192,32768] seed 0, 32 q heads; local 16 kv hd256 window "
+           "1024 (bf16); global 4 kv hd512 (bf16); page 16, shuffled page pool",
+    "12b": "12B-shaped decode: B32, L~U[512,4096] (rows 0-2 = 1023/1024/1025), 16 q heads; local "
+           "8 kv hd256 window 1024; global 2 kv hd512; bf16; page 16",
+    "long": "long-context 31B-shaped decode: B4, L=131072, 32 q heads; local 16 kv hd256 window "
+            "1024; global 4 kv hd512; bf16; page 16",
+    "ragged": "ragged 31B-shaped decode: B256, lognormal L (median 2048, sigma 1, clip "
+              "[1,65536]); 50 local (fp8-e4m3, per-head scales) + 10 global (bf16) layers in 5:1 "
+              "order; page 16",
+}
 
 
 def run_ga(args):
@@ -285,13 +344,13 @@ def run_ga(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
         pg = dist
-    wl, fams, err = build_step(device, args.seed + rank, args.rows)
-    loc, glo = fams["local"], fams["global"]
-    stream = torch.cuda.current_stream()
+    wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
+                                         args.pools)
 
-    def step(ev_local=None, ev_global=None):
-        n = launch_family(ga, loc, err, ev_local)
-        n += launch_family(ga, glo, err, ev_global)
+    def step(evs=None):
+        n = 0
+        for i, layer in enumerate(schedule):
+            n += launch_layer(ga, layer, err, None if evs is None else evs[i])
         return n
 
     for _ in range(max(3, args.warmup)):
@@ -302,7 +361,7 @@ def run_ga(args):
 
     # ---- device-timed region: K steps, events around each decode launch
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)] for _ in range(2)]
+           for _ in schedule] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     if pg:
@@ -311,7 +370,7 @@ def run_ga(args):
     with ClockSampler(local_rank) as clocks:
         start.record()
         for k in range(args.steps):
-            launches += step(ev[0][k], ev[1][k])
+            launches += step(ev[k])
         end.record()
         torch.cuda.synchronize()
     elapsed = start.elapsed_time(end) / 1e3
@@ -321,43 +380,62 @@ def run_ga(args):
         elapsed = float(t.item())
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
-    local_ms = [a.elapsed_time(b) for a, b in ev[0]]
-    global_ms = [a.elapsed_time(b) for a, b in ev[1]]
 
-    step_bytes = sum(f["bytes"] + f["append_bytes"] for f in fams.values())
+    # per family: decode-kernel time and algorithmic bytes over all its launches
+    fam_ms, fam_bytes, fam_keys, fam_n = {}, {}, {}, {}
+    for k in range(args.steps):
+        for i, layer in enumerate(schedule):
+            name = layer["fam"].name
+            a, b = ev[k][i]
+            fam_ms[name] = fam_ms.get(name, 0.0) + a.elapsed_time(b)
+            fam_bytes[name] = fam_bytes.get(name, 0) + layer["bytes"]
+            fam_keys[name] = fam_keys.get(name, 0) + layer["keys"]
+            fam_n[name] = fam_n.get(name, 0) + 1
+    families = {}
+    for name in fam_ms:
+        t = fam_ms[name] / 1e3
+        families[name] = {
+            "launches_per_step": fam_n[name] // args.steps,
+            "decode_ms_per_launch": fam_ms[name] / fam_n[name],
+            "decode_gbs": fam_bytes[name] / t / 1e9,
+            "algorithmic_bytes_per_launch": fam_bytes[name] // fam_n[name],
+            "attended_kv_tokens_per_s_per_layer": fam_keys[name] / t,
+            "kv_dtype": "e4m3" if sets[name][0]["fam"].kv_dtype else "bf16"}
+    dominant = max(fam_ms, key=fam_ms.get)
+    step_bytes = sum(layer["bytes"] + layer["append_bytes"] for layer in schedule)
     value = step_bytes * args.steps * world / elapsed / 1e9
     peak, peak_kind = measured_peak_gbs()
-    g_avg = sum(global_ms) / len(global_ms) / 1e3
-    l_avg = sum(local_ms) / len(local_ms) / 1e3
-    g_ach = glo["bytes"] / g_avg / 1e9
-    l_ach = loc["bytes"] / l_avg / 1e9
-    traffic = committed_traffic("decode_global_hd512")
+    dom_ach = families[dominant]["decode_gbs"]
+    kname = "decode_global_hd512" if dominant == "global" else "decode_local_hd256"
+    traffic = committed_traffic(kname) if args.workload == "31b" and not args.rows else None
 
     # ---- end to end through host buffers: H2D inputs, the C-ABI calls, D2H outputs
     e2e = None
     if not args.no_e2e:
         host = {}
-        for name, f in fams.items():
-            fi = f["fi"]
-            host[name] = {k: getattr(fi, k).cpu().pin_memory() for k in ("q", "k_new", "v_new",
-                                                                         "seq_lens")}
-            host[name]["pos"] = f["pos"].cpu().pin_memory()
-            host[name]["out"] = torch.empty_like(f["out"], device="cpu").pin_memory()
-        h2d = sum(t.numel() * t.element_size() for h in host.values()
-                  for k, t in h.items() if k != "out")
-        d2h = sum(h["out"].numel() * h["out"].element_size() for h in host.values())
+        uniq = [layer for fam_layers in sets.values() for layer in fam_layers]
+        for layer in uniq:
+            fi = layer["fi"]
+            h = {k: getattr(fi, k).cpu().pin_memory() for k in ("q", "k_new", "v_new",
+                                                                  "seq_lens")}
+            h["pos"] = layer["pos"].cpu().pin_memory()
+            h["out"] = torch.empty_like(layer["out"], device="cpu").pin_memory()
+            host[id(layer)] = h
+        h2d = sum(t.numel() * t.element_size() for layer in schedule
+                  for k, t in host[id(layer)].items() if k != "out")
+        d2h = sum(host[id(layer)]["out"].numel() * 2 for layer in schedule)
 
         def e2e_step():
             n = 0
-            for name, f in fams.items():
-                fi, h = f["fi"], host[name]
+            for layer in schedule:
+                fi, h = layer["fi"], host[id(layer)]
                 fi.q.copy_(h["q"], non_blocking=True)
                 fi.k_new.copy_(h["k_new"], non_blocking=True)
                 fi.v_new.copy_(h["v_new"], non_blocking=True)
                 fi.seq_lens.copy_(h["seq_lens"], non_blocking=True)
-                f["pos"].copy_(h["pos"], non_blocking=True)
-                n += launch_family(ga, f, err)
-                h["out"].copy_(f["out"], non_blocking=True)
+                layer["pos"].copy_(h["pos"], non_blocking=True)
+                n += launch_layer(ga, layer, err)
+                h["out"].copy_(layer["out"], non_blocking=True)
             return n
 
         for _ in range(3):
@@ -382,38 +460,36 @@ def run_ga(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = run_cpu_baseline(args.seed)
+        cpu = run_cpu_baseline(sets, wl.batch)
 
     if rank == 0:
         def plan_desc(p):
             return {"mode": ["none", "count", "chunk"][p.mode], "chunk_pages": p.chunk_pages,
                     "units": p.units, "grid": p.grid}
 
+        text = WORKLOAD_TEXT[args.workload]
+        if args.rows:
+            text += f" -- PROFILING SUBSET: first {args.rows} rows"
+        if args.workload == "ragged":
+            text += f"; {args.pools} distinct pools per family rotated over the layers"
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {
-                "workload": ("31B-shaped decode: B64, L~U[8192,32768] seed 0, 32 q heads; local "
-                             "16 kv hd256 window 1024 (bf16); global 4 kv hd512 (bf16); "
-                             "page 16, shuffled page pool")
-                            + (f" -- PROFILING SUBSET: first {args.rows} rows" if args.rows else ""),
-                "global_batch": wl.batch * world, "step": "append+decode(+combine), both families",
-                "l2": "inputs larger than L2 (global KV pools ~10.4 GB, local ~1.1 GB); no flush",
-                "plans": {n: plan_desc(f["plan"]) for n, f in fams.items()},
+                "workload": text,
+                "global_batch": wl.batch * world,
+                "step": f"{len(schedule)} layers, each append+decode(+combine)",
+                "l2": "inputs larger than L2 (KV pools of each layer > 129 MB); no flush",
+                "plans": {n: plan_desc(layers[0]["plan"]) for n, layers in sets.items()},
             },
             "pct_of_peak": {"measured": value / peak, "nominal_8TBs": value / NOMINAL_HBM_GBS},
-            "families": {
-                n: {"decode_ms": (g_avg if n == "global" else l_avg) * 1e3,
-                    "decode_gbs": g_ach if n == "global" else l_ach,
-                    "attended_kv_tokens_per_s_per_layer":
-                        f["keys"] / (g_avg if n == "global" else l_avg),
-                    "algorithmic_bytes": f["bytes"]}
-                for n, f in fams.items()},
-            "roofline": {"kernel": "decode_global_hd512 (decode kernel, combine excluded)",
-                         "bound": "hbm", "achieved": g_ach, "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s", "frac": g_ach / peak,
+            "families": families,
+            "roofline": {"kernel": f"{kname} (decode kernel, combine excluded)",
+                         "bound": "hbm", "achieved": dom_ach, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_ach / peak,
+                         "frac_of_nominal_8TBs": dom_ach / NOMINAL_HBM_GBS,
                          "traffic": traffic},
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -434,6 +510,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--workload", default="31b", choices=sorted(WORKLOADS))
+    ap.add_argument("--pools", type=int, default=4,
+                    help="ragged workload: distinct KV pools per family rotated over layers")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: the first N rows of the batch (not a bench line)")
     args = ap.parse_args()

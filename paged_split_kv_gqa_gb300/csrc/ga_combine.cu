@@ -51,23 +51,22 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     float M = -CUDART_INF_F;
     for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(lse + (int64_t)s * p.Hq));
     const int d = threadIdx.x * 4;
+    const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    if (M != -CUDART_INF_F) {
-        for (int s = 0; s < S; ++s) {
-            const float ls = __ldg(lse + (int64_t)s * p.Hq);
-            if (ls == -CUDART_INF_F) continue;
-            const float wgt = expf(ls - M);
-            den += wgt;
-            const float4 v = __ldg(reinterpret_cast<const float4*>(
-                p.po + ((rc0 + s) * p.Hq + h) * (int64_t)p.D + d));
-            acc.x += wgt * v.x;
-            acc.y += wgt * v.y;
-            acc.z += wgt * v.z;
-            acc.w += wgt * v.w;
-        }
+    for (int s = 0; s < S; ++s) {
+        const float ls = __ldg(lse + (int64_t)s * p.Hq);
+        if (ls == -CUDART_INF_F) continue;                 // empty chunk (NaN is kept)
+        const float wgt = expf(ls - Ms);
+        den += wgt;
+        const float4 v = __ldg(reinterpret_cast<const float4*>(
+            p.po + ((rc0 + s) * p.Hq + h) * (int64_t)p.D + d));
+        acc.x += wgt * v.x;
+        acc.y += wgt * v.y;
+        acc.z += wgt * v.z;
+        acc.w += wgt * v.w;
     }
-    const float inv = den > 0.f ? 1.0f / den : 0.f;
+    const float inv = (den == 0.f) ? 0.f : 1.0f / den;
     uint2 o;
     o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
     o.y = pack_bf16x2(acc.z * inv, acc.w * inv);

@@ -509,7 +509,9 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                 Lt += mlw[C::NCW * kHeadTile + ww * kHeadTile + col] *
                       exp2f(mlw[ww * kHeadTile + col] - Ms);
             const float mown = (e == 0) ? m0 : m1;
-            fac[e] = (Lt > 0.f) ? exp2f(mown - Ms) * (vfac / Lt) : 0.f;
+            // only an exactly empty sum means "no keys"; NaN in attended K / V
+            // propagates to the output as in the definition
+            fac[e] = (Lt == 0.f) ? 0.f : exp2f(mown - Ms) * (vfac / Lt);
         }
         // warps add their scaled O into one buffer in turn (fixed order:
         // deterministic, so results do not depend on timing)
@@ -576,7 +578,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                       exp2f(mlw[ww * kHeadTile + tid] - Ms);
             // natural-log LSE of the chunk's scaled scores
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
-                (Lt > 0.f) ? (Ms + log2f(Lt)) * CUDART_LN2_F : -CUDART_INF_F;
+                (Lt == 0.f) ? -CUDART_INF_F : (Ms + log2f(Lt)) * CUDART_LN2_F;
         }
     }
 }

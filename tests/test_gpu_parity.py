@@ -396,6 +396,25 @@ def test_bad_page_id_and_length_report_without_nan(ga, err):
     assert torch.all(out[1] == 0)
 
 
+@pytest.mark.parametrize("split", [dict(requested_splits=1), dict(requested_splits=3)])
+def test_nan_in_attended_kv_propagates(ga, err, split):
+    """A NaN in an attended K or V row makes that head's output NaN, as in the
+    oracle; rows and heads that never see it stay finite and correct."""
+    fam = _fam(8, 2, 512, 0)
+    fi = _inputs([100, 70, 300], fam, seed=16, poison=False)
+    p0 = int(fi.page_table[0, 3])                 # row 0, keys 48..63
+    fi.k_pool[p0, 1, 5, 7] = float("nan")         # kv head 1 -> query heads 4..7
+    p2 = int(fi.page_table[2, 10])
+    fi.v_pool[p2, 0, 2, 100] = float("nan")       # row 2, kv head 0 -> heads 0..3
+    out = run_decode(ga, fi, _plan(ga, fi, **split), err=err).float().cpu().numpy()
+    torch.cuda.synchronize()
+    ref = oracle_decode(fi)
+    assert np.array_equal(np.isnan(out), np.isnan(ref))
+    assert np.isnan(out[0, 4:8]).all() and np.isnan(out[2, 0:4, 100]).all()
+    ok = ~np.isnan(ref)
+    assert_close(out[ok], ref[ok], what="finite part")
+
+
 def test_capacity_check(ga, err):
     fam = _fam(8, 2, 512, 0)
     fi = _inputs([100, 50], fam, seed=13, poison=False)

@@ -75,7 +75,7 @@ enum {
     GA_DEVERR_PAGE_ID = 1,       /* a page id outside [0, num_pages) was met */
     GA_DEVERR_SEQ_LEN = 2,       /* seq_len < 0 or > pt_stride * page_size */
     GA_DEVERR_CAPACITY = 4,      /* seq_lens need more split chunks than the plan holds */
-    GA_DEVERR_Q_RANGE = 8,       /* E4M3 path: |q| beyond the f16 range it is staged in */
+    GA_DEVERR_Q_RANGE = 8,       /* E4M3 path: q holds an infinite value */
     GA_DEVERR_TIMEOUT = 16,      /* a bounded wait for a bulk copy ran out */
     GA_DEVERR_POSITION = 32,     /* append: position / page_table[pos / P] invalid */
     GA_DEVERR_SELF_CHECK = 64    /* GA_CHECKED builds: an access outside its buffer was skipped */
@@ -180,7 +180,8 @@ int ga_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_poo
  *
  *   q [batch, num_q_heads, 256] bf16; num_q_heads % num_kv_heads == 0.
  *   kv_dtype GA_KV_BF16 or GA_KV_E4M3 (with k_scale, v_scale [Hkv] fp32;
- *       with E4M3 the q operand is staged in f16, |q| <= 65504).
+ *       with E4M3 the products run on E4M3 tensor cores: q is scaled per head
+ *       and split into two E4M3 parts, P likewise, about bf16 precision).
  *   seq_lens [batch] int32 device; window >= 1.
  *   scale: softmax scale (e.g. 1/sqrt(256), or 1.0 for the Gemma convention).
  *   plan: from ga_plan_splits with the same batch, heads, head_dim, window

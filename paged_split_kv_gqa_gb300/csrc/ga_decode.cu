@@ -42,9 +42,6 @@
 
 namespace ga {
 
-// Slack (log2 units) by which a score may exceed the running max before the
-// max is raised and the accumulators rescaled.
-constexpr float kMaxSlack = 8.0f;
 
 struct DecodeParams {
     const __nv_bfloat16* q;       // [B, Hq, D]
@@ -92,6 +89,10 @@ struct DecodeCfg {
     static constexpr int KSTEPS = D / 16;
     static constexpr int MTILES = D / 16;
     static constexpr bool Q_IN_REGS = (D <= 256);
+    // E4M3 runs its MMAs on E4M3 operands: P is scaled by PSCALE so that with a
+    // max slack of 2^MAX_SLACK it stays within E4M3's range (<= 256 < 448).
+    static constexpr float MAX_SLACK = KV == GA_KV_BF16 ? 8.0f : 2.0f;
+    static constexpr float PSCALE = KV == GA_KV_BF16 ? 1.0f : 64.0f;
     static constexpr int MSTRIDE = D + 4;           // floats per head row of the merge buffer
     // shared-memory map; every region starts on a 128-byte boundary (the
     // mbarriers need 8, the float4 / uint2 accesses 16)
@@ -100,7 +101,8 @@ struct DecodeCfg {
     static constexpr int OFF_QF = al(OFF_RING + NS * STAGE_BYTES);
     static constexpr int OFF_MERGE = al(OFF_QF + KSTEPS * 32 * 8);
     static constexpr int OFF_ML = al(OFF_MERGE + kHeadTile * MSTRIDE * 4);
-    static constexpr int OFF_PREFIX = al(OFF_ML + 2 * NCW * kHeadTile * 4);
+    static constexpr int OFF_QSC = al(OFF_ML + 2 * NCW * kHeadTile * 4);   // [2][8] q amax / scale
+    static constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
     static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
     static constexpr int OFF_BARS = al(OFF_FLAGS + NS * 4);
     static constexpr int SMEM_USED = al(OFF_BARS + 2 * NS * 8);
@@ -155,12 +157,14 @@ template <class C>
 __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
                          const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
                          volatile uint32_t* flags, volatile int* abort_flag) {
+    // Lanes 0 .. kIssueLanes-1 each take one of that many consecutive pages:
+    // the per-page chain (wait for a free stage, arm its barrier, issue the two
+    // bulk copies) runs for several stages at once.
+    constexpr int kIssueLanes = 4;
+    static_assert(C::NS >= kIssueLanes && C::NS <= 32, "ring depth");
     const int lane = threadIdx.x & 31;
     const uint64_t policy = l2_evict_first_policy();
-    uint32_t seq = 0;
-    int32_t issued_round[C::NS];
-#pragma unroll
-    for (int s = 0; s < C::NS; ++s) issued_round[s] = -1;
+    uint32_t seq = 0;                 // pages handed to the ring so far
     bool stop = false;
     for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
         const UnitInfo x = unit_info(p, pre, u);
@@ -171,21 +175,22 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
         int32_t id_nxt = (32 + lane < x.np) ? __ldg(tbl + x.p0 + 32 + lane) : -1;
         for (int i0 = 0; i0 < x.np && !stop; i0 += 32) {
             const int cnt = min(32, x.np - i0);
-            for (int k = 0; k < cnt; ++k) {
-                const int32_t pid = __shfl_sync(0xffffffffu, id_cur, k);
-                if (lane == 0 && !stop) {
-                    const uint32_t slot = seq % C::NS;
-                    const uint32_t round = seq / C::NS;
+            for (int k = 0; k < cnt && !stop; k += kIssueLanes) {
+                const int32_t pid = __shfl_sync(0xffffffffu, id_cur, (k + lane) & 31);
+                bool fail = false;
+                if (lane < kIssueLanes && k + lane < cnt) {
+                    const uint32_t n = seq + (uint32_t)(k + lane);
+                    const uint32_t slot = n % C::NS;
+                    const uint32_t round = n / C::NS;
                     const uint32_t full = bars + 8 * slot;
                     const uint32_t empty = bars + 8 * (C::NS + slot);
                     if (*abort_flag || !mbar_wait(empty, (round & 1) ^ 1)) {
                         report(p.err_word, kErrTimeout);
                         *abort_flag = 1;
-                        stop = true;
+                        fail = true;
                     } else if (page_ok(pid, p.num_pages) &&
                                GA_CHK(page_block_row(pid, x.c, p.Hkv) >= 0 &&
-                                      page_block_row(pid, x.c, p.Hkv) + kPageSize <= p.pool_rows &&
-                                      slot < (uint32_t)C::NS)) {
+                                      page_block_row(pid, x.c, p.Hkv) + kPageSize <= p.pool_rows)) {
                         flags[slot] = 0;
                         mbar_arrive_expect_tx(full, C::STAGE_BYTES);
                         const int32_t y = page_block_row(pid, x.c, p.Hkv);
@@ -193,30 +198,29 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                         // one 3-D box per block: the whole page-head block of K, then V
                         tma_load_3d(dst, tmK, full, 0, y, 0, policy);
                         tma_load_3d(dst + C::BLOCK_BYTES, tmV, full, 0, y, 0, policy);
-                        issued_round[slot] = (int32_t)round;
                     } else {
                         flags[slot] = 1;
                         report(p.err_word, page_ok(pid, p.num_pages) ? kErrSelfCheck : kErrPageId);
                         mbar_arrive(full);
                     }
-                    if (log && i0 + k < p.touch_stride && GA_CHK(x.rc < p.rc_capacity))
-                        p.touch_log[x.rc * p.touch_stride + i0 + k] = pid;
+                    if (log && i0 + k + lane < p.touch_stride && GA_CHK(x.rc < p.rc_capacity))
+                        p.touch_log[x.rc * p.touch_stride + i0 + k + lane] = pid;
                 }
-                stop = __shfl_sync(0xffffffffu, stop, 0);
-                ++seq;
+                stop = __any_sync(0xffffffffu, fail);
             }
+            seq += (uint32_t)cnt;
             id_cur = id_nxt;
             id_nxt = (i0 + 64 + lane < x.np) ? __ldg(tbl + x.p0 + i0 + 64 + lane) : -1;
         }
     }
-    // Never leave with a copy in flight into this CTA's shared memory.
-    if (lane == 0) {
-        for (int s = 0; s < C::NS; ++s) {
-            if (issued_round[s] >= 0 &&
-                !mbar_wait(bars + 8 * s, (uint32_t)issued_round[s] & 1)) {
-                report(p.err_word, kErrTimeout);
-                *abort_flag = 1;
-            }
+    // Never leave with a copy in flight into this CTA's shared memory: wait
+    // for the last round each stage was armed for (already complete unless
+    // the kernel is aborting, and bounded either way).
+    if (lane < C::NS && (uint32_t)lane < seq) {
+        const uint32_t last = (uint32_t)lane + ((seq - 1 - (uint32_t)lane) / C::NS) * C::NS;
+        if (!mbar_wait(bars + 8 * lane, (last / C::NS) & 1)) {
+            report(p.err_word, kErrTimeout);
+            *abort_flag = 1;
         }
     }
 }
@@ -224,13 +228,40 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
 // ------------------------------------------------------------------ consumer
 
 // Builds the per-lane B fragments of Q^T for one unit in shared memory:
-// qf[ks][lane] = {b0, b1}.  bf16: b0 = q[n][16ks+2t .. +1], b1 = q[n][16ks+2t+8 .. +9]
-// with n = lane/4 the head column, t = lane%4.  E4M3: the four dims
-// 16ks+4t .. +3 in f16 (k order permuted to match the byte layout of the
-// E4M3 K fragments; the dot product does not depend on the order).
+// qf[ks][lane] = {b0, b1}, n = lane/4 the head column, t = lane%4.
+//  bf16: b0 = q[n][16ks+2t .. +1], b1 = q[n][16ks+2t+8 .. +9] (m16n8k16).
+//  E4M3 (m16n8k32, K = the 16 dims of chunk ks twice): q of head n is scaled
+//   by 448 / amax_n and split into two E4M3 parts, hi = E4M3(q') and
+//   lo = E4M3(q' - hi); b0 = hi[n][16ks+4t .. +3], b1 = lo[n][16ks+4t .. +3],
+//   so one MMA against the K codes stacked twice yields K (hi + lo).  The
+//   scale amax_n / 448 goes to qsc[8 + n] and multiplies the scores.
 template <class C>
 __device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInfo& x,
-                                            uint2* qf, int tid) {
+                                            uint2* qf, float* qsc, int tid) {
+    if constexpr (C::KV == GA_KV_E4M3) {
+        unsigned* amax = reinterpret_cast<unsigned*>(qsc);
+        if (tid < kHeadTile) amax[tid] = 0u;
+        named_barrier(1, C::NCT);
+        constexpr int D8 = C::D / 8;
+        for (int e = tid; e < x.nvalid * D8; e += C::NCT) {
+            const int n = e / D8, d = (e % D8) * 8;
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+                p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D + d));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            float m = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
+            atomicMax(amax + n, __float_as_uint(m));      // non-negative floats order as ints
+        }
+        named_barrier(1, C::NCT);
+        if (tid < kHeadTile) {
+            const float am = __uint_as_float(amax[tid]);
+            if (tid < x.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
+            qsc[kHeadTile + tid] = (am > 0.f) ? am * (1.0f / 448.0f) : 1.0f;
+        }
+        named_barrier(1, C::NCT);
+    }
     for (int e = tid; e < C::KSTEPS * 32; e += C::NCT) {
         const int ks = e >> 5, ln = e & 31, n = ln >> 2, t = ln & 3;
         uint2 v = make_uint2(0u, 0u);
@@ -243,17 +274,18 @@ __device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInf
                 v.y = __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t + 8));
             } else {
                 const uint2 w = __ldg(reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t));
-                const float f0 = bf16_lo(w.x), f1 = bf16_hi(w.x);
-                const float f2 = bf16_lo(w.y), f3 = bf16_hi(w.y);
-                v.x = pack_f16x2(f0, f1);
-                v.y = pack_f16x2(f2, f3);
-                const __half2 h0 = *reinterpret_cast<__half2*>(&v.x);
-                const __half2 h1 = *reinterpret_cast<__half2*>(&v.y);
-                const bool big = (fabsf(f0) < CUDART_INF_F && __hisinf(__low2half(h0))) ||
-                                 (fabsf(f1) < CUDART_INF_F && __hisinf(__high2half(h0))) ||
-                                 (fabsf(f2) < CUDART_INF_F && __hisinf(__low2half(h1))) ||
-                                 (fabsf(f3) < CUDART_INF_F && __hisinf(__high2half(h1)));
-                if (big) report(p.err_word, kErrQRange);
+                const float inv = 1.0f / qsc[kHeadTile + n];
+                const float f[4] = {bf16_lo(w.x) * inv, bf16_hi(w.x) * inv,
+                                    bf16_lo(w.y) * inv, bf16_hi(w.y) * inv};
+                const uint32_t h01 = f32x2_to_e4m3x2(f[0], f[1]);
+                const uint32_t h23 = f32x2_to_e4m3x2(f[2], f[3]);
+                const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
+                const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&d01));
+                const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&d23));
+                const uint32_t l01 = f32x2_to_e4m3x2(f[0] - g01.x, f[1] - g01.y);
+                const uint32_t l23 = f32x2_to_e4m3x2(f[2] - g23.x, f[3] - g23.y);
+                v.x = h01 | (h23 << 16);
+                v.y = l01 | (l23 << 16);
             }
         }
         qf[e] = v;
@@ -276,6 +308,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
     uint2* qf = reinterpret_cast<uint2*>(smem + C::OFF_QF);
     float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
     float* mlw = reinterpret_cast<float*>(smem + C::OFF_ML);   // [2][NCW][8]
+    float* qsc = reinterpret_cast<float*>(smem + C::OFF_QSC);  // [8] amax bits, [8] q scale
 
     uint32_t seq_base = 0;
     for (int64_t u = blockIdx.x; u < U; u += gridDim.x) {
@@ -286,8 +319,13 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             kfac *= __ldg(p.k_scale + x.c);
             vfac = __ldg(p.v_scale + x.c);
         }
-        fill_qfrags<C>(p, x, qf, tid);
+        fill_qfrags<C>(p, x, qf, qsc, tid);
         named_barrier(1, C::NCT);
+        float kf0 = kfac, kf1 = kfac;                 // per head column (2t, 2t+1)
+        if constexpr (C::KV == GA_KV_E4M3) {
+            kf0 *= qsc[kHeadTile + 2 * t];
+            kf1 *= qsc[kHeadTile + 2 * t + 1];
+        }
 
         uint32_t qr[C::Q_IN_REGS ? C::KSTEPS : 1][2];
         if constexpr (C::Q_IN_REGS) {
@@ -342,6 +380,9 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                         mma_bf16(sa[ks & 3], a, b0, b1);
                     }
                 } else {
+                    // K codes feed the E4M3 MMA directly: ldmatrix gives, per
+                    // 16-dim chunk, the A fragment rows (keys) x k 0..15; K of the
+                    // MMA carries the chunk twice (hi and lo parts of q).
 #pragma unroll
                     for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
                         uint32_t r[4];
@@ -350,11 +391,6 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
 #pragma unroll
                         for (int hs = 0; hs < 2; ++hs) {
                             const int ks = 2 * kp + hs;
-                            uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2(r[2 * hs] & 0xFFFFu);
-                            a[1] = e4m3x2_to_f16x2(r[2 * hs + 1] & 0xFFFFu);
-                            a[2] = e4m3x2_to_f16x2(r[2 * hs] >> 16);
-                            a[3] = e4m3x2_to_f16x2(r[2 * hs + 1] >> 16);
                             uint32_t b0, b1;
                             if constexpr (C::Q_IN_REGS) {
                                 b0 = qr[ks][0];
@@ -364,14 +400,15 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                                 b0 = v.x;
                                 b1 = v.y;
                             }
-                            mma_f16(sa[ks & 3], a, b0, b1);
+                            mma_e4m3(sa[ks & 3], r[2 * hs], r[2 * hs + 1], r[2 * hs],
+                                     r[2 * hs + 1], b0, b1);
                         }
                     }
                 }
                 float s[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    s[r] = ((sa[0][r] + sa[1][r]) + (sa[2][r] + sa[3][r])) * kfac;
+                    s[r] = ((sa[0][r] + sa[1][r]) + (sa[2][r] + sa[3][r])) * ((r & 1) ? kf1 : kf0);
                 // ---- window / length mask (first and last page of the range only)
                 const int32_t key0 = (x.p0 + i) * kPageSize;
                 const bool partial = key0 < x.g.lo || key0 + kPageSize > x.g.len;
@@ -386,19 +423,27 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                         const int32_t kk = key0 + k;
                         return kk >= x.g.lo && kk < x.g.len;
                     };
-                    mk01 = (valid(2 * t) ? 0x0000ffffu : 0u) | (valid(2 * t + 1) ? 0xffff0000u : 0u);
-                    mk89 = (valid(2 * t + 8) ? 0x0000ffffu : 0u) |
-                           (valid(2 * t + 9) ? 0xffff0000u : 0u);
+                    if constexpr (C::KV == GA_KV_BF16) {
+                        mk01 = (valid(2 * t) ? 0x0000ffffu : 0u) |
+                               (valid(2 * t + 1) ? 0xffff0000u : 0u);
+                        mk89 = (valid(2 * t + 8) ? 0x0000ffffu : 0u) |
+                               (valid(2 * t + 9) ? 0xffff0000u : 0u);
+                    } else {   // E4M3 V fragment bytes hold keys 2t, 2t+1, 2t+8, 2t+9
+                        mk01 = (valid(2 * t) ? 0x000000ffu : 0u) |
+                               (valid(2 * t + 1) ? 0x0000ff00u : 0u) |
+                               (valid(2 * t + 8) ? 0x00ff0000u : 0u) |
+                               (valid(2 * t + 9) ? 0xff000000u : 0u);
+                    }
                 }
                 // ---- online softmax (base 2) over this page, per head column.
                 // The running max m is only raised when some score exceeds it by
-                // more than kMaxSlack, so p <= 2^kMaxSlack between updates; the
+                // more than MAX_SLACK, so p <= 2^MAX_SLACK between updates; the
                 // common page needs one warp vote instead of a shuffle reduction
                 // and an O rescale.  m stays uniform across the 8 lanes of a
                 // column because it only changes on the warp-uniform slow path.
                 {
                     float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-                    const bool grow = (mx0 > m0 + kMaxSlack) || (mx1 > m1 + kMaxSlack);
+                    const bool grow = (mx0 > m0 + C::MAX_SLACK) || (mx1 > m1 + C::MAX_SLACK);
                     if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
                         for (int off = 4; off < 32; off <<= 1) {
@@ -433,8 +478,21 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                     pb0 = movmatrix_t(pack_bf16x2(p0, p1));
                     pb1 = movmatrix_t(pack_bf16x2(p2, p3));
                 } else {
-                    pb0 = movmatrix_t(pack_f16x2(p0, p1));
-                    pb1 = movmatrix_t(pack_f16x2(p2, p3));
+                    // (keys 2t, 2t+1) and (keys 2t+8, 2t+9) of head column g in f16,
+                    // scaled by PSCALE, split into E4M3 hi + lo parts: b0 / b1 of the
+                    // PV MMA, whose K carries these four keys twice.
+                    const uint32_t h01 = movmatrix_t(pack_f16x2(p0 * C::PSCALE, p1 * C::PSCALE));
+                    const uint32_t h89 = movmatrix_t(pack_f16x2(p2 * C::PSCALE, p3 * C::PSCALE));
+                    const uint32_t e01 = f16x2_to_e4m3x2(h01), e89 = f16x2_to_e4m3x2(h89);
+                    const uint32_t r01 = e4m3x2_to_f16x2(e01), r89 = e4m3x2_to_f16x2(e89);
+                    const __half2 d01 = __hsub2(*reinterpret_cast<const __half2*>(&h01),
+                                                *reinterpret_cast<const __half2*>(&r01));
+                    const __half2 d89 = __hsub2(*reinterpret_cast<const __half2*>(&h89),
+                                                *reinterpret_cast<const __half2*>(&r89));
+                    const uint32_t l01 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&d01));
+                    const uint32_t l89 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&d89));
+                    pb0 = e01 | (e89 << 16);
+                    pb1 = l01 | (l89 << 16);
                 }
                 // ---- O^T += V^T P^T (V rows of unattended slots zeroed on partial pages)
                 auto pv = [&](auto masked) {
@@ -454,23 +512,25 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                             mma_bf16(o[mt], a, pb0, pb1);
                         }
                     } else {
+                        // V^T fragments from ldmatrix.trans: per 32-dim group the
+                        // b16 transpose gives, per lane, keys (2t, 2t+1) x dims
+                        // (2g, 2g+1) of two 8-key halves; one byte_perm per register
+                        // forms the A rows of the even-dim (E) and odd-dim (O)
+                        // m-tiles with K order keys 2t, 2t+1, 2t+8, 2t+9 (twice).
 #pragma unroll
                         for (int mp = 0; mp < C::MTILES / 2; ++mp) {
                             uint32_t r[4];
                             const uint32_t ch = (uint32_t)(((mp & 3) << 1) + vhi);
                             ldsm_x4_t(vb + (mp >> 2) * C::TILE_BYTES + voff + ((ch ^ vx) << 4), r);
-                            uint32_t ev[4], od[4];
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                ev[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0020u));
-                                od[q4] = e4m3x2_to_f16x2(__byte_perm(r[q4], 0u, 0x0031u));
-                            }
+                            uint32_t e0 = __byte_perm(r[0], r[2], 0x6420u);
+                            uint32_t e1 = __byte_perm(r[1], r[3], 0x6420u);
+                            uint32_t o0 = __byte_perm(r[0], r[2], 0x7531u);
+                            uint32_t o1 = __byte_perm(r[1], r[3], 0x7531u);
                             if constexpr (kMask) {
-                                ev[0] &= mk01; ev[1] &= mk01; ev[2] &= mk89; ev[3] &= mk89;
-                                od[0] &= mk01; od[1] &= mk01; od[2] &= mk89; od[3] &= mk89;
+                                e0 &= mk01; e1 &= mk01; o0 &= mk01; o1 &= mk01;
                             }
-                            mma_f16(o[2 * mp], ev, pb0, pb1);
-                            mma_f16(o[2 * mp + 1], od, pb0, pb1);
+                            mma_e4m3(o[2 * mp], e0, e1, e0, e1, pb0, pb1);
+                            mma_e4m3(o[2 * mp + 1], o0, o1, o0, o1, pb0, pb1);
                         }
                     }
                 };
@@ -511,7 +571,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             const float mown = (e == 0) ? m0 : m1;
             // only an exactly empty sum means "no keys"; NaN in attended K / V
             // propagates to the output as in the definition
-            fac[e] = (Lt == 0.f) ? 0.f : exp2f(mown - Ms) * (vfac / Lt);
+            fac[e] = (Lt == 0.f) ? 0.f : exp2f(mown - Ms) * (vfac / (Lt * C::PSCALE));
         }
         // warps add their scaled O into one buffer in turn (fixed order:
         // deterministic, so results do not depend on timing)
@@ -714,7 +774,7 @@ static int run(const DecodeArgs& a, int slot) {
 #define GA_LB_NS 12
 #endif
 #ifndef GA_LE_NCW
-#define GA_LE_NCW 3
+#define GA_LE_NCW 4
 #define GA_LE_NS 24
 #endif
 #ifndef GA_GB_NCW
@@ -722,7 +782,7 @@ static int run(const DecodeArgs& a, int slot) {
 #define GA_GB_NS 6
 #endif
 #ifndef GA_GE_NCW
-#define GA_GE_NCW 4
+#define GA_GE_NCW 6
 #define GA_GE_NS 12
 #endif
 using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, GA_LB_NCW, GA_LB_NS>;

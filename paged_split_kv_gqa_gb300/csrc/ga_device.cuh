@@ -146,6 +146,19 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D += A(16x32, row) * B(32x8, col) on E4M3 operands, fp32 accumulate.
+// Fragments: a0 = (row g, k 4t..4t+3), a1 = (row g+8, k 4t..), a2 = (row g,
+// k 16+4t..), a3 = (row g+8, k 16+4t..); b0 = (k 4t..4t+3, col g),
+// b1 = (k 16+4t.., col g); lowest byte = lowest k.
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -167,6 +180,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
         static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// f16x2 -> two E4M3 codes (round to nearest even, saturate to +-448) in the
+// low 16 bits; first element in the low byte.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+    __half2_raw r;
+    r.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+    r.y = static_cast<unsigned short>(h2 >> 16);
+    return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

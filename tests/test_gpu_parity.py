@@ -425,10 +425,18 @@ def test_capacity_check(ga, err):
     assert int(err.item()) & ga.GA_DEVERR_CAPACITY
 
 
-def test_e4m3_q_range_reported(ga, err):
+def test_e4m3_large_q_is_exact_enough_and_inf_q_reported(ga, err):
+    """E4M3 decode scales q per head, so a large finite q (beyond f16 range)
+    still matches the oracle; an infinite q is reported."""
     fam = _fam(8, 2, 256, 64, kv=1)
     fi = _inputs([40, 70], fam, seed=14)
-    fi.q[1, 3, 5] = 1e6
+    fi.q[1, 3] *= 3e4                         # |q| up to ~1e5, peaked softmax for head 3
+    out = run_decode(ga, fi, _plan(ga, fi), err=err, scale=1e-5)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(out.float().cpu().numpy(), oracle_decode(fi, scale=1e-5), kv_dtype=1,
+                 what="large q")
+    fi.q[0, 5, 7] = float("inf")
     run_decode(ga, fi, _plan(ga, fi), err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & ga.GA_DEVERR_Q_RANGE

@@ -130,7 +130,7 @@ class ClockSampler:
 WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 
 
-def make_layer(device, wl, fam, seed, layer):
+def make_layer(device, wl, fam, seed, layer, kv_alias=False):
     import torch
     from paged_split_kv_gqa_gb300 import ga
     from paged_split_kv_gqa_gb300 import metrics as M
@@ -138,6 +138,10 @@ def make_layer(device, wl, fam, seed, layer):
 
     fi = W.make_family_inputs(wl, fam, device=device, seed=seed, layer=layer,
                               release_old=(fam.window > 0))
+    alias = kv_alias and fam.window == 0
+    if alias:                      # K == V: one pool serves both (global family)
+        fi.v_pool = fi.k_pool
+        fi.v_scale = fi.k_scale
     plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                              window=fam.window, flags=ga.GA_PLAN_EXTERNAL_COMBINE)
@@ -150,13 +154,14 @@ def make_layer(device, wl, fam, seed, layer):
         scale=1.0 / math.sqrt(fam.head_dim),
         bytes=M.decode_bytes(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
-                             window=fam.window, page_size=wl.page_size, kv_bytes_per_elem=esz),
+                             window=fam.window, page_size=wl.page_size, kv_bytes_per_elem=esz,
+                             kv_alias=alias),
         append_bytes=M.append_bytes(wl.batch, num_kv_heads=fam.num_kv_heads,
                                     head_dim=fam.head_dim, kv_bytes_per_elem=esz),
         keys=int(M.attended_keys(wl.seq_lens, fam.window).sum()))
 
 
-def build_step(device, seed, workload="31b", rows=0, pools=4):
+def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2)."""
@@ -168,7 +173,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4):
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
-    sets = {fam.name: [make_layer(device, wl, fam, seed, i) for i in range(npool)]
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias) for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
         schedule, nl, ng = [], 0, 0
@@ -345,7 +350,7 @@ def run_ga(args):
         dist.init_process_group("nccl", device_id=device)
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
-                                         args.pools)
+                                         args.pools, args.kv_alias)
 
     def step(evs=None):
         n = 0
@@ -359,9 +364,19 @@ def run_ga(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during warm-up")
 
-    # ---- device-timed region: K steps, events around each decode launch
+    # --graph: the whole step captured once in a CUDA graph and replayed
+    graph, per_step = None, 0
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            per_step = step()
+        graph.replay()
+        torch.cuda.synchronize()
+
+    # ---- device-timed region: K steps (eager: events around each decode launch)
+    ev_steps = min(args.steps, 50) if graph is not None else args.steps
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in schedule] for _ in range(args.steps)]
+           for _ in schedule] for _ in range(ev_steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     if pg:
@@ -370,10 +385,18 @@ def run_ga(args):
     with ClockSampler(local_rank) as clocks:
         start.record()
         for k in range(args.steps):
-            launches += step(ev[k])
+            if graph is not None:
+                graph.replay()
+                launches += per_step
+            else:
+                launches += step(ev[k])
         end.record()
         torch.cuda.synchronize()
     elapsed = start.elapsed_time(end) / 1e3
+    if graph is not None:          # per-family kernel times from an eager pass
+        for k in range(ev_steps):
+            step(ev[k])
+        torch.cuda.synchronize()
     if pg:
         t = torch.tensor([elapsed], device=device)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -383,7 +406,7 @@ def run_ga(args):
 
     # per family: decode-kernel time and algorithmic bytes over all its launches
     fam_ms, fam_bytes, fam_keys, fam_n = {}, {}, {}, {}
-    for k in range(args.steps):
+    for k in range(ev_steps):
         for i, layer in enumerate(schedule):
             name = layer["fam"].name
             a, b = ev[k][i]
@@ -395,7 +418,7 @@ def run_ga(args):
     for name in fam_ms:
         t = fam_ms[name] / 1e3
         families[name] = {
-            "launches_per_step": fam_n[name] // args.steps,
+            "launches_per_step": fam_n[name] // ev_steps,
             "decode_ms_per_launch": fam_ms[name] / fam_n[name],
             "decode_gbs": fam_bytes[name] / t / 1e9,
             "algorithmic_bytes_per_launch": fam_bytes[name] // fam_n[name],
@@ -472,6 +495,8 @@ def run_ga(args):
             text += f" -- PROFILING SUBSET: first {args.rows} rows"
         if args.workload == "ragged":
             text += f"; {args.pools} distinct pools per family rotated over the layers"
+        if args.kv_alias:
+            text += "; global family with K == V (one pool, read once)"
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
@@ -480,7 +505,8 @@ def run_ga(args):
             "config": {
                 "workload": text,
                 "global_batch": wl.batch * world,
-                "step": f"{len(schedule)} layers, each append+decode(+combine)",
+                "step": f"{len(schedule)} layers, each append+decode(+combine)"
+                        + ("" if args.eager else "; captured in one CUDA graph, replayed"),
                 "l2": "inputs larger than L2 (KV pools of each layer > 129 MB); no flush",
                 "plans": {n: plan_desc(layers[0]["plan"]) for n, layers in sets.items()},
             },
@@ -511,6 +537,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", default="31b", choices=sorted(WORKLOADS))
+    ap.add_argument("--kv-alias", action="store_true",
+                    help="global family with K == V: one pool, each block read once")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every call from Python in the timed loop instead of replaying "
+                         "one captured CUDA graph of the step")
     ap.add_argument("--pools", type=int, default=4,
                     help="ragged workload: distinct KV pools per family rotated over layers")
     ap.add_argument("--rows", type=int, default=0,

@@ -206,7 +206,9 @@ int ga_decode_local_hd256(const void* q, const void* k_pool, const void* v_pool,
  * ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is mandatory here" and
  * hybrid-pf64 numerics gate: S=1 decode over the whole cache, no causal mask,
  * 32 query heads x 512 over 4 KV heads).  Arguments as for the local call
- * without `window`; head_dim is 512.
+ * without `window`; head_dim is 512.  Passing the same pool as k_pool and
+ * v_pool (K == V, as with a shared K/V projection: "[Model] Gemma 4 M1 12B",
+ * Description) reads each page-head block once and uses it for both products.
  */
 int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool,
                            int32_t kv_dtype, const float* k_scale, const float* v_scale,

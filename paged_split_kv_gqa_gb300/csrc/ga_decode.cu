@@ -71,12 +71,15 @@ struct DecodeParams {
 #define GA_CHK(cond) true
 #endif
 
-template <int D_, int KV_, int NCW_, int NS_>
+template <int D_, int KV_, int NCW_, int NS_, bool ALIAS_ = false>
 struct DecodeCfg {
     static constexpr int D = D_;
     static constexpr int KV = KV_;                  // GA_KV_BF16 / GA_KV_E4M3
     static constexpr int NCW = NCW_;                // consumer warps
     static constexpr int NS = NS_;                  // ring stages (one page each)
+    // K and V are one pool (K == V, e.g. a shared K/V projection): each page-head
+    // block is fetched once and serves both products.
+    static constexpr bool ALIAS = ALIAS_;
 
     static constexpr int NCT = NCW * 32;            // consumer threads
     static constexpr int NTHREADS = NCT + 32;
@@ -85,7 +88,7 @@ struct DecodeCfg {
     static constexpr int NTILES = D * ESZ / 128;    // boxes per page-head block
     static constexpr int TILE_BYTES = kPageSize * 128;
     static constexpr int BLOCK_BYTES = NTILES * TILE_BYTES;
-    static constexpr int STAGE_BYTES = 2 * BLOCK_BYTES;   // K block + V block
+    static constexpr int STAGE_BYTES = (ALIAS ? 1 : 2) * BLOCK_BYTES;   // K block (+ V block)
     static constexpr int KSTEPS = D / 16;
     static constexpr int MTILES = D / 16;
     static constexpr bool Q_IN_REGS = (D <= 256);
@@ -197,7 +200,8 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                         const uint32_t dst = ring + slot * C::STAGE_BYTES;
                         // one 3-D box per block: the whole page-head block of K, then V
                         tma_load_3d(dst, tmK, full, 0, y, 0, policy);
-                        tma_load_3d(dst + C::BLOCK_BYTES, tmV, full, 0, y, 0, policy);
+                        if constexpr (!C::ALIAS)
+                            tma_load_3d(dst + C::BLOCK_BYTES, tmV, full, 0, y, 0, policy);
                     } else {
                         flags[slot] = 1;
                         report(p.err_word, page_ok(pid, p.num_pages) ? kErrSelfCheck : kErrPageId);
@@ -357,7 +361,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             ready = __all_sync(0xffffffffu, ready);
             if (ready && flags[slot] == 0) {
                 const uint32_t kb = ring + slot * C::STAGE_BYTES;
-                const uint32_t vb = kb + C::BLOCK_BYTES;
+                const uint32_t vb = C::ALIAS ? kb : kb + C::BLOCK_BYTES;
                 // ---- S^T = K Q^T (16 keys x 8 heads), 4 independent chains
                 float sa[4][4];
 #pragma unroll
@@ -789,10 +793,16 @@ using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, GA_LB_NCW, GA_LB_NS>;
 using CfgLocalE4m3 = DecodeCfg<256, GA_KV_E4M3, GA_LE_NCW, GA_LE_NS>;
 using CfgGlobalBf16 = DecodeCfg<512, GA_KV_BF16, GA_GB_NCW, GA_GB_NS>;
 using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, GA_GE_NS>;
+// K == V (one pool): half-size stages, twice as many.
+using CfgGlobalBf16Alias = DecodeCfg<512, GA_KV_BF16, GA_GB_NCW, 2 * GA_GB_NS, true>;
+using CfgGlobalE4m3Alias = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, 2 * GA_GE_NS, true>;
 
 int launch_decode(const DecodeArgs& a) {
     if (a.head_dim == 256)
         return a.kv_dtype == GA_KV_BF16 ? run<CfgLocalBf16>(a, 0) : run<CfgLocalE4m3>(a, 1);
+    if (a.head_dim == 512 && a.k_pool == a.v_pool)
+        return a.kv_dtype == GA_KV_BF16 ? run<CfgGlobalBf16Alias>(a, 4)
+                                        : run<CfgGlobalE4m3Alias>(a, 5);
     if (a.head_dim == 512)
         return a.kv_dtype == GA_KV_BF16 ? run<CfgGlobalBf16>(a, 2) : run<CfgGlobalE4m3>(a, 3);
     return GA_ERR_UNSUPPORTED;

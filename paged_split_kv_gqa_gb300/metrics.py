@@ -28,11 +28,14 @@ def pages_read(seq_lens, window: int, page_size: int) -> np.ndarray:
 
 
 def decode_bytes(seq_lens, *, num_q_heads, num_kv_heads, head_dim, window, page_size,
-                 kv_bytes_per_elem) -> int:
-    """Algorithmic HBM bytes of one decode launch over a batch."""
+                 kv_bytes_per_elem, kv_alias=False) -> int:
+    """Algorithmic HBM bytes of one decode launch over a batch (K == V one
+    pool: each attended key row is read once)."""
     B = len(seq_lens)
     n = int(attended_keys(seq_lens, window).sum())
     kv = n * kv_bytes_per_token(num_kv_heads, head_dim, kv_bytes_per_elem)
+    if kv_alias:
+        kv //= 2
     qo = 2 * B * num_q_heads * head_dim * 2
     table = 4 * int(pages_read(seq_lens, window, page_size).sum())
     scales = 8 * num_kv_heads if kv_bytes_per_elem == 1 else 0

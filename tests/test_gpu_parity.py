@@ -415,6 +415,28 @@ def test_nan_in_attended_kv_propagates(ga, err, split):
     assert_close(out[ok], ref[ok], what="finite part")
 
 
+@pytest.mark.parametrize("kv", [0, 1])
+def test_kv_alias_one_pool(ga, err, kv):
+    """k_pool is v_pool (K == V): the one-fetch kernel gives bit for bit what
+    the two-pool kernel gives on a copy, and matches the oracle with V = K."""
+    fam = _fam(32, 4, 512, 0, kv=kv)
+    fi = _inputs([700, 33, 1500, 1], fam, seed=17)
+    fi.v_pool = fi.k_pool
+    if kv:
+        fi.v_scale = fi.k_scale * 1.5
+    for split in (dict(requested_splits=1), dict(fixed_chunk_tokens=128)):
+        plan = _plan(ga, fi, **split)
+        one = run_decode(ga, fi, plan, err=err).clone()
+        two_fi = W.FamilyInputs(fam, fi.q, fi.k_pool, fi.k_pool.clone(), fi.k_scale, fi.v_scale,
+                                fi.page_table, fi.seq_lens, fi.k_new, fi.v_new, fi.num_pages)
+        two = run_decode(ga, two_fi, plan, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(one, two)
+        assert_close(one.float().cpu().numpy(), oracle_decode(fi), kv_dtype=kv,
+                     what=f"alias kv={kv} {split}")
+
+
 def test_capacity_check(ga, err):
     fam = _fam(8, 2, 512, 0)
     fi = _inputs([100, 50], fam, seed=13, poison=False)

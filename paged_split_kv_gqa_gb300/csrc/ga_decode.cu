@@ -794,7 +794,11 @@ using CfgLocalE4m3 = DecodeCfg<256, GA_KV_E4M3, GA_LE_NCW, GA_LE_NS>;
 using CfgGlobalBf16 = DecodeCfg<512, GA_KV_BF16, GA_GB_NCW, GA_GB_NS>;
 using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, GA_GE_NS>;
 // K == V (one pool): half-size stages, twice as many.
-using CfgGlobalBf16Alias = DecodeCfg<512, GA_KV_BF16, GA_GB_NCW, 2 * GA_GB_NS, true>;
+#ifndef GA_GA_NCW
+#define GA_GA_NCW 4
+#define GA_GA_NS 12
+#endif
+using CfgGlobalBf16Alias = DecodeCfg<512, GA_KV_BF16, GA_GA_NCW, GA_GA_NS, true>;
 using CfgGlobalE4m3Alias = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, 2 * GA_GE_NS, true>;
 
 int launch_decode(const DecodeArgs& a) {

@@ -417,8 +417,10 @@ def test_nan_in_attended_kv_propagates(ga, err, split):
 
 @pytest.mark.parametrize("kv", [0, 1])
 def test_kv_alias_one_pool(ga, err, kv):
-    """k_pool is v_pool (K == V): the one-fetch kernel gives bit for bit what
-    the two-pool kernel gives on a copy, and matches the oracle with V = K."""
+    """k_pool is v_pool (K == V): the one-fetch kernel matches the two-pool
+    kernel on a copy and the oracle with V = K.  The two kernels may split a
+    chunk's pages over different numbers of consumer warps, so their merge
+    order (and the last bit) can differ; both are held to the oracle's bar."""
     fam = _fam(32, 4, 512, 0, kv=kv)
     fi = _inputs([700, 33, 1500, 1], fam, seed=17)
     fi.v_pool = fi.k_pool
@@ -432,9 +434,10 @@ def test_kv_alias_one_pool(ga, err, kv):
         two = run_decode(ga, two_fi, plan, err=err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        assert torch.equal(one, two)
-        assert_close(one.float().cpu().numpy(), oracle_decode(fi), kv_dtype=kv,
-                     what=f"alias kv={kv} {split}")
+        ref = oracle_decode(fi)
+        assert_close(one.float().cpu().numpy(), ref, kv_dtype=kv, what=f"alias kv={kv} {split}")
+        assert_close(two.float().cpu().numpy(), ref, kv_dtype=kv, what=f"copy kv={kv} {split}")
+        assert np.array_equal(np.isnan(one.float().cpu().numpy()), np.isnan(two.float().cpu().numpy()))
 
 
 def test_capacity_check(ga, err):

@@ -130,7 +130,7 @@ class ClockSampler:
 WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 
 
-def make_layer(device, wl, fam, seed, layer, kv_alias=False):
+def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0):
     import torch
     from paged_split_kv_gqa_gb300 import ga
     from paged_split_kv_gqa_gb300 import metrics as M
@@ -144,7 +144,8 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False):
         fi.v_scale = fi.k_scale
     plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
-                             window=fam.window, flags=ga.GA_PLAN_EXTERNAL_COMBINE)
+                             window=fam.window, requested_splits=splits,
+                             flags=ga.GA_PLAN_EXTERNAL_COMBINE)
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
     esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
@@ -161,10 +162,11 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False):
         keys=int(M.attended_keys(wl.seq_lens, fam.window).sum()))
 
 
-def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False):
+def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
-    layers of a family rotating over `pools` distinct KV pools (each > L2)."""
+    layers of a family rotating over `pools` distinct KV pools (each > L2).
+    splits: 0 lets the planner choose, s > 0 asks every plan for s chunks per row."""
     import torch
     from paged_split_kv_gqa_gb300 import workloads as W
 
@@ -173,7 +175,8 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False):
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
-    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias) for i in range(npool)]
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits)
+                       for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
         schedule, nl, ng = [], 0, 0
@@ -350,7 +353,7 @@ def run_ga(args):
         dist.init_process_group("nccl", device_id=device)
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
-                                         args.pools, args.kv_alias)
+                                         args.pools, args.kv_alias, args.splits)
 
     def step(evs=None):
         n = 0
@@ -430,7 +433,10 @@ def run_ga(args):
     peak, peak_kind = measured_peak_gbs()
     dom_ach = families[dominant]["decode_gbs"]
     kname = "decode_global_hd512" if dominant == "global" else "decode_local_hd256"
-    traffic = committed_traffic(kname) if args.workload == "31b" and not args.rows else None
+    # the committed counters cover the default 31B step (planner's splits, two pools)
+    default_step = (args.workload == "31b" and not args.rows and not args.splits
+                    and not args.kv_alias)
+    traffic = committed_traffic(kname) if default_step else None
 
     # ---- end to end through host buffers: H2D inputs, the C-ABI calls, D2H outputs
     e2e = None
@@ -487,7 +493,8 @@ def run_ga(args):
 
     if rank == 0:
         def plan_desc(p):
-            return {"mode": ["none", "count", "chunk"][p.mode], "chunk_pages": p.chunk_pages,
+            return {"mode": ["none", "count", "chunk"][p.mode], "splits": p.splits,
+                    "chunk_pages": p.chunk_pages,
                     "units": p.units, "grid": p.grid}
 
         text = WORKLOAD_TEXT[args.workload]
@@ -497,6 +504,8 @@ def run_ga(args):
             text += f"; {args.pools} distinct pools per family rotated over the layers"
         if args.kv_alias:
             text += "; global family with K == V (one pool, read once)"
+        if args.splits:
+            text += f"; split-KV count fixed at {args.splits} chunks per row"
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
@@ -546,6 +555,8 @@ def main():
                     help="ragged workload: distinct KV pools per family rotated over layers")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: the first N rows of the batch (not a bench line)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="split-KV chunks per row for every plan (0 = planner's choice)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -110,7 +110,7 @@ struct DecodeCfg {
     static constexpr int OFF_BARS = al(OFF_FLAGS + NS * 4);
     static constexpr int SMEM_USED = al(OFF_BARS + 2 * NS * 8);
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
-    static_assert(D % 64 == 0 && NTILES >= 1, "head_dim");
+    static_assert(D % 128 == 0 && NTILES >= 1, "head_dim (the merge takes m-tiles 8 at a time)");
     static_assert(OFF_BARS % 8 == 0 && OFF_QF % 16 == 0 && OFF_MERGE % 16 == 0, "alignment");
     static_assert(STAGE_BYTES % 1024 == 0, "swizzle-128B boxes need 1024-byte aligned stages");
     // Every ring slot must always be consumed by the same warp: page n sits in
@@ -172,6 +172,13 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
     for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
         const UnitInfo x = unit_info(p, pre, u);
         const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride;
+        // the unit's q rows (heads h0 .. h0+nvalid-1, contiguous) into L2 while
+        // the consumers still work on earlier pages
+        if (((int64_t)x.b * p.Hq + x.h0 + x.nvalid) * C::D <= p.out_elems) {
+            const char* qrow = reinterpret_cast<const char*>(
+                p.q + ((int64_t)x.b * p.Hq + x.h0) * C::D);
+            for (int l = lane; l * 128 < x.nvalid * C::D * 2; l += 32) prefetch_l2(qrow + 128 * l);
+        }
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
         // page ids of this unit, 32 at a time (the next batch loads one batch ahead)
         int32_t id_cur = (lane < x.np) ? __ldg(tbl + x.p0 + lane) : -1;
@@ -239,24 +246,58 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
 //   lo = E4M3(q' - hi); b0 = hi[n][16ks+4t .. +3], b1 = lo[n][16ks+4t .. +3],
 //   so one MMA against the K codes stacked twice yields K (hi + lo).  The
 //   scale amax_n / 448 goes to qsc[8 + n] and multiplies the scores.
+// The unit's q rows are read as 16-byte pieces (piece (n, j) = dims 8j .. 8j+7
+// of head n), all loads issued before any is used: one memory latency per
+// unit, not one per piece.
 template <class C>
 __device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInfo& x,
-                                            uint2* qf, float* qsc, int tid) {
-    if constexpr (C::KV == GA_KV_E4M3) {
+                                            uint32_t* qf, float* qsc, int tid) {
+    constexpr int D8 = C::D / 8;
+    constexpr int PIECES = kHeadTile * D8;
+    constexpr int PER = (PIECES + C::NCT - 1) / C::NCT;
+    uint4 w[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int e = tid + k * C::NCT;
+        const int n = e / D8, j = e % D8;
+        w[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < PIECES && n < x.nvalid) {
+            if (GA_CHK(((int64_t)x.b * p.Hq + x.h0 + n + 1) * C::D <= p.out_elems))
+                w[k] = __ldg(reinterpret_cast<const uint4*>(
+                    p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D + 8 * j));
+            else
+                report(p.err_word, kErrSelfCheck);
+        }
+    }
+    if constexpr (C::KV == GA_KV_BF16) {
+        // piece (n, j): ks = j/2, half = j%2 (b0 or b1), its four words go to t = 0..3
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int e = tid + k * C::NCT;
+            if (e < PIECES) {
+                const int n = e / D8, j = e % D8;
+                uint32_t* dst = qf + ((j >> 1) * 32 + n * 4) * 2 + (j & 1);
+                dst[0] = w[k].x;
+                dst[2] = w[k].y;
+                dst[4] = w[k].z;
+                dst[6] = w[k].w;
+            }
+        }
+    } else {
         unsigned* amax = reinterpret_cast<unsigned*>(qsc);
         if (tid < kHeadTile) amax[tid] = 0u;
         named_barrier(1, C::NCT);
-        constexpr int D8 = C::D / 8;
-        for (int e = tid; e < x.nvalid * D8; e += C::NCT) {
-            const int n = e / D8, d = (e % D8) * 8;
-            const uint4 w = __ldg(reinterpret_cast<const uint4*>(
-                p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D + d));
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-            float m = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
-            atomicMax(amax + n, __float_as_uint(m));      // non-negative floats order as ints
+        for (int k = 0; k < PER; ++k) {
+            const int e = tid + k * C::NCT;
+            if (e < PIECES && e / D8 < x.nvalid) {
+                const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                float m = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[i])), fabsf(bf16_hi(ww[i]))));
+                atomicMax(amax + e / D8, __float_as_uint(m));   // non-negative floats order as ints
+            }
         }
         named_barrier(1, C::NCT);
         if (tid < kHeadTile) {
@@ -265,34 +306,32 @@ __device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInf
             qsc[kHeadTile + tid] = (am > 0.f) ? am * (1.0f / 448.0f) : 1.0f;
         }
         named_barrier(1, C::NCT);
-    }
-    for (int e = tid; e < C::KSTEPS * 32; e += C::NCT) {
-        const int ks = e >> 5, ln = e & 31, n = ln >> 2, t = ln & 3;
-        uint2 v = make_uint2(0u, 0u);
-        if (n < x.nvalid && !GA_CHK(((int64_t)x.b * p.Hq + x.h0 + n + 1) * C::D <= p.out_elems)) {
-            report(p.err_word, kErrSelfCheck);
-        } else if (n < x.nvalid) {
-            const __nv_bfloat16* row = p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D;
-            if (C::KV == GA_KV_BF16) {
-                v.x = __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t));
-                v.y = __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t + 8));
-            } else {
-                const uint2 w = __ldg(reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t));
+        // piece (n, j): ks = j/2; dims 0..3 -> lane t = 2 (j%2), dims 4..7 -> t + 1
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int e = tid + k * C::NCT;
+            if (e < PIECES) {
+                const int n = e / D8, j = e % D8;
                 const float inv = 1.0f / qsc[kHeadTile + n];
-                const float f[4] = {bf16_lo(w.x) * inv, bf16_hi(w.x) * inv,
-                                    bf16_lo(w.y) * inv, bf16_hi(w.y) * inv};
-                const uint32_t h01 = f32x2_to_e4m3x2(f[0], f[1]);
-                const uint32_t h23 = f32x2_to_e4m3x2(f[2], f[3]);
-                const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
-                const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&d01));
-                const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&d23));
-                const uint32_t l01 = f32x2_to_e4m3x2(f[0] - g01.x, f[1] - g01.y);
-                const uint32_t l23 = f32x2_to_e4m3x2(f[2] - g23.x, f[3] - g23.y);
-                v.x = h01 | (h23 << 16);
-                v.y = l01 | (l23 << 16);
+                const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                uint32_t* dst = qf + ((j >> 1) * 32 + n * 4 + 2 * (j & 1)) * 2;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float f[4] = {bf16_lo(ww[2 * h]) * inv, bf16_hi(ww[2 * h]) * inv,
+                                        bf16_lo(ww[2 * h + 1]) * inv,
+                                        bf16_hi(ww[2 * h + 1]) * inv};
+                    const uint32_t h01 = f32x2_to_e4m3x2(f[0], f[1]);
+                    const uint32_t h23 = f32x2_to_e4m3x2(f[2], f[3]);
+                    const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
+                    const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&d01));
+                    const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&d23));
+                    const uint32_t l01 = f32x2_to_e4m3x2(f[0] - g01.x, f[1] - g01.y);
+                    const uint32_t l23 = f32x2_to_e4m3x2(f[2] - g23.x, f[3] - g23.y);
+                    dst[2 * h] = h01 | (h23 << 16);
+                    dst[2 * h + 1] = l01 | (l23 << 16);
+                }
             }
         }
-        qf[e] = v;
     }
 }
 
@@ -309,7 +348,8 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
     const uint32_t koff = krow * 128, kx = krow & 7;
     const uint32_t voff = vrow * 128, vx = vrow & 7;
 
-    uint2* qf = reinterpret_cast<uint2*>(smem + C::OFF_QF);
+    uint32_t* qf32 = reinterpret_cast<uint32_t*>(smem + C::OFF_QF);
+    const uint2* qf = reinterpret_cast<const uint2*>(qf32);
     float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
     float* mlw = reinterpret_cast<float*>(smem + C::OFF_ML);   // [2][NCW][8]
     float* qsc = reinterpret_cast<float*>(smem + C::OFF_QSC);  // [8] amax bits, [8] q scale
@@ -323,7 +363,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             kfac *= __ldg(p.k_scale + x.c);
             vfac = __ldg(p.v_scale + x.c);
         }
-        fill_qfrags<C>(p, x, qf, qsc, tid);
+        fill_qfrags<C>(p, x, qf32, qsc, tid);
         named_barrier(1, C::NCT);
         float kf0 = kfac, kf1 = kfac;                 // per head column (2t, 2t+1)
         if constexpr (C::KV == GA_KV_E4M3) {
@@ -578,29 +618,57 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             fac[e] = (Lt == 0.f) ? 0.f : exp2f(mown - Ms) * (vfac / (Lt * C::PSCALE));
         }
         // warps add their scaled O into one buffer in turn (fixed order:
-        // deterministic, so results do not depend on timing)
-        for (int ww = 0; ww < C::NCW; ++ww) {
-            if (w == ww) {
-                float* r0 = merge + (2 * t) * C::MSTRIDE;
-                float* r1 = r0 + C::MSTRIDE;
-                const bool c0 = 2 * t < x.nvalid, c1 = 2 * t + 1 < x.nvalid;
-                if (!GA_CHK(2 * t + 1 < kHeadTile)) report(p.err_word, kErrSelfCheck);
+        // deterministic, so results do not depend on timing).  Every lane
+        // writes both its head columns: rows of heads past the unit's valid
+        // ones are never read, and straight-line code lets the loads of a
+        // batch issue together.
+        if (!GA_CHK(2 * t + 1 < kHeadTile)) report(p.err_word, kErrSelfCheck);
+        float* r0 = merge + (2 * t) * C::MSTRIDE;
+        float* r1 = r0 + C::MSTRIDE;
+        auto dims = [](int mt, int& d0, int& d1) {
+            if constexpr (C::KV == GA_KV_BF16) {
+                d0 = 16 * mt + (threadIdx.x & 31) / 4;
+                d1 = d0 + 8;
+            } else {   // E4M3 m-tile pairs hold even / odd dims of 32-dim groups
+                d0 = 32 * (mt >> 1) + 2 * ((threadIdx.x & 31) / 4) + (mt & 1);
+                d1 = d0 + 16;
+            }
+        };
+        if (w == 0) {
 #pragma unroll
-                for (int mt = 0; mt < C::MTILES; ++mt) {
-                    int d0, d1;
-                    if constexpr (C::KV == GA_KV_BF16) {
-                        d0 = 16 * mt + gid;
-                        d1 = d0 + 8;
-                    } else {   // E4M3 m-tile pairs hold even / odd dims of 32-dim groups
-                        d0 = 32 * (mt >> 1) + 2 * gid + (mt & 1);
-                        d1 = d0 + 16;
+            for (int mt = 0; mt < C::MTILES; ++mt) {
+                int d0, d1;
+                dims(mt, d0, d1);
+                r0[d0] = o[mt][0] * fac[0];
+                r1[d0] = o[mt][1] * fac[1];
+                r0[d1] = o[mt][2] * fac[0];
+                r1[d1] = o[mt][3] * fac[1];
+            }
+        }
+        named_barrier(1, C::NCT);
+        for (int ww = 1; ww < C::NCW; ++ww) {
+            if (w == ww) {
+                constexpr int MB = 8;                  // m-tiles per batch of loads
+#pragma unroll
+                for (int m0b = 0; m0b < C::MTILES; m0b += MB) {
+                    float prev[MB][4];
+#pragma unroll
+                    for (int i = 0; i < MB; ++i) {
+                        int d0, d1;
+                        dims(m0b + i, d0, d1);
+                        prev[i][0] = r0[d0];
+                        prev[i][1] = r1[d0];
+                        prev[i][2] = r0[d1];
+                        prev[i][3] = r1[d1];
                     }
-                    if (ww == 0) {
-                        if (c0) { r0[d0] = o[mt][0] * fac[0]; r0[d1] = o[mt][2] * fac[0]; }
-                        if (c1) { r1[d0] = o[mt][1] * fac[1]; r1[d1] = o[mt][3] * fac[1]; }
-                    } else {
-                        if (c0) { r0[d0] += o[mt][0] * fac[0]; r0[d1] += o[mt][2] * fac[0]; }
-                        if (c1) { r1[d0] += o[mt][1] * fac[1]; r1[d1] += o[mt][3] * fac[1]; }
+#pragma unroll
+                    for (int i = 0; i < MB; ++i) {
+                        int d0, d1;
+                        dims(m0b + i, d0, d1);
+                        r0[d0] = prev[i][0] + o[m0b + i][0] * fac[0];
+                        r1[d0] = prev[i][1] + o[m0b + i][1] * fac[1];
+                        r0[d1] = prev[i][2] + o[m0b + i][2] * fac[0];
+                        r1[d1] = prev[i][3] + o[m0b + i][3] * fac[1];
                     }
                 }
             }

@@ -45,8 +45,8 @@ static EncodeTiledFn encode_fn() {
 // chunk column.  One box {e, 16, D*esize/128} is a whole page-head block and
 // lands in shared memory as [chunk column][key row][128 bytes] with the
 // 128-byte swizzle, i.e. one 2 KB tile per 128-byte column.
-int encode_pool_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_t rows,
-                    int32_t head_dim) {
+int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_t rows,
+                    int32_t head_dim, int32_t box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return GA_ERR_CUDA;
     const int esz = kv_dtype == GA_KV_BF16 ? 2 : 1;
@@ -54,12 +54,12 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_
     const cuuint32_t cols = (cuuint32_t)(head_dim * esz / 128);
     const cuuint64_t dims[3] = {(cuuint64_t)e, (cuuint64_t)rows, (cuuint64_t)cols};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * esz, 128};
-    const cuuint32_t box[3] = {e, (cuuint32_t)kPageSize, cols};
+    const cuuint32_t box[3] = {e, (cuuint32_t)box_rows, cols};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(map,
                            kv_dtype == GA_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                           3, const_cast<void*>(pool), dims, strides, box, estr,
+                           3, const_cast<void*>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -100,18 +100,34 @@ struct DecodeCfg {
     // shared-memory map; every region starts on a 128-byte boundary (the
     // mbarriers need 8, the float4 / uint2 accesses 16)
     static constexpr int al(int x) { return (x + 127) / 128 * 128; }
+    // The unit's q rows land as one 3-D box like a page-head block: D/64
+    // tiles of [8 heads][128 bytes], 128-byte swizzled.  The E4M3 path turns
+    // them into fragments in place (same size).
+    static constexpr int Q_BYTES = kHeadTile * D * 2;
+    // The merge buffer: one region of [8 heads][MSTRIDE] floats per consumer
+    // warp when shared memory allows (each warp writes its own, one barrier),
+    // else one region the warps add into in turn.
+    static constexpr int REGION_FLOATS = kHeadTile * MSTRIDE;
+    static constexpr int BEFORE_MERGE = al(al(NS * STAGE_BYTES) + Q_BYTES);
+    static constexpr int AFTER_MERGE = al(2 * NCW * kHeadTile * 4) + al(2 * kHeadTile * 4) +
+                                       al((kMaxBatch + 1) * 4) + al(NS * 4) + al((2 * NS + 1) * 8);
+    static constexpr int MREG =
+        (BEFORE_MERGE + al(NCW * REGION_FLOATS * 4) + AFTER_MERGE + 1024 <= 227 * 1024) ? NCW
+                                                                                        : 1;
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_QF = al(OFF_RING + NS * STAGE_BYTES);
-    static constexpr int OFF_MERGE = al(OFF_QF + KSTEPS * 32 * 8);
-    static constexpr int OFF_ML = al(OFF_MERGE + kHeadTile * MSTRIDE * 4);
+    static constexpr int OFF_Q = al(OFF_RING + NS * STAGE_BYTES);
+    static constexpr int OFF_MERGE = al(OFF_Q + Q_BYTES);
+    static constexpr int OFF_ML = al(OFF_MERGE + MREG * REGION_FLOATS * 4);
     static constexpr int OFF_QSC = al(OFF_ML + 2 * NCW * kHeadTile * 4);   // [2][8] q amax / scale
     static constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
     static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
     static constexpr int OFF_BARS = al(OFF_FLAGS + NS * 4);
-    static constexpr int SMEM_USED = al(OFF_BARS + 2 * NS * 8);
+    static constexpr int SMEM_USED = al(OFF_BARS + (2 * NS + 1) * 8);   // full, empty, q tile
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
     static_assert(D % 128 == 0 && NTILES >= 1, "head_dim (the merge takes m-tiles 8 at a time)");
-    static_assert(OFF_BARS % 8 == 0 && OFF_QF % 16 == 0 && OFF_MERGE % 16 == 0, "alignment");
+    static_assert(OFF_BARS % 8 == 0 && OFF_Q % 1024 == 0 && OFF_MERGE % 16 == 0, "alignment");
+    static_assert(KSTEPS * 32 * 8 == Q_BYTES, "E4M3 fragments reuse the q tile");
+    static_assert(REGION_FLOATS % 4 == 0 && MSTRIDE % 4 == 0, "float4 access to merge regions");
     static_assert(STAGE_BYTES % 1024 == 0, "swizzle-128B boxes need 1024-byte aligned stages");
     // Every ring slot must always be consumed by the same warp: page n sits in
     // slot n % NS and, within a unit, goes to warp n % NCW (up to the unit's
@@ -139,19 +155,55 @@ struct UnitInfo {
     RowGeom g;
 };
 
-__device__ __forceinline__ UnitInfo unit_info(const DecodeParams& p, const int32_t* pre,
-                                              int64_t u) {
+// A unit's coordinates from shared memory only; its length load can be issued
+// right after and consumed later (finish_unit), off the critical path.
+struct UnitLoc {
+    int64_t rc;
+    int32_t b, c, hg;
+};
+
+__device__ __forceinline__ UnitLoc locate_unit(const DecodeParams& p, const int32_t* pre,
+                                               int64_t u) {
+    UnitLoc l;
+    if (u < (int64_t(1) << 31)) {      // unit_coords in 32 bits (64-bit division is slow)
+        const uint32_t v = (uint32_t)u, hg = (uint32_t)p.HG, hkv = (uint32_t)p.Hkv;
+        const uint32_t q1 = (hg == 1) ? v : v / hg;
+        const uint32_t r = q1 / hkv;
+        l.hg = (int32_t)(v - q1 * hg);
+        l.c = (int32_t)(q1 - r * hkv);
+        l.rc = r;
+    } else {
+        unit_coords(u, p.Hkv, p.HG, &l.rc, &l.c, &l.hg);
+    }
+    l.b = find_row(pre, p.B, l.rc);
+    return l;
+}
+
+// First q row (in the [B * Hq, D] view) of a unit's head group.
+__device__ __forceinline__ int32_t unit_q_row(const DecodeParams& p, const UnitLoc& l) {
+    return l.b * p.Hq + l.c * p.group + l.hg * kHeadTile;
+}
+
+__device__ __forceinline__ UnitInfo finish_unit(const DecodeParams& p, const int32_t* pre,
+                                                const UnitLoc& l, int32_t len) {
     UnitInfo x;
-    unit_coords(u, p.Hkv, p.HG, &x.rc, &x.c, &x.hg);
-    x.b = find_row(pre, p.B, x.rc);
+    x.rc = l.rc;
+    x.b = l.b;
+    x.c = l.c;
+    x.hg = l.hg;
     x.j = (int32_t)(x.rc - pre[x.b]);
-    x.g = row_geometry(__ldg(p.seq_lens + x.b), p.window, p.pt_stride, p.mode, p.splits,
-                       p.chunk_pages);
+    x.g = row_geometry(len, p.window, p.pt_stride, p.mode, p.splits, p.chunk_pages);
     chunk_pages_of(x.g, x.j, &x.p0, &x.np);
     x.h0 = x.c * p.group + x.hg * kHeadTile;
     int nv = p.group - x.hg * kHeadTile;
     x.nvalid = nv < kHeadTile ? nv : kHeadTile;
     return x;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const DecodeParams& p, const int32_t* pre,
+                                              int64_t u) {
+    const UnitLoc l = locate_unit(p, pre, u);
+    return finish_unit(p, pre, l, __ldg(p.seq_lens + l.b));
 }
 
 // ------------------------------------------------------------------ producer
@@ -169,11 +221,42 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
     const uint64_t policy = l2_evict_first_policy();
     uint32_t seq = 0;                 // pages handed to the ring so far
     bool stop = false;
-    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
-        const UnitInfo x = unit_info(p, pre, u);
+    // Look-ahead: while a unit's pages are issued, the next unit's length and
+    // first page ids are already on their way, so moving to it costs no
+    // dependent global loads.
+    auto first_ids = [&](const UnitInfo& y, int32_t& a, int32_t& b) {
+        const int32_t* t = p.page_table + (int64_t)y.b * p.pt_stride + y.p0;
+        a = (lane < y.np) ? __ldg(t + lane) : -1;
+        b = (32 + lane < y.np) ? __ldg(t + 32 + lane) : -1;
+    };
+    int64_t u = blockIdx.x;
+    UnitInfo x = {};
+    int32_t id_cur = -1, id_nxt = -1;
+    if (u < U) {
+        x = unit_info(p, pre, u);
+        first_ids(x, id_cur, id_nxt);
+    }
+    while (u < U && !stop) {
+        const int64_t un = u + gridDim.x;
+        UnitLoc nl = {};
+        int32_t nlen = 0;
+        if (un < U) {
+            nl = locate_unit(p, pre, un);
+            nlen = __ldg(p.seq_lens + nl.b);
+        }
+        UnitInfo nx = x;
+        int32_t nid_cur = -1, nid_nxt = -1;
+        bool nx_ready = !(un < U);
+        auto ready_next = [&]() {
+            if (!nx_ready) {
+                nx = finish_unit(p, pre, nl, nlen);
+                first_ids(nx, nid_cur, nid_nxt);
+                nx_ready = true;
+            }
+        };
         const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride;
-        // the unit's q rows (heads h0 .. h0+nvalid-1, contiguous) into L2 while
-        // the consumers still work on earlier pages
+        // the unit's q rows (heads h0 .. h0+nvalid-1, contiguous) into L2 ahead
+        // of the consumers' bulk copy of them
         if (((int64_t)x.b * p.Hq + x.h0 + x.nvalid) * C::D <= p.out_elems) {
             const char* qrow = reinterpret_cast<const char*>(
                 p.q + ((int64_t)x.b * p.Hq + x.h0) * C::D);
@@ -181,8 +264,6 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
         }
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
         // page ids of this unit, 32 at a time (the next batch loads one batch ahead)
-        int32_t id_cur = (lane < x.np) ? __ldg(tbl + x.p0 + lane) : -1;
-        int32_t id_nxt = (32 + lane < x.np) ? __ldg(tbl + x.p0 + 32 + lane) : -1;
         for (int i0 = 0; i0 < x.np && !stop; i0 += 32) {
             const int cnt = min(32, x.np - i0);
             for (int k = 0; k < cnt && !stop; k += kIssueLanes) {
@@ -218,11 +299,17 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                         p.touch_log[x.rc * p.touch_stride + i0 + k + lane] = pid;
                 }
                 stop = __any_sync(0xffffffffu, fail);
+                ready_next();          // after the first group: its length has arrived
             }
             seq += (uint32_t)cnt;
             id_cur = id_nxt;
             id_nxt = (i0 + 64 + lane < x.np) ? __ldg(tbl + x.p0 + i0 + 64 + lane) : -1;
         }
+        ready_next();                  // a unit without pages
+        u = un;
+        x = nx;
+        id_cur = nid_cur;
+        id_nxt = nid_nxt;
     }
     // Never leave with a copy in flight into this CTA's shared memory: wait
     // for the last round each stage was armed for (already complete unless
@@ -238,20 +325,20 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
 
 // ------------------------------------------------------------------ consumer
 
-// Builds the per-lane B fragments of Q^T for one unit in shared memory:
-// qf[ks][lane] = {b0, b1}, n = lane/4 the head column, t = lane%4.
-//  bf16: b0 = q[n][16ks+2t .. +1], b1 = q[n][16ks+2t+8 .. +9] (m16n8k16).
+// B fragments of Q^T, per lane: n = lane/4 the head column, t = lane%4.
+//  bf16 (m16n8k16): b0 = q[n][16ks+2t .. +1], b1 = q[n][16ks+2t+8 .. +9],
+//   read with ldmatrix straight from the unit's q tile.
 //  E4M3 (m16n8k32, K = the 16 dims of chunk ks twice): q of head n is scaled
 //   by 448 / amax_n and split into two E4M3 parts, hi = E4M3(q') and
 //   lo = E4M3(q' - hi); b0 = hi[n][16ks+4t .. +3], b1 = lo[n][16ks+4t .. +3],
 //   so one MMA against the K codes stacked twice yields K (hi + lo).  The
 //   scale amax_n / 448 goes to qsc[8 + n] and multiplies the scores.
-// The unit's q rows are read as 16-byte pieces (piece (n, j) = dims 8j .. 8j+7
-// of head n), all loads issued before any is used: one memory latency per
-// unit, not one per piece.
+//   fill_qfrags_e4m3 writes qf[ks][lane] = {b0, b1} over the q tile itself.
+// The q tile holds piece (n, j) = dims 8j .. 8j+7 of head n at tile j/8, row
+// n, 16-byte chunk (j%8) ^ n.
 template <class C>
-__device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInfo& x,
-                                            uint32_t* qf, float* qsc, int tid) {
+__device__ __forceinline__ void fill_qfrags_e4m3(const DecodeParams& p, const UnitInfo& x,
+                                                 uint8_t* qtile, float* qsc, int tid) {
     constexpr int D8 = C::D / 8;
     constexpr int PIECES = kHeadTile * D8;
     constexpr int PER = (PIECES + C::NCT - 1) / C::NCT;
@@ -261,84 +348,66 @@ __device__ __forceinline__ void fill_qfrags(const DecodeParams& p, const UnitInf
         const int e = tid + k * C::NCT;
         const int n = e / D8, j = e % D8;
         w[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (e < PIECES && n < x.nvalid) {
-            if (GA_CHK(((int64_t)x.b * p.Hq + x.h0 + n + 1) * C::D <= p.out_elems))
-                w[k] = __ldg(reinterpret_cast<const uint4*>(
-                    p.q + ((int64_t)x.b * p.Hq + x.h0 + n) * C::D + 8 * j));
-            else
-                report(p.err_word, kErrSelfCheck);
+        if (e < PIECES && n < x.nvalid)
+            w[k] = *reinterpret_cast<const uint4*>(qtile + (j >> 3) * 1024 + n * 128 +
+                                                   (((j & 7) ^ n) << 4));
+    }
+    unsigned* amax = reinterpret_cast<unsigned*>(qsc);
+    if (tid < kHeadTile) amax[tid] = 0u;
+    named_barrier(1, C::NCT);        // also: the whole tile is read before fragments overwrite it
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int e = tid + k * C::NCT;
+        if (e < PIECES && e / D8 < x.nvalid) {
+            const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+            float m = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[i])), fabsf(bf16_hi(ww[i]))));
+            atomicMax(amax + e / D8, __float_as_uint(m));   // non-negative floats order as ints
         }
     }
-    if constexpr (C::KV == GA_KV_BF16) {
-        // piece (n, j): ks = j/2, half = j%2 (b0 or b1), its four words go to t = 0..3
+    named_barrier(1, C::NCT);
+    if (tid < kHeadTile) {
+        const float am = __uint_as_float(amax[tid]);
+        if (tid < x.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
+        qsc[kHeadTile + tid] = (am > 0.f) ? am * (1.0f / 448.0f) : 1.0f;
+    }
+    named_barrier(1, C::NCT);
+    // piece (n, j): ks = j/2; dims 0..3 -> lane t = 2 (j%2), dims 4..7 -> t + 1
+    uint32_t* qf = reinterpret_cast<uint32_t*>(qtile);
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int e = tid + k * C::NCT;
-            if (e < PIECES) {
-                const int n = e / D8, j = e % D8;
-                uint32_t* dst = qf + ((j >> 1) * 32 + n * 4) * 2 + (j & 1);
-                dst[0] = w[k].x;
-                dst[2] = w[k].y;
-                dst[4] = w[k].z;
-                dst[6] = w[k].w;
-            }
-        }
-    } else {
-        unsigned* amax = reinterpret_cast<unsigned*>(qsc);
-        if (tid < kHeadTile) amax[tid] = 0u;
-        named_barrier(1, C::NCT);
+    for (int k = 0; k < PER; ++k) {
+        const int e = tid + k * C::NCT;
+        if (e < PIECES) {
+            const int n = e / D8, j = e % D8;
+            const float inv = 1.0f / qsc[kHeadTile + n];
+            const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+            uint32_t* dst = qf + ((j >> 1) * 32 + n * 4 + 2 * (j & 1)) * 2;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int e = tid + k * C::NCT;
-            if (e < PIECES && e / D8 < x.nvalid) {
-                const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-                float m = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[i])), fabsf(bf16_hi(ww[i]))));
-                atomicMax(amax + e / D8, __float_as_uint(m));   // non-negative floats order as ints
-            }
-        }
-        named_barrier(1, C::NCT);
-        if (tid < kHeadTile) {
-            const float am = __uint_as_float(amax[tid]);
-            if (tid < x.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
-            qsc[kHeadTile + tid] = (am > 0.f) ? am * (1.0f / 448.0f) : 1.0f;
-        }
-        named_barrier(1, C::NCT);
-        // piece (n, j): ks = j/2; dims 0..3 -> lane t = 2 (j%2), dims 4..7 -> t + 1
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int e = tid + k * C::NCT;
-            if (e < PIECES) {
-                const int n = e / D8, j = e % D8;
-                const float inv = 1.0f / qsc[kHeadTile + n];
-                const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-                uint32_t* dst = qf + ((j >> 1) * 32 + n * 4 + 2 * (j & 1)) * 2;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float f[4] = {bf16_lo(ww[2 * h]) * inv, bf16_hi(ww[2 * h]) * inv,
-                                        bf16_lo(ww[2 * h + 1]) * inv,
-                                        bf16_hi(ww[2 * h + 1]) * inv};
-                    const uint32_t h01 = f32x2_to_e4m3x2(f[0], f[1]);
-                    const uint32_t h23 = f32x2_to_e4m3x2(f[2], f[3]);
-                    const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
-                    const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&d01));
-                    const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&d23));
-                    const uint32_t l01 = f32x2_to_e4m3x2(f[0] - g01.x, f[1] - g01.y);
-                    const uint32_t l23 = f32x2_to_e4m3x2(f[2] - g23.x, f[3] - g23.y);
-                    dst[2 * h] = h01 | (h23 << 16);
-                    dst[2 * h + 1] = l01 | (l23 << 16);
-                }
+            for (int h = 0; h < 2; ++h) {
+                const float f[4] = {bf16_lo(ww[2 * h]) * inv, bf16_hi(ww[2 * h]) * inv,
+                                    bf16_lo(ww[2 * h + 1]) * inv, bf16_hi(ww[2 * h + 1]) * inv};
+                const uint32_t h01 = f32x2_to_e4m3x2(f[0], f[1]);
+                const uint32_t h23 = f32x2_to_e4m3x2(f[2], f[3]);
+                const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
+                const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&d01));
+                const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&d23));
+                const uint32_t l01 = f32x2_to_e4m3x2(f[0] - g01.x, f[1] - g01.y);
+                const uint32_t l23 = f32x2_to_e4m3x2(f[2] - g23.x, f[3] - g23.y);
+                dst[2 * h] = h01 | (h23 << 16);
+                dst[2 * h + 1] = l01 | (l23 << 16);
             }
         }
     }
+    named_barrier(1, C::NCT);
 }
 
 template <class C>
-__device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
-                         uint32_t ring, uint32_t bars, volatile uint32_t* flags,
-                         volatile int* abort_flag) {
+__device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const int32_t* pre,
+                         int64_t U, uint8_t* smem, uint32_t ring, uint32_t bars,
+                         volatile uint32_t* flags, volatile int* abort_flag,
+                         volatile int* q_issued) {
     const int tid = threadIdx.x;            // 0 .. NCT-1
     const int w = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, t = lane & 3;
@@ -348,36 +417,96 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
     const uint32_t koff = krow * 128, kx = krow & 7;
     const uint32_t voff = vrow * 128, vx = vrow & 7;
 
-    uint32_t* qf32 = reinterpret_cast<uint32_t*>(smem + C::OFF_QF);
-    const uint2* qf = reinterpret_cast<const uint2*>(qf32);
+    uint8_t* qtile = smem + C::OFF_Q;
+    const uint32_t qtile_s = smem_addr(qtile);
+    const uint32_t qbar = bars + 8 * (2 * C::NS);
+    const uint2* qf = reinterpret_cast<const uint2*>(qtile);   // E4M3 fragments, over the tile
+    // ldmatrix selectors for the q tile: lanes 8m .. 8m+7 give the rows (heads)
+    // of matrix m = (k-step ks + m/2, half m%2)
+    const int qrow = lane & 7, qmat = lane >> 3;
+    auto q_addr = [&](int ks) -> uint32_t {        // fragments of k-steps ks, ks+1 (ks even)
+        const int ksi = ks + (qmat >> 1);
+        const uint32_t ch = (uint32_t)(((ksi & 3) << 1) + (qmat & 1));
+        return qtile_s + (uint32_t)(ksi >> 2) * 1024u + (uint32_t)qrow * 128u +
+               ((ch ^ (uint32_t)qrow) << 4);
+    };
+    const uint64_t qpolicy = l2_evict_last_policy();
     float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
     float* mlw = reinterpret_cast<float*>(smem + C::OFF_ML);   // [2][NCW][8]
     float* qsc = reinterpret_cast<float*>(smem + C::OFF_QSC);  // [8] amax bits, [8] q scale
 
     uint32_t seq_base = 0;
-    for (int64_t u = blockIdx.x; u < U; u += gridDim.x) {
-        const UnitInfo x = unit_info(p, pre, u);
+    uint32_t kunit = 0;                       // units done by this CTA: the q tile's phase
+    // The next unit's coordinates, length and scales, loaded one unit ahead
+    // (before the merge) so that a unit starts without a dependent load.
+    UnitLoc nl = {};
+    int32_t nlen = 0;
+    float nks = 1.0f, nvs = 1.0f;
+    auto locate_next = [&](int64_t un) {
+        nl = locate_unit(p, pre, un);
+        nlen = __ldg(p.seq_lens + nl.b);
+        if constexpr (C::KV == GA_KV_E4M3) {
+            nks = __ldg(p.k_scale + nl.c);
+            nvs = __ldg(p.v_scale + nl.c);
+        }
+    };
+    if (blockIdx.x < U) locate_next(blockIdx.x);
+    for (int64_t u = blockIdx.x; u < U; u += gridDim.x, ++kunit) {
+        const UnitInfo x = finish_unit(p, pre, nl, nlen);
         const bool single = (x.g.chunks == 1);
         float kfac = p.scale_log2, vfac = 1.0f;
         if (C::KV == GA_KV_E4M3) {
-            kfac *= __ldg(p.k_scale + x.c);
-            vfac = __ldg(p.v_scale + x.c);
+            kfac *= nks;
+            vfac = nvs;
         }
-        fill_qfrags<C>(p, x, qf32, qsc, tid);
-        named_barrier(1, C::NCT);
+        // This unit's q tile (copied during the previous unit's merge).  The
+        // wait is bounded and taken even when aborting, whenever a copy was
+        // issued: none may be left in flight into shared memory.  q_issued is
+        // CTA-uniform here (written before a merge barrier).
+        if ((kunit == 0 || *q_issued) && !mbar_wait(qbar, kunit & 1)) {
+            if (lane == 0) report(p.err_word, kErrTimeout);
+            *abort_flag = 1;
+        }
+        if constexpr (C::KV == GA_KV_E4M3) fill_qfrags_e4m3<C>(p, x, qtile, qsc, tid);
         float kf0 = kfac, kf1 = kfac;                 // per head column (2t, 2t+1)
         if constexpr (C::KV == GA_KV_E4M3) {
             kf0 *= qsc[kHeadTile + 2 * t];
             kf1 *= qsc[kHeadTile + 2 * t + 1];
         }
 
+        // Head columns past the unit's valid ones read other heads' rows of the
+        // tile (or its zero fill): their q is zeroed.
         uint32_t qr[C::Q_IN_REGS ? C::KSTEPS : 1][2];
         if constexpr (C::Q_IN_REGS) {
+            if constexpr (C::KV == GA_KV_BF16) {
+                const uint32_t keep = (gid < x.nvalid) ? 0xffffffffu : 0u;
 #pragma unroll
-            for (int ks = 0; ks < C::KSTEPS; ++ks) {
-                const uint2 v = qf[ks * 32 + lane];
-                qr[ks][0] = v.x;
-                qr[ks][1] = v.y;
+                for (int ks = 0; ks < C::KSTEPS; ks += 2) {
+                    uint32_t r[4];
+                    ldsm_x4(q_addr(ks), r);
+                    qr[ks][0] = r[0] & keep;
+                    qr[ks][1] = r[1] & keep;
+                    qr[ks + 1][0] = r[2] & keep;
+                    qr[ks + 1][1] = r[3] & keep;
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS; ++ks) {
+                    const uint2 v = qf[ks * 32 + lane];
+                    qr[ks][0] = v.x;
+                    qr[ks][1] = v.y;
+                }
+            }
+        } else if constexpr (C::KV == GA_KV_BF16) {
+            if (x.nvalid < kHeadTile) {        // unit-uniform: zero those rows of the tile once
+                constexpr int QT = C::D / 64;
+                const int nz = (kHeadTile - x.nvalid) * QT * 8;
+                for (int e = tid; e < nz; e += C::NCT) {
+                    const int n = x.nvalid + e / (QT * 8), tl = (e / 8) % QT, c = e % 8;
+                    *reinterpret_cast<uint4*>(qtile + tl * 1024 + n * 128 + c * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                named_barrier(1, C::NCT);
             }
         }
 
@@ -408,20 +537,24 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                 for (int r = 0; r < 4; ++r) sa[r][0] = sa[r][1] = sa[r][2] = sa[r][3] = 0.f;
                 if constexpr (C::KV == GA_KV_BF16) {
 #pragma unroll
-                    for (int ks = 0; ks < C::KSTEPS; ++ks) {
-                        uint32_t a[4];
-                        const uint32_t ch = (uint32_t)(((ks & 3) << 1) + khi);
-                        ldsm_x4(kb + (ks >> 2) * C::TILE_BYTES + koff + ((ch ^ kx) << 4), a);
-                        uint32_t b0, b1;
+                    for (int ks0 = 0; ks0 < C::KSTEPS; ks0 += 2) {
+                        uint32_t qb[4];
                         if constexpr (C::Q_IN_REGS) {
-                            b0 = qr[ks][0];
-                            b1 = qr[ks][1];
+                            qb[0] = qr[ks0][0];
+                            qb[1] = qr[ks0][1];
+                            qb[2] = qr[ks0 + 1][0];
+                            qb[3] = qr[ks0 + 1][1];
                         } else {
-                            const uint2 v = qf[ks * 32 + lane];
-                            b0 = v.x;
-                            b1 = v.y;
+                            ldsm_x4(q_addr(ks0), qb);
                         }
-                        mma_bf16(sa[ks & 3], a, b0, b1);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int ks = ks0 + h;
+                            uint32_t a[4];
+                            const uint32_t ch = (uint32_t)(((ks & 3) << 1) + khi);
+                            ldsm_x4(kb + (ks >> 2) * C::TILE_BYTES + koff + ((ch ^ kx) << 4), a);
+                            mma_bf16(sa[ks & 3], a, qb[2 * h], qb[2 * h + 1]);
+                        }
                     }
                 } else {
                     // K codes feed the E4M3 MMA directly: ldmatrix gives, per
@@ -587,6 +720,12 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             if (lane == 0) mbar_arrive(bars + 8 * (C::NS + slot));
         }
         seq_base += (uint32_t)x.np;
+        const int64_t un = u + gridDim.x;
+        if (un < U) locate_next(un);
+        // generic writes to the q tile (E4M3 fragments, zeroed rows) are ordered
+        // before the next bulk copy into it (reads need no proxy fence)
+        if (C::KV == GA_KV_E4M3 || (!C::Q_IN_REGS && x.nvalid < kHeadTile))
+            fence_proxy_async_shared();
 
         // ---- merge the warps' (m, l, O) in a fixed order
 #pragma unroll
@@ -601,6 +740,16 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             mlw[C::NCW * kHeadTile + w * kHeadTile + 2 * t + 1] = l1;
         }
         named_barrier(1, C::NCT);
+        // every warp is past its pages: the next unit's q tile can be fetched
+        // while the merge runs
+        if (tid == 0) {
+            const int issue = (un < U && !*abort_flag) ? 1 : 0;
+            *q_issued = issue;
+            if (issue) {
+                mbar_arrive_expect_tx(qbar, C::Q_BYTES);
+                tma_load_3d(qtile_s, tmQ, qbar, 0, unit_q_row(p, nl), 0, qpolicy);
+            }
+        }
         float fac[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -615,15 +764,29 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             const float mown = (e == 0) ? m0 : m1;
             // only an exactly empty sum means "no keys"; NaN in attended K / V
             // propagates to the output as in the definition
-            fac[e] = (Lt == 0.f) ? 0.f : exp2f(mown - Ms) * (vfac / (Lt * C::PSCALE));
+            fac[e] = (Lt == 0.f) ? 0.f : exp2f(mown - Ms) * __fdividef(vfac, Lt * C::PSCALE);
         }
-        // warps add their scaled O into one buffer in turn (fixed order:
-        // deterministic, so results do not depend on timing).  Every lane
-        // writes both its head columns: rows of heads past the unit's valid
-        // ones are never read, and straight-line code lets the loads of a
-        // batch issue together.
+        // natural-log LSE of the chunk's scaled scores for head tid (read here:
+        // the next unit may overwrite the per-warp (m, l) once past the merge)
+        float lse = -CUDART_INF_F;
+        if (!single && tid < x.nvalid) {
+            float M = -CUDART_INF_F;
+            for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, mlw[ww * kHeadTile + tid]);
+            const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
+            float Lt = 0.f;
+            for (int ww = 0; ww < C::NCW; ++ww)
+                Lt += mlw[C::NCW * kHeadTile + ww * kHeadTile + tid] *
+                      exp2f(mlw[ww * kHeadTile + tid] - Ms);
+            lse = (Lt == 0.f) ? -CUDART_INF_F : (Ms + log2f(Lt)) * CUDART_LN2_F;
+        }
+        // Each warp's scaled O goes to its own region, summed in warp order by
+        // the output loop; with one shared region the warps add into it in
+        // turn.  Either way the order is fixed: deterministic results.  Every
+        // lane writes both its head columns: rows of heads past the unit's
+        // valid ones are never read, and straight-line code lets the loads of
+        // a batch issue together.
         if (!GA_CHK(2 * t + 1 < kHeadTile)) report(p.err_word, kErrSelfCheck);
-        float* r0 = merge + (2 * t) * C::MSTRIDE;
+        float* r0 = merge + (C::MREG > 1 ? w * C::REGION_FLOATS : 0) + (2 * t) * C::MSTRIDE;
         float* r1 = r0 + C::MSTRIDE;
         auto dims = [](int mt, int& d0, int& d1) {
             if constexpr (C::KV == GA_KV_BF16) {
@@ -634,7 +797,7 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                 d1 = d0 + 16;
             }
         };
-        if (w == 0) {
+        if constexpr (C::MREG > 1) {
 #pragma unroll
             for (int mt = 0; mt < C::MTILES; ++mt) {
                 int d0, d1;
@@ -644,42 +807,61 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
                 r0[d1] = o[mt][2] * fac[0];
                 r1[d1] = o[mt][3] * fac[1];
             }
-        }
-        named_barrier(1, C::NCT);
-        for (int ww = 1; ww < C::NCW; ++ww) {
-            if (w == ww) {
-                constexpr int MB = 8;                  // m-tiles per batch of loads
+            named_barrier(1, C::NCT);
+        } else {
+            if (w == 0) {
 #pragma unroll
-                for (int m0b = 0; m0b < C::MTILES; m0b += MB) {
-                    float prev[MB][4];
-#pragma unroll
-                    for (int i = 0; i < MB; ++i) {
-                        int d0, d1;
-                        dims(m0b + i, d0, d1);
-                        prev[i][0] = r0[d0];
-                        prev[i][1] = r1[d0];
-                        prev[i][2] = r0[d1];
-                        prev[i][3] = r1[d1];
-                    }
-#pragma unroll
-                    for (int i = 0; i < MB; ++i) {
-                        int d0, d1;
-                        dims(m0b + i, d0, d1);
-                        r0[d0] = prev[i][0] + o[m0b + i][0] * fac[0];
-                        r1[d0] = prev[i][1] + o[m0b + i][1] * fac[1];
-                        r0[d1] = prev[i][2] + o[m0b + i][2] * fac[0];
-                        r1[d1] = prev[i][3] + o[m0b + i][3] * fac[1];
-                    }
+                for (int mt = 0; mt < C::MTILES; ++mt) {
+                    int d0, d1;
+                    dims(mt, d0, d1);
+                    r0[d0] = o[mt][0] * fac[0];
+                    r1[d0] = o[mt][1] * fac[1];
+                    r0[d1] = o[mt][2] * fac[0];
+                    r1[d1] = o[mt][3] * fac[1];
                 }
             }
             named_barrier(1, C::NCT);
+            for (int ww = 1; ww < C::NCW; ++ww) {
+                if (w == ww) {
+                    constexpr int MB = 8;
+#pragma unroll
+                    for (int m0b = 0; m0b < C::MTILES; m0b += MB) {
+                        float prev[MB][4];
+#pragma unroll
+                        for (int i = 0; i < MB; ++i) {
+                            int d0, d1;
+                            dims(m0b + i, d0, d1);
+                            prev[i][0] = r0[d0];
+                            prev[i][1] = r1[d0];
+                            prev[i][2] = r0[d1];
+                            prev[i][3] = r1[d1];
+                        }
+#pragma unroll
+                        for (int i = 0; i < MB; ++i) {
+                            int d0, d1;
+                            dims(m0b + i, d0, d1);
+                            r0[d0] = prev[i][0] + o[m0b + i][0] * fac[0];
+                            r1[d0] = prev[i][1] + o[m0b + i][1] * fac[1];
+                            r0[d1] = prev[i][2] + o[m0b + i][2] * fac[0];
+                            r1[d1] = prev[i][3] + o[m0b + i][3] * fac[1];
+                        }
+                    }
+                }
+                named_barrier(1, C::NCT);
+            }
         }
         constexpr int D8 = C::D / 8;
         for (int e = tid; e < x.nvalid * D8; e += C::NCT) {
             const int n = e / D8, d = (e % D8) * 8;
             const float4* src = reinterpret_cast<const float4*>(merge + n * C::MSTRIDE + d);
-            const float4 a = src[0], b = src[1];
-            const float acc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float4 a = src[0], b = src[1];
+#pragma unroll
+            for (int r = 1; r < C::MREG; ++r) {
+                const float4* sr = src + r * (C::REGION_FLOATS / 4);
+                const float4 ar = sr[0], br = sr[1];
+                a.x += ar.x; a.y += ar.y; a.z += ar.z; a.w += ar.w;
+                b.x += br.x; b.y += br.y; b.z += br.z; b.w += br.w;
+            }
             const int h = x.h0 + n;
             if (!GA_CHK(((int64_t)x.b * p.Hq + h) * C::D + d + 8 <= p.out_elems &&
                         (single || (x.rc < p.rc_capacity && p.partial_o != nullptr)))) {
@@ -688,30 +870,20 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
             }
             if (single) {
                 uint4 v;
-                v.x = pack_bf16x2(acc[0], acc[1]);
-                v.y = pack_bf16x2(acc[2], acc[3]);
-                v.z = pack_bf16x2(acc[4], acc[5]);
-                v.w = pack_bf16x2(acc[6], acc[7]);
+                v.x = pack_bf16x2(a.x, a.y);
+                v.y = pack_bf16x2(a.z, a.w);
+                v.z = pack_bf16x2(b.x, b.y);
+                v.w = pack_bf16x2(b.z, b.w);
                 *reinterpret_cast<uint4*>(p.out + ((int64_t)x.b * p.Hq + h) * C::D + d) = v;
             } else {
                 float4* dst = reinterpret_cast<float4*>(
                     p.partial_o + (x.rc * p.Hq + h) * (int64_t)C::D + d);
-                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                dst[0] = a;
+                dst[1] = b;
             }
         }
-        if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity)) {
-            float M = -CUDART_INF_F;
-            for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, mlw[ww * kHeadTile + tid]);
-            const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
-            float Lt = 0.f;
-            for (int ww = 0; ww < C::NCW; ++ww)
-                Lt += mlw[C::NCW * kHeadTile + ww * kHeadTile + tid] *
-                      exp2f(mlw[ww * kHeadTile + tid] - Ms);
-            // natural-log LSE of the chunk's scaled scores
-            p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
-                (Lt == 0.f) ? -CUDART_INF_F : (Ms + log2f(Lt)) * CUDART_LN2_F;
-        }
+        if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity))
+            p.partial_lse[x.rc * p.Hq + x.h0 + tid] = lse;
     }
 }
 
@@ -719,10 +891,11 @@ __device__ void consumer(const DecodeParams& p, const int32_t* pre, int64_t U, u
 
 template <class C>
 __global__ void __launch_bounds__(C::NTHREADS, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmQ, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
+    __shared__ int q_issued;          // the q tile of the next unit was requested
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -736,12 +909,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             mbar_init(bars + 8 * s, 1);
             mbar_init(bars + 8 * (C::NS + s), 1);
         }
+        mbar_init(bars + 8 * (2 * C::NS), 1);      // q tile
         mbar_init_fence();
         abort_flag = 0;
     }
     if (warp == C::NCW && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmQ);
     }
     // chunk count of every row, then an inclusive prefix: pre[b+1] = sum_{b'<=b}
     int bad = 0;
@@ -778,10 +953,16 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         return;
     }
     const int64_t U = total_rc * p.Hkv * p.HG;
+    // the first unit's q tile; later ones are fetched during each merge
+    if (threadIdx.x == 0 && (int64_t)blockIdx.x < U) {
+        mbar_arrive_expect_tx(bars + 8 * (2 * C::NS), C::Q_BYTES);
+        tma_load_3d(smem_addr(smem + C::OFF_Q), &tmQ, bars + 8 * (2 * C::NS), 0,
+                    unit_q_row(p, locate_unit(p, pre, blockIdx.x)), 0, l2_evict_last_policy());
+    }
     if (warp == C::NCW)
         producer<C>(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
     else
-        consumer<C>(p, pre, U, smem, ring, bars, flags, &abort_flag);
+        consumer<C>(&tmQ, p, pre, U, smem, ring, bars, flags, &abort_flag, &q_issued);
 }
 
 // ------------------------------------------------------------------ host
@@ -793,10 +974,15 @@ static int run(const DecodeArgs& a, int slot) {
     if (rc != GA_OK) return rc;
     const ga_plan& pl = *a.plan;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
-    CUtensorMap tmK, tmV;
-    rc = encode_pool_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim);
+    CUtensorMap tmK, tmV, tmQ;
+    rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize);
     if (rc != GA_OK) return rc;
-    rc = encode_pool_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim);
+    rc = encode_rows_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim, kPageSize);
+    if (rc != GA_OK) return rc;
+    // q as [B * Hq, D] bf16, boxes of one head group (8 rows; rows past the
+    // end read as zeros)
+    rc = encode_rows_map(&tmQ, a.q, GA_KV_BF16, (int64_t)a.batch * a.num_q_heads, a.head_dim,
+                         kHeadTile);
     if (rc != GA_OK) return rc;
 
     DecodeParams p;
@@ -831,7 +1017,7 @@ static int run(const DecodeArgs& a, int slot) {
     p.pool_rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
     p.out_elems = (int64_t)a.batch * a.num_q_heads * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    decode_kernel<C><<<grid, C::NTHREADS, C::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
+    decode_kernel<C><<<grid, C::NTHREADS, C::SMEM_BYTES, a.stream>>>(tmK, tmV, tmQ, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
     if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,

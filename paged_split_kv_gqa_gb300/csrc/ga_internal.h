@@ -35,10 +35,11 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
-// Builds a 2-D tensor map over a pool viewed as [num_pages * Hkv * P, D]
-// elements with 128-byte swizzled boxes of [P rows, 128 bytes].
-int encode_pool_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_t rows,
-                    int32_t head_dim);
+// Builds a 3-D tensor map over a row-major [rows, D] array (a KV pool as
+// [num_pages * Hkv * P, D], or q as [B * Hq, D]) whose box is box_rows rows:
+// D * elem / 128 tiles of [box_rows][128 bytes], 128-byte swizzled.
+int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_t rows,
+                    int32_t head_dim, int32_t box_rows);
 
 int launch_decode(const DecodeArgs& a);
 

@@ -1032,8 +1032,8 @@ static int run(const DecodeArgs& a, int slot) {
 #define GA_LB_NS 12
 #endif
 #ifndef GA_LE_NCW
-#define GA_LE_NCW 4
-#define GA_LE_NS 24
+#define GA_LE_NCW 7
+#define GA_LE_NS 14
 #endif
 #ifndef GA_GB_NCW
 #define GA_GB_NCW 2

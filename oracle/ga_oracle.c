@@ -29,6 +29,16 @@
  *              sum_s e^{lse_s - M}, M = max_s lse_s, empty chunks (lse = -inf)
  *              weigh nothing ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa
  *              is mandatory here": flash-decode with split factor 8).
+ *   multi-query decode -- S query tokens per row, the last S positions of the
+ *              row: query i (0 <= i < S) sits at position p_i = L_b - S + i
+ *              and attends exactly the keys a one-query decode of a row of
+ *              length p_i + 1 would: causal inside the chunk, and for the
+ *              sliding family the window ends at its own position
+ *              ("visible-cx/Gemma-4-31B-CoreAI", hybrid-pf64/ bundles: the prefill entry has
+ *              a query axis with an intra-chunk causal mask, and the chunk
+ *              parity gate -- chunked and token-by-token walks must agree;
+ *              "Gemma 4 31B on vLLM", LIGHT recipe: EAGLE3 verify of 3
+ *              speculative tokens).  A query with p_i < 0 attends nothing.
  *   append  -- writes token position pos_b into page page_table[b][pos_b / P],
  *              slot pos_b % P, for every kv head; the fp8 pool stores
  *              E4M3FN(RNE, saturate-to-finite)(fp32(x) / scale[c])
@@ -45,6 +55,7 @@
  *   page_table  [B, pt_stride]         int32
  *   seq_lens    [B]                    int32 (keys attended end at L_b - 1)
  *   out         [nrows, Hq, D]         double
+ *   multi-query: q [B, Hq, S, D], out [B, Hq, S, D], lse [B, Hq, S]
  *
  * Return value: 0 on success, a negative number for an argument the
  * definition cannot evaluate (bad page id, length beyond the table, ...).
@@ -291,6 +302,73 @@ int oracle_decode(const uint16_t* q, const void* k_pool, const void* v_pool, int
             if (lse_out) lse_out[(int64_t)r * Hq + h] = lse;
         }
         free(K); free(V); free(s); free(qd);
+    }
+    return status;
+}
+
+/*
+ * Multi-query decode: S query tokens per row at positions L_b - S .. L_b - 1.
+ * q [B, Hq, S, D] bf16; out [B, Hq, S, D]; lse_out [B, Hq, S] (may be NULL).
+ * Query i of row b is the one-query decode of a row of length L_b - S + i + 1
+ * over the same pages.
+ */
+int oracle_decode_mq(const uint16_t* q, const void* k_pool, const void* v_pool, int kv_dtype,
+                     const float* k_scale, const float* v_scale,
+                     const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                     int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t W, int32_t P,
+                     int64_t num_pages, int32_t S, double scale, double* out,
+                     double* lse_out, int32_t nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || S <= 0) return -1;
+    if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_E4M3) return -1;
+    pool_view pv = {k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride,
+                    Hkv, D, P, num_pages};
+    const int32_t g = Hq / Hkv;
+    int status = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t unit = 0; unit < (int64_t)B * Hkv; ++unit) {
+        int32_t b = (int32_t)(unit / Hkv);
+        int32_t c = (int32_t)(unit % Hkv);
+        int32_t L = seq_lens[b];
+        /* keys any of the S queries attends: from the first query's window
+           start to the last query's position */
+        int32_t lo0, hi0, loS, hiS;
+        oracle_key_range(L - S + 1, W, &lo0, &hi0);
+        oracle_key_range(L, W, &loS, &hiS);
+        int32_t glo = lo0, ghi = hiS;
+        int64_t n = ghi > glo ? ghi - glo : 0;
+        double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
+        double* sbuf = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        double* qd = (double*)malloc(sizeof(double) * D);
+        int rc = n > 0 ? gather(&pv, b, c, glo, ghi, K, V) : 0;
+        if (rc) {
+#pragma omp atomic write
+            status = rc;
+        }
+        for (int32_t hj = 0; hj < g && rc == 0; ++hj) {
+            int32_t h = c * g + hj;
+            for (int32_t i = 0; i < S; ++i) {
+                int64_t row = ((int64_t)b * Hq + h) * S + i;
+                for (int32_t d = 0; d < D; ++d)
+                    qd[d] = oracle_bf16_to_double(q[row * D + d]);
+                /* query i: the keys of a one-query row of length L - S + i + 1 */
+                int32_t lo, hi;
+                oracle_key_range(L - S + i + 1, W, &lo, &hi);
+                double lse;
+                if (hi <= lo) {
+                    for (int32_t d = 0; d < D; ++d) out[row * D + d] = 0.0;
+                    lse = -INFINITY;
+                } else {
+                    lse = attend(qd, K + (int64_t)(lo - glo) * D, V + (int64_t)(lo - glo) * D,
+                                 hi - lo, D, scale, sbuf, out + row * D);
+                }
+                if (lse_out) lse_out[row] = lse;
+            }
+        }
+        free(K); free(V); free(sbuf); free(qd);
     }
     return status;
 }

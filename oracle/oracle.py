@@ -84,6 +84,10 @@ def lib():
                                         c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_d,
                                         c_p, c_i32, c_i32, c_p, c_p, c_i32]
             L.oracle_decode.restype = ctypes.c_int
+            L.oracle_decode_mq.argtypes = [c_p, c_p, c_p, ctypes.c_int, c_p, c_p, c_p, c_i64,
+                                           c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                           c_i64, c_i32, c_d, c_p, c_p, c_i32]
+            L.oracle_decode_mq.restype = ctypes.c_int
             L.oracle_combine.argtypes = [c_p, c_p, c_i32, c_i32, c_p]
             L.oracle_combine.restype = c_d
             L.oracle_kv_append.argtypes = [c_p, c_p, c_p, c_p, ctypes.c_int, c_p, c_p, c_p, c_i64,
@@ -190,6 +194,37 @@ def decode(q, k_pool, v_pool, page_table, seq_lens, *, num_kv_heads, window, sca
     return (out, lse) if return_lse else out
 
 
+def decode_mq(q, k_pool, v_pool, page_table, seq_lens, *, num_kv_heads, window, scale,
+              kv_dtype=KV_BF16, k_scale=None, v_scale=None, nthreads=0, return_lse=False):
+    """O1 multi-query decode: q [B, Hq, S, D] bf16 -> out [B, Hq, S, D] float64.
+
+    Query i of row b sits at position L_b - S + i and attends the keys of a
+    one-query row of length L_b - S + i + 1 (causal inside the chunk; the
+    sliding window ends at its own position).
+    """
+    qn = _np(q)
+    assert qn.dtype == np.uint16 and qn.ndim == 4
+    B, Hq, S, D = qn.shape
+    kp, vp = _np(k_pool), _np(v_pool)
+    num_pages, Hkv, P, D2 = kp.shape
+    assert D2 == D and Hkv == num_kv_heads and vp.shape == kp.shape
+    assert kp.dtype == (np.uint16 if kv_dtype == KV_BF16 else np.uint8)
+    pt = _np(page_table, np.int32)
+    sl = _np(seq_lens, np.int32)
+    ks = _np(k_scale, np.float32) if k_scale is not None else None
+    vs = _np(v_scale, np.float32) if v_scale is not None else None
+    if kv_dtype == KV_E4M3:
+        assert ks is not None and vs is not None
+    out = np.zeros((B, Hq, S, D), dtype=np.float64)
+    lse = np.zeros((B, Hq, S), dtype=np.float64)
+    rc = lib().oracle_decode_mq(_ptr(qn), _ptr(kp), _ptr(vp), kv_dtype, _ptr(ks), _ptr(vs),
+                                _ptr(pt), pt.shape[1], _ptr(sl), B, Hq, Hkv, D, int(window), P,
+                                num_pages, S, float(scale), _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_mq: invalid input (code {rc})")
+    return (out, lse) if return_lse else out
+
+
 def combine(partial_o, partial_lse):
     """LSE merge of S partials: partial_o [S, D], partial_lse [S] -> (o [D], lse)."""
     po = np.ascontiguousarray(partial_o, dtype=np.float64)
@@ -269,6 +304,45 @@ def brute_decode(q, k_pool, v_pool, page_table, seq_lens, *, num_kv_heads, windo
             s = np.where(mask, s, -np.inf)
             w = np.exp(s - s.max())
             out[b, h] = (w[:, None] * V).sum(0) / w.sum()
+    return out
+
+
+def brute_decode_mq(q, k_pool, v_pool, page_table, seq_lens, *, num_kv_heads, window, scale):
+    """O2 multi-query (bf16 pools, tiny inputs): q [B, Hq, S, D] -> [B, Hq, S, D].
+
+    The whole row 0..L-1 is materialised; query i at position t = L - S + i
+    keeps key j iff j <= t (causal) and t - j < window (sliding family).
+    """
+    qn = bf16_bits_to_f64(_np(q))
+    kp, vp = _np(k_pool), _np(v_pool)
+    num_pages, Hkv, P, D = kp.shape
+    Kf, Vf = bf16_bits_to_f64(kp), bf16_bits_to_f64(vp)
+    pt = _np(page_table, np.int64)
+    sl = _np(seq_lens, np.int64)
+    B, Hq, S, _ = qn.shape
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, S, D), dtype=np.float64)
+    for b in range(B):
+        L = int(sl[b])
+        if L <= 0:
+            continue
+        pos = np.arange(L)
+        phys = pt[b, pos // P]
+        slot = pos % P
+        for h in range(Hq):
+            c = h // g
+            K = Kf[phys, c, slot, :]
+            V = Vf[phys, c, slot, :]
+            for i in range(S):
+                t = L - S + i
+                mask = pos <= t
+                if window > 0:
+                    mask &= (t - pos) < window
+                if not mask.any():
+                    continue
+                s = np.where(mask, scale * (K @ qn[b, h, i]), -np.inf)
+                w = np.exp(s - s.max())
+                out[b, h, i] = (w[:, None] * V).sum(0) / w.sum()
     return out
 
 

@@ -130,14 +130,31 @@ class ClockSampler:
 WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 
 
-def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0):
+def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1):
+    """One layer's inputs.  q_len > 1: a multi-query step (q_len new tokens
+    per row at its last positions, e.g. a speculative-decoding verify): the
+    pools keep the union of the queries' windows, q / out are
+    [B, Hq, q_len, D] and q_len tokens are appended per row."""
+    import dataclasses
+
     import torch
     from paged_split_kv_gqa_gb300 import ga
     from paged_split_kv_gqa_gb300 import metrics as M
     from paged_split_kv_gqa_gb300 import workloads as W
 
-    fi = W.make_family_inputs(wl, fam, device=device, seed=seed, layer=layer,
+    S = q_len
+    alloc = fam if S == 1 else dataclasses.replace(fam, window=M.union_window(fam.window, S))
+    fi = W.make_family_inputs(wl, alloc, device=device, seed=seed, layer=layer,
                               release_old=(fam.window > 0))
+    if S == 1:
+        q, kn, vn = fi.q, fi.k_new[None], fi.v_new[None]
+    else:
+        g = torch.Generator().manual_seed(seed * 7919 + layer * 31 + 5)
+        B, Hq, D = fi.q.shape
+        q = torch.randn(B, Hq, S, D, generator=g).to(torch.bfloat16).to(device)
+        kn = torch.randn((S,) + tuple(fi.k_new.shape), generator=g).to(torch.bfloat16).to(device)
+        vn = torch.randn((S,) + tuple(fi.v_new.shape), generator=g).to(torch.bfloat16).to(device)
+    pos = torch.stack([fi.seq_lens - S + i for i in range(S)]).to(torch.int32).contiguous()
     alias = kv_alias and fam.window == 0
     if alias:                      # K == V: one pool serves both (global family)
         fi.v_pool = fi.k_pool
@@ -145,24 +162,24 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0):
     plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                              window=fam.window, requested_splits=splits,
-                             flags=ga.GA_PLAN_EXTERNAL_COMBINE)
+                             flags=ga.GA_PLAN_EXTERNAL_COMBINE, q_len=S)
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
     esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
     return dict(
-        fam=fam, fi=fi, plan=plan, ws=ws, po=po, plse=plse,
-        out=torch.empty_like(fi.q), pos=(fi.seq_lens - 1).contiguous(),
-        scale=1.0 / math.sqrt(fam.head_dim),
+        fam=fam, fi=fi, plan=plan, ws=ws, po=po, plse=plse, q=q, kn=kn, vn=vn, pos=pos,
+        out=torch.empty_like(q), scale=1.0 / math.sqrt(fam.head_dim),
         bytes=M.decode_bytes(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                              window=fam.window, page_size=wl.page_size, kv_bytes_per_elem=esz,
-                             kv_alias=alias),
-        append_bytes=M.append_bytes(wl.batch, num_kv_heads=fam.num_kv_heads,
-                                    head_dim=fam.head_dim, kv_bytes_per_elem=esz),
-        keys=int(M.attended_keys(wl.seq_lens, fam.window).sum()))
+                             kv_alias=alias, q_len=S),
+        append_bytes=S * M.append_bytes(wl.batch, num_kv_heads=fam.num_kv_heads,
+                                        head_dim=fam.head_dim, kv_bytes_per_elem=esz),
+        keys=int(M.attended_keys(wl.seq_lens, M.union_window(fam.window, S)).sum()))
 
 
-def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0):
+def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
+               q_len=1):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -175,7 +192,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
-    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits)
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len)
                        for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
@@ -195,20 +212,23 @@ def launch_layer(ga, f, err, events=None):
     """append + decode (+ combine) of one layer on the current stream.
     Returns the number of kernels launched."""
     fi, fam, plan = f["fi"], f["fam"], f["plan"]
-    ga.ga_kv_append(fi.k_new, fi.v_new, fi.k_pool, fi.v_pool, fi.page_table, f["pos"],
-                    k_scale=fi.k_scale, v_scale=fi.v_scale, err_word=err)
+    S = f["kn"].shape[0]
+    for i in range(S):                 # this step's new token(s) of every row
+        ga.ga_kv_append(f["kn"][i], f["vn"][i], fi.k_pool, fi.v_pool, fi.page_table, f["pos"][i],
+                        k_scale=fi.k_scale, v_scale=fi.v_scale, err_word=err)
     kw = dict(scale=f["scale"], plan=plan, workspace=f["ws"], out=f["out"], k_scale=fi.k_scale,
               v_scale=fi.v_scale, err_word=err)
     if events is not None:
         events[0].record()
     if fam.window > 0:
-        ga.ga_decode_local_hd256(fi.q, fi.k_pool, fi.v_pool, fi.page_table, fi.seq_lens,
+        ga.ga_decode_local_hd256(f["q"], fi.k_pool, fi.v_pool, fi.page_table, fi.seq_lens,
                                  window=fam.window, **kw)
     else:
-        ga.ga_decode_global_hd512(fi.q, fi.k_pool, fi.v_pool, fi.page_table, fi.seq_lens, **kw)
+        ga.ga_decode_global_hd512(f["q"], fi.k_pool, fi.v_pool, fi.page_table, fi.seq_lens,
+                                  **kw)
     if events is not None:
         events[1].record()
-    n = 2
+    n = S + 1
     if plan.mode != ga.GA_SPLIT_NONE:
         ga.ga_splitkv_combine(f["po"], f["plse"], plan, fi.seq_lens, fi.page_table.shape[1],
                               f["out"], err_word=err)
@@ -223,10 +243,11 @@ def oracle_sample(fams_cpu):
     from oracle import oracle as O
     t0 = time.perf_counter()
     for f in fams_cpu:
-        O.decode(f.q, f.k_pool, f.v_pool, f.page_table, f.seq_lens,
-                 num_kv_heads=f.family.num_kv_heads, window=f.family.window,
-                 scale=1.0 / math.sqrt(f.family.head_dim), kv_dtype=f.family.kv_dtype,
-                 k_scale=f.k_scale, v_scale=f.v_scale)
+        fn = O.decode_mq if f.q.dim() == 4 else O.decode      # [B, Hq, S, D]: S queries
+        fn(f.q, f.k_pool, f.v_pool, f.page_table, f.seq_lens,
+           num_kv_heads=f.family.num_kv_heads, window=f.family.window,
+           scale=1.0 / math.sqrt(f.family.head_dim), kv_dtype=f.family.kv_dtype,
+           k_scale=f.k_scale, v_scale=f.v_scale)
     return time.perf_counter() - t0
 
 
@@ -260,7 +281,10 @@ def gather_rows_to_host(layer, nrows):
     remap[used] = np.arange(len(used))
     sub = np.where(table >= 0, remap[np.maximum(table, 0)], -1).astype(np.int32)
     idx = torch.as_tensor(used, device=fi.k_pool.device)
-    return W.FamilyInputs(fi.family, fi.q[:nrows].cpu(), fi.k_pool.index_select(0, idx).cpu(),
+    q = layer["q"][:nrows].cpu()
+    if q.dim() == 4 and q.shape[2] == 1:
+        q = q[:, :, 0].contiguous()
+    return W.FamilyInputs(layer["fam"], q, fi.k_pool.index_select(0, idx).cpu(),
                           fi.v_pool.index_select(0, idx).cpu(),
                           None if fi.k_scale is None else fi.k_scale.cpu(),
                           None if fi.v_scale is None else fi.v_scale.cpu(),
@@ -286,7 +310,8 @@ def run_cpu_baseline(sets, batch, target_s=10.0):
     nbytes = sum(M.decode_bytes(lens, num_q_heads=f.family.num_q_heads,
                                 num_kv_heads=f.family.num_kv_heads, head_dim=f.family.head_dim,
                                 window=f.family.window, page_size=16,
-                                kv_bytes_per_elem=1 if f.family.kv_dtype == W.KV_E4M3 else 2)
+                                kv_bytes_per_elem=1 if f.family.kv_dtype == W.KV_E4M3 else 2,
+                                q_len=f.q.shape[2] if f.q.dim() == 4 else 1)
                  for f in fams)
     return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": O.max_threads(), "kind": "oracle",
             "sample": f"first {nrows} of {batch} rows of the bench batch, one layer per family, "
@@ -353,7 +378,7 @@ def run_ga(args):
         dist.init_process_group("nccl", device_id=device)
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
-                                         args.pools, args.kv_alias, args.splits)
+                                         args.pools, args.kv_alias, args.splits, args.q_len)
 
     def step(evs=None):
         n = 0
@@ -435,7 +460,7 @@ def run_ga(args):
     kname = "decode_global_hd512" if dominant == "global" else "decode_local_hd256"
     # the committed counters cover the default 31B step (planner's splits, two pools)
     default_step = (args.workload == "31b" and not args.rows and not args.splits
-                    and not args.kv_alias)
+                    and not args.kv_alias and args.q_len == 1)
     traffic = committed_traffic(kname) if default_step else None
 
     # ---- end to end through host buffers: H2D inputs, the C-ABI calls, D2H outputs
@@ -445,9 +470,8 @@ def run_ga(args):
         uniq = [layer for fam_layers in sets.values() for layer in fam_layers]
         for layer in uniq:
             fi = layer["fi"]
-            h = {k: getattr(fi, k).cpu().pin_memory() for k in ("q", "k_new", "v_new",
-                                                                  "seq_lens")}
-            h["pos"] = layer["pos"].cpu().pin_memory()
+            h = {k: layer[k].cpu().pin_memory() for k in ("q", "kn", "vn", "pos")}
+            h["seq_lens"] = fi.seq_lens.cpu().pin_memory()
             h["out"] = torch.empty_like(layer["out"], device="cpu").pin_memory()
             host[id(layer)] = h
         h2d = sum(t.numel() * t.element_size() for layer in schedule
@@ -458,11 +482,9 @@ def run_ga(args):
             n = 0
             for layer in schedule:
                 fi, h = layer["fi"], host[id(layer)]
-                fi.q.copy_(h["q"], non_blocking=True)
-                fi.k_new.copy_(h["k_new"], non_blocking=True)
-                fi.v_new.copy_(h["v_new"], non_blocking=True)
+                for k in ("q", "kn", "vn", "pos"):
+                    layer[k].copy_(h[k], non_blocking=True)
                 fi.seq_lens.copy_(h["seq_lens"], non_blocking=True)
-                layer["pos"].copy_(h["pos"], non_blocking=True)
                 n += launch_layer(ga, layer, err)
                 h["out"].copy_(layer["out"], non_blocking=True)
             return n
@@ -506,6 +528,9 @@ def run_ga(args):
             text += "; global family with K == V (one pool, read once)"
         if args.splits:
             text += f"; split-KV count fixed at {args.splits} chunks per row"
+        if args.q_len > 1:
+            text += (f"; {args.q_len} query tokens per row at its last positions (causal "
+                     f"within the chunk), {args.q_len} appends per row and layer")
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
@@ -557,6 +582,8 @@ def main():
                     help="profiling only: the first N rows of the batch (not a bench line)")
     ap.add_argument("--splits", type=int, default=0,
                     help="split-KV chunks per row for every plan (0 = planner's choice)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per row (> 1: a multi-query / speculative-verify step)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -23,7 +23,7 @@
  *     synchronises.  Work is enqueued on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and returns before it runs.
  *   - Layouts are dense, row-major (C order):
- *       q, out      [B, Hq, D]            bf16
+ *       q, out      [B, Hq, D]            bf16  ([B, Hq, S, D] for S-query decode)
  *       k_new,v_new [B, Hkv, D]           bf16
  *       pools       [num_pages, Hkv, P, D] bf16 (GA_KV_BF16) or OCP E4M3FN
  *                   codes (GA_KV_E4M3), one page-head block of P*D elements
@@ -115,6 +115,8 @@ typedef struct ga_plan {
     int32_t grid;            /* CTAs the decode launch uses */
     int32_t flags;           /* GA_PLAN_* */
     int32_t touch_stride;    /* touch-log entries per row-chunk (flag set) */
+    int32_t q_len;           /* query tokens per row S (1 = one-query decode) */
+    int32_t reserved;        /* 0 */
     int64_t row_chunks;      /* (row, chunk) pairs the workspace holds */
     int64_t units;           /* work units (row-chunk x kv head x head group) planned */
     int64_t workspace_bytes; /* device workspace the decode call needs (0 if none) */
@@ -147,6 +149,24 @@ int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_he
                    int32_t num_kv_heads, int32_t head_dim, int32_t window, int32_t page_size,
                    int32_t num_sms, int32_t requested_splits, int32_t fixed_chunk_tokens,
                    int32_t flags, ga_plan* plan_out);
+
+/*
+ * ga_plan_splits_mq -- ga_plan_splits for multi-query decode: q_len (S, 1 ..
+ * GA_MAX_Q_LEN) query tokens per row, the row's last S positions
+ * ("visible-cx/Gemma-4-31B-CoreAI", hybrid-pf64/ bundles: a query axis with
+ * an intra-chunk causal mask, and chunked walks that must agree with
+ * token-by-token ones; "Gemma 4 31B on vLLM -- operating-point reference",
+ * LIGHT recipe: EAGLE3 verify of 3 speculative tokens, i.e. 4 queries per
+ * row).  The plan covers the pages any of a row's S queries attends (the
+ * window grows by S - 1 for the sliding family) and work units over the
+ * S x (Hq / Hkv) (query, head) columns of each kv head.  q_len = 1 is
+ * ga_plan_splits.  Other arguments and errors as for ga_plan_splits.
+ */
+#define GA_MAX_Q_LEN 64
+int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t window, int32_t page_size,
+                      int32_t q_len, int32_t num_sms, int32_t requested_splits,
+                      int32_t fixed_chunk_tokens, int32_t flags, ga_plan* plan_out);
 
 /*
  * ga_kv_append -- write this step's new K and V token of every row into its
@@ -192,6 +212,11 @@ int ga_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_poo
  *       GA_PLAN_EXTERNAL_COMBINE).
  *   out [batch, num_q_heads, 256] bf16.
  * Rows with L_b = 0 produce zeros.
+ * Multi-query decode (plan from ga_plan_splits_mq with q_len = S > 1): q and
+ *   out are [batch, num_q_heads, S, 256] (a head's S query tokens adjacent);
+ *   query i of row b sits at position p = L_b - S + i and attends keys
+ *   [max(0, p - window + 1), p] (causal inside the chunk, the window ending
+ *   at its own position); a query with p < 0 produces zeros.
  */
 int ga_decode_local_hd256(const void* q, const void* k_pool, const void* v_pool,
                           int32_t kv_dtype, const float* k_scale, const float* v_scale,
@@ -209,6 +234,8 @@ int ga_decode_local_hd256(const void* q, const void* k_pool, const void* v_pool,
  * without `window`; head_dim is 512.  Passing the same pool as k_pool and
  * v_pool (K == V, as with a shared K/V projection: "[Model] Gemma 4 M1 12B",
  * Description) reads each page-head block once and uses it for both products.
+ * Multi-query decode as for the local call: q, out [batch, num_q_heads, S,
+ * 512], query i at position L_b - S + i attends keys [0, L_b - S + i].
  */
 int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool,
                            int32_t kv_dtype, const float* k_scale, const float* v_scale,
@@ -226,14 +253,15 @@ int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool
  * with o_s normalised within its chunk and lse_s = ln sum_{j in chunk s} e^{s_j}
  * (natural log; an empty chunk has lse_s = -inf and weighs nothing).
  *
- *   partial_o [plan->row_chunks, Hq, D] fp32 and partial_lse
- *       [plan->row_chunks, Hq] fp32, device: row-chunk r of row b is
+ *   partial_o [plan->row_chunks, Hq * S, D] fp32 and partial_lse
+ *       [plan->row_chunks, Hq * S] fp32 (S = plan->q_len; query i of head h
+ *       is column h * S + i), device: row-chunk r of row b is
  *       rc_b + j, rc_b = sum over rows b' < b of that row's chunk count, in
  *       the chunking the plan defines for the device seq_lens.
  *   seq_lens [plan->batch] int32 device and pt_stride: the same values the
  *   decode call got (a length beyond pt_stride * page_size counts as 0).
  *   Rows whose chunk count is 1 are left untouched (the decode call wrote
- *   them).  out [plan->batch, Hq, D] bf16.
+ *   them).  out [plan->batch, Hq, S, D] bf16.
  * The decode calls invoke this themselves when split; it is exported for
  * testing and for callers that write their own partials.
  */

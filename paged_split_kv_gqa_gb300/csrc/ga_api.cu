@@ -85,7 +85,7 @@ namespace {
 
 struct PlanInput {
     const int32_t* lens;
-    int32_t B, Hq, Hkv, D, W, num_sms;
+    int32_t B, Hq, Hkv, D, W, num_sms, S;    // W: the window of the union of S queries
 };
 
 // Row-chunk count and per-unit page counts of a candidate chunking.
@@ -97,7 +97,7 @@ struct Candidate {
 };
 
 void evaluate(const PlanInput& in, Candidate& cand) {
-    const int32_t HG = head_groups(in.Hq / in.Hkv);
+    const int32_t HG = head_groups(in.Hq / in.Hkv * in.S);
     const int64_t per_rc = (int64_t)in.Hkv * HG;
     std::vector<int32_t> rc_pages;
     rc_pages.reserve(in.B * 4);
@@ -131,7 +131,7 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     double combine = 0;
     if (split_rows_rc > 0) {
         const double page_bytes = 2.0 * kPageSize * in.D * 2.0;   // K + V page-head, bf16
-        const double partial_bytes = 2.0 * (double)split_rows_rc * in.Hq * in.D * 4.0;
+        const double partial_bytes = 2.0 * (double)split_rows_rc * in.Hq * in.S * in.D * 4.0;
         combine = partial_bytes / page_bytes / in.num_sms + 4.0;
     }
     cand.cost = makespan + combine;
@@ -145,7 +145,7 @@ using namespace ga;
 
 extern "C" {
 
-int32_t ga_version(void) { return 0x000100; }
+int32_t ga_version(void) { return 0x000200; }
 
 const char* ga_strerror(int status) {
     switch (status) {
@@ -165,8 +165,19 @@ int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_he
                    int32_t num_kv_heads, int32_t head_dim, int32_t window, int32_t page_size,
                    int32_t num_sms, int32_t requested_splits, int32_t fixed_chunk_tokens,
                    int32_t flags, ga_plan* plan_out) {
+    return ga_plan_splits_mq(seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, window,
+                             page_size, 1, num_sms, requested_splits, fixed_chunk_tokens, flags,
+                             plan_out);
+}
+
+int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t window, int32_t page_size,
+                      int32_t q_len, int32_t num_sms, int32_t requested_splits,
+                      int32_t fixed_chunk_tokens, int32_t flags, ga_plan* plan_out) {
     if (plan_out == nullptr || batch < 0 || (batch > 0 && seq_lens_host == nullptr))
         return GA_ERR_INVALID_ARG;
+    if (q_len < 1) return GA_ERR_INVALID_ARG;
+    if (q_len > kMaxQLen) return GA_ERR_UNSUPPORTED;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || window < 0 ||
         num_sms < 1 || requested_splits < 0 || fixed_chunk_tokens < 0 ||
         (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~(GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE)))
@@ -178,7 +189,8 @@ int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_he
     for (int32_t b = 0; b < batch; ++b)
         if (seq_lens_host[b] < 0) return GA_ERR_INVALID_ARG;
 
-    PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, window, num_sms};
+    const int32_t weff = effective_window(window, q_len);
+    PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len};
     Candidate best;
     if (requested_splits == 1) {
         best = Candidate{kSplitNone, 0, 0};
@@ -195,7 +207,7 @@ int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_he
         int32_t max_np = 0;
         for (int32_t b = 0; b < batch; ++b)
             max_np = std::max(max_np,
-                              row_geometry(seq_lens_host[b], window, INT64_MAX / 64, kSplitNone,
+                              row_geometry(seq_lens_host[b], weff, INT64_MAX / 64, kSplitNone,
                                            0, 0).npages);
         for (int32_t cp = 4; cp < max_np; cp *= 2) {
             Candidate c{kSplitChunk, 0, cp};
@@ -214,6 +226,7 @@ int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_he
     p.window = window;
     p.page_size = page_size;
     p.flags = flags;
+    p.q_len = q_len;
     p.row_chunks = best.row_chunks;
     p.units = best.units;
     p.grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(best.units, num_sms));
@@ -224,8 +237,8 @@ int ga_plan_splits(const int32_t* seq_lens_host, int32_t batch, int32_t num_q_he
         return at;
     };
     if (p.mode != kSplitNone) {
-        p.partial_o_offset = take(p.row_chunks * num_q_heads * (int64_t)head_dim * 4);
-        p.partial_lse_offset = take(p.row_chunks * num_q_heads * 4);
+        p.partial_o_offset = take(p.row_chunks * num_q_heads * (int64_t)q_len * head_dim * 4);
+        p.partial_lse_offset = take(p.row_chunks * num_q_heads * (int64_t)q_len * 4);
     }
     if (flags & GA_PLAN_TOUCH_LOG) {
         p.touch_stride = std::max(best.max_cp, 1);
@@ -274,7 +287,8 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
         return GA_ERR_UNSUPPORTED;
     if (plan->batch != batch || plan->num_q_heads != num_q_heads ||
         plan->num_kv_heads != num_kv_heads || plan->head_dim != head_dim ||
-        plan->window != window || plan->page_size != page_size)
+        plan->window != window || plan->page_size != page_size || plan->q_len < 1 ||
+        plan->q_len > kMaxQLen)
         return GA_ERR_INVALID_ARG;
     if (batch == 0) return GA_OK;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return GA_ERR_INVALID_ARG;
@@ -321,7 +335,8 @@ int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool
 int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
                        const int32_t* seq_lens, int64_t pt_stride, void* out,
                        int32_t* err_word, ga_stream_t stream) {
-    if (plan == nullptr || pt_stride < 1) return GA_ERR_INVALID_ARG;
+    if (plan == nullptr || pt_stride < 1 || plan->q_len < 1 || plan->q_len > kMaxQLen)
+        return GA_ERR_INVALID_ARG;
     if (plan->head_dim != 256 && plan->head_dim != 512) return GA_ERR_UNSUPPORTED;
     if (plan->batch == 0 || plan->mode == GA_SPLIT_NONE) return GA_OK;
     if (!partial_o || !partial_lse || !seq_lens || !out) return GA_ERR_INVALID_ARG;

@@ -85,9 +85,11 @@ int launch_combine(const float* partial_o, const float* partial_lse, const ga_pl
     p.pt_stride = pt_stride;
     p.rc_capacity = plan->row_chunks;
     p.B = plan->batch;
-    p.Hq = plan->num_q_heads;
+    // an S-query plan has S (query, head) columns per query head, laid out
+    // [B, Hq, S, D]: the combine sees them as Hq * S heads
+    p.Hq = plan->num_q_heads * plan->q_len;
     p.D = plan->head_dim;
-    p.window = plan->window;
+    p.window = effective_window(plan->window, plan->q_len);
     p.mode = plan->mode;
     p.splits = plan->splits;
     p.chunk_pages = plan->chunk_pages;

@@ -57,7 +57,12 @@ struct DecodeParams {
     int64_t pt_stride;
     int64_t num_pages;
     int64_t rc_capacity;
+    // Hq and group count (query, head) columns: an S-query decode has
+    // Hq * S columns, S adjacent per query head ([B, Hq, S, D]); window is
+    // the union window of a row's S queries (page ranges), mask_window the
+    // real one (per-column masks).
     int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
+    int32_t S, mask_window;
     float scale_log2;             // softmax scale * log2(e)
     int64_t out_elems;            // B * Hq * D
     int64_t pool_rows;            // num_pages * Hkv * P
@@ -454,6 +459,23 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
     for (int64_t u = blockIdx.x; u < U; u += gridDim.x, ++kunit) {
         const UnitInfo x = finish_unit(p, pre, nl, nlen);
         const bool single = (x.g.chunks == 1);
+        // This lane's two columns (2t, 2t+1) of the unit: query i = column % S
+        // sits at position L - S + i and attends keys [clo, chi) (causal in
+        // the chunk; the window ends at its own position).  Pages needing a
+        // mask reach below the last query's window start or past the first
+        // query's position: for S = 1 the first and last page of the range.
+        int32_t clo0, chi0, clo1, chi1;
+        {
+            const int32_t f0 = x.hg * kHeadTile + 2 * t;
+            const int32_t pos0 = x.g.len - p.S + f0 % p.S;
+            const int32_t pos1 = x.g.len - p.S + (f0 + 1) % p.S;
+            chi0 = pos0 + 1;
+            chi1 = pos1 + 1;
+            clo0 = p.mask_window > 0 ? max(0, pos0 - p.mask_window + 1) : 0;
+            clo1 = p.mask_window > 0 ? max(0, pos1 - p.mask_window + 1) : 0;
+        }
+        const int32_t plo = p.mask_window > 0 ? max(0, x.g.len - p.mask_window) : 0;
+        const int32_t phi = x.g.len - p.S + 1;
         float kfac = p.scale_log2, vfac = 1.0f;
         if (C::KV == GA_KV_E4M3) {
             kfac *= nks;
@@ -588,14 +610,16 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
                     s[r] = ((sa[0][r] + sa[1][r]) + (sa[2][r] + sa[3][r])) * ((r & 1) ? kf1 : kf0);
                 // ---- window / length mask (first and last page of the range only)
                 const int32_t key0 = (x.p0 + i) * kPageSize;
-                const bool partial = key0 < x.g.lo || key0 + kPageSize > x.g.len;
+                const bool partial = key0 < plo || key0 + kPageSize > phi;
                 uint32_t mk01 = 0xffffffffu, mk89 = 0xffffffffu;
                 if (partial) {
+                    // scores: per (key, column); V rows: keys no query of the row
+                    // attends (outside [lo, L) of the union window) hold no data
                     const int32_t ka = key0 + gid, kb8 = key0 + gid + 8;
-                    const bool va = ka >= x.g.lo && ka < x.g.len;
-                    const bool vb = kb8 >= x.g.lo && kb8 < x.g.len;
-                    if (!va) { s[0] = -CUDART_INF_F; s[1] = -CUDART_INF_F; }
-                    if (!vb) { s[2] = -CUDART_INF_F; s[3] = -CUDART_INF_F; }
+                    if (!(ka >= clo0 && ka < chi0)) s[0] = -CUDART_INF_F;
+                    if (!(ka >= clo1 && ka < chi1)) s[1] = -CUDART_INF_F;
+                    if (!(kb8 >= clo0 && kb8 < chi0)) s[2] = -CUDART_INF_F;
+                    if (!(kb8 >= clo1 && kb8 < chi1)) s[3] = -CUDART_INF_F;
                     auto valid = [&](int k) {
                         const int32_t kk = key0 + k;
                         return kk >= x.g.lo && kk < x.g.len;
@@ -973,15 +997,16 @@ static int run(const DecodeArgs& a, int slot) {
     int rc = ensure_smem_attr(fn, C::SMEM_BYTES, slot);
     if (rc != GA_OK) return rc;
     const ga_plan& pl = *a.plan;
+    const int32_t S = pl.q_len;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
     CUtensorMap tmK, tmV, tmQ;
     rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize);
     if (rc != GA_OK) return rc;
     rc = encode_rows_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim, kPageSize);
     if (rc != GA_OK) return rc;
-    // q as [B * Hq, D] bf16, boxes of one head group (8 rows; rows past the
-    // end read as zeros)
-    rc = encode_rows_map(&tmQ, a.q, GA_KV_BF16, (int64_t)a.batch * a.num_q_heads, a.head_dim,
+    // q as [B * Hq * S, D] bf16, boxes of one group of 8 (query, head)
+    // columns (rows past the end read as zeros)
+    rc = encode_rows_map(&tmQ, a.q, GA_KV_BF16, (int64_t)a.batch * a.num_q_heads * S, a.head_dim,
                          kHeadTile);
     if (rc != GA_OK) return rc;
 
@@ -1004,18 +1029,20 @@ static int run(const DecodeArgs& a, int slot) {
     p.num_pages = a.num_pages;
     p.rc_capacity = pl.row_chunks;
     p.B = a.batch;
-    p.Hq = a.num_q_heads;
+    p.Hq = a.num_q_heads * S;
     p.Hkv = a.num_kv_heads;
-    p.group = a.num_q_heads / a.num_kv_heads;
+    p.group = a.num_q_heads / a.num_kv_heads * S;
     p.HG = head_groups(p.group);
-    p.window = a.window;
+    p.window = effective_window(a.window, S);
+    p.S = S;
+    p.mask_window = a.window;
     p.mode = pl.mode;
     p.splits = pl.splits;
     p.chunk_pages = pl.chunk_pages;
     p.touch_stride = pl.touch_stride;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.pool_rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
-    p.out_elems = (int64_t)a.batch * a.num_q_heads * a.head_dim;
+    p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
     decode_kernel<C><<<grid, C::NTHREADS, C::SMEM_BYTES, a.stream>>>(tmK, tmV, tmQ, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;

@@ -20,6 +20,7 @@ namespace ga {
 constexpr int kPageSize = 16;     // keys per page; one page = one 16-key MMA tile
 constexpr int kHeadTile = 8;      // query heads per unit (MMA N)
 constexpr int kMaxBatch = 2048;   // rows per call (decode keeps a row prefix in smem)
+constexpr int kMaxQLen = 64;      // query tokens per row of a multi-query decode
 
 enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
 
@@ -56,6 +57,14 @@ GA_HD RowGeom row_geometry(int32_t L, int32_t window, int64_t pt_stride, int32_t
     g.cp = cp;
     g.chunks = g.npages > 0 ? ceil_div(g.npages, cp) : 1;
     return g;
+}
+
+// Window of the keys any of a row's S queries attends (the last S positions,
+// each with its own window): W + S - 1 for the sliding family, 0 (global)
+// stays 0.  Saturates instead of overflowing.
+GA_HD int32_t effective_window(int32_t window, int32_t S) {
+    if (window <= 0) return 0;
+    return window > 0x7fffffff - (S - 1) ? 0x7fffffff : window + (S - 1);
 }
 
 // Logical page range [*p0, *p0 + *np) of chunk j of a row.

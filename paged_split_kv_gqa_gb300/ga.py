@@ -41,6 +41,7 @@ GA_SPLIT_CHUNK = 2
 GA_PLAN_TOUCH_LOG = 1
 GA_PLAN_EXTERNAL_COMBINE = 2
 PAGE_SIZE = 16
+MAX_Q_LEN = 64
 
 
 class GAError(RuntimeError):
@@ -52,7 +53,7 @@ class GAError(RuntimeError):
 class ga_plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "splits", "chunk_pages", "batch", "num_q_heads", "num_kv_heads", "head_dim",
-        "window", "page_size", "grid", "flags", "touch_stride")] + [
+        "window", "page_size", "grid", "flags", "touch_stride", "q_len", "reserved")] + [
         (n, ctypes.c_int64) for n in ("row_chunks", "units", "workspace_bytes",
                                        "partial_o_offset", "partial_lse_offset",
                                        "touch_log_offset")]
@@ -69,6 +70,7 @@ def _load():
     i32, i64, p, f32, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
     P = ctypes.POINTER(ga_plan)
     lib.ga_plan_splits.argtypes = [p, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P]
+    lib.ga_plan_splits_mq.argtypes = [p, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P]
     lib.ga_kv_append.argtypes = [p, p, p, p, i32, p, p, p, i64, p, i32, i32, i32, i32, i64, p, p]
     lib.ga_decode_local_hd256.argtypes = [p, p, p, i32, p, p, p, i64, p, i32, i32, i32, i32, i32,
                                           i64, f32, P, p, sz, p, p, p]
@@ -77,7 +79,7 @@ def _load():
     lib.ga_splitkv_combine.argtypes = [p, p, P, p, i64, p, p, p]
     lib.ga_decode_global_hd512_noalloc.argtypes = [p, p, p, i32, p, p, p, i64, p, i32, i32, i32,
                                                    i32, i64, f32, P, p, p, p]
-    for fn in ("ga_plan_splits", "ga_kv_append", "ga_decode_local_hd256",
+    for fn in ("ga_plan_splits", "ga_plan_splits_mq", "ga_kv_append", "ga_decode_local_hd256",
                "ga_decode_global_hd512", "ga_splitkv_combine", "ga_check_error_word",
                "ga_decode_global_hd512_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
@@ -139,16 +141,24 @@ def num_sms(device=None) -> int:
 def ga_plan_splits(seq_lens_host: Sequence[int], *, num_q_heads: int, num_kv_heads: int,
                    head_dim: int, window: int, page_size: int = PAGE_SIZE,
                    num_sms: Optional[int] = None, requested_splits: int = 0,
-                   fixed_chunk_tokens: int = 0, flags: int = 0) -> ga_plan:
-    """Host-only planner (no CUDA call unless num_sms is looked up)."""
+                   fixed_chunk_tokens: int = 0, flags: int = 0, q_len: int = 1) -> ga_plan:
+    """Host-only planner (no CUDA call unless num_sms is looked up).  q_len > 1
+    plans a multi-query decode (ga_plan_splits_mq)."""
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32).reshape(-1))
     if num_sms is None:
         num_sms = globals()["num_sms"]()
     plan = ga_plan()
-    st = _lib.ga_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), len(lens), num_q_heads,
-                             num_kv_heads, head_dim, window, page_size, num_sms,
-                             requested_splits, fixed_chunk_tokens, flags, ctypes.byref(plan))
-    _check(st, "ga_plan_splits")
+    if q_len == 1:
+        st = _lib.ga_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), len(lens), num_q_heads,
+                                 num_kv_heads, head_dim, window, page_size, num_sms,
+                                 requested_splits, fixed_chunk_tokens, flags, ctypes.byref(plan))
+        _check(st, "ga_plan_splits")
+    else:
+        st = _lib.ga_plan_splits_mq(lens.ctypes.data_as(ctypes.c_void_p), len(lens), num_q_heads,
+                                    num_kv_heads, head_dim, window, page_size, q_len, num_sms,
+                                    requested_splits, fixed_chunk_tokens, flags,
+                                    ctypes.byref(plan))
+        _check(st, "ga_plan_splits_mq")
     return plan
 
 
@@ -171,7 +181,13 @@ def ga_kv_append(k_new, v_new, k_pool, v_pool, page_table, positions, *, k_scale
 
 def _decode(fn, name, q, k_pool, v_pool, page_table, seq_lens, *, window, scale, plan,
             workspace, out, k_scale, v_scale, err_word, stream):
-    B, Hq, D = q.shape
+    # q / out: [B, Hq, D], or [B, Hq, S, D] with S = plan.q_len query tokens per row
+    if q.dim() == 4:
+        B, Hq, S, D = q.shape
+    else:
+        (B, Hq, D), S = q.shape, 1
+    if S != plan.q_len or out.shape != q.shape:
+        raise GAError(GA_ERR_INVALID_ARG, f"{name}: q / out shape vs plan.q_len = {plan.q_len}")
     Hkv = k_pool.shape[1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = [_ptr(q), _ptr(k_pool), _ptr(v_pool), _kv_dtype(k_pool), _ptr(k_scale), _ptr(v_scale),
@@ -215,7 +231,7 @@ def ga_decode_global_hd512_noalloc(q, k_pool, v_pool, page_table, seq_lens, *, s
     array (no workspace argument): for callers that cannot allocate device
     memory at decode time.  Calls that overlap on the GPU share that array and
     race; plans needing more than NOALLOC_SCRATCH_BYTES are rejected."""
-    B, Hq, D = q.shape
+    B, Hq = q.shape[0], q.shape[1]
     st = _lib.ga_decode_global_hd512_noalloc(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _kv_dtype(k_pool), _ptr(k_scale), _ptr(v_scale),
         _ptr(page_table), page_table.shape[1], _ptr(seq_lens), B, Hq, k_pool.shape[1],
@@ -239,8 +255,9 @@ def ga_check_error_word(word: int) -> int:
 
 
 def workspace_views(plan: ga_plan, workspace: torch.Tensor):
-    """(partial_o [rc, Hq, D], partial_lse [rc, Hq], touch_log [rc, stride]) views."""
-    rc, Hq, D = plan.row_chunks, plan.num_q_heads, plan.head_dim
+    """(partial_o [rc, Hq * S, D], partial_lse [rc, Hq * S], touch_log [rc, stride]) views
+    (S = plan.q_len; column h * S + i is query i of head h)."""
+    rc, Hq, D = plan.row_chunks, plan.num_q_heads * plan.q_len, plan.head_dim
     po = plo = log = None
     if plan.mode != GA_SPLIT_NONE:
         po = workspace[plan.partial_o_offset: plan.partial_o_offset + rc * Hq * D * 4] \
@@ -252,3 +269,8 @@ def workspace_views(plan: ga_plan, workspace: torch.Tensor):
         log = workspace[plan.touch_log_offset: plan.touch_log_offset + n * 4] \
             .view(torch.int32).view(rc, plan.touch_stride)
     return po, plo, log
+
+
+def ga_plan_splits_mq(seq_lens_host: Sequence[int], *, q_len: int, **kw) -> ga_plan:
+    """Multi-query planner: q_len query tokens per row (the last q_len positions)."""
+    return ga_plan_splits(seq_lens_host, q_len=q_len, **kw)

@@ -27,16 +27,25 @@ def pages_read(seq_lens, window: int, page_size: int) -> np.ndarray:
     return np.where(L > 0, (L - 1) // page_size - lo // page_size + 1, 0)
 
 
+def union_window(window: int, q_len: int) -> int:
+    """Window of the keys any of a row's q_len queries (its last q_len
+    positions, each with its own window) attends; 0 (global) stays 0."""
+    return window + q_len - 1 if window > 0 else 0
+
+
 def decode_bytes(seq_lens, *, num_q_heads, num_kv_heads, head_dim, window, page_size,
-                 kv_bytes_per_elem, kv_alias=False) -> int:
+                 kv_bytes_per_elem, kv_alias=False, q_len=1) -> int:
     """Algorithmic HBM bytes of one decode launch over a batch (K == V one
-    pool: each attended key row is read once)."""
+    pool: each attended key row is read once).  With q_len queries per row
+    the keys are those of the union of their windows, read once, and q / out
+    carry q_len rows per head."""
     B = len(seq_lens)
+    window = union_window(window, q_len)
     n = int(attended_keys(seq_lens, window).sum())
     kv = n * kv_bytes_per_token(num_kv_heads, head_dim, kv_bytes_per_elem)
     if kv_alias:
         kv //= 2
-    qo = 2 * B * num_q_heads * head_dim * 2
+    qo = 2 * B * num_q_heads * q_len * head_dim * 2
     table = 4 * int(pages_read(seq_lens, window, page_size).sum())
     scales = 8 * num_kv_heads if kv_bytes_per_elem == 1 else 0
     return int(kv + qo + table + 4 * B + scales)

@@ -47,14 +47,44 @@ def test_strerror_and_version(ga):
     assert ga.strerror(0) == "GA_OK"
     assert "WORKSPACE" in ga.strerror(3)
     assert "unknown" in ga.strerror(99)
-    assert ga.ga_version() == 0x000100
+    assert ga.ga_version() == 0x000200
     assert ga.ga_check_error_word(0) == ga.GA_OK
     assert ga.ga_check_error_word(ga.GA_DEVERR_PAGE_ID) == ga.GA_ERR_DEVICE_CHECK
 
 
 def test_plan_struct_layout_matches_header(ga):
-    # 12 int32 then 6 int64, no padding surprises
-    assert ctypes.sizeof(ga.ga_plan) == 12 * 4 + 6 * 8
+    # 14 int32 (the last two: q_len, reserved) then 6 int64, no padding surprises
+    assert ctypes.sizeof(ga.ga_plan) == 14 * 4 + 6 * 8
+    assert ga.ga_plan.q_len.offset == 12 * 4 and ga.ga_plan.row_chunks.offset == 14 * 4
+
+
+def test_multi_query_plan(ga):
+    """ga_plan_splits_mq: q_len recorded, range checked, partials sized for
+    Hq * S columns, pages of the union window of the S queries planned."""
+    kw = dict(num_q_heads=4, num_kv_heads=2, head_dim=256, window=32, num_sms=8,
+              requested_splits=2)
+    one = ga.ga_plan_splits([40, 33], **kw)
+    four = ga.ga_plan_splits_mq([40, 33], q_len=4, **kw)
+    assert one.q_len == 1 and four.q_len == 4
+    assert four.partial_o_offset == one.partial_o_offset == 0
+    # partial O: row_chunks x (Hq * S) x D fp32, 256-byte aligned regions
+    assert four.partial_lse_offset >= four.row_chunks * 4 * 4 * 256 * 4
+    # 4 queries x group 2 = 8 columns: still one head group per kv head
+    assert four.units == one.units
+    eight = ga.ga_plan_splits_mq([40, 33], q_len=8, **kw)
+    assert eight.units == 2 * one.units
+    # union window, row of length 33, W = 16: one query reads keys 17..32
+    # (pages 1..2); four queries (positions 29..32) read keys 14..32 (pages 0..2)
+    w1 = ga.ga_plan_splits([33], num_q_heads=2, num_kv_heads=2, head_dim=256, window=16,
+                           num_sms=8, flags=ga.GA_PLAN_TOUCH_LOG)
+    w4 = ga.ga_plan_splits_mq([33], q_len=4, num_q_heads=2, num_kv_heads=2, head_dim=256,
+                              window=16, num_sms=8, flags=ga.GA_PLAN_TOUCH_LOG)
+    assert w1.touch_stride == 2 and w4.touch_stride == 3     # keys 17..32 vs 14..32
+    with pytest.raises(ga.GAError):
+        ga.ga_plan_splits_mq([40], q_len=0, **kw)
+    with pytest.raises(ga.GAError) as e:
+        ga.ga_plan_splits_mq([40], q_len=ga.MAX_Q_LEN + 1, **kw)
+    assert e.value.status == ga.GA_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------------ host-side rejection
@@ -98,6 +128,11 @@ def test_decode_rejects_before_launch(ga):
     assert _decode_local(ga, split, ws=FAKE, wsb=split.workspace_bytes - 1) == \
         ga.GA_ERR_WORKSPACE_TOO_SMALL
     assert _decode_local(ga, plan, B=0) == ga.GA_ERR_INVALID_ARG           # plan says B=2
+    bad = _plan(ga)
+    bad.q_len = 0
+    assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG                 # corrupted plan
+    bad.q_len = ga.MAX_Q_LEN + 1
+    assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
 
 
 def test_append_rejects_before_launch(ga):

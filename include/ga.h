@@ -116,7 +116,8 @@ typedef struct ga_plan {
     int32_t flags;           /* GA_PLAN_* */
     int32_t touch_stride;    /* touch-log entries per row-chunk (flag set) */
     int32_t q_len;           /* query tokens per row S (1 = one-query decode) */
-    int32_t reserved;        /* 0 */
+    int32_t col_tile;        /* (query, head) columns per work unit: 8, or 32 when a kv
+                                head has more than 8 (column-parallel units) */
     int64_t row_chunks;      /* (row, chunk) pairs the workspace holds */
     int64_t units;           /* work units (row-chunk x kv head x head group) planned */
     int64_t workspace_bytes; /* device workspace the decode call needs (0 if none) */

@@ -86,6 +86,7 @@ namespace {
 struct PlanInput {
     const int32_t* lens;
     int32_t B, Hq, Hkv, D, W, num_sms, S;    // W: the window of the union of S queries
+    int32_t TW;                              // columns per work unit
 };
 
 // Row-chunk count and per-unit page counts of a candidate chunking.
@@ -97,7 +98,7 @@ struct Candidate {
 };
 
 void evaluate(const PlanInput& in, Candidate& cand) {
-    const int32_t HG = head_groups(in.Hq / in.Hkv * in.S);
+    const int32_t HG = ceil_div(in.Hq / in.Hkv * in.S, in.TW);
     const int64_t per_rc = (int64_t)in.Hkv * HG;
     std::vector<int32_t> rc_pages;
     rc_pages.reserve(in.B * 4);
@@ -190,7 +191,12 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
         if (seq_lens_host[b] < 0) return GA_ERR_INVALID_ARG;
 
     const int32_t weff = effective_window(window, q_len);
-    PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len};
+    // more than 8 (query, head) columns per kv head: column-parallel units of
+    // 4 tiles of 8 (every page read once for all of them)
+    const int32_t cols = num_q_heads / num_kv_heads * q_len;
+    const int32_t tw = cols > kHeadTile ? 4 * kHeadTile : kHeadTile;
+    PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len,
+                 tw};
     Candidate best;
     if (requested_splits == 1) {
         best = Candidate{kSplitNone, 0, 0};
@@ -227,6 +233,7 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     p.page_size = page_size;
     p.flags = flags;
     p.q_len = q_len;
+    p.col_tile = tw;
     p.row_chunks = best.row_chunks;
     p.units = best.units;
     p.grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(best.units, num_sms));
@@ -288,7 +295,7 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
     if (plan->batch != batch || plan->num_q_heads != num_q_heads ||
         plan->num_kv_heads != num_kv_heads || plan->head_dim != head_dim ||
         plan->window != window || plan->page_size != page_size || plan->q_len < 1 ||
-        plan->q_len > kMaxQLen)
+        plan->q_len > kMaxQLen || (plan->col_tile != kHeadTile && plan->col_tile != 4 * kHeadTile))
         return GA_ERR_INVALID_ARG;
     if (batch == 0) return GA_OK;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return GA_ERR_INVALID_ARG;

@@ -63,6 +63,7 @@ struct DecodeParams {
     // real one (per-column masks).
     int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
     int32_t S, mask_window;
+    int32_t TW;                   // columns per work unit (8, or 8 x warps column-parallel)
     float scale_log2;             // softmax scale * log2(e)
     int64_t out_elems;            // B * Hq * D
     int64_t pool_rows;            // num_pages * Hkv * P
@@ -76,7 +77,7 @@ struct DecodeParams {
 #define GA_CHK(cond) true
 #endif
 
-template <int D_, int KV_, int NCW_, int NS_, bool ALIAS_ = false>
+template <int D_, int KV_, int NCW_, int NS_, bool ALIAS_ = false, bool COLPAR_ = false>
 struct DecodeCfg {
     static constexpr int D = D_;
     static constexpr int KV = KV_;                  // GA_KV_BF16 / GA_KV_E4M3
@@ -85,6 +86,12 @@ struct DecodeCfg {
     // K and V are one pool (K == V, e.g. a shared K/V projection): each page-head
     // block is fetched once and serves both products.
     static constexpr bool ALIAS = ALIAS_;
+    // Column-parallel: a unit holds NCW tiles of 8 (query, head) columns and
+    // warp w owns tile w over every page of the unit (each page is read once
+    // for all of them; no cross-warp merge).  Page-parallel (default): a unit
+    // is one tile of 8 columns and the warps share out its pages.
+    static constexpr bool COLPAR = COLPAR_;
+    static constexpr int TW = COLPAR ? 8 * NCW : kHeadTile;     // columns per unit
 
     static constexpr int NCT = NCW * 32;            // consumer threads
     static constexpr int NTHREADS = NCT + 32;
@@ -108,7 +115,8 @@ struct DecodeCfg {
     // The unit's q rows land as one 3-D box like a page-head block: D/64
     // tiles of [8 heads][128 bytes], 128-byte swizzled.  The E4M3 path turns
     // them into fragments in place (same size).
-    static constexpr int Q_BYTES = kHeadTile * D * 2;
+    static constexpr int Q_BYTES = TW * D * 2;
+    static constexpr int QTILE_STRIDE = TW * 128;   // bytes per 64-element column tile
     // The merge buffer: one region of [8 heads][MSTRIDE] floats per consumer
     // warp when shared memory allows (each warp writes its own, one barrier),
     // else one region the warps add into in turn.
@@ -117,8 +125,9 @@ struct DecodeCfg {
     static constexpr int AFTER_MERGE = al(2 * NCW * kHeadTile * 4) + al(2 * kHeadTile * 4) +
                                        al((kMaxBatch + 1) * 4) + al(NS * 4) + al((2 * NS + 1) * 8);
     static constexpr int MREG =
-        (BEFORE_MERGE + al(NCW * REGION_FLOATS * 4) + AFTER_MERGE + 1024 <= 227 * 1024) ? NCW
-                                                                                        : 1;
+        COLPAR ? 0
+        : (BEFORE_MERGE + al(NCW * REGION_FLOATS * 4) + AFTER_MERGE + 1024 <= 227 * 1024) ? NCW
+                                                                                         : 1;
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_Q = al(OFF_RING + NS * STAGE_BYTES);
     static constexpr int OFF_MERGE = al(OFF_Q + Q_BYTES);
@@ -131,7 +140,8 @@ struct DecodeCfg {
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
     static_assert(D % 128 == 0 && NTILES >= 1, "head_dim (the merge takes m-tiles 8 at a time)");
     static_assert(OFF_BARS % 8 == 0 && OFF_Q % 1024 == 0 && OFF_MERGE % 16 == 0, "alignment");
-    static_assert(KSTEPS * 32 * 8 == Q_BYTES, "E4M3 fragments reuse the q tile");
+    static_assert(KV != GA_KV_E4M3 || (KSTEPS * 32 * 8 == Q_BYTES && !COLPAR),
+                  "E4M3 fragments reuse the q tile (page-parallel only)");
     static_assert(REGION_FLOATS % 4 == 0 && MSTRIDE % 4 == 0, "float4 access to merge regions");
     static_assert(STAGE_BYTES % 1024 == 0, "swizzle-128B boxes need 1024-byte aligned stages");
     // Every ring slot must always be consumed by the same warp: page n sits in
@@ -140,7 +150,8 @@ struct DecodeCfg {
     // of that slot itself, so the parity wait cannot be satisfied by an older
     // phase of the same parity; unit boundaries are ordered by the merge
     // barrier.  With NS % NCW != 0 a fast warp could see a stale completion.
-    static_assert(NS % NCW == 0, "ring stages must be a multiple of consumer warps");
+    // (Column-parallel: every warp consumes every slot, so any depth works.)
+    static_assert(COLPAR || NS % NCW == 0, "ring stages must be a multiple of consumer warps");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -186,7 +197,7 @@ __device__ __forceinline__ UnitLoc locate_unit(const DecodeParams& p, const int3
 
 // First q row (in the [B * Hq, D] view) of a unit's head group.
 __device__ __forceinline__ int32_t unit_q_row(const DecodeParams& p, const UnitLoc& l) {
-    return l.b * p.Hq + l.c * p.group + l.hg * kHeadTile;
+    return l.b * p.Hq + l.c * p.group + l.hg * p.TW;
 }
 
 __device__ __forceinline__ UnitInfo finish_unit(const DecodeParams& p, const int32_t* pre,
@@ -199,9 +210,9 @@ __device__ __forceinline__ UnitInfo finish_unit(const DecodeParams& p, const int
     x.j = (int32_t)(x.rc - pre[x.b]);
     x.g = row_geometry(len, p.window, p.pt_stride, p.mode, p.splits, p.chunk_pages);
     chunk_pages_of(x.g, x.j, &x.p0, &x.np);
-    x.h0 = x.c * p.group + x.hg * kHeadTile;
-    int nv = p.group - x.hg * kHeadTile;
-    x.nvalid = nv < kHeadTile ? nv : kHeadTile;
+    x.h0 = x.c * p.group + x.hg * p.TW;
+    int nv = p.group - x.hg * p.TW;
+    x.nvalid = nv < p.TW ? nv : p.TW;
     return x;
 }
 
@@ -427,13 +438,15 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
     const uint32_t qbar = bars + 8 * (2 * C::NS);
     const uint2* qf = reinterpret_cast<const uint2*>(qtile);   // E4M3 fragments, over the tile
     // ldmatrix selectors for the q tile: lanes 8m .. 8m+7 give the rows (heads)
-    // of matrix m = (k-step ks + m/2, half m%2)
+    // of matrix m = (k-step ks + m/2, half m%2); column-parallel warps read
+    // their own 8 rows (one 128-byte swizzle atom of each column tile)
     const int qrow = lane & 7, qmat = lane >> 3;
+    const uint32_t qrow_base = C::COLPAR ? 8u * (uint32_t)w : 0u;
     auto q_addr = [&](int ks) -> uint32_t {        // fragments of k-steps ks, ks+1 (ks even)
         const int ksi = ks + (qmat >> 1);
         const uint32_t ch = (uint32_t)(((ksi & 3) << 1) + (qmat & 1));
-        return qtile_s + (uint32_t)(ksi >> 2) * 1024u + (uint32_t)qrow * 128u +
-               ((ch ^ (uint32_t)qrow) << 4);
+        return qtile_s + (uint32_t)(ksi >> 2) * (uint32_t)C::QTILE_STRIDE +
+               (qrow_base + (uint32_t)qrow) * 128u + ((ch ^ (uint32_t)qrow) << 4);
     };
     const uint64_t qpolicy = l2_evict_last_policy();
     float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
@@ -466,7 +479,7 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
         // query's position: for S = 1 the first and last page of the range.
         int32_t clo0, chi0, clo1, chi1;
         {
-            const int32_t f0 = x.hg * kHeadTile + 2 * t;
+            const int32_t f0 = x.hg * C::TW + (C::COLPAR ? 8 * w : 0) + 2 * t;
             const int32_t pos0 = x.g.len - p.S + f0 % p.S;
             const int32_t pos1 = x.g.len - p.S + (f0 + 1) % p.S;
             chi0 = pos0 + 1;
@@ -497,11 +510,13 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
         }
 
         // Head columns past the unit's valid ones read other heads' rows of the
-        // tile (or its zero fill): their q is zeroed.
+        // tile (or its zero fill): their q is zeroed.  wvalid: valid columns
+        // of this warp's tile (column-parallel), else of the unit.
+        const int wvalid = C::COLPAR ? min(max(x.nvalid - 8 * w, 0), 8) : x.nvalid;
         uint32_t qr[C::Q_IN_REGS ? C::KSTEPS : 1][2];
         if constexpr (C::Q_IN_REGS) {
             if constexpr (C::KV == GA_KV_BF16) {
-                const uint32_t keep = (gid < x.nvalid) ? 0xffffffffu : 0u;
+                const uint32_t keep = (gid < wvalid) ? 0xffffffffu : 0u;
 #pragma unroll
                 for (int ks = 0; ks < C::KSTEPS; ks += 2) {
                     uint32_t r[4];
@@ -519,13 +534,24 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
                     qr[ks][1] = v.y;
                 }
             }
+        } else if constexpr (C::KV == GA_KV_BF16 && C::COLPAR) {
+            if (wvalid < 8) {                  // warp-uniform: zero this warp's rows past the valid ones
+                constexpr int QT = C::D / 64;
+                const int nz = (8 - wvalid) * QT * 8;
+                for (int e = lane; e < nz; e += 32) {
+                    const int n = 8 * w + wvalid + e / (QT * 8), tl = (e / 8) % QT, c = e % 8;
+                    *reinterpret_cast<uint4*>(qtile + tl * C::QTILE_STRIDE + n * 128 + c * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
         } else if constexpr (C::KV == GA_KV_BF16) {
             if (x.nvalid < kHeadTile) {        // unit-uniform: zero those rows of the tile once
                 constexpr int QT = C::D / 64;
                 const int nz = (kHeadTile - x.nvalid) * QT * 8;
                 for (int e = tid; e < nz; e += C::NCT) {
                     const int n = x.nvalid + e / (QT * 8), tl = (e / 8) % QT, c = e % 8;
-                    *reinterpret_cast<uint4*>(qtile + tl * 1024 + n * 128 + c * 16) =
+                    *reinterpret_cast<uint4*>(qtile + tl * C::QTILE_STRIDE + n * 128 + c * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 named_barrier(1, C::NCT);
@@ -537,7 +563,9 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
 #pragma unroll
         for (int mt = 0; mt < C::MTILES; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-        for (int i = w; i < x.np; i += C::NCW) {
+        // page-parallel: warp w takes pages w, w + NCW, ...; column-parallel:
+        // every warp takes every page
+        for (int i = C::COLPAR ? 0 : w; i < x.np; i += C::COLPAR ? 1 : C::NCW) {
             const uint32_t n = seq_base + (uint32_t)i;
             const uint32_t slot = n % C::NS;
             const uint32_t full = bars + 8 * slot;
@@ -550,7 +578,7 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
                 }
             }
             ready = __all_sync(0xffffffffu, ready);
-            if (ready && flags[slot] == 0) {
+            if (ready && flags[slot] == 0 && (!C::COLPAR || wvalid > 0)) {
                 const uint32_t kb = ring + slot * C::STAGE_BYTES;
                 const uint32_t vb = C::ALIAS ? kb : kb + C::BLOCK_BYTES;
                 // ---- S^T = K Q^T (16 keys x 8 heads), 4 independent chains
@@ -748,7 +776,7 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
         if (un < U) locate_next(un);
         // generic writes to the q tile (E4M3 fragments, zeroed rows) are ordered
         // before the next bulk copy into it (reads need no proxy fence)
-        if (C::KV == GA_KV_E4M3 || (!C::Q_IN_REGS && x.nvalid < kHeadTile))
+        if (C::KV == GA_KV_E4M3 || (!C::Q_IN_REGS && x.nvalid < C::TW))
             fence_proxy_async_shared();
 
         // ---- merge the warps' (m, l, O) in a fixed order
@@ -756,6 +784,62 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        if constexpr (C::COLPAR) {
+            // Column-parallel: each warp holds the whole softmax of its own
+            // columns; after the q tile is released, it scales and stores them.
+            named_barrier(1, C::NCT);
+            if (tid == 0) {
+                const int issue = (un < U && !*abort_flag) ? 1 : 0;
+                *q_issued = issue;
+                if (issue) {
+                    mbar_arrive_expect_tx(qbar, C::Q_BYTES);
+                    tma_load_3d(qtile_s, tmQ, qbar, 0, unit_q_row(p, nl), 0, qpolicy);
+                }
+            }
+            const float fa0 = (l0 == 0.f) ? 0.f : __fdividef(vfac, l0 * C::PSCALE);
+            const float fa1 = (l1 == 0.f) ? 0.f : __fdividef(vfac, l1 * C::PSCALE);
+            const bool c0 = 2 * t < wvalid, c1 = 2 * t + 1 < wvalid;
+            const int64_t h = x.h0 + 8 * w + 2 * t;          // column 2t of this lane
+            const int64_t r0 = (int64_t)x.b * p.Hq + h;      // its output row
+            const bool ok0 = c0 && GA_CHK((r0 + 1) * C::D <= p.out_elems &&
+                                          (single || (x.rc < p.rc_capacity && p.partial_o)));
+            const bool ok1 = c1 && GA_CHK((r0 + 2) * C::D <= p.out_elems &&
+                                          (single || (x.rc < p.rc_capacity && p.partial_o)));
+            if ((c0 && !ok0) || (c1 && !ok1)) report(p.err_word, kErrSelfCheck);
+#pragma unroll
+            for (int mt = 0; mt < C::MTILES; ++mt) {
+                const int d0 = 16 * mt + gid, d1 = d0 + 8;
+                if (single) {
+                    if (ok0) {
+                        p.out[r0 * C::D + d0] = __float2bfloat16_rn(o[mt][0] * fa0);
+                        p.out[r0 * C::D + d1] = __float2bfloat16_rn(o[mt][2] * fa0);
+                    }
+                    if (ok1) {
+                        p.out[(r0 + 1) * C::D + d0] = __float2bfloat16_rn(o[mt][1] * fa1);
+                        p.out[(r0 + 1) * C::D + d1] = __float2bfloat16_rn(o[mt][3] * fa1);
+                    }
+                } else {
+                    float* po = p.partial_o + (x.rc * p.Hq + h) * (int64_t)C::D;
+                    if (ok0) {
+                        po[d0] = o[mt][0] * fa0;
+                        po[d1] = o[mt][2] * fa0;
+                    }
+                    if (ok1) {
+                        po[C::D + d0] = o[mt][1] * fa1;
+                        po[C::D + d1] = o[mt][3] * fa1;
+                    }
+                }
+            }
+            if (!single && gid == 0) {        // natural-log LSE of each column
+                if (ok0)
+                    p.partial_lse[x.rc * p.Hq + h] =
+                        (l0 == 0.f) ? -CUDART_INF_F : (m0 + log2f(l0)) * CUDART_LN2_F;
+                if (ok1)
+                    p.partial_lse[x.rc * p.Hq + h + 1] =
+                        (l1 == 0.f) ? -CUDART_INF_F : (m1 + log2f(l1)) * CUDART_LN2_F;
+            }
+            continue;
         }
         if (gid == 0) {
             mlw[w * kHeadTile + 2 * t] = m0;
@@ -931,7 +1015,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(bars + 8 * s, 1);
-            mbar_init(bars + 8 * (C::NS + s), 1);
+            mbar_init(bars + 8 * (C::NS + s), C::COLPAR ? C::NCW : 1);   // consumers of a stage
         }
         mbar_init(bars + 8 * (2 * C::NS), 1);      // q tile
         mbar_init_fence();
@@ -1007,7 +1091,7 @@ static int run(const DecodeArgs& a, int slot) {
     // q as [B * Hq * S, D] bf16, boxes of one group of 8 (query, head)
     // columns (rows past the end read as zeros)
     rc = encode_rows_map(&tmQ, a.q, GA_KV_BF16, (int64_t)a.batch * a.num_q_heads * S, a.head_dim,
-                         kHeadTile);
+                         C::TW);
     if (rc != GA_OK) return rc;
 
     DecodeParams p;
@@ -1032,7 +1116,8 @@ static int run(const DecodeArgs& a, int slot) {
     p.Hq = a.num_q_heads * S;
     p.Hkv = a.num_kv_heads;
     p.group = a.num_q_heads / a.num_kv_heads * S;
-    p.HG = head_groups(p.group);
+    p.TW = C::TW;
+    p.HG = (p.group + C::TW - 1) / C::TW;
     p.window = effective_window(a.window, S);
     p.S = S;
     p.mask_window = a.window;
@@ -1080,9 +1165,24 @@ using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, GA_GE_NS>;
 #define GA_GA_NS 12
 #endif
 using CfgGlobalBf16Alias = DecodeCfg<512, GA_KV_BF16, GA_GA_NCW, GA_GA_NS, true>;
+// Column-parallel (4 tiles of 8 columns per unit, every warp on every page).
+#ifndef GA_CL_NS
+#define GA_CL_NS 12
+#endif
+#ifndef GA_CG_NS
+#define GA_CG_NS 5
+#endif
+using CfgLocalBf16Col = DecodeCfg<256, GA_KV_BF16, 4, GA_CL_NS, false, true>;
+using CfgGlobalBf16Col = DecodeCfg<512, GA_KV_BF16, 4, GA_CG_NS, false, true>;
 using CfgGlobalE4m3Alias = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, 2 * GA_GE_NS, true>;
 
 int launch_decode(const DecodeArgs& a) {
+    // more than one tile of (query, head) columns per kv head (multi-query
+    // decode, wide groups) and a plan made for column-parallel units
+    const bool colpar = a.plan->col_tile > kHeadTile && a.kv_dtype == GA_KV_BF16 &&
+                        a.k_pool != a.v_pool;
+    if (colpar)
+        return a.head_dim == 256 ? run<CfgLocalBf16Col>(a, 6) : run<CfgGlobalBf16Col>(a, 7);
     if (a.head_dim == 256)
         return a.kv_dtype == GA_KV_BF16 ? run<CfgLocalBf16>(a, 0) : run<CfgLocalE4m3>(a, 1);
     if (a.head_dim == 512 && a.k_pool == a.v_pool)

@@ -53,7 +53,7 @@ class GAError(RuntimeError):
 class ga_plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "splits", "chunk_pages", "batch", "num_q_heads", "num_kv_heads", "head_dim",
-        "window", "page_size", "grid", "flags", "touch_stride", "q_len", "reserved")] + [
+        "window", "page_size", "grid", "flags", "touch_stride", "q_len", "col_tile")] + [
         (n, ctypes.c_int64) for n in ("row_chunks", "units", "workspace_bytes",
                                        "partial_o_offset", "partial_lse_offset",
                                        "touch_log_offset")]

@@ -71,8 +71,12 @@ def test_multi_query_plan(ga):
     assert four.partial_lse_offset >= four.row_chunks * 4 * 4 * 256 * 4
     # 4 queries x group 2 = 8 columns: still one head group per kv head
     assert four.units == one.units
+    assert one.col_tile == four.col_tile == 8
+    # 8 queries x group 2 = 16 columns: one column-parallel unit of 4 tiles of 8
     eight = ga.ga_plan_splits_mq([40, 33], q_len=8, **kw)
-    assert eight.units == 2 * one.units
+    assert eight.col_tile == 32 and eight.units == one.units
+    wide = ga.ga_plan_splits_mq([40, 33], q_len=40, **kw)        # 80 columns: 3 units
+    assert wide.units == 3 * one.units
     # union window, row of length 33, W = 16: one query reads keys 17..32
     # (pages 1..2); four queries (positions 29..32) read keys 14..32 (pages 0..2)
     w1 = ga.ga_plan_splits([33], num_q_heads=2, num_kv_heads=2, head_dim=256, window=16,
@@ -132,6 +136,9 @@ def test_decode_rejects_before_launch(ga):
     bad.q_len = 0
     assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG                 # corrupted plan
     bad.q_len = ga.MAX_Q_LEN + 1
+    assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
+    bad = _plan(ga)
+    bad.col_tile = 16
     assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
 
 

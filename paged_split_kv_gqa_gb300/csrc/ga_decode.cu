@@ -1140,16 +1140,16 @@ static int run(const DecodeArgs& a, int slot) {
 // Tuned shapes per (head_dim, KV type): consumer warps, ring stages (a
 // multiple of the warps).  The macros let a build sweep them.
 #ifndef GA_LB_NCW
-#define GA_LB_NCW 2
-#define GA_LB_NS 12
+#define GA_LB_NCW 3
+#define GA_LB_NS 9
 #endif
 #ifndef GA_LE_NCW
 #define GA_LE_NCW 7
 #define GA_LE_NS 14
 #endif
 #ifndef GA_GB_NCW
-#define GA_GB_NCW 2
-#define GA_GB_NS 6
+#define GA_GB_NCW 4
+#define GA_GB_NS 4
 #endif
 #ifndef GA_GE_NCW
 #define GA_GE_NCW 6

@@ -1159,10 +1159,10 @@ using CfgLocalBf16 = DecodeCfg<256, GA_KV_BF16, GA_LB_NCW, GA_LB_NS>;
 using CfgLocalE4m3 = DecodeCfg<256, GA_KV_E4M3, GA_LE_NCW, GA_LE_NS>;
 using CfgGlobalBf16 = DecodeCfg<512, GA_KV_BF16, GA_GB_NCW, GA_GB_NS>;
 using CfgGlobalE4m3 = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, GA_GE_NS>;
-// K == V (one pool): half-size stages, twice as many.
+// K == V (one pool): half-size stages; four per-warp merge regions fit.
 #ifndef GA_GA_NCW
 #define GA_GA_NCW 4
-#define GA_GA_NS 12
+#define GA_GA_NS 8
 #endif
 using CfgGlobalBf16Alias = DecodeCfg<512, GA_KV_BF16, GA_GA_NCW, GA_GA_NS, true>;
 // Column-parallel (4 tiles of 8 columns per unit, every warp on every page).

@@ -94,8 +94,12 @@ enum {
 /* Plan flags. */
 enum {
     GA_PLAN_TOUCH_LOG = 1,        /* decode records every physical page it reads (tests) */
-    GA_PLAN_EXTERNAL_COMBINE = 2  /* a split decode call leaves the partials in the
+    GA_PLAN_EXTERNAL_COMBINE = 2, /* a split decode call leaves the partials in the
                                      workspace; the caller runs ga_splitkv_combine */
+    GA_PLAN_TEST_WAIT_TIMEOUT = 4 /* test hook: CTA 0 of the decode launch issues no page, so
+                                     its consumers' bounded waits run out (~2 s) and the
+                                     call reports GA_DEVERR_TIMEOUT; CTA 0's rows are then
+                                     undefined.  Never set outside tests. */
 };
 
 /*

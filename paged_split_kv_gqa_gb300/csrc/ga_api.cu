@@ -181,7 +181,7 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     if (q_len > kMaxQLen) return GA_ERR_UNSUPPORTED;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || window < 0 ||
         num_sms < 1 || requested_splits < 0 || fixed_chunk_tokens < 0 ||
-        (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~(GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE)))
+        (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~(GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE | GA_PLAN_TEST_WAIT_TIMEOUT)))
         return GA_ERR_INVALID_ARG;
     if (batch > kMaxBatch) return GA_ERR_UNSUPPORTED;
     if (head_dim != 256 && head_dim != 512) return GA_ERR_UNSUPPORTED;

@@ -64,6 +64,7 @@ struct DecodeParams {
     int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
     int32_t S, mask_window;
     int32_t TW;                   // columns per work unit (8, or 8 x warps column-parallel)
+    int32_t test_wait_timeout;    // test hook: CTA 0's producer issues nothing
     float scale_log2;             // softmax scale * log2(e)
     int64_t out_elems;            // B * Hq * D
     int64_t pool_rows;            // num_pages * Hkv * P
@@ -234,6 +235,9 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
     constexpr int kIssueLanes = 4;
     static_assert(C::NS >= kIssueLanes && C::NS <= 32, "ring depth");
     const int lane = threadIdx.x & 31;
+    // Test hook: nothing is armed or copied for CTA 0, so its consumers' bounded
+    // waits run out and report GA_DEVERR_TIMEOUT (no copy is left in flight).
+    if (p.test_wait_timeout && blockIdx.x == 0) return;
     const uint64_t policy = l2_evict_first_policy();
     uint32_t seq = 0;                 // pages handed to the ring so far
     bool stop = false;
@@ -1125,6 +1129,7 @@ static int run(const DecodeArgs& a, int slot) {
     p.splits = pl.splits;
     p.chunk_pages = pl.chunk_pages;
     p.touch_stride = pl.touch_stride;
+    p.test_wait_timeout = (pl.flags & GA_PLAN_TEST_WAIT_TIMEOUT) ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.pool_rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
     p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;

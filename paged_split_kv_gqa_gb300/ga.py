@@ -40,6 +40,7 @@ GA_SPLIT_COUNT = 1
 GA_SPLIT_CHUNK = 2
 GA_PLAN_TOUCH_LOG = 1
 GA_PLAN_EXTERNAL_COMBINE = 2
+GA_PLAN_TEST_WAIT_TIMEOUT = 4
 PAGE_SIZE = 16
 MAX_Q_LEN = 64
 

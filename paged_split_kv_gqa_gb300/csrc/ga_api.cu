@@ -44,9 +44,10 @@ static EncodeTiledFn encode_fn() {
 // key row, chunk column): strides D*esize bytes per key row and 128 bytes per
 // chunk column.  One box {e, 16, D*esize/128} is a whole page-head block and
 // lands in shared memory as [chunk column][key row][128 bytes] with the
-// 128-byte swizzle, i.e. one 2 KB tile per 128-byte column.
+// 128-byte swizzle, i.e. one 2 KB tile per 128-byte column; box_cols > 0
+// narrows the box to that many chunk columns.
 int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_t rows,
-                    int32_t head_dim, int32_t box_rows) {
+                    int32_t head_dim, int32_t box_rows, int32_t box_cols) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return GA_ERR_CUDA;
     const int esz = kv_dtype == GA_KV_BF16 ? 2 : 1;
@@ -54,7 +55,8 @@ int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_
     const cuuint32_t cols = (cuuint32_t)(head_dim * esz / 128);
     const cuuint64_t dims[3] = {(cuuint64_t)e, (cuuint64_t)rows, (cuuint64_t)cols};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * esz, 128};
-    const cuuint32_t box[3] = {e, (cuuint32_t)box_rows, cols};
+    const cuuint32_t box[3] = {e, (cuuint32_t)box_rows,
+                               box_cols > 0 ? (cuuint32_t)box_cols : cols};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(map,
                            kv_dtype == GA_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -67,7 +69,7 @@ int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_
 }
 
 int ensure_smem_attr(const void* func, int bytes, int slot) {
-    static std::atomic<uint64_t> done[8];
+    static std::atomic<uint64_t> done[16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GA_ERR_CUDA;
     const uint64_t bit = 1ull << (dev & 63);

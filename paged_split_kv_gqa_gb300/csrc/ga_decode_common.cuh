@@ -1,0 +1,159 @@
+// ga_decode_common.cuh -- what every decode kernel shares: the launch
+// parameters, the work-unit geometry (row-chunk, kv head, head group) and the
+// per-CTA prefix of row chunks that maps a unit index to its row.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ga_device.cuh"
+#include "ga_internal.h"
+
+namespace ga {
+
+struct DecodeParams {
+    const __nv_bfloat16* q;       // [B, Hq, D]
+    const int32_t* page_table;    // [B, pt_stride]
+    const int32_t* seq_lens;      // [B]
+    const float* k_scale;         // [Hkv] (E4M3)
+    const float* v_scale;
+    __nv_bfloat16* out;           // [B, Hq, D]
+    float* partial_o;             // [rc_capacity, Hq, D]
+    float* partial_lse;           // [rc_capacity, Hq]
+    int32_t* touch_log;           // [rc_capacity, touch_stride] or null
+    int32_t* err_word;
+    int64_t pt_stride;
+    int64_t num_pages;
+    int64_t rc_capacity;
+    // Hq and group count (query, head) columns: an S-query decode has
+    // Hq * S columns, S adjacent per query head ([B, Hq, S, D]); window is
+    // the union window of a row's S queries (page ranges), mask_window the
+    // real one (per-column masks).
+    int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
+    int32_t S, mask_window;
+    int32_t TW;                   // columns per work unit (8, or 8 x warps column-parallel)
+    int32_t test_wait_timeout;    // test hook: CTA 0's producer issues nothing
+    float scale_log2;             // softmax scale * log2(e)
+    int64_t out_elems;            // B * Hq * D
+    int64_t pool_rows;            // num_pages * Hkv * P
+};
+
+// GA_CHECKED builds test every shared- and global-memory access of the decode
+// kernels against its buffer, record GA_DEVERR_SELF_CHECK and skip the access.
+#ifdef GA_CHECKED
+#define GA_CHK(cond) (cond)
+#else
+#define GA_CHK(cond) true
+#endif
+
+// Row owning row-chunk rc: largest b with pre[b] <= rc.
+__device__ __forceinline__ int find_row(const int32_t* pre, int B, int64_t rc) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)pre[mid] <= rc) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct UnitInfo {
+    int64_t rc;
+    int32_t b, c, hg, j, p0, np, h0, nvalid;
+    RowGeom g;
+};
+
+// A unit's coordinates from shared memory only; its length load can be issued
+// right after and consumed later (finish_unit), off the critical path.
+struct UnitLoc {
+    int64_t rc;
+    int32_t b, c, hg;
+};
+
+__device__ __forceinline__ UnitLoc locate_unit(const DecodeParams& p, const int32_t* pre,
+                                               int64_t u) {
+    UnitLoc l;
+    if (u < (int64_t(1) << 31)) {      // unit_coords in 32 bits (64-bit division is slow)
+        const uint32_t v = (uint32_t)u, hg = (uint32_t)p.HG, hkv = (uint32_t)p.Hkv;
+        const uint32_t q1 = (hg == 1) ? v : v / hg;
+        const uint32_t r = q1 / hkv;
+        l.hg = (int32_t)(v - q1 * hg);
+        l.c = (int32_t)(q1 - r * hkv);
+        l.rc = r;
+    } else {
+        unit_coords(u, p.Hkv, p.HG, &l.rc, &l.c, &l.hg);
+    }
+    l.b = find_row(pre, p.B, l.rc);
+    return l;
+}
+
+// First q row (in the [B * Hq, D] view) of a unit's head group.
+__device__ __forceinline__ int32_t unit_q_row(const DecodeParams& p, const UnitLoc& l) {
+    return l.b * p.Hq + l.c * p.group + l.hg * p.TW;
+}
+
+__device__ __forceinline__ UnitInfo finish_unit(const DecodeParams& p, const int32_t* pre,
+                                                const UnitLoc& l, int32_t len) {
+    UnitInfo x;
+    x.rc = l.rc;
+    x.b = l.b;
+    x.c = l.c;
+    x.hg = l.hg;
+    x.j = (int32_t)(x.rc - pre[x.b]);
+    x.g = row_geometry(len, p.window, p.pt_stride, p.mode, p.splits, p.chunk_pages);
+    chunk_pages_of(x.g, x.j, &x.p0, &x.np);
+    x.h0 = x.c * p.group + x.hg * p.TW;
+    int nv = p.group - x.hg * p.TW;
+    x.nvalid = nv < p.TW ? nv : p.TW;
+    return x;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const DecodeParams& p, const int32_t* pre,
+                                              int64_t u) {
+    const UnitLoc l = locate_unit(p, pre, u);
+    return finish_unit(p, pre, l, __ldg(p.seq_lens + l.b));
+}
+
+// Every thread of the block: chunk count of every row, then an inclusive
+// prefix pre[b+1] = sum_{b' <= b} in shared memory.  Reports invalid lengths
+// (block 0) and returns false (the whole block must then exit) when a split
+// plan's row-chunk capacity is too small.
+__device__ __forceinline__ bool build_row_prefix(const DecodeParams& p, int32_t* pre,
+                                                 int nthreads, int64_t* total_rc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int bad = 0;
+    for (int b = threadIdx.x; b < p.B; b += nthreads) {
+        const RowGeom g = row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride, p.mode,
+                                       p.splits, p.chunk_pages);
+        pre[b + 1] = g.chunks;
+        bad |= g.bad_len ? 1 : 0;
+    }
+    bad = __syncthreads_or(bad);
+    if (warp == 0) {
+        const int seg = (p.B + 31) / 32;
+        const int lo = min(p.B, lane * seg), hi = min(p.B, lo + seg);
+        int run = 0;
+        for (int b = lo; b < hi; ++b) {
+            run += pre[b + 1];
+            pre[b + 1] = run;
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const int excl = incl - run;
+        for (int b = lo; b < hi; ++b) pre[b + 1] += excl;
+        if (lane == 0) pre[0] = 0;
+    }
+    __syncthreads();
+    if (bad && blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrSeqLen);
+    *total_rc = pre[p.B];
+    if (p.mode != kSplitNone && *total_rc > p.rc_capacity) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrCapacity);
+        return false;
+    }
+    return true;
+}
+
+}  // namespace ga

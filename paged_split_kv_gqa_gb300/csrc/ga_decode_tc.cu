@@ -1,0 +1,730 @@
+// ga_decode_tc.cu -- sliding-window (hd256) decode over an E4M3 KV pool with
+// both products on the fifth-generation tensor cores (tcgen05, accumulators
+// in tensor memory).
+//
+// Why a separate kernel.  With E4M3 pages a decode warp that runs its own
+// m16n8k32 MMAs spends its time on per-warp latency chains (QK, softmax, P
+// split, PV per 16-key page), not on bandwidth.  Here one thread issues the
+// MMAs for a whole 128-key "superstage" (8 pages) and four warps only run the
+// softmax, so the warps' work per byte falls by an order of magnitude.  The
+// method is unchanged: the paged softmax attention of the sliding family
+// ("[Model] Gemma 4 M3 31B", Acceptance Criteria: windows of 1024 with the
+// 1023 / 1024 / 1025 boundaries; "[Model] Gemma 4 M2 26B-A4B", Proposed Plan:
+// opt-in FP8 pool for the sliding family).
+//
+// Layout of one superstage in shared memory (64 KB): four 16 KB regions,
+// K dims 0-127, K dims 128-255, V dims 0-127, V dims 128-255, each a dense
+// [128 keys][128 bytes] tile with the 128-byte swizzle.  Page i of the
+// superstage fills rows 16i .. 16i+15 of each region (four 2 KB bulk tensor
+// copies per page), so the key rows of 8 pages sit at one uniform stride and
+// a single MMA descriptor spans them.
+//
+// Products (M = 128, N = 16, K = 32 per instruction, fp32 accumulate):
+//   S   [keys x 16]  = K [keys x dims]  . Qs^T   (A K-major, B K-major)
+//   O^T [dims x 16] += V^T [dims x keys] . Ps^T  (A MN-major, B K-major)
+// The 16 columns are 8 (query, head) columns twice: q scaled per column by
+// 448 / amax and split into E4M3 hi and lo parts (columns f and 8 + f), and
+// likewise P (scaled by 2^6) into hi and lo; a column's result is the sum of
+// its two halves.  S sits in TMEM lanes = keys, O^T in lanes = dims, so
+// softmax thread t owns key t of a superstage and dim t of each 128-dim half.
+//
+// Roles (192 threads): warps 0-3 softmax and output, warp 4 allocates TMEM
+// and its lane 0 issues every MMA, warp 5 streams pages with bulk tensor
+// copies.  Hand-offs are mbarriers; every wait is bounded.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math_constants.h>
+
+#include "ga_decode_common.cuh"
+
+namespace ga {
+
+namespace tc {
+
+constexpr int D = 256;
+constexpr int NSS = 3;                            // superstages in the ring
+constexpr int SS_PAGES = 8;                       // pages per superstage: 128 keys = MMA M
+constexpr int CHUNK_BYTES = SS_PAGES * kPageSize * 128;   // [128 keys][128 B]
+constexpr int SS_BYTES = 4 * CHUNK_BYTES;         // K lo, K hi, V lo, V hi halves
+constexpr int PAGE_BYTES = 2 * kPageSize * D;     // K + V of one page-head block
+constexpr int QBUF_BYTES = 2 * 16 * 128;          // [dim half][16 rows][128 B]
+constexpr int PBUF_BYTES = 16 * 128;              // [16 rows][128 keys]
+constexpr int NSW = 4;                            // softmax warps
+constexpr int MMA_WARP = 4, PROD_WARP = 5;
+constexpr int NTHREADS = 192;
+constexpr int TMEM_COLS = 128;                    // S: 2 x 16 columns, O: 2 x 32 columns
+constexpr int TM_S = 0, TM_O = 32;
+constexpr float PSCALE = 64.0f;                   // P scale: with slack 2^2, P <= 256 < 448
+constexpr float MAX_SLACK = 2.0f;
+
+constexpr int al(int x) { return (x + 127) / 128 * 128; }
+constexpr int OFF_RING = 0;
+constexpr int OFF_Q = OFF_RING + NSS * SS_BYTES;
+constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
+constexpr int OFF_RED = OFF_P + 2 * PBUF_BYTES;                 // [2][4 warps][8] floats
+constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4);  // [2][8] q scales
+constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
+constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
+constexpr int OFF_BARS = al(OFF_FLAGS + NSS * 4);
+// barriers: full[NSS], empty[NSS], then two each of s_full, s_free, p_full,
+// pv_done, o_free, q_full, and fin
+constexpr int B_FULL = 0, B_EMPTY = NSS, B_SFULL = 2 * NSS, B_SFREE = B_SFULL + 2,
+              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2,
+              B_QFULL = B_OFREE + 2, B_FIN = B_QFULL + 2, NBARS = B_FIN + 1;
+constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
+constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack for 1024-byte alignment
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && SS_BYTES % 1024 == 0,
+              "swizzle-128B operands need 1024-byte aligned tiles");
+static_assert(NSS >= 2, "ring depth");
+
+__device__ __forceinline__ uint32_t bar(uint32_t bars, int i) { return bars + 8u * (uint32_t)i; }
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t b, uint32_t parity,
+                                              volatile int* abort_flag) {
+    if (mbar_try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, parity)) {
+        if (*abort_flag || clock64() - t0 > kWaitBudgetCycles) return false;
+    }
+    return true;
+}
+
+// Two values -> two E4M3 codes (hi) and the E4M3 codes of their remainders
+// (lo), low byte first: hi + lo carries ~8 bits of the value.
+__device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = f32x2_to_e4m3x2(a, b);
+    const uint32_t h = e4m3x2_to_f16x2(hi);
+    const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    lo = f32x2_to_e4m3x2(a - r.x, b - r.y);
+}
+
+// ------------------------------------------------------------------ producer
+
+// Warp 5.  For each superstage of each unit: wait until the slot is free,
+// arm its "full" barrier with the bytes of the good pages, and let lanes
+// 0..7 each copy one page (K and V, both dim halves).  Pages with an invalid
+// id are flagged (bit i of flags[slot]) and not copied.
+__device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
+                         const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
+                         volatile uint32_t* flags, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    // Test hook: nothing is armed or copied for CTA 0, so the other roles'
+    // bounded waits run out and report GA_DEVERR_TIMEOUT.
+    if (p.test_wait_timeout && blockIdx.x == 0) return;
+    const uint64_t policy = l2_evict_first_policy();
+    uint32_t seq = 0;                 // superstages armed so far
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
+        const UnitInfo x = unit_info(p, pre, u);
+        // the next unit's q rows into L2 for the softmax warps, which prepare
+        // them while this unit streams
+        const int64_t un = u + gridDim.x;
+        if (un < U) {
+            const int64_t r = (int64_t)unit_q_row(p, locate_unit(p, pre, un)) + (lane >> 2);
+            if ((r + 1) * D <= p.out_elems)
+                prefetch_l2(reinterpret_cast<const char*>(p.q + r * D) + 128 * (lane & 3));
+        }
+        const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride + x.p0;
+        int32_t ids = (lane < x.np) ? __ldg(tbl + lane) : -1;               // pages 0..31
+        int32_t ids_nxt = (32 + lane < x.np) ? __ldg(tbl + 32 + lane) : -1; // pages 32..63
+        const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
+        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        for (int s = 0; s < nss; ++s) {
+            if (s > 0 && (s & 3) == 0) {      // next batch of 32 page ids, one batch ahead
+                ids = ids_nxt;
+                const int nb = 32 * (s / 4 + 1) + lane;
+                ids_nxt = (nb < x.np) ? __ldg(tbl + nb) : -1;
+            }
+            const uint32_t n = seq, slot = n % NSS, round = n / NSS;
+            bool ok = true;
+            if (lane == 0) ok = !*abort_flag && wait_or_abort(bar(bars, B_EMPTY + slot), (round & 1) ^ 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) {
+                    report(p.err_word, kErrTimeout);
+                    *abort_flag = 1;
+                }
+                stop = true;
+                break;
+            }
+            const int pi = SS_PAGES * s + (lane & 7);
+            const int32_t pid = __shfl_sync(0xffffffffu, ids, (8 * (s & 3) + (lane & 7)) & 31);
+            const bool present = lane < SS_PAGES && pi < x.np;
+            const bool valid_id = present && page_ok(pid, p.num_pages);
+            const int32_t y = valid_id ? page_block_row(pid, x.c, p.Hkv) : 0;
+            const bool good = valid_id && GA_CHK(y >= 0 && (int64_t)y + kPageSize <= p.pool_rows);
+            const uint32_t gm = __ballot_sync(0xffffffffu, good);
+            const uint32_t pm = __ballot_sync(0xffffffffu, present);
+            const uint32_t full = bar(bars, B_FULL + slot);
+            if (lane == 0) {
+                flags[slot] = pm & ~gm;
+                mbar_arrive_expect_tx(full, (uint32_t)__popc(gm) * PAGE_BYTES);
+            }
+            __syncwarp();
+            if (good) {
+                const uint32_t dst = ring + slot * SS_BYTES + (uint32_t)lane * (kPageSize * 128);
+                tma_load_3d(dst, tmK, full, 0, y, 0, policy);
+                tma_load_3d(dst + CHUNK_BYTES, tmK, full, 0, y, 1, policy);
+                tma_load_3d(dst + 2 * CHUNK_BYTES, tmV, full, 0, y, 0, policy);
+                tma_load_3d(dst + 3 * CHUNK_BYTES, tmV, full, 0, y, 1, policy);
+            } else if (present) {
+                report(p.err_word, valid_id ? kErrSelfCheck : kErrPageId);
+            }
+            if (log && present && pi < p.touch_stride && GA_CHK(x.rc < p.rc_capacity))
+                p.touch_log[x.rc * p.touch_stride + pi] = pid;
+            ++seq;
+        }
+    }
+    // Never leave with a copy in flight into this CTA's shared memory.
+    if (lane < NSS && (uint32_t)lane < seq) {
+        const uint32_t last = (uint32_t)lane + ((seq - 1 - (uint32_t)lane) / NSS) * NSS;
+        if (!mbar_wait(bar(bars, B_FULL + lane), (last / NSS) & 1)) {
+            report(p.err_word, kErrTimeout);
+            *abort_flag = 1;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+// Warp 4, lane 0.  Over the CTA's superstages in order it issues S(m) = K q^T
+// and then O += V^T P^T for the previous superstage (m - 1), so the softmax of
+// m can start while P(m - 1) is being formed.  A unit's first PV overwrites its
+// O buffer (accumulate off), after the epilogue two active units back freed it.
+__device__ void mma_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
+                           uint32_t qbuf, uint32_t pbuf, uint32_t bars, uint32_t tmem,
+                           volatile int* abort_flag) {
+    constexpr uint32_t IQK = idesc_e4m3(128, 16, false, false);
+    constexpr uint32_t IPV = idesc_e4m3(128, 16, true, false);
+    bool stop = false;
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        if (stop) return false;
+        if (*abort_flag || !wait_or_abort(bar(bars, b), parity, abort_flag)) {
+            report(p.err_word, kErrTimeout);
+            *abort_flag = 1;
+            stop = true;
+            return false;
+        }
+        return true;
+    };
+    // the superstage whose PV is still to be issued
+    bool pend = false;
+    uint32_t pn = 0, pk = 0;
+    int pnpg = 0;
+    bool pfirst = false;
+    auto issue_pv = [&]() {
+        pend = false;
+        const uint32_t pb = pn & 1, ob = pk & 1;
+        if (pfirst && !wait(B_OFREE + (int)ob, ((pk >> 1) & 1) ^ 1)) return;
+        if (!wait(B_PFULL + (int)pb, (pn >> 1) & 1)) return;
+        tc_fence_after();
+        const uint32_t slot = pn % NSS;
+        const int nks = (pnpg + 1) / 2;           // 32 keys (two pages) per instruction
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const uint32_t d = tmem + TM_O + 32 * ob + 16 * c;
+            const uint32_t va = ring + slot * SS_BYTES + (2 + c) * CHUNK_BYTES;
+            for (int ks = 0; ks < nks; ++ks)
+                tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, CHUNK_BYTES, 1024),
+                            smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024), IPV,
+                            (pfirst && ks == 0) ? 0u : 1u);
+        }
+        tc_commit(bar(bars, B_EMPTY + slot));     // the slot may be refilled
+        tc_commit(bar(bars, B_PVDONE + pb));      // P buffer free, O up to date
+    };
+    uint32_t n = 0, k = 0;                        // superstages, active units so far
+    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
+        const UnitInfo x = unit_info(p, pre, u);
+        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        if (nss == 0) continue;
+        const uint32_t qb = k & 1;
+        if (!wait(B_QFULL + (int)qb, (k >> 1) & 1)) break;
+        for (int s = 0; s < nss; ++s) {
+            const uint32_t m = n + s, slot = m % NSS, sb = m & 1;
+            if (!wait(B_FULL + (int)slot, (m / NSS) & 1)) break;
+            if (!wait(B_SFREE + (int)sb, ((m >> 1) & 1) ^ 1)) break;
+            tc_fence_after();
+            const uint32_t ka = ring + slot * SS_BYTES, qa = qbuf + qb * QBUF_BYTES;
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_e4m3(tmem + TM_S + 16 * sb,
+                                smem_desc_sw128(ka + c * CHUNK_BYTES + 32 * kk, 16, 1024),
+                                smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
+                                (c | kk) != 0 ? 1u : 0u);
+            tc_commit(bar(bars, B_SFULL + sb));
+            if (pend) issue_pv();
+            if (stop) break;
+            pend = true;
+            pn = m;
+            pk = k;
+            pnpg = min(SS_PAGES, x.np - SS_PAGES * s);
+            pfirst = (s == 0);
+        }
+        n += (uint32_t)nss;
+        ++k;
+    }
+    if (pend && !stop) issue_pv();
+    // Every MMA issued has completed before the block may free TMEM.
+    tc_commit(bar(bars, B_FIN));
+    if (!mbar_wait(bar(bars, B_FIN), 0)) {
+        report(p.err_word, kErrTimeout);
+        *abort_flag = 1;
+    }
+}
+
+// ------------------------------------------------------------------ softmax warps
+
+// Warps 0-3.  Thread t owns key t of every superstage (TMEM lane t of S) and
+// dim t of each 128-dim half of O.  Per superstage: read S, mask, online
+// softmax in base 2 (the running max is raised only when a score exceeds it
+// by more than MAX_SLACK; then O is rescaled in TMEM), write P's hi / lo
+// E4M3 parts as the PV operand, zero V rows the PV reads but no query
+// attends.  Per unit: prepare the next active unit's q operand, and at the
+// end read O and write the output (or a split partial and its LSE).
+__device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
+                              uint32_t bars, uint32_t tmem, volatile uint32_t* flags,
+                              volatile int* abort_flag) {
+    const int tid = threadIdx.x;
+    const int w = tid >> 5, lane = tid & 31;
+    const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);     // this warp's TMEM lanes
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [max | sum][4 warps][8]
+    float* qsc = reinterpret_cast<float*>(smem + OFF_QSC);     // [2][8]
+    uint8_t* qbuf = smem + OFF_Q;
+    uint8_t* pbuf = smem + OFF_P;
+    uint8_t* ring = smem + OFF_RING;
+    bool stop = false;
+
+    // Bounded wait by all 128 threads with one outcome for all of them.
+    auto wait_all = [&](int b, uint32_t parity) -> bool {
+        const bool ok = wait_or_abort(bar(bars, b), parity, abort_flag);
+        if (named_barrier_or(1, 128, !ok)) {
+            if (tid == 0) {
+                report(p.err_word, kErrTimeout);
+                *abort_flag = 1;
+            }
+            stop = true;
+            return false;
+        }
+        return true;
+    };
+
+    // q of unit y as the QK operand in buffer qb: column f scaled by
+    // 448 / amax_f, E4M3 hi part in row f and lo part in row 8 + f of each
+    // dim half ([16 rows][128 B], 128-byte swizzle).  Thread t takes column
+    // t / 16, dims 16 (t % 16) .. +15; rows of columns past the unit's valid
+    // ones are zero.
+    auto prep_q = [&](const UnitInfo& y, uint32_t qb) {
+        const int f = tid >> 4, d0 = 16 * (tid & 15);
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+        const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
+        if (f < y.nvalid) {
+            if (GA_CHK((row + 1) * D <= p.out_elems)) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + row * D + d0);
+                a = __ldg(src);
+                b = __ldg(src + 1);
+            } else {
+                report(p.err_word, kErrSelfCheck);
+            }
+        }
+        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float v[16];
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = bf16_lo(wv[i]);
+            v[2 * i + 1] = bf16_hi(wv[i]);
+            am = fmaxf(am, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+        if ((tid & 15) == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
+        const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
+        if ((tid & 15) == 0) qsc[qb * kHeadTile + f] = sc;
+        const float inv = 1.0f / sc;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t h01, l01, h23, l23;
+            split_e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv, h01, l01);
+            split_e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv, h23, l23);
+            hw[j] = h01 | (h23 << 16);
+            lw[j] = l01 | (l23 << 16);
+        }
+        const int c = d0 >> 7, jj = (d0 & 127) >> 4;
+        uint8_t* base = qbuf + qb * QBUF_BYTES + c * 2048;
+        *reinterpret_cast<uint4*>(base + f * 128 + ((jj ^ (f & 7)) << 4)) =
+            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(base + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
+            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bars, B_QFULL + (int)qb));
+    };
+
+    // A unit with no attended key: zero output (or a zero partial with an
+    // empty LSE).
+    auto write_empty = [&](const UnitInfo& x, bool single) {
+        for (int f = 0; f < x.nvalid; ++f) {
+            const int64_t h = x.h0 + f;
+            if (single) {
+                const int64_t r = (int64_t)x.b * p.Hq + h;
+                if (!GA_CHK((r + 1) * D <= p.out_elems)) continue;
+                p.out[r * D + tid] = __float2bfloat16_rn(0.f);
+                p.out[r * D + 128 + tid] = __float2bfloat16_rn(0.f);
+            } else if (GA_CHK(x.rc < p.rc_capacity && p.partial_o != nullptr)) {
+                float* po = p.partial_o + (x.rc * p.Hq + h) * (int64_t)D;
+                po[tid] = 0.f;
+                po[128 + tid] = 0.f;
+            }
+        }
+        if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity))
+            p.partial_lse[x.rc * p.Hq + x.h0 + tid] = -CUDART_INF_F;
+    };
+
+    uint32_t n = 0, k = 0;                      // superstages, active units so far
+    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
+        const UnitInfo x = unit_info(p, pre, u);
+        const bool single = (x.g.chunks == 1);
+        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        if (nss == 0) {
+            write_empty(x, single);
+            continue;
+        }
+        if (k == 0) prep_q(x, 0);
+        for (int64_t v = u + gridDim.x; v < U; v += gridDim.x) {   // next active unit's q
+            const UnitInfo y = unit_info(p, pre, v);
+            if (y.np > 0) {
+                prep_q(y, (k + 1) & 1);
+                break;
+            }
+        }
+        named_barrier(1, 128);                  // this unit's q scales are visible
+        const float ksc = __ldg(p.k_scale + x.c), vsc = __ldg(p.v_scale + x.c);
+        float kf[kHeadTile], m[kHeadTile], l[kHeadTile];
+        int32_t clo[kHeadTile], chi[kHeadTile];
+#pragma unroll
+        for (int f = 0; f < kHeadTile; ++f) {
+            kf[f] = p.scale_log2 * ksc * qsc[(k & 1) * kHeadTile + f];
+            // query i = column % S sits at position L - S + i: keys [clo, chi)
+            const int32_t pos = x.g.len - p.S + (x.hg * kHeadTile + f) % p.S;
+            chi[f] = f < x.nvalid ? pos + 1 : 0;
+            clo[f] = f < x.nvalid ? (p.mask_window > 0 ? max(0, pos - p.mask_window + 1) : 0) : 0;
+            m[f] = -CUDART_INF_F;
+            l[f] = 0.f;
+        }
+        const uint32_t ob = k & 1;
+        const uint32_t to = tl + TM_O + 32 * ob;   // this unit's O^T columns
+        for (int s = 0; s < nss; ++s) {
+            const uint32_t ms = n + (uint32_t)s, slot = ms % NSS, sb = ms & 1;
+            if (!wait_all(B_SFULL + (int)sb, (ms >> 1) & 1)) break;
+            if (!wait_all(B_FULL + (int)slot, (ms / NSS) & 1)) break;
+            tc_fence_after();
+            uint32_t sr[16];
+            tmem_ld16(tl + TM_S + 16 * sb, sr);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars, B_SFREE + (int)sb));
+            const int pg = tid >> 4;
+            const int npg = min(SS_PAGES, x.np - SS_PAGES * s);
+            const bool present = pg < npg && !((flags[slot] >> pg) & 1u);
+            const int32_t kj = (x.p0 + SS_PAGES * s + pg) * kPageSize + (tid & 15);
+            float sc[kHeadTile];
+            bool grow = false;
+#pragma unroll
+            for (int f = 0; f < kHeadTile; ++f) {
+                const bool valid = present && kj >= clo[f] && kj < chi[f];
+                sc[f] = valid ? (__uint_as_float(sr[f]) + __uint_as_float(sr[8 + f])) * kf[f]
+                              : -CUDART_INF_F;
+                grow |= sc[f] > m[f] + MAX_SLACK;
+            }
+            if (named_barrier_or(1, 128, grow)) {
+                float alpha[kHeadTile];
+#pragma unroll
+                for (int f = 0; f < kHeadTile; ++f) {
+                    if (f < x.nvalid) {
+                        float mx = sc[f];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                        if (lane == 0) red[w * kHeadTile + f] = mx;
+                    }
+                }
+                named_barrier(1, 128);
+#pragma unroll
+                for (int f = 0; f < kHeadTile; ++f) {
+                    alpha[f] = 1.f;
+                    if (f < x.nvalid) {
+                        const float M =
+                            fmaxf(m[f], fmaxf(fmaxf(red[f], red[kHeadTile + f]),
+                                              fmaxf(red[2 * kHeadTile + f], red[3 * kHeadTile + f])));
+                        alpha[f] = (m[f] == -CUDART_INF_F) ? 0.f : exp2f(m[f] - M);
+                        l[f] *= alpha[f];
+                        m[f] = M;
+                    }
+                }
+                named_barrier(1, 128);          // maxima read before anyone rewrites them
+                if (s > 0) {                    // O holds this unit's earlier superstages
+                    const uint32_t mp = ms - 1;
+                    if (!wait_all(B_PVDONE + (int)(mp & 1), (mp >> 1) & 1)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[16];
+                        tmem_ld16(to + 16 * c, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int f = 0; f < kHeadTile; ++f) {
+                            o[f] = __float_as_uint(__uint_as_float(o[f]) * alpha[f]);
+                            o[8 + f] = __float_as_uint(__uint_as_float(o[8 + f]) * alpha[f]);
+                        }
+                        tmem_st16(to + 16 * c, o);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                }
+            }
+            // P = 2^(s - m) x 2^6 as E4M3 hi (row f) and lo (row 8 + f)
+            uint32_t hb = 0, lb = 0, hb2 = 0, lb2 = 0;      // bytes of rows 0..3, 4..7
+#pragma unroll
+            for (int f = 0; f < kHeadTile; f += 2) {
+                const float m0 = (m[f] == -CUDART_INF_F) ? 0.f : m[f];
+                const float m1 = (m[f + 1] == -CUDART_INF_F) ? 0.f : m[f + 1];
+                const float p0 = exp2f(sc[f] - m0), p1 = exp2f(sc[f + 1] - m1);
+                l[f] += p0;
+                l[f + 1] += p1;
+                uint32_t h, lo;
+                split_e4m3x2(p0 * PSCALE, p1 * PSCALE, h, lo);
+                if (f < 4) {
+                    hb |= h << (8 * f);
+                    lb |= lo << (8 * f);
+                } else {
+                    hb2 |= h << (8 * (f - 4));
+                    lb2 |= lo << (8 * (f - 4));
+                }
+            }
+            // P buffer sb is free once the PV two superstages back is done
+            if (ms >= 2 && !wait_all(B_PVDONE + (int)sb, ((ms - 2) >> 1) & 1)) break;
+            uint8_t* pb = pbuf + sb * PBUF_BYTES;
+            const int kc = tid >> 4, kb = tid & 15;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const uint32_t word = r < 4 ? hb : r < 8 ? hb2 : r < 12 ? lb : lb2;
+                pb[r * 128 + (((kc ^ (r & 7)) << 4) | kb)] = (uint8_t)(word >> (8 * (r & 3)));
+            }
+            // V rows inside the PV's 32-key steps that no query of the row
+            // attends (window edges, a flagged page, the page after an odd
+            // last one) may hold anything, NaN included: zero them
+            const int nks = (npg + 1) / 2;
+            if (tid < 32 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint4* vr = reinterpret_cast<uint4*>(ring + slot * SS_BYTES +
+                                                         (2 + c) * CHUNK_BYTES + tid * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars, B_PFULL + (int)sb));
+        }
+        if (stop) break;
+
+        // ---- epilogue: column sums, then O^T from TMEM
+#pragma unroll
+        for (int f = 0; f < kHeadTile; ++f) {
+            if (f < x.nvalid) {
+                float v = l[f];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) red[NSW * kHeadTile + w * kHeadTile + f] = v;
+            }
+        }
+        named_barrier(1, 128);
+        float Lt[kHeadTile];
+#pragma unroll
+        for (int f = 0; f < kHeadTile; ++f) {
+            const float* r = red + NSW * kHeadTile + f;
+            Lt[f] = f < x.nvalid ? ((r[0] + r[kHeadTile]) + (r[2 * kHeadTile] + r[3 * kHeadTile]))
+                                 : 0.f;
+        }
+        const uint32_t ml = n + (uint32_t)nss - 1;
+        if (!wait_all(B_PVDONE + (int)(ml & 1), (ml >> 1) & 1)) break;
+        tc_fence_after();
+        uint32_t o0[16], o1[16];
+        tmem_ld16(to, o0);
+        tmem_ld16(to + 16, o1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bars, B_OFREE + (int)ob));
+#pragma unroll
+        for (int f = 0; f < kHeadTile; ++f) {
+            if (f >= x.nvalid) continue;
+            // only an exactly empty sum means "no keys"; NaN in attended K / V
+            // reaches the output as in the definition
+            const float L = Lt[f];
+            const float fac = (L == 0.f) ? 0.f : __fdividef(vsc, L * PSCALE);
+            const float v0 = (L == 0.f) ? 0.f : (__uint_as_float(o0[f]) + __uint_as_float(o0[8 + f])) * fac;
+            const float v1 = (L == 0.f) ? 0.f : (__uint_as_float(o1[f]) + __uint_as_float(o1[8 + f])) * fac;
+            const int64_t h = x.h0 + f;
+            if (single) {
+                const int64_t r = (int64_t)x.b * p.Hq + h;
+                if (GA_CHK((r + 1) * D <= p.out_elems)) {
+                    p.out[r * D + tid] = __float2bfloat16_rn(v0);
+                    p.out[r * D + 128 + tid] = __float2bfloat16_rn(v1);
+                } else {
+                    report(p.err_word, kErrSelfCheck);
+                }
+            } else if (GA_CHK(x.rc < p.rc_capacity && p.partial_o != nullptr)) {
+                float* po = p.partial_o + (x.rc * p.Hq + h) * (int64_t)D;
+                po[tid] = v0;
+                po[128 + tid] = v1;
+            }
+        }
+        if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity)) {
+            float mm = -CUDART_INF_F, LL = 0.f;      // natural-log LSE of column tid
+#pragma unroll
+            for (int f = 0; f < kHeadTile; ++f)
+                if (f == tid) {
+                    mm = m[f];
+                    LL = Lt[f];
+                }
+            p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
+                (LL == 0.f) ? -CUDART_INF_F : (mm + log2f(LL)) * CUDART_LN2_F;
+        }
+        n += (uint32_t)nss;
+        ++k;
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int abort_flag;
+    __shared__ uint32_t tmem_slot;
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* pre = reinterpret_cast<int32_t*>(smem + OFF_PREFIX);
+    volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + OFF_FLAGS);
+    const uint32_t ring = smem_addr(smem + OFF_RING);
+    const uint32_t bars = smem_addr(smem + OFF_BARS);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSS; ++s) {
+            mbar_init(bar(bars, B_FULL + s), 1);       // producer's arm (+ copied bytes)
+            mbar_init(bar(bars, B_EMPTY + s), 1);      // PV commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(bars, B_SFULL + i), 1);      // QK commit
+            mbar_init(bar(bars, B_SFREE + i), NSW);    // each softmax warp read S
+            mbar_init(bar(bars, B_PFULL + i), NSW);    // each softmax warp wrote P
+            mbar_init(bar(bars, B_PVDONE + i), 1);     // PV commit
+            mbar_init(bar(bars, B_OFREE + i), NSW);    // each softmax warp read O
+            mbar_init(bar(bars, B_QFULL + i), NSW);    // each softmax warp wrote q
+        }
+        mbar_init(bar(bars, B_FIN), 1);
+        mbar_init_fence();
+        abort_flag = 0;
+    }
+    if (warp == PROD_WARP && lane == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    int64_t total_rc = 0;
+    if (!build_row_prefix(p, pre, NTHREADS, &total_rc)) return;
+    const int64_t U = total_rc * p.Hkv * p.HG;
+    if (warp == MMA_WARP) tmem_alloc(smem_addr(&tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (warp < NSW) {
+        softmax_warps(p, pre, U, smem, bars, tmem, flags, &abort_flag);
+    } else if (warp == MMA_WARP) {
+        if (lane == 0)
+            mma_issuer(p, pre, U, ring, smem_addr(smem + OFF_Q), smem_addr(smem + OFF_P), bars,
+                       tmem, &abort_flag);
+        __syncwarp();
+    } else {
+        producer(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace tc
+
+// ------------------------------------------------------------------ host
+
+int launch_decode_tc(const DecodeArgs& a) {
+    const void* fn = reinterpret_cast<const void*>(&tc::decode_tc_kernel);
+    int rc = ensure_smem_attr(fn, tc::SMEM_BYTES, 8);
+    if (rc != GA_OK) return rc;
+    const ga_plan& pl = *a.plan;
+    const int32_t S = pl.q_len;
+    const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
+    // one box = one 128-dim half of a page-head block: [16 keys][128 B]
+    CUtensorMap tmK, tmV;
+    rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
+    if (rc != GA_OK) return rc;
+    rc = encode_rows_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
+    if (rc != GA_OK) return rc;
+
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.page_table = a.page_table;
+    p.seq_lens = a.seq_lens;
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    const bool split = pl.mode != GA_SPLIT_NONE;
+    p.partial_o = split ? reinterpret_cast<float*>(ws + pl.partial_o_offset) : nullptr;
+    p.partial_lse = split ? reinterpret_cast<float*>(ws + pl.partial_lse_offset) : nullptr;
+    p.touch_log = (pl.flags & GA_PLAN_TOUCH_LOG)
+                      ? reinterpret_cast<int32_t*>(ws + pl.touch_log_offset)
+                      : nullptr;
+    p.err_word = a.err_word;
+    p.pt_stride = a.pt_stride;
+    p.num_pages = a.num_pages;
+    p.rc_capacity = pl.row_chunks;
+    p.B = a.batch;
+    p.Hq = a.num_q_heads * S;
+    p.Hkv = a.num_kv_heads;
+    p.group = a.num_q_heads / a.num_kv_heads * S;
+    p.TW = kHeadTile;
+    p.HG = (p.group + kHeadTile - 1) / kHeadTile;
+    p.window = effective_window(a.window, S);
+    p.S = S;
+    p.mask_window = a.window;
+    p.mode = pl.mode;
+    p.splits = pl.splits;
+    p.chunk_pages = pl.chunk_pages;
+    p.touch_stride = pl.touch_stride;
+    p.test_wait_timeout = (pl.flags & GA_PLAN_TEST_WAIT_TIMEOUT) ? 1 : 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.pool_rows = rows;
+    p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;
+    const int grid = pl.grid > 0 ? pl.grid : 1;
+    tc::decode_tc_kernel<<<grid, tc::NTHREADS, tc::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
+    if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
+    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
+        return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
+                              a.pt_stride, a.stream);
+    return GA_OK;
+}
+
+}  // namespace ga

@@ -37,17 +37,22 @@ struct DecodeArgs {
 
 // Builds a 3-D tensor map over a row-major [rows, D] array (a KV pool as
 // [num_pages * Hkv * P, D], or q as [B * Hq, D]) whose box is box_rows rows:
-// D * elem / 128 tiles of [box_rows][128 bytes], 128-byte swizzled.
+// D * elem / 128 tiles of [box_rows][128 bytes], 128-byte swizzled (box_cols
+// > 0: only that many 128-byte columns per box).
 int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_t rows,
-                    int32_t head_dim, int32_t box_rows);
+                    int32_t head_dim, int32_t box_rows, int32_t box_cols = 0);
 
 int launch_decode(const DecodeArgs& a);
+
+// Sliding-window hd256 decode over an E4M3 pool on tcgen05 tensor cores.
+int launch_decode_tc(const DecodeArgs& a);
 
 int launch_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
                    const int32_t* seq_lens, void* out, int32_t* err_word, int64_t pt_stride,
                    cudaStream_t stream);
 
-// Sets the dynamic shared-memory limit of `func` once per device.
+// Sets the dynamic shared-memory limit of `func` once per device (slot < 16
+// identifies the kernel).
 int ensure_smem_attr(const void* func, int bytes, int slot);
 
 }  // namespace ga

@@ -28,9 +28,14 @@
 // its two halves.  S sits in TMEM lanes = keys, O^T in lanes = dims, so
 // softmax thread t owns key t of a superstage and dim t of each 128-dim half.
 //
-// Roles (192 threads): warps 0-3 softmax and output, warp 4 allocates TMEM
-// and its lane 0 issues every MMA, warp 5 streams pages with bulk tensor
-// copies.  Hand-offs are mbarriers; every wait is bounded.
+// Roles (256 threads): warps 0-3 softmax and output, warp 4 allocates TMEM
+// and its lane 0 issues the QK products, warp 7's lane 0 the PV products
+// (an MMA issue holds its thread for ~100 cycles, so one thread for both
+// made each product wait behind the other), warp 5 streams pages with bulk
+// tensor copies, warp 6 turns each unit's q rows into the E4M3 operand one
+// unit ahead.  Every role reads the next unit's length (and the producer its page
+// ids) while it works on the current one, so a unit boundary waits on no
+// global load.  Hand-offs are mbarriers; every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,9 +55,11 @@ constexpr int SS_BYTES = 4 * CHUNK_BYTES;         // K lo, K hi, V lo, V hi halv
 constexpr int PAGE_BYTES = 2 * kPageSize * D;     // K + V of one page-head block
 constexpr int QBUF_BYTES = 2 * 16 * 128;          // [dim half][16 rows][128 B]
 constexpr int PBUF_BYTES = 16 * 128;              // [16 rows][128 keys]
+constexpr int NPB = 4;                            // P buffers: the PV of a superstage
+                                                  // completes well after the next one's P
 constexpr int NSW = 4;                            // softmax warps
-constexpr int MMA_WARP = 4, PROD_WARP = 5;
-constexpr int NTHREADS = 192;
+constexpr int MMA_WARP = 4, PROD_WARP = 5, Q_WARP = 6, PV_WARP = 7;
+constexpr int NTHREADS = 256;
 constexpr int TMEM_COLS = 128;                    // S: 2 x 16 columns, O: 2 x 32 columns
 constexpr int TM_S = 0, TM_O = 32;
 constexpr float PSCALE = 64.0f;                   // P scale: with slack 2^2, P <= 256 < 448
@@ -62,16 +69,17 @@ constexpr int al(int x) { return (x + 127) / 128 * 128; }
 constexpr int OFF_RING = 0;
 constexpr int OFF_Q = OFF_RING + NSS * SS_BYTES;
 constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
-constexpr int OFF_RED = OFF_P + 2 * PBUF_BYTES;                 // [2][4 warps][8] floats
+constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;               // [2][4 warps][8] floats
 constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4);  // [2][8] q scales
 constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
 constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
 constexpr int OFF_BARS = al(OFF_FLAGS + NSS * 4);
-// barriers: full[NSS], empty[NSS], then two each of s_full, s_free, p_full,
-// pv_done, o_free, q_full, and fin
+// barriers: full[NSS], empty[NSS], two each of s_full, s_free, NPB each of
+// p_full, pv_done, two each of o_free, q_full, q_free, and fin
 constexpr int B_FULL = 0, B_EMPTY = NSS, B_SFULL = 2 * NSS, B_SFREE = B_SFULL + 2,
-              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2,
-              B_QFULL = B_OFREE + 2, B_FIN = B_QFULL + 2, NBARS = B_FIN + 1;
+              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + NPB, B_OFREE = B_PVDONE + NPB,
+              B_QFULL = B_OFREE + 2, B_QFREE = B_QFULL + 2, B_FIN = B_QFREE + 2,
+              NBARS = B_FIN + 1;
 constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
 constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -101,6 +109,30 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
     lo = f32x2_to_e4m3x2(a - r.x, b - r.y);
 }
 
+// Walks a CTA's units (blockIdx.x, + gridDim.x, ...) with the next unit's
+// length load in flight while the current one is processed.
+struct UnitCursor {
+    int64_t u, U;
+    UnitLoc nl;
+    int32_t nlen;
+    __device__ __forceinline__ UnitCursor(const DecodeParams& p, const int32_t* pre, int64_t U_)
+        : u(blockIdx.x), U(U_), nl(), nlen(0) {
+        if (u < U) fetch(p, pre);
+    }
+    __device__ __forceinline__ void fetch(const DecodeParams& p, const int32_t* pre) {
+        nl = locate_unit(p, pre, u);
+        nlen = __ldg(p.seq_lens + nl.b);
+    }
+    // The current unit's geometry; starts the next unit's length load.
+    __device__ __forceinline__ UnitInfo take(const DecodeParams& p, const int32_t* pre) {
+        const UnitInfo x = finish_unit(p, pre, nl, nlen);
+        u += gridDim.x;
+        if (u < U) fetch(p, pre);
+        return x;
+    }
+    __device__ __forceinline__ bool more() const { return u < U; }
+};
+
 // ------------------------------------------------------------------ producer
 
 // Warp 5.  For each superstage of each unit: wait until the slot is free,
@@ -115,21 +147,42 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
     // bounded waits run out and report GA_DEVERR_TIMEOUT.
     if (p.test_wait_timeout && blockIdx.x == 0) return;
     const uint64_t policy = l2_evict_first_policy();
+    // page ids of pages 0..31 and 32..63 of a unit, one per lane
+    auto first_ids = [&](const UnitInfo& y, int32_t& a, int32_t& b) {
+        const int32_t* t = p.page_table + (int64_t)y.b * p.pt_stride + y.p0;
+        a = (lane < y.np) ? __ldg(t + lane) : -1;
+        b = (32 + lane < y.np) ? __ldg(t + 32 + lane) : -1;
+    };
+    UnitCursor cur(p, pre, U);
+    bool have = cur.more();
+    UnitInfo x = {};
+    int32_t ids = -1, ids_nxt = -1;
+    if (have) {
+        x = cur.take(p, pre);
+        first_ids(x, ids, ids_nxt);
+    }
     uint32_t seq = 0;                 // superstages armed so far
     bool stop = false;
-    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
-        const UnitInfo x = unit_info(p, pre, u);
-        // the next unit's q rows into L2 for the softmax warps, which prepare
-        // them while this unit streams
-        const int64_t un = u + gridDim.x;
-        if (un < U) {
-            const int64_t r = (int64_t)unit_q_row(p, locate_unit(p, pre, un)) + (lane >> 2);
+    while (have && !stop) {
+        // The next unit: its length is on its way; once it has arrived (after
+        // this unit's first superstage) its first page ids are loaded too.
+        const bool has_next = cur.more();
+        UnitInfo nx = {};
+        int32_t nids = -1, nids_nxt = -1;
+        bool nx_ready = !has_next;
+        auto ready_next = [&]() {
+            if (!nx_ready) {
+                nx = cur.take(p, pre);
+                first_ids(nx, nids, nids_nxt);
+                nx_ready = true;
+            }
+        };
+        if (has_next) {               // the next unit's q rows into L2 for the q warp
+            const int64_t r = (int64_t)unit_q_row(p, cur.nl) + (lane >> 2);
             if ((r + 1) * D <= p.out_elems)
                 prefetch_l2(reinterpret_cast<const char*>(p.q + r * D) + 128 * (lane & 3));
         }
         const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride + x.p0;
-        int32_t ids = (lane < x.np) ? __ldg(tbl + lane) : -1;               // pages 0..31
-        int32_t ids_nxt = (32 + lane < x.np) ? __ldg(tbl + 32 + lane) : -1; // pages 32..63
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
         const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
         for (int s = 0; s < nss; ++s) {
@@ -140,7 +193,9 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             }
             const uint32_t n = seq, slot = n % NSS, round = n / NSS;
             bool ok = true;
-            if (lane == 0) ok = !*abort_flag && wait_or_abort(bar(bars, B_EMPTY + slot), (round & 1) ^ 1, abort_flag);
+            if (lane == 0)
+                ok = !*abort_flag &&
+                     wait_or_abort(bar(bars, B_EMPTY + slot), (round & 1) ^ 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) {
                 if (lane == 0) {
@@ -176,7 +231,13 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             if (log && present && pi < p.touch_stride && GA_CHK(x.rc < p.rc_capacity))
                 p.touch_log[x.rc * p.touch_stride + pi] = pid;
             ++seq;
+            ready_next();
         }
+        ready_next();                 // a unit without pages
+        have = has_next;
+        x = nx;
+        ids = nids;
+        ids_nxt = nids_nxt;
     }
     // Never leave with a copy in flight into this CTA's shared memory.
     if (lane < NSS && (uint32_t)lane < seq) {
@@ -188,64 +249,39 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
     }
 }
 
-// ------------------------------------------------------------------ MMA issuer
+// ------------------------------------------------------------------ MMA issuers
 
-// Warp 4, lane 0.  Over the CTA's superstages in order it issues S(m) = K q^T
-// and then O += V^T P^T for the previous superstage (m - 1), so the softmax of
-// m can start while P(m - 1) is being formed.  A unit's first PV overwrites its
-// O buffer (accumulate off), after the epilogue two active units back freed it.
-__device__ void mma_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
-                           uint32_t qbuf, uint32_t pbuf, uint32_t bars, uint32_t tmem,
-                           volatile int* abort_flag) {
+// Bounded wait of one issuing thread; on a timeout or an abort elsewhere it
+// reports, raises the abort flag and returns false.
+__device__ __forceinline__ bool issuer_wait(const DecodeParams& p, uint32_t b, uint32_t parity,
+                                            volatile int* abort_flag) {
+    if (!*abort_flag && wait_or_abort(b, parity, abort_flag)) return true;
+    report(p.err_word, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+}
+
+// Warp 4, lane 0: S(m) = K q^T for the CTA's superstages in order, once the
+// stage has landed, the S buffer is free and the unit's q operand is ready.
+__device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
+                          uint32_t qbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
     constexpr uint32_t IQK = idesc_e4m3(128, 16, false, false);
-    constexpr uint32_t IPV = idesc_e4m3(128, 16, true, false);
+    uint32_t m = 0, k = 0;                        // superstages, active units so far
     bool stop = false;
-    auto wait = [&](int b, uint32_t parity) -> bool {
-        if (stop) return false;
-        if (*abort_flag || !wait_or_abort(bar(bars, b), parity, abort_flag)) {
-            report(p.err_word, kErrTimeout);
-            *abort_flag = 1;
-            stop = true;
-            return false;
-        }
-        return true;
-    };
-    // the superstage whose PV is still to be issued
-    bool pend = false;
-    uint32_t pn = 0, pk = 0;
-    int pnpg = 0;
-    bool pfirst = false;
-    auto issue_pv = [&]() {
-        pend = false;
-        const uint32_t pb = pn & 1, ob = pk & 1;
-        if (pfirst && !wait(B_OFREE + (int)ob, ((pk >> 1) & 1) ^ 1)) return;
-        if (!wait(B_PFULL + (int)pb, (pn >> 1) & 1)) return;
-        tc_fence_after();
-        const uint32_t slot = pn % NSS;
-        const int nks = (pnpg + 1) / 2;           // 32 keys (two pages) per instruction
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const uint32_t d = tmem + TM_O + 32 * ob + 16 * c;
-            const uint32_t va = ring + slot * SS_BYTES + (2 + c) * CHUNK_BYTES;
-            for (int ks = 0; ks < nks; ++ks)
-                tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, CHUNK_BYTES, 1024),
-                            smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024), IPV,
-                            (pfirst && ks == 0) ? 0u : 1u);
-        }
-        tc_commit(bar(bars, B_EMPTY + slot));     // the slot may be refilled
-        tc_commit(bar(bars, B_PVDONE + pb));      // P buffer free, O up to date
-    };
-    uint32_t n = 0, k = 0;                        // superstages, active units so far
-    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
-        const UnitInfo x = unit_info(p, pre, u);
+    UnitCursor cur(p, pre, U);
+    while (cur.more() && !stop) {
+        const UnitInfo x = cur.take(p, pre);
         const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
         if (nss == 0) continue;
         const uint32_t qb = k & 1;
-        if (!wait(B_QFULL + (int)qb, (k >> 1) & 1)) break;
-        for (int s = 0; s < nss; ++s) {
-            const uint32_t m = n + s, slot = m % NSS, sb = m & 1;
-            if (!wait(B_FULL + (int)slot, (m / NSS) & 1)) break;
-            if (!wait(B_SFREE + (int)sb, ((m >> 1) & 1) ^ 1)) break;
+        if (!issuer_wait(p, bar(bars, B_QFULL + (int)qb), (k >> 1) & 1, abort_flag)) break;
+        for (int s = 0; s < nss; ++s, ++m) {
+            const uint32_t slot = m % NSS, sb = m & 1;
+            if (!issuer_wait(p, bar(bars, B_FULL + (int)slot), (m / NSS) & 1, abort_flag) ||
+                !issuer_wait(p, bar(bars, B_SFREE + (int)sb), ((m >> 1) & 1) ^ 1, abort_flag)) {
+                stop = true;
+                break;
+            }
             tc_fence_after();
             const uint32_t ka = ring + slot * SS_BYTES, qa = qbuf + qb * QBUF_BYTES;
 #pragma unroll
@@ -256,24 +292,133 @@ __device__ void mma_issuer(const DecodeParams& p, const int32_t* pre, int64_t U,
                                 smem_desc_sw128(ka + c * CHUNK_BYTES + 32 * kk, 16, 1024),
                                 smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
                                 (c | kk) != 0 ? 1u : 0u);
-            tc_commit(bar(bars, B_SFULL + sb));
-            if (pend) issue_pv();
-            if (stop) break;
-            pend = true;
-            pn = m;
-            pk = k;
-            pnpg = min(SS_PAGES, x.np - SS_PAGES * s);
-            pfirst = (s == 0);
+            tc_commit(bar(bars, B_SFULL + (int)sb));
         }
-        n += (uint32_t)nss;
         ++k;
     }
-    if (pend && !stop) issue_pv();
-    // Every MMA issued has completed before the block may free TMEM.
-    tc_commit(bar(bars, B_FIN));
-    if (!mbar_wait(bar(bars, B_FIN), 0)) {
-        report(p.err_word, kErrTimeout);
-        *abort_flag = 1;
+}
+
+// Warp 7, lane 0: O += V^T P^T for the CTA's superstages in order, once the
+// softmax warps have written P(m).  Its commit frees the ring slot and the P
+// buffer.  A unit's first PV overwrites its O buffer (accumulate off) once
+// the epilogue two active units back has read it.
+__device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
+                          uint32_t pbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
+    constexpr uint32_t IPV = idesc_e4m3(128, 16, true, false);
+    uint32_t m = 0, k = 0;
+    bool stop = false;
+    UnitCursor cur(p, pre, U);
+    while (cur.more() && !stop) {
+        const UnitInfo x = cur.take(p, pre);
+        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        if (nss == 0) continue;
+        const uint32_t ob = k & 1;
+        for (int s = 0; s < nss; ++s, ++m) {
+            const uint32_t slot = m % NSS, pb = m % NPB;
+            if ((s == 0 &&
+                 !issuer_wait(p, bar(bars, B_OFREE + (int)ob), ((k >> 1) & 1) ^ 1, abort_flag)) ||
+                !issuer_wait(p, bar(bars, B_PFULL + (int)pb), (m / NPB) & 1, abort_flag)) {
+                stop = true;
+                break;
+            }
+            tc_fence_after();
+            const int nks = (min(SS_PAGES, x.np - SS_PAGES * s) + 1) / 2;   // 32 keys per MMA
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t d = tmem + TM_O + 32 * ob + 16 * c;
+                const uint32_t va = ring + slot * SS_BYTES + (2 + c) * CHUNK_BYTES;
+                for (int ks = 0; ks < nks; ++ks)
+                    tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, CHUNK_BYTES, 1024),
+                                smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024), IPV,
+                                (s == 0 && ks == 0) ? 0u : 1u);
+            }
+            tc_commit(bar(bars, B_EMPTY + (int)slot));   // the slot may be refilled
+            tc_commit(bar(bars, B_PVDONE + (int)pb));    // P buffer free, O up to date
+        }
+        ++k;
+    }
+}
+
+// ------------------------------------------------------------------ q warp
+
+// Warp 6.  For each active unit (one with pages), in the order the MMA issuer
+// takes them: the unit's q rows as the QK operand in buffer k % 2 -- column f
+// scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row 8 + f
+// of each 128-dim half ([16 rows][128 B], 128-byte swizzle); rows of columns
+// past the unit's valid ones are zero.  Lane l takes column l / 4, dims
+// 64 (l % 4) .. +63.  Buffer k % 2 is rewritten once the softmax warps are
+// done with active unit k - 2 (its scales read, all its S consumed).
+__device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
+                       uint32_t bars, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    float* qsc = reinterpret_cast<float*>(smem + OFF_QSC);     // [2][8]
+    uint8_t* qbuf = smem + OFF_Q;
+    const int f = lane >> 2, d0 = 64 * (lane & 3);
+    UnitCursor cur(p, pre, U);
+    uint32_t k = 0;
+    while (cur.more()) {
+        const UnitInfo y = cur.take(p, pre);
+        if (y.np == 0) continue;
+        const uint32_t qb = k & 1;
+        bool ok = k < 2 || wait_or_abort(bar(bars, B_QFREE + (int)qb), ((k - 2) >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) {
+                report(p.err_word, kErrTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        uint4 wv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wv[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
+        if (f < y.nvalid) {
+            if (GA_CHK((row + 1) * D <= p.out_elems)) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + row * D + d0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) wv[i] = __ldg(src + i);
+            } else {
+                report(p.err_word, kErrSelfCheck);
+            }
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                am = fmaxf(am, fmaxf(fabsf(bf16_lo(e[j])), fabsf(bf16_hi(e[j]))));
+        }
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        if ((lane & 3) == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
+        const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
+        const float inv = 1.0f / sc;
+        uint8_t* half = qbuf + qb * QBUF_BYTES + (d0 >> 7) * 2048;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {          // 16 dims: elements of wv[i], wv[i + 1]
+            const uint32_t e[8] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w,
+                                   wv[i + 1].x, wv[i + 1].y, wv[i + 1].z, wv[i + 1].w};
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t h01, l01, h23, l23;
+                split_e4m3x2(bf16_lo(e[2 * j]) * inv, bf16_hi(e[2 * j]) * inv, h01, l01);
+                split_e4m3x2(bf16_lo(e[2 * j + 1]) * inv, bf16_hi(e[2 * j + 1]) * inv, h23, l23);
+                hw[j] = h01 | (h23 << 16);
+                lw[j] = l01 | (l23 << 16);
+            }
+            const int jj = ((d0 & 127) >> 4) + (i >> 1);     // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(half + f * 128 + ((jj ^ (f & 7)) << 4)) =
+                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(half + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        if ((lane & 3) == 0) qsc[qb * kHeadTile + f] = sc;
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bars, B_QFULL + (int)qb));
+        ++k;
     }
 }
 
@@ -284,8 +429,10 @@ __device__ void mma_issuer(const DecodeParams& p, const int32_t* pre, int64_t U,
 // softmax in base 2 (the running max is raised only when a score exceeds it
 // by more than MAX_SLACK; then O is rescaled in TMEM), write P's hi / lo
 // E4M3 parts as the PV operand, zero V rows the PV reads but no query
-// attends.  Per unit: prepare the next active unit's q operand, and at the
-// end read O and write the output (or a split partial and its LSE).
+// attends.  At the end of a unit: read O and write the output (or a split
+// partial and its LSE).  NV (2, 4 or 8) bounds the valid (query, head)
+// columns of every unit; columns NV.. of P stay zero.
+template <int NV>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile uint32_t* flags,
                               volatile int* abort_flag) {
@@ -293,15 +440,23 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
     const int w = tid >> 5, lane = tid & 31;
     const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);     // this warp's TMEM lanes
     float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [max | sum][4 warps][8]
-    float* qsc = reinterpret_cast<float*>(smem + OFF_QSC);     // [2][8]
-    uint8_t* qbuf = smem + OFF_Q;
+    const float* qsc = reinterpret_cast<const float*>(smem + OFF_QSC);
     uint8_t* pbuf = smem + OFF_P;
     uint8_t* ring = smem + OFF_RING;
     bool stop = false;
 
-    // Bounded wait by all 128 threads with one outcome for all of them.
-    auto wait_all = [&](int b, uint32_t parity) -> bool {
-        const bool ok = wait_or_abort(bar(bars, b), parity, abort_flag);
+    // P columns past NV are never written: zero them once.
+    for (int i = tid; i < NPB * PBUF_BYTES / 16; i += 128)
+        reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+
+    // A wait polled by one lane per warp, with one outcome for all 128 threads
+    // (the named barrier also orders the lanes after the poller).
+    auto poll = [&](int b, uint32_t parity) -> bool {
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(bar(bars, b), parity, abort_flag);
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    auto settle = [&](bool ok) -> bool {
         if (named_barrier_or(1, 128, !ok)) {
             if (tid == 0) {
                 report(p.err_word, kErrTimeout);
@@ -312,59 +467,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         }
         return true;
     };
-
-    // q of unit y as the QK operand in buffer qb: column f scaled by
-    // 448 / amax_f, E4M3 hi part in row f and lo part in row 8 + f of each
-    // dim half ([16 rows][128 B], 128-byte swizzle).  Thread t takes column
-    // t / 16, dims 16 (t % 16) .. +15; rows of columns past the unit's valid
-    // ones are zero.
-    auto prep_q = [&](const UnitInfo& y, uint32_t qb) {
-        const int f = tid >> 4, d0 = 16 * (tid & 15);
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
-        if (f < y.nvalid) {
-            if (GA_CHK((row + 1) * D <= p.out_elems)) {
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + row * D + d0);
-                a = __ldg(src);
-                b = __ldg(src + 1);
-            } else {
-                report(p.err_word, kErrSelfCheck);
-            }
-        }
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float v[16];
-        float am = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[2 * i] = bf16_lo(wv[i]);
-            v[2 * i + 1] = bf16_hi(wv[i]);
-            am = fmaxf(am, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-        }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-        if ((tid & 15) == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
-        const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
-        if ((tid & 15) == 0) qsc[qb * kHeadTile + f] = sc;
-        const float inv = 1.0f / sc;
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t h01, l01, h23, l23;
-            split_e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv, h01, l01);
-            split_e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv, h23, l23);
-            hw[j] = h01 | (h23 << 16);
-            lw[j] = l01 | (l23 << 16);
-        }
-        const int c = d0 >> 7, jj = (d0 & 127) >> 4;
-        uint8_t* base = qbuf + qb * QBUF_BYTES + c * 2048;
-        *reinterpret_cast<uint4*>(base + f * 128 + ((jj ^ (f & 7)) << 4)) =
-            make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(base + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
-            make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bars, B_QFULL + (int)qb));
-    };
+    auto wait_all = [&](int b, uint32_t parity) -> bool { return settle(poll(b, parity)); };
 
     // A unit with no attended key: zero output (or a zero partial with an
     // empty LSE).
@@ -387,29 +490,32 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
     };
 
     uint32_t n = 0, k = 0;                      // superstages, active units so far
-    for (int64_t u = blockIdx.x; u < U && !stop; u += gridDim.x) {
-        const UnitInfo x = unit_info(p, pre, u);
+    UnitCursor cur(p, pre, U);
+    float nks = 1.f, nvs = 1.f;                 // the pending unit's K / V scales
+    if (cur.more()) {
+        nks = __ldg(p.k_scale + cur.nl.c);
+        nvs = __ldg(p.v_scale + cur.nl.c);
+    }
+    while (cur.more() && !stop) {
+        const UnitInfo x = cur.take(p, pre);
+        const float ksc = nks, vsc = nvs;
+        if (cur.more()) {
+            nks = __ldg(p.k_scale + cur.nl.c);
+            nvs = __ldg(p.v_scale + cur.nl.c);
+        }
         const bool single = (x.g.chunks == 1);
         const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
         if (nss == 0) {
             write_empty(x, single);
             continue;
         }
-        if (k == 0) prep_q(x, 0);
-        for (int64_t v = u + gridDim.x; v < U; v += gridDim.x) {   // next active unit's q
-            const UnitInfo y = unit_info(p, pre, v);
-            if (y.np > 0) {
-                prep_q(y, (k + 1) & 1);
-                break;
-            }
-        }
-        named_barrier(1, 128);                  // this unit's q scales are visible
-        const float ksc = __ldg(p.k_scale + x.c), vsc = __ldg(p.v_scale + x.c);
-        float kf[kHeadTile], m[kHeadTile], l[kHeadTile];
-        int32_t clo[kHeadTile], chi[kHeadTile];
+        const uint32_t qb = k & 1;
+        if (!wait_all(B_QFULL + (int)qb, (k >> 1) & 1)) break;     // this unit's q scales
+        float kf[NV], m[NV], l[NV];
+        int32_t clo[NV], chi[NV];
 #pragma unroll
-        for (int f = 0; f < kHeadTile; ++f) {
-            kf[f] = p.scale_log2 * ksc * qsc[(k & 1) * kHeadTile + f];
+        for (int f = 0; f < NV; ++f) {
+            kf[f] = p.scale_log2 * ksc * qsc[qb * kHeadTile + f];
             // query i = column % S sits at position L - S + i: keys [clo, chi)
             const int32_t pos = x.g.len - p.S + (x.hg * kHeadTile + f) % p.S;
             chi[f] = f < x.nvalid ? pos + 1 : 0;
@@ -420,9 +526,16 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         const uint32_t ob = k & 1;
         const uint32_t to = tl + TM_O + 32 * ob;   // this unit's O^T columns
         for (int s = 0; s < nss; ++s) {
-            const uint32_t ms = n + (uint32_t)s, slot = ms % NSS, sb = ms & 1;
-            if (!wait_all(B_SFULL + (int)sb, (ms >> 1) & 1)) break;
-            if (!wait_all(B_FULL + (int)slot, (ms / NSS) & 1)) break;
+            const uint32_t ms = n + (uint32_t)s, slot = ms % NSS, sb = ms & 1, pbi = ms % NPB;
+            // S of this superstage, the stage's copies (for the flags and the
+            // V rows below) and the P buffer's previous PV
+            bool ok = true;
+            if (lane == 0)
+                ok = wait_or_abort(bar(bars, B_SFULL + (int)sb), (ms >> 1) & 1, abort_flag) &&
+                     wait_or_abort(bar(bars, B_FULL + (int)slot), (ms / NSS) & 1, abort_flag) &&
+                     (ms < NPB || wait_or_abort(bar(bars, B_PVDONE + (int)pbi),
+                                                ((ms - NPB) / NPB) & 1, abort_flag));
+            if (!settle(__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0)) break;
             tc_fence_after();
             uint32_t sr[16];
             tmem_ld16(tl + TM_S + 16 * sb, sr);
@@ -434,44 +547,39 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             const int npg = min(SS_PAGES, x.np - SS_PAGES * s);
             const bool present = pg < npg && !((flags[slot] >> pg) & 1u);
             const int32_t kj = (x.p0 + SS_PAGES * s + pg) * kPageSize + (tid & 15);
-            float sc[kHeadTile];
+            float sc[NV];
             bool grow = false;
 #pragma unroll
-            for (int f = 0; f < kHeadTile; ++f) {
+            for (int f = 0; f < NV; ++f) {
                 const bool valid = present && kj >= clo[f] && kj < chi[f];
                 sc[f] = valid ? (__uint_as_float(sr[f]) + __uint_as_float(sr[8 + f])) * kf[f]
                               : -CUDART_INF_F;
                 grow |= sc[f] > m[f] + MAX_SLACK;
             }
             if (named_barrier_or(1, 128, grow)) {
-                float alpha[kHeadTile];
+                float alpha[NV];
 #pragma unroll
-                for (int f = 0; f < kHeadTile; ++f) {
-                    if (f < x.nvalid) {
-                        float mx = sc[f];
+                for (int f = 0; f < NV; ++f) {
+                    float mx = sc[f];
 #pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                        if (lane == 0) red[w * kHeadTile + f] = mx;
-                    }
+                    for (int off = 16; off > 0; off >>= 1)
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    if (lane == 0) red[w * kHeadTile + f] = mx;
                 }
                 named_barrier(1, 128);
 #pragma unroll
-                for (int f = 0; f < kHeadTile; ++f) {
-                    alpha[f] = 1.f;
-                    if (f < x.nvalid) {
-                        const float M =
-                            fmaxf(m[f], fmaxf(fmaxf(red[f], red[kHeadTile + f]),
-                                              fmaxf(red[2 * kHeadTile + f], red[3 * kHeadTile + f])));
-                        alpha[f] = (m[f] == -CUDART_INF_F) ? 0.f : exp2f(m[f] - M);
-                        l[f] *= alpha[f];
-                        m[f] = M;
-                    }
+                for (int f = 0; f < NV; ++f) {
+                    const float M =
+                        fmaxf(m[f], fmaxf(fmaxf(red[f], red[kHeadTile + f]),
+                                          fmaxf(red[2 * kHeadTile + f], red[3 * kHeadTile + f])));
+                    alpha[f] = (m[f] == -CUDART_INF_F) ? 0.f : exp2f(m[f] - M);
+                    l[f] *= alpha[f];
+                    m[f] = M;
                 }
                 named_barrier(1, 128);          // maxima read before anyone rewrites them
                 if (s > 0) {                    // O holds this unit's earlier superstages
                     const uint32_t mp = ms - 1;
-                    if (!wait_all(B_PVDONE + (int)(mp & 1), (mp >> 1) & 1)) break;
+                    if (!wait_all(B_PVDONE + (int)(mp % NPB), (mp / NPB) & 1)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -479,7 +587,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                         tmem_ld16(to + 16 * c, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int f = 0; f < kHeadTile; ++f) {
+                        for (int f = 0; f < NV; ++f) {
                             o[f] = __float_as_uint(__uint_as_float(o[f]) * alpha[f]);
                             o[8 + f] = __float_as_uint(__uint_as_float(o[8 + f]) * alpha[f]);
                         }
@@ -490,32 +598,23 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 }
             }
             // P = 2^(s - m) x 2^6 as E4M3 hi (row f) and lo (row 8 + f)
-            uint32_t hb = 0, lb = 0, hb2 = 0, lb2 = 0;      // bytes of rows 0..3, 4..7
+            uint32_t hb[NV / 2], lb[NV / 2];      // two columns' bytes each
 #pragma unroll
-            for (int f = 0; f < kHeadTile; f += 2) {
+            for (int f = 0; f < NV; f += 2) {
                 const float m0 = (m[f] == -CUDART_INF_F) ? 0.f : m[f];
                 const float m1 = (m[f + 1] == -CUDART_INF_F) ? 0.f : m[f + 1];
                 const float p0 = exp2f(sc[f] - m0), p1 = exp2f(sc[f + 1] - m1);
                 l[f] += p0;
                 l[f + 1] += p1;
-                uint32_t h, lo;
-                split_e4m3x2(p0 * PSCALE, p1 * PSCALE, h, lo);
-                if (f < 4) {
-                    hb |= h << (8 * f);
-                    lb |= lo << (8 * f);
-                } else {
-                    hb2 |= h << (8 * (f - 4));
-                    lb2 |= lo << (8 * (f - 4));
-                }
+                split_e4m3x2(p0 * PSCALE, p1 * PSCALE, hb[f / 2], lb[f / 2]);
             }
-            // P buffer sb is free once the PV two superstages back is done
-            if (ms >= 2 && !wait_all(B_PVDONE + (int)sb, ((ms - 2) >> 1) & 1)) break;
-            uint8_t* pb = pbuf + sb * PBUF_BYTES;
+            uint8_t* pb = pbuf + pbi * PBUF_BYTES;
             const int kc = tid >> 4, kb = tid & 15;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const uint32_t word = r < 4 ? hb : r < 8 ? hb2 : r < 12 ? lb : lb2;
-                pb[r * 128 + (((kc ^ (r & 7)) << 4) | kb)] = (uint8_t)(word >> (8 * (r & 3)));
+            for (int f = 0; f < NV; ++f) {
+                const int sh = 8 * (f & 1);
+                pb[f * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(hb[f / 2] >> sh);
+                pb[(8 + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[f / 2] >> sh);
             }
             // V rows inside the PV's 32-key steps that no query of the row
             // attends (window edges, a flagged page, the page after an odd
@@ -532,30 +631,29 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             }
             fence_proxy_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bars, B_PFULL + (int)sb));
+            if (lane == 0) mbar_arrive(bar(bars, B_PFULL + (int)pbi));
         }
         if (stop) break;
+        __syncwarp();                           // q buffer qb: scales read, all S consumed
+        if (lane == 0) mbar_arrive(bar(bars, B_QFREE + (int)qb));
 
         // ---- epilogue: column sums, then O^T from TMEM
 #pragma unroll
-        for (int f = 0; f < kHeadTile; ++f) {
-            if (f < x.nvalid) {
-                float v = l[f];
+        for (int f = 0; f < NV; ++f) {
+            float v = l[f];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == 0) red[NSW * kHeadTile + w * kHeadTile + f] = v;
-            }
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) red[NSW * kHeadTile + w * kHeadTile + f] = v;
         }
-        named_barrier(1, 128);
-        float Lt[kHeadTile];
+        const uint32_t ml = n + (uint32_t)nss - 1;
+        if (!wait_all(B_PVDONE + (int)(ml % NPB), (ml / NPB) & 1)) break;   // also publishes red
+        float Lt[NV];
 #pragma unroll
-        for (int f = 0; f < kHeadTile; ++f) {
+        for (int f = 0; f < NV; ++f) {
             const float* r = red + NSW * kHeadTile + f;
             Lt[f] = f < x.nvalid ? ((r[0] + r[kHeadTile]) + (r[2 * kHeadTile] + r[3 * kHeadTile]))
                                  : 0.f;
         }
-        const uint32_t ml = n + (uint32_t)nss - 1;
-        if (!wait_all(B_PVDONE + (int)(ml & 1), (ml >> 1) & 1)) break;
         tc_fence_after();
         uint32_t o0[16], o1[16];
         tmem_ld16(to, o0);
@@ -565,7 +663,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bars, B_OFREE + (int)ob));
 #pragma unroll
-        for (int f = 0; f < kHeadTile; ++f) {
+        for (int f = 0; f < NV; ++f) {
             if (f >= x.nvalid) continue;
             // only an exactly empty sum means "no keys"; NaN in attended K / V
             // reaches the output as in the definition
@@ -591,7 +689,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity)) {
             float mm = -CUDART_INF_F, LL = 0.f;      // natural-log LSE of column tid
 #pragma unroll
-            for (int f = 0; f < kHeadTile; ++f)
+            for (int f = 0; f < NV; ++f)
                 if (f == tid) {
                     mm = m[f];
                     LL = Lt[f];
@@ -606,6 +704,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
 
 // ------------------------------------------------------------------ kernel
 
+template <int NV>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -625,15 +724,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar(bars, B_FULL + s), 1);       // producer's arm (+ copied bytes)
             mbar_init(bar(bars, B_EMPTY + s), 1);      // PV commit
         }
+        for (int i = 0; i < NPB; ++i) {
+            mbar_init(bar(bars, B_PFULL + i), NSW);    // each softmax warp wrote P
+            mbar_init(bar(bars, B_PVDONE + i), 1);     // PV commit
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(bars, B_SFULL + i), 1);      // QK commit
             mbar_init(bar(bars, B_SFREE + i), NSW);    // each softmax warp read S
-            mbar_init(bar(bars, B_PFULL + i), NSW);    // each softmax warp wrote P
-            mbar_init(bar(bars, B_PVDONE + i), 1);     // PV commit
             mbar_init(bar(bars, B_OFREE + i), NSW);    // each softmax warp read O
-            mbar_init(bar(bars, B_QFULL + i), NSW);    // each softmax warp wrote q
+            mbar_init(bar(bars, B_QFULL + i), 1);      // the q warp wrote q
+            mbar_init(bar(bars, B_QFREE + i), NSW);    // each softmax warp is done with it
         }
-        mbar_init(bar(bars, B_FIN), 1);
+        mbar_init(bar(bars, B_FIN), 2);                // both issuers' last commits
         mbar_init_fence();
         abort_flag = 0;
     }
@@ -650,14 +752,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     if (warp < NSW) {
-        softmax_warps(p, pre, U, smem, bars, tmem, flags, &abort_flag);
-    } else if (warp == MMA_WARP) {
-        if (lane == 0)
-            mma_issuer(p, pre, U, ring, smem_addr(smem + OFF_Q), smem_addr(smem + OFF_P), bars,
-                       tmem, &abort_flag);
+        softmax_warps<NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag);
+    } else if (warp == MMA_WARP || warp == PV_WARP) {
+        if (lane == 0) {
+            if (warp == MMA_WARP)
+                qk_issuer(p, pre, U, ring, smem_addr(smem + OFF_Q), bars, tmem, &abort_flag);
+            else
+                pv_issuer(p, pre, U, ring, smem_addr(smem + OFF_P), bars, tmem, &abort_flag);
+            // every MMA this thread issued has completed before TMEM is freed
+            tc_commit(bar(bars, B_FIN));
+            if (!mbar_wait(bar(bars, B_FIN), 0)) {
+                report(p.err_word, kErrTimeout);
+                abort_flag = 1;
+            }
+        }
         __syncwarp();
-    } else {
+    } else if (warp == PROD_WARP) {
         producer(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
+    } else if (warp == Q_WARP) {
+        q_warp(p, pre, U, smem, bars, &abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -670,11 +783,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ------------------------------------------------------------------ host
 
 int launch_decode_tc(const DecodeArgs& a) {
-    const void* fn = reinterpret_cast<const void*>(&tc::decode_tc_kernel);
-    int rc = ensure_smem_attr(fn, tc::SMEM_BYTES, 8);
-    if (rc != GA_OK) return rc;
     const ga_plan& pl = *a.plan;
     const int32_t S = pl.q_len;
+    // (query, head) columns of a kv head, at most 8 per unit
+    const int32_t cols = a.num_q_heads / a.num_kv_heads * S;
+    const int nv = cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
+    auto kern = nv == 2 ? &tc::decode_tc_kernel<2>
+              : nv == 4 ? &tc::decode_tc_kernel<4> : &tc::decode_tc_kernel<8>;
+    int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), tc::SMEM_BYTES,
+                              nv == 2 ? 8 : nv == 4 ? 9 : 10);
+    if (rc != GA_OK) return rc;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
     // one box = one 128-dim half of a page-head block: [16 keys][128 B]
     CUtensorMap tmK, tmV;
@@ -719,7 +837,7 @@ int launch_decode_tc(const DecodeArgs& a) {
     p.pool_rows = rows;
     p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    tc::decode_tc_kernel<<<grid, tc::NTHREADS, tc::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
+    kern<<<grid, tc::NTHREADS, tc::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
     if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,

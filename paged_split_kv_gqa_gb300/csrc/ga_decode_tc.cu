@@ -12,12 +12,15 @@
 // 1023 / 1024 / 1025 boundaries; "[Model] Gemma 4 M2 26B-A4B", Proposed Plan:
 // opt-in FP8 pool for the sliding family).
 //
-// Layout of one superstage in shared memory (64 KB): four 16 KB regions,
-// K dims 0-127, K dims 128-255, V dims 0-127, V dims 128-255, each a dense
-// [128 keys][128 bytes] tile with the 128-byte swizzle.  Page i of the
-// superstage fills rows 16i .. 16i+15 of each region (four 2 KB bulk tensor
-// copies per page), so the key rows of 8 pages sit at one uniform stride and
-// a single MMA descriptor spans them.
+// Layout of one superstage in shared memory: a K slot and a V slot of 32 KB,
+// each two 16 KB regions (dims 0-127, dims 128-255), each a dense [128 keys]
+// [128 bytes] tile with the 128-byte swizzle.  Page i of the superstage fills
+// rows 16i .. 16i+15 of each region (four 2 KB bulk tensor copies per page),
+// so the key rows of 8 pages sit at one uniform stride and a single MMA
+// descriptor spans them.  K and V slots are separate rings: a K slot is free
+// again as soon as its QK product has run, a V slot only after the softmax
+// and the PV product, so V gets more slots (2 K + 4 V in 192 KB keep the
+// copy engine busy).
 //
 // Products (M = 128, N = 16, K = 32 per instruction, fp32 accumulate):
 //   S   [keys x 16]  = K [keys x dims]  . Qs^T   (A K-major, B K-major)
@@ -48,11 +51,12 @@ namespace ga {
 namespace tc {
 
 constexpr int D = 256;
-constexpr int NSS = 3;                            // superstages in the ring
+constexpr int NKS = 2;                            // K slots (freed by the QK product)
+constexpr int NVS = 4;                            // V slots (freed by the PV product)
 constexpr int SS_PAGES = 8;                       // pages per superstage: 128 keys = MMA M
 constexpr int CHUNK_BYTES = SS_PAGES * kPageSize * 128;   // [128 keys][128 B]
-constexpr int SS_BYTES = 4 * CHUNK_BYTES;         // K lo, K hi, V lo, V hi halves
-constexpr int PAGE_BYTES = 2 * kPageSize * D;     // K + V of one page-head block
+constexpr int SLOT_BYTES = 2 * CHUNK_BYTES;       // K or V of a superstage: two dim halves
+constexpr int BLOCK_BYTES = kPageSize * D;        // K or V of one page-head block
 constexpr int QBUF_BYTES = 2 * 16 * 128;          // [dim half][16 rows][128 B]
 constexpr int PBUF_BYTES = 16 * 128;              // [16 rows][128 keys]
 constexpr int NPB = 4;                            // P buffers: the PV of a superstage
@@ -66,26 +70,29 @@ constexpr float PSCALE = 64.0f;                   // P scale: with slack 2^2, P 
 constexpr float MAX_SLACK = 2.0f;
 
 constexpr int al(int x) { return (x + 127) / 128 * 128; }
-constexpr int OFF_RING = 0;
-constexpr int OFF_Q = OFF_RING + NSS * SS_BYTES;
+constexpr int OFF_RING = 0;                       // K slots, then V slots
+constexpr int OFF_VRING = OFF_RING + NKS * SLOT_BYTES;
+constexpr int OFF_Q = OFF_VRING + NVS * SLOT_BYTES;
 constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
 constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;               // [2][4 warps][8] floats
 constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4);  // [2][8] q scales
 constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
 constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
-constexpr int OFF_BARS = al(OFF_FLAGS + NSS * 4);
-// barriers: full[NSS], empty[NSS], two each of s_full, s_free, NPB each of
-// p_full, pv_done, two each of o_free, q_full, q_free, and fin
-constexpr int B_FULL = 0, B_EMPTY = NSS, B_SFULL = 2 * NSS, B_SFREE = B_SFULL + 2,
+constexpr int OFF_BARS = al(OFF_FLAGS + NVS * 4);
+// barriers: k_full / k_empty [NKS], v_full / v_empty [NVS], two each of
+// s_full, s_free, NPB each of p_full, pv_done, two each of o_free, q_full,
+// q_free, and fin
+constexpr int B_KFULL = 0, B_KEMPTY = NKS, B_VFULL = 2 * NKS, B_VEMPTY = 2 * NKS + NVS,
+              B_SFULL = 2 * NKS + 2 * NVS, B_SFREE = B_SFULL + 2,
               B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + NPB, B_OFREE = B_PVDONE + NPB,
               B_QFULL = B_OFREE + 2, B_QFREE = B_QFULL + 2, B_FIN = B_QFREE + 2,
               NBARS = B_FIN + 1;
 constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
 constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && SS_BYTES % 1024 == 0,
+static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && SLOT_BYTES % 1024 == 0,
               "swizzle-128B operands need 1024-byte aligned tiles");
-static_assert(NSS >= 2, "ring depth");
+static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
 
 __device__ __forceinline__ uint32_t bar(uint32_t bars, int i) { return bars + 8u * (uint32_t)i; }
 
@@ -135,10 +142,11 @@ struct UnitCursor {
 
 // ------------------------------------------------------------------ producer
 
-// Warp 5.  For each superstage of each unit: wait until the slot is free,
-// arm its "full" barrier with the bytes of the good pages, and let lanes
-// 0..7 each copy one page (K and V, both dim halves).  Pages with an invalid
-// id are flagged (bit i of flags[slot]) and not copied.
+// Warp 5.  For each superstage m of each unit: wait until K slot m % NKS and
+// V slot m % NVS are free, arm their "full" barriers with the bytes of the
+// good pages, and let lanes 0..7 each copy one page, K (both dim halves)
+// before V.  Pages with an invalid id are flagged (bit i of flags[m % NVS])
+// and not copied.
 __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
                          const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
                          volatile uint32_t* flags, volatile int* abort_flag) {
@@ -191,11 +199,12 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                 const int nb = 32 * (s / 4 + 1) + lane;
                 ids_nxt = (nb < x.np) ? __ldg(tbl + nb) : -1;
             }
-            const uint32_t n = seq, slot = n % NSS, round = n / NSS;
+            const uint32_t n = seq, kslot = n % NKS, vslot = n % NVS;
             bool ok = true;
             if (lane == 0)
                 ok = !*abort_flag &&
-                     wait_or_abort(bar(bars, B_EMPTY + slot), (round & 1) ^ 1, abort_flag);
+                     wait_or_abort(bar(bars, B_KEMPTY + kslot), ((n / NKS) & 1) ^ 1, abort_flag) &&
+                     wait_or_abort(bar(bars, B_VEMPTY + vslot), ((n / NVS) & 1) ^ 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) {
                 if (lane == 0) {
@@ -213,18 +222,21 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             const bool good = valid_id && GA_CHK(y >= 0 && (int64_t)y + kPageSize <= p.pool_rows);
             const uint32_t gm = __ballot_sync(0xffffffffu, good);
             const uint32_t pm = __ballot_sync(0xffffffffu, present);
-            const uint32_t full = bar(bars, B_FULL + slot);
+            const uint32_t kfull = bar(bars, B_KFULL + kslot), vfull = bar(bars, B_VFULL + vslot);
             if (lane == 0) {
-                flags[slot] = pm & ~gm;
-                mbar_arrive_expect_tx(full, (uint32_t)__popc(gm) * PAGE_BYTES);
+                flags[vslot] = pm & ~gm;
+                mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * BLOCK_BYTES);
+                mbar_arrive_expect_tx(vfull, (uint32_t)__popc(gm) * BLOCK_BYTES);
             }
             __syncwarp();
             if (good) {
-                const uint32_t dst = ring + slot * SS_BYTES + (uint32_t)lane * (kPageSize * 128);
-                tma_load_3d(dst, tmK, full, 0, y, 0, policy);
-                tma_load_3d(dst + CHUNK_BYTES, tmK, full, 0, y, 1, policy);
-                tma_load_3d(dst + 2 * CHUNK_BYTES, tmV, full, 0, y, 0, policy);
-                tma_load_3d(dst + 3 * CHUNK_BYTES, tmV, full, 0, y, 1, policy);
+                const uint32_t kd = ring + kslot * SLOT_BYTES + (uint32_t)lane * (kPageSize * 128);
+                const uint32_t vd = ring + (uint32_t)OFF_VRING + vslot * SLOT_BYTES +
+                                    (uint32_t)lane * (kPageSize * 128);
+                tma_load_3d(kd, tmK, kfull, 0, y, 0, policy);
+                tma_load_3d(kd + CHUNK_BYTES, tmK, kfull, 0, y, 1, policy);
+                tma_load_3d(vd, tmV, vfull, 0, y, 0, policy);
+                tma_load_3d(vd + CHUNK_BYTES, tmV, vfull, 0, y, 1, policy);
             } else if (present) {
                 report(p.err_word, valid_id ? kErrSelfCheck : kErrPageId);
             }
@@ -239,14 +251,19 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
         ids = nids;
         ids_nxt = nids_nxt;
     }
-    // Never leave with a copy in flight into this CTA's shared memory.
-    if (lane < NSS && (uint32_t)lane < seq) {
-        const uint32_t last = (uint32_t)lane + ((seq - 1 - (uint32_t)lane) / NSS) * NSS;
-        if (!mbar_wait(bar(bars, B_FULL + lane), (last / NSS) & 1)) {
-            report(p.err_word, kErrTimeout);
-            *abort_flag = 1;
+    // Never leave with a copy in flight into this CTA's shared memory: wait
+    // for the last round each K and V slot was armed for.
+    auto drain = [&](int base, int nslots) {
+        if (lane < nslots && (uint32_t)lane < seq) {
+            const uint32_t last = (uint32_t)lane + ((seq - 1 - (uint32_t)lane) / nslots) * nslots;
+            if (!mbar_wait(bar(bars, base + lane), (last / nslots) & 1)) {
+                report(p.err_word, kErrTimeout);
+                *abort_flag = 1;
+            }
         }
-    }
+    };
+    drain(B_KFULL, NKS);
+    drain(B_VFULL, NVS);
 }
 
 // ------------------------------------------------------------------ MMA issuers
@@ -262,7 +279,8 @@ __device__ __forceinline__ bool issuer_wait(const DecodeParams& p, uint32_t b, u
 }
 
 // Warp 4, lane 0: S(m) = K q^T for the CTA's superstages in order, once the
-// stage has landed, the S buffer is free and the unit's q operand is ready.
+// stage's K half has landed, the S buffer is free and the unit's q operand
+// is ready.
 __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
                           uint32_t qbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
     constexpr uint32_t IQK = idesc_e4m3(128, 16, false, false);
@@ -276,14 +294,14 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
         const uint32_t qb = k & 1;
         if (!issuer_wait(p, bar(bars, B_QFULL + (int)qb), (k >> 1) & 1, abort_flag)) break;
         for (int s = 0; s < nss; ++s, ++m) {
-            const uint32_t slot = m % NSS, sb = m & 1;
-            if (!issuer_wait(p, bar(bars, B_FULL + (int)slot), (m / NSS) & 1, abort_flag) ||
+            const uint32_t slot = m % NKS, sb = m & 1;
+            if (!issuer_wait(p, bar(bars, B_KFULL + (int)slot), (m / NKS) & 1, abort_flag) ||
                 !issuer_wait(p, bar(bars, B_SFREE + (int)sb), ((m >> 1) & 1) ^ 1, abort_flag)) {
                 stop = true;
                 break;
             }
             tc_fence_after();
-            const uint32_t ka = ring + slot * SS_BYTES, qa = qbuf + qb * QBUF_BYTES;
+            const uint32_t ka = ring + slot * SLOT_BYTES, qa = qbuf + qb * QBUF_BYTES;
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -293,13 +311,14 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                                 smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
                                 (c | kk) != 0 ? 1u : 0u);
             tc_commit(bar(bars, B_SFULL + (int)sb));
+            tc_commit(bar(bars, B_KEMPTY + (int)slot));  // the K slot may be refilled
         }
         ++k;
     }
 }
 
 // Warp 7, lane 0: O += V^T P^T for the CTA's superstages in order, once the
-// softmax warps have written P(m).  Its commit frees the ring slot and the P
+// softmax warps have written P(m) and the stage's V half has landed.  Its commit frees the V slot and the P
 // buffer.  A unit's first PV overwrites its O buffer (accumulate off) once
 // the epilogue two active units back has read it.
 __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
@@ -314,10 +333,11 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
         if (nss == 0) continue;
         const uint32_t ob = k & 1;
         for (int s = 0; s < nss; ++s, ++m) {
-            const uint32_t slot = m % NSS, pb = m % NPB;
+            const uint32_t slot = m % NVS, pb = m % NPB;
             if ((s == 0 &&
                  !issuer_wait(p, bar(bars, B_OFREE + (int)ob), ((k >> 1) & 1) ^ 1, abort_flag)) ||
-                !issuer_wait(p, bar(bars, B_PFULL + (int)pb), (m / NPB) & 1, abort_flag)) {
+                !issuer_wait(p, bar(bars, B_PFULL + (int)pb), (m / NPB) & 1, abort_flag) ||
+                !issuer_wait(p, bar(bars, B_VFULL + (int)slot), (m / NVS) & 1, abort_flag)) {
                 stop = true;
                 break;
             }
@@ -326,13 +346,13 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const uint32_t d = tmem + TM_O + 32 * ob + 16 * c;
-                const uint32_t va = ring + slot * SS_BYTES + (2 + c) * CHUNK_BYTES;
+                const uint32_t va = ring + (uint32_t)OFF_VRING + slot * SLOT_BYTES + c * CHUNK_BYTES;
                 for (int ks = 0; ks < nks; ++ks)
                     tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, CHUNK_BYTES, 1024),
                                 smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024), IPV,
                                 (s == 0 && ks == 0) ? 0u : 1u);
             }
-            tc_commit(bar(bars, B_EMPTY + (int)slot));   // the slot may be refilled
+            tc_commit(bar(bars, B_VEMPTY + (int)slot));  // the V slot may be refilled
             tc_commit(bar(bars, B_PVDONE + (int)pb));    // P buffer free, O up to date
         }
         ++k;
@@ -526,13 +546,14 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         const uint32_t ob = k & 1;
         const uint32_t to = tl + TM_O + 32 * ob;   // this unit's O^T columns
         for (int s = 0; s < nss; ++s) {
-            const uint32_t ms = n + (uint32_t)s, slot = ms % NSS, sb = ms & 1, pbi = ms % NPB;
-            // S of this superstage, the stage's copies (for the flags and the
-            // V rows below) and the P buffer's previous PV
+            const uint32_t ms = n + (uint32_t)s, slot = ms % NVS, sb = ms & 1, pbi = ms % NPB;
+            // S of this superstage, the stage's V copies (they carry the
+            // flags, and V rows may be zeroed below) and the P buffer's
+            // previous PV
             bool ok = true;
             if (lane == 0)
                 ok = wait_or_abort(bar(bars, B_SFULL + (int)sb), (ms >> 1) & 1, abort_flag) &&
-                     wait_or_abort(bar(bars, B_FULL + (int)slot), (ms / NSS) & 1, abort_flag) &&
+                     wait_or_abort(bar(bars, B_VFULL + (int)slot), (ms / NVS) & 1, abort_flag) &&
                      (ms < NPB || wait_or_abort(bar(bars, B_PVDONE + (int)pbi),
                                                 ((ms - NPB) / NPB) & 1, abort_flag));
             if (!settle(__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0)) break;
@@ -623,8 +644,8 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             if (tid < 32 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    uint4* vr = reinterpret_cast<uint4*>(ring + slot * SS_BYTES +
-                                                         (2 + c) * CHUNK_BYTES + tid * 128);
+                    uint4* vr = reinterpret_cast<uint4*>(ring + OFF_VRING + slot * SLOT_BYTES +
+                                                         c * CHUNK_BYTES + tid * 128);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -720,9 +741,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t bars = smem_addr(smem + OFF_BARS);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSS; ++s) {
-            mbar_init(bar(bars, B_FULL + s), 1);       // producer's arm (+ copied bytes)
-            mbar_init(bar(bars, B_EMPTY + s), 1);      // PV commit
+        for (int s = 0; s < NKS; ++s) {
+            mbar_init(bar(bars, B_KFULL + s), 1);      // producer's arm (+ copied K bytes)
+            mbar_init(bar(bars, B_KEMPTY + s), 1);     // QK commit
+        }
+        for (int s = 0; s < NVS; ++s) {
+            mbar_init(bar(bars, B_VFULL + s), 1);      // producer's arm (+ copied V bytes)
+            mbar_init(bar(bars, B_VEMPTY + s), 1);     // PV commit
         }
         for (int i = 0; i < NPB; ++i) {
             mbar_init(bar(bars, B_PFULL + i), NSW);    // each softmax warp wrote P

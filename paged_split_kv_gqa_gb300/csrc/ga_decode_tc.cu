@@ -51,8 +51,12 @@ namespace ga {
 namespace tc {
 
 constexpr int D = 256;
-constexpr int NKS = 2;                            // K slots (freed by the QK product)
-constexpr int NVS = 4;                            // V slots (freed by the PV product)
+#ifndef GA_TC_NKS
+#define GA_TC_NKS 2
+#define GA_TC_NVS 4
+#endif
+constexpr int NKS = GA_TC_NKS;                    // K slots (freed by the QK product)
+constexpr int NVS = GA_TC_NVS;                    // V slots (freed by the PV product)
 constexpr int SS_PAGES = 8;                       // pages per superstage: 128 keys = MMA M
 constexpr int CHUNK_BYTES = SS_PAGES * kPageSize * 128;   // [128 keys][128 B]
 constexpr int SLOT_BYTES = 2 * CHUNK_BYTES;       // K or V of a superstage: two dim halves

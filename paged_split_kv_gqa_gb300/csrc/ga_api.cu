@@ -120,10 +120,12 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     cand.units = cand.row_chunks * per_rc;
     // Static round-robin schedule of the persistent grid: unit u -> CTA u % G.
     // Cost in "page loads per SM": each unit costs its pages plus a fixed
-    // overhead (warp merge, pipeline refill); a split adds the partial
-    // round trip spread over all SMs plus one extra launch.
+    // overhead (warp merge, pipeline refill: ~3.5K cycles, about 4 pages of
+    // stream time); a split adds the partial round trip spread over all SMs
+    // plus one extra launch.  (With 2 pages the ragged 256-row global family
+    // got 32-page chunks, 6411 GB/s; 64-page chunks measure 6559 GB/s.)
     const int64_t G = std::max<int64_t>(1, std::min<int64_t>(cand.units, in.num_sms));
-    const double unit_ovh = 2.0;
+    const double unit_ovh = 4.0;
     std::vector<double> load((size_t)G, 0.0);
     for (int64_t u = 0; u < cand.units; ++u) {
         const int64_t rc = u / per_rc;

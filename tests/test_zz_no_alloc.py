@@ -32,8 +32,9 @@ def ga():
 def test_noalloc_rejects_plan_beyond_scratch(ga):
     """Runs without a GPU: the size check comes before any CUDA call."""
     wl = W.config(5)
+    # 256-token chunks: ~200 MB of partials, well past the scratch array
     plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=32, num_kv_heads=4, head_dim=512,
-                             window=0, num_sms=152)
+                             window=0, num_sms=152, fixed_chunk_tokens=256)
     assert plan.workspace_bytes > ga.NOALLOC_SCRATCH_BYTES
     with pytest.raises(ga.GAError) as exc:
         st = ga.lib.ga_decode_global_hd512_noalloc(

@@ -1,35 +1,41 @@
-// ga_decode_tc.cu -- sliding-window (hd256) decode over an E4M3 KV pool with
-// both products on the fifth-generation tensor cores (tcgen05, accumulators
-// in tensor memory).
+// ga_decode_tc.cu -- paged decode over an E4M3 KV pool (sliding-window hd256
+// and full-context hd512) with both products on the fifth-generation tensor
+// cores (tcgen05, accumulators in tensor memory).
 //
 // Why a separate kernel.  With E4M3 pages a decode warp that runs its own
 // m16n8k32 MMAs spends its time on per-warp latency chains (QK, softmax, P
 // split, PV per 16-key page), not on bandwidth.  Here one thread issues the
-// MMAs for a whole 128-key "superstage" (8 pages) and four warps only run the
-// softmax, so the warps' work per byte falls by an order of magnitude.  The
-// method is unchanged: the paged softmax attention of the sliding family
-// ("[Model] Gemma 4 M3 31B", Acceptance Criteria: windows of 1024 with the
-// 1023 / 1024 / 1025 boundaries; "[Model] Gemma 4 M2 26B-A4B", Proposed Plan:
-// opt-in FP8 pool for the sliding family).
+// MMAs for a whole "superstage" (8 pages = 128 keys at hd256, 4 pages = 64
+// keys at hd512) and four warps only run the softmax, so the warps' work per
+// byte falls by an order of magnitude.  The method is unchanged: the paged
+// softmax attention of the sliding family ("[Model] Gemma 4 M3 31B",
+// Acceptance Criteria: windows of 1024 with the 1023 / 1024 / 1025
+// boundaries; "[Model] Gemma 4 M2 26B-A4B", Proposed Plan: opt-in FP8 pool
+// for the sliding family) and of the global family over the same kind of
+// pool ("Gemma 4 31B on vLLM -- operating-point reference": an FP8 KV cache
+// covers every layer).
 //
 // Layout of one superstage in shared memory: a K slot and a V slot of 32 KB,
-// each two 16 KB regions (dims 0-127, dims 128-255), each a dense [128 keys]
-// [128 bytes] tile with the 128-byte swizzle.  Page i of the superstage fills
-// rows 16i .. 16i+15 of each region (four 2 KB bulk tensor copies per page),
-// so the key rows of 8 pages sit at one uniform stride and a single MMA
-// descriptor spans them.  K and V slots are separate rings: a K slot is free
+// each D/128 regions (one per 128 dims), each a dense [keys][128 bytes] tile
+// with the 128-byte swizzle.  Page i of the superstage fills rows 16i ..
+// 16i+15 of each region (one 2 KB bulk tensor copy per page and region), so
+// the key rows of the superstage's pages sit at one uniform stride and a
+// single MMA descriptor spans them.  K and V slots are separate rings: a K slot is free
 // again as soon as its QK product has run, a V slot only after the softmax
 // and the PV product, so V gets more slots (2 K + 4 V in 192 KB keep the
 // copy engine busy).
 //
-// Products (M = 128, N = 16, K = 32 per instruction, fp32 accumulate):
-//   S   [keys x 16]  = K [keys x dims]  . Qs^T   (A K-major, B K-major)
-//   O^T [dims x 16] += V^T [dims x keys] . Ps^T  (A MN-major, B K-major)
+// Products (N = 16, K = 32 per instruction, fp32 accumulate):
+//   S   [keys x 16]  = K [keys x dims]  . Qs^T   (A K-major, B K-major; M = keys
+//                                                 of a superstage, 128 or 64)
+//   O^T [dims x 16] += V^T [dims x keys] . Ps^T  (A MN-major, B K-major; M = 128
+//                                                 dims, one product per region)
 // The 16 columns are 8 (query, head) columns twice: q scaled per column by
 // 448 / amax and split into E4M3 hi and lo parts (columns f and 8 + f), and
 // likewise P (scaled by 2^6) into hi and lo; a column's result is the sum of
-// its two halves.  S sits in TMEM lanes = keys, O^T in lanes = dims, so
-// softmax thread t owns key t of a superstage and dim t of each 128-dim half.
+// its two halves.  S sits in TMEM lanes = keys (M = 64: key r in lane
+// 32 (r / 16) + r % 16), O^T in lanes = dims, so a softmax thread owns one key
+// of a superstage and dim t of each 128-dim region.
 //
 // Roles (256 threads): warps 0-3 softmax and output, warp 4 allocates TMEM
 // and its lane 0 issues the QK products, warp 7's lane 0 the PV products
@@ -50,39 +56,23 @@ namespace ga {
 
 namespace tc {
 
-constexpr int D = 256;
 #ifndef GA_TC_NKS
 #define GA_TC_NKS 2
 #define GA_TC_NVS 4
 #endif
 constexpr int NKS = GA_TC_NKS;                    // K slots (freed by the QK product)
 constexpr int NVS = GA_TC_NVS;                    // V slots (freed by the PV product)
-constexpr int SS_PAGES = 8;                       // pages per superstage: 128 keys = MMA M
-constexpr int CHUNK_BYTES = SS_PAGES * kPageSize * 128;   // [128 keys][128 B]
-constexpr int SLOT_BYTES = 2 * CHUNK_BYTES;       // K or V of a superstage: two dim halves
-constexpr int BLOCK_BYTES = kPageSize * D;        // K or V of one page-head block
-constexpr int QBUF_BYTES = 2 * 16 * 128;          // [dim half][16 rows][128 B]
-constexpr int PBUF_BYTES = 16 * 128;              // [16 rows][128 keys]
+constexpr int PBUF_BYTES = 16 * 128;              // [16 rows][up to 128 keys]
 constexpr int NPB = 4;                            // P buffers: the PV of a superstage
                                                   // completes well after the next one's P
 constexpr int NSW = 4;                            // softmax warps
 constexpr int MMA_WARP = 4, PROD_WARP = 5, Q_WARP = 6, PV_WARP = 7;
 constexpr int NTHREADS = 256;
-constexpr int TMEM_COLS = 128;                    // S: 2 x 16 columns, O: 2 x 32 columns
-constexpr int TM_S = 0, TM_O = 32;
+constexpr int TM_S = 0, TM_O = 32;               // S: 2 x 16 columns, then 2 O buffers
 constexpr float PSCALE = 64.0f;                   // P scale: with slack 2^2, P <= 256 < 448
 constexpr float MAX_SLACK = 2.0f;
 
 constexpr int al(int x) { return (x + 127) / 128 * 128; }
-constexpr int OFF_RING = 0;                       // K slots, then V slots
-constexpr int OFF_VRING = OFF_RING + NKS * SLOT_BYTES;
-constexpr int OFF_Q = OFF_VRING + NVS * SLOT_BYTES;
-constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
-constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;               // [2][4 warps][8] floats
-constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4);  // [2][8] q scales
-constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
-constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
-constexpr int OFF_BARS = al(OFF_FLAGS + NVS * 4);
 // barriers: k_full / k_empty [NKS], v_full / v_empty [NVS], two each of
 // s_full, s_free, NPB each of p_full, pv_done, two each of o_free, q_full,
 // q_free, and fin
@@ -91,12 +81,38 @@ constexpr int B_KFULL = 0, B_KEMPTY = NKS, B_VFULL = 2 * NKS, B_VEMPTY = 2 * NKS
               B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + NPB, B_OFREE = B_PVDONE + NPB,
               B_QFULL = B_OFREE + 2, B_QFREE = B_QFULL + 2, B_FIN = B_QFREE + 2,
               NBARS = B_FIN + 1;
-constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
-constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack for 1024-byte alignment
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && SLOT_BYTES % 1024 == 0,
-              "swizzle-128B operands need 1024-byte aligned tiles");
 static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
+
+// Geometry per head dim.  Both give 32 KB K and V slots.
+template <int D_>
+struct Geo {
+    static constexpr int D = D_;
+    static constexpr int NCH = D / 128;                  // 128-dim regions (128 B of E4M3)
+    static constexpr int SSP = D == 256 ? 8 : 4;          // pages per superstage
+    static constexpr int MQ = SSP * kPageSize;            // keys per superstage = QK's M
+    static constexpr int CHUNK_BYTES = MQ * 128;          // one region: [MQ keys][128 B]
+    static constexpr int SLOT_BYTES = NCH * CHUNK_BYTES;  // K or V of a superstage
+    static constexpr int BLOCK_BYTES = kPageSize * D;     // K or V of one page-head block
+    static constexpr int QBUF_BYTES = NCH * 16 * 128;     // [region][16 rows][128 B]
+    static constexpr int O_COLS = 16 * NCH;               // TMEM columns of one O buffer
+    static constexpr int TMEM_COLS = TM_O + 2 * O_COLS <= 128 ? 128 : 256;
+    static constexpr int OFF_RING = 0;                    // K slots, then V slots
+    static constexpr int OFF_VRING = OFF_RING + NKS * SLOT_BYTES;
+    static constexpr int OFF_Q = OFF_VRING + NVS * SLOT_BYTES;
+    static constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
+    static constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;              // [2][4 warps][8]
+    static constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4); // [2][8] q scales
+    static constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
+    static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
+    static constexpr int OFF_BARS = al(OFF_FLAGS + NVS * 4);
+    static constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && CHUNK_BYTES % 1024 == 0,
+                  "swizzle-128B operands need 1024-byte aligned tiles");
+    static_assert((MQ == 128 || MQ == 64) && SSP * NCH <= 32, "superstage shape");
+    static_assert(TM_O + 2 * O_COLS <= TMEM_COLS, "tensor memory");
+};
 
 __device__ __forceinline__ uint32_t bar(uint32_t bars, int i) { return bars + 8u * (uint32_t)i; }
 
@@ -148,9 +164,10 @@ struct UnitCursor {
 
 // Warp 5.  For each superstage m of each unit: wait until K slot m % NKS and
 // V slot m % NVS are free, arm their "full" barriers with the bytes of the
-// good pages, and let lanes 0..7 each copy one page, K (both dim halves)
-// before V.  Pages with an invalid id are flagged (bit i of flags[m % NVS])
-// and not copied.
+// good pages, and let lanes 0..SSP-1 each copy one page, K (every 128-dim
+// region) before V.  Pages with an invalid id are flagged (bit i of
+// flags[m % NVS]) and not copied.
+template <class G>
 __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
                          const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
                          volatile uint32_t* flags, volatile int* abort_flag) {
@@ -190,17 +207,21 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             }
         };
         if (has_next) {               // the next unit's q rows into L2 for the q warp
-            const int64_t r = (int64_t)unit_q_row(p, cur.nl) + (lane >> 2);
-            if ((r + 1) * D <= p.out_elems)
-                prefetch_l2(reinterpret_cast<const char*>(p.q + r * D) + 128 * (lane & 3));
+            constexpr int LPR = G::D * 2 / 128;           // 128-byte lines per q row
+            for (int l = lane; l < kHeadTile * LPR; l += 32) {
+                const int64_t r = (int64_t)unit_q_row(p, cur.nl) + l / LPR;
+                if ((r + 1) * G::D <= p.out_elems)
+                    prefetch_l2(reinterpret_cast<const char*>(p.q + r * G::D) + 128 * (l % LPR));
+            }
         }
         const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride + x.p0;
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
-        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        constexpr int SPB = 32 / G::SSP;  // superstages per batch of 32 page ids
+        const int nss = (x.np + G::SSP - 1) / G::SSP;
         for (int s = 0; s < nss; ++s) {
-            if (s > 0 && (s & 3) == 0) {      // next batch of 32 page ids, one batch ahead
+            if (s > 0 && s % SPB == 0) {      // next batch of 32 page ids, one batch ahead
                 ids = ids_nxt;
-                const int nb = 32 * (s / 4 + 1) + lane;
+                const int nb = 32 * (s / SPB + 1) + lane;
                 ids_nxt = (nb < x.np) ? __ldg(tbl + nb) : -1;
             }
             const uint32_t n = seq, kslot = n % NKS, vslot = n % NVS;
@@ -218,9 +239,10 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                 stop = true;
                 break;
             }
-            const int pi = SS_PAGES * s + (lane & 7);
-            const int32_t pid = __shfl_sync(0xffffffffu, ids, (8 * (s & 3) + (lane & 7)) & 31);
-            const bool present = lane < SS_PAGES && pi < x.np;
+            const int pl = lane % G::SSP;
+            const int pi = G::SSP * s + pl;
+            const int32_t pid = __shfl_sync(0xffffffffu, ids, (G::SSP * (s % SPB) + pl) & 31);
+            const bool present = lane < G::SSP && pi < x.np;
             const bool valid_id = present && page_ok(pid, p.num_pages);
             const int32_t y = valid_id ? page_block_row(pid, x.c, p.Hkv) : 0;
             const bool good = valid_id && GA_CHK(y >= 0 && (int64_t)y + kPageSize <= p.pool_rows);
@@ -229,18 +251,20 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             const uint32_t kfull = bar(bars, B_KFULL + kslot), vfull = bar(bars, B_VFULL + vslot);
             if (lane == 0) {
                 flags[vslot] = pm & ~gm;
-                mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * BLOCK_BYTES);
-                mbar_arrive_expect_tx(vfull, (uint32_t)__popc(gm) * BLOCK_BYTES);
+                mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
+                mbar_arrive_expect_tx(vfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
             }
             __syncwarp();
             if (good) {
-                const uint32_t kd = ring + kslot * SLOT_BYTES + (uint32_t)lane * (kPageSize * 128);
-                const uint32_t vd = ring + (uint32_t)OFF_VRING + vslot * SLOT_BYTES +
+                const uint32_t kd = ring + kslot * G::SLOT_BYTES + (uint32_t)lane * (kPageSize * 128);
+                const uint32_t vd = ring + (uint32_t)G::OFF_VRING + vslot * G::SLOT_BYTES +
                                     (uint32_t)lane * (kPageSize * 128);
-                tma_load_3d(kd, tmK, kfull, 0, y, 0, policy);
-                tma_load_3d(kd + CHUNK_BYTES, tmK, kfull, 0, y, 1, policy);
-                tma_load_3d(vd, tmV, vfull, 0, y, 0, policy);
-                tma_load_3d(vd + CHUNK_BYTES, tmV, vfull, 0, y, 1, policy);
+#pragma unroll
+                for (int c = 0; c < G::NCH; ++c)
+                    tma_load_3d(kd + c * G::CHUNK_BYTES, tmK, kfull, 0, y, c, policy);
+#pragma unroll
+                for (int c = 0; c < G::NCH; ++c)
+                    tma_load_3d(vd + c * G::CHUNK_BYTES, tmV, vfull, 0, y, c, policy);
             } else if (present) {
                 report(p.err_word, valid_id ? kErrSelfCheck : kErrPageId);
             }
@@ -285,15 +309,16 @@ __device__ __forceinline__ bool issuer_wait(const DecodeParams& p, uint32_t b, u
 // Warp 4, lane 0: S(m) = K q^T for the CTA's superstages in order, once the
 // stage's K half has landed, the S buffer is free and the unit's q operand
 // is ready.
+template <class G>
 __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
                           uint32_t qbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
-    constexpr uint32_t IQK = idesc_e4m3(128, 16, false, false);
+    constexpr uint32_t IQK = idesc_e4m3(G::MQ, 16, false, false);
     uint32_t m = 0, k = 0;                        // superstages, active units so far
     bool stop = false;
     UnitCursor cur(p, pre, U);
     while (cur.more() && !stop) {
         const UnitInfo x = cur.take(p, pre);
-        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        const int nss = (x.np + G::SSP - 1) / G::SSP;
         if (nss == 0) continue;
         const uint32_t qb = k & 1;
         if (!issuer_wait(p, bar(bars, B_QFULL + (int)qb), (k >> 1) & 1, abort_flag)) break;
@@ -305,13 +330,13 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                 break;
             }
             tc_fence_after();
-            const uint32_t ka = ring + slot * SLOT_BYTES, qa = qbuf + qb * QBUF_BYTES;
+            const uint32_t ka = ring + slot * G::SLOT_BYTES, qa = qbuf + qb * G::QBUF_BYTES;
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < G::NCH; ++c)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_e4m3(tmem + TM_S + 16 * sb,
-                                smem_desc_sw128(ka + c * CHUNK_BYTES + 32 * kk, 16, 1024),
+                                smem_desc_sw128(ka + c * G::CHUNK_BYTES + 32 * kk, 16, 1024),
                                 smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
                                 (c | kk) != 0 ? 1u : 0u);
             tc_commit(bar(bars, B_SFULL + (int)sb));
@@ -325,6 +350,7 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 // softmax warps have written P(m) and the stage's V half has landed.  Its commit frees the V slot and the P
 // buffer.  A unit's first PV overwrites its O buffer (accumulate off) once
 // the epilogue two active units back has read it.
+template <class G>
 __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
                           uint32_t pbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
     constexpr uint32_t IPV = idesc_e4m3(128, 16, true, false);
@@ -333,7 +359,7 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
     UnitCursor cur(p, pre, U);
     while (cur.more() && !stop) {
         const UnitInfo x = cur.take(p, pre);
-        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        const int nss = (x.np + G::SSP - 1) / G::SSP;
         if (nss == 0) continue;
         const uint32_t ob = k & 1;
         for (int s = 0; s < nss; ++s, ++m) {
@@ -346,13 +372,14 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                 break;
             }
             tc_fence_after();
-            const int nks = (min(SS_PAGES, x.np - SS_PAGES * s) + 1) / 2;   // 32 keys per MMA
+            const int nks = (min(G::SSP, x.np - G::SSP * s) + 1) / 2;   // 32 keys per MMA
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const uint32_t d = tmem + TM_O + 32 * ob + 16 * c;
-                const uint32_t va = ring + (uint32_t)OFF_VRING + slot * SLOT_BYTES + c * CHUNK_BYTES;
+            for (int c = 0; c < G::NCH; ++c) {
+                const uint32_t d = tmem + TM_O + G::O_COLS * ob + 16 * c;
+                const uint32_t va =
+                    ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::CHUNK_BYTES;
                 for (int ks = 0; ks < nks; ++ks)
-                    tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, CHUNK_BYTES, 1024),
+                    tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, G::CHUNK_BYTES, 1024),
                                 smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024), IPV,
                                 (s == 0 && ks == 0) ? 0u : 1u);
             }
@@ -368,16 +395,18 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 // Warp 6.  For each active unit (one with pages), in the order the MMA issuer
 // takes them: the unit's q rows as the QK operand in buffer k % 2 -- column f
 // scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row 8 + f
-// of each 128-dim half ([16 rows][128 B], 128-byte swizzle); rows of columns
-// past the unit's valid ones are zero.  Lane l takes column l / 4, dims
-// 64 (l % 4) .. +63.  Buffer k % 2 is rewritten once the softmax warps are
-// done with active unit k - 2 (its scales read, all its S consumed).
+// of each 128-dim region ([16 rows][128 B], 128-byte swizzle); rows of
+// columns past the unit's valid ones are zero.  Lane l takes column l / 4,
+// dims D/4 (l % 4) .. +D/4-1.  Buffer k % 2 is rewritten once the softmax
+// warps are done with active unit k - 2 (its scales read, all its S consumed).
+template <class G>
 __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                        uint32_t bars, volatile int* abort_flag) {
+    constexpr int NW = G::D / 32;                  // 16-byte loads per lane (8 dims each)
     const int lane = threadIdx.x & 31;
-    float* qsc = reinterpret_cast<float*>(smem + OFF_QSC);     // [2][8]
-    uint8_t* qbuf = smem + OFF_Q;
-    const int f = lane >> 2, d0 = 64 * (lane & 3);
+    float* qsc = reinterpret_cast<float*>(smem + G::OFF_QSC);  // [2][8]
+    uint8_t* qbuf = smem + G::OFF_Q;
+    const int f = lane >> 2, d0 = (G::D / 4) * (lane & 3);
     UnitCursor cur(p, pre, U);
     uint32_t k = 0;
     while (cur.more()) {
@@ -392,22 +421,22 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
             }
             break;
         }
-        uint4 wv[8];
+        uint4 wv[NW];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wv[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < NW; ++i) wv[i] = make_uint4(0u, 0u, 0u, 0u);
         const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
         if (f < y.nvalid) {
-            if (GA_CHK((row + 1) * D <= p.out_elems)) {
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + row * D + d0);
+            if (GA_CHK((row + 1) * G::D <= p.out_elems)) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + row * G::D + d0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) wv[i] = __ldg(src + i);
+                for (int i = 0; i < NW; ++i) wv[i] = __ldg(src + i);
             } else {
                 report(p.err_word, kErrSelfCheck);
             }
         }
         float am = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NW; ++i) {
             const uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -418,9 +447,8 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
         if ((lane & 3) == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
         const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
         const float inv = 1.0f / sc;
-        uint8_t* half = qbuf + qb * QBUF_BYTES + (d0 >> 7) * 2048;
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {          // 16 dims: elements of wv[i], wv[i + 1]
+        for (int i = 0; i < NW; i += 2) {         // 16 dims: elements of wv[i], wv[i + 1]
             const uint32_t e[8] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w,
                                    wv[i + 1].x, wv[i + 1].y, wv[i + 1].z, wv[i + 1].w};
             uint32_t hw[4], lw[4];
@@ -432,7 +460,9 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
                 hw[j] = h01 | (h23 << 16);
                 lw[j] = l01 | (l23 << 16);
             }
-            const int jj = ((d0 & 127) >> 4) + (i >> 1);     // 16-byte chunk of the 128-byte row
+            const int dd = d0 + 8 * i;                       // first dim of the piece
+            const int jj = (dd & 127) >> 4;                  // 16-byte chunk of the 128-byte row
+            uint8_t* half = qbuf + qb * G::QBUF_BYTES + (dd >> 7) * 2048;
             *reinterpret_cast<uint4*>(half + f * 128 + ((jj ^ (f & 7)) << 4)) =
                 make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(half + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
@@ -448,25 +478,31 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
 
 // ------------------------------------------------------------------ softmax warps
 
-// Warps 0-3.  Thread t owns key t of every superstage (TMEM lane t of S) and
-// dim t of each 128-dim half of O.  Per superstage: read S, mask, online
+// Warps 0-3.  Thread t owns one key of every superstage (M = 128: key t;
+// M = 64: key 16 w + lane for lanes 0..15 of warp w, the TMEM lanes the
+// product writes) and dim t of each 128-dim region of O.  Per superstage:
+// read S, mask, online
 // softmax in base 2 (the running max is raised only when a score exceeds it
 // by more than MAX_SLACK; then O is rescaled in TMEM), write P's hi / lo
 // E4M3 parts as the PV operand, zero V rows the PV reads but no query
 // attends.  At the end of a unit: read O and write the output (or a split
 // partial and its LSE).  NV (2, 4 or 8) bounds the valid (query, head)
 // columns of every unit; columns NV.. of P stay zero.
-template <int NV>
+template <class G, int NV>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile uint32_t* flags,
                               volatile int* abort_flag) {
+    constexpr int D = G::D;
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
     const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);     // this warp's TMEM lanes
-    float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [max | sum][4 warps][8]
-    const float* qsc = reinterpret_cast<const float*>(smem + OFF_QSC);
-    uint8_t* pbuf = smem + OFF_P;
-    uint8_t* ring = smem + OFF_RING;
+    float* red = reinterpret_cast<float*>(smem + G::OFF_RED);  // [max | sum][4 warps][8]
+    const float* qsc = reinterpret_cast<const float*>(smem + G::OFF_QSC);
+    uint8_t* pbuf = smem + G::OFF_P;
+    uint8_t* ring = smem + G::OFF_RING;
+    // this thread's key within a superstage, and whether it has one
+    const bool key_lane = G::MQ == 128 || lane < 16;
+    const int kss = G::MQ == 128 ? tid : 16 * w + (lane & 15);
     bool stop = false;
 
     // P columns past NV are never written: zero them once.
@@ -501,12 +537,13 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             if (single) {
                 const int64_t r = (int64_t)x.b * p.Hq + h;
                 if (!GA_CHK((r + 1) * D <= p.out_elems)) continue;
-                p.out[r * D + tid] = __float2bfloat16_rn(0.f);
-                p.out[r * D + 128 + tid] = __float2bfloat16_rn(0.f);
+#pragma unroll
+                for (int c = 0; c < G::NCH; ++c)
+                    p.out[r * D + 128 * c + tid] = __float2bfloat16_rn(0.f);
             } else if (GA_CHK(x.rc < p.rc_capacity && p.partial_o != nullptr)) {
                 float* po = p.partial_o + (x.rc * p.Hq + h) * (int64_t)D;
-                po[tid] = 0.f;
-                po[128 + tid] = 0.f;
+#pragma unroll
+                for (int c = 0; c < G::NCH; ++c) po[128 * c + tid] = 0.f;
             }
         }
         if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity))
@@ -528,7 +565,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             nvs = __ldg(p.v_scale + cur.nl.c);
         }
         const bool single = (x.g.chunks == 1);
-        const int nss = (x.np + SS_PAGES - 1) / SS_PAGES;
+        const int nss = (x.np + G::SSP - 1) / G::SSP;
         if (nss == 0) {
             write_empty(x, single);
             continue;
@@ -548,7 +585,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             l[f] = 0.f;
         }
         const uint32_t ob = k & 1;
-        const uint32_t to = tl + TM_O + 32 * ob;   // this unit's O^T columns
+        const uint32_t to = tl + TM_O + G::O_COLS * ob;   // this unit's O^T columns
         for (int s = 0; s < nss; ++s) {
             const uint32_t ms = n + (uint32_t)s, slot = ms % NVS, sb = ms & 1, pbi = ms % NPB;
             // S of this superstage, the stage's V copies (they carry the
@@ -568,10 +605,10 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bars, B_SFREE + (int)sb));
-            const int pg = tid >> 4;
-            const int npg = min(SS_PAGES, x.np - SS_PAGES * s);
-            const bool present = pg < npg && !((flags[slot] >> pg) & 1u);
-            const int32_t kj = (x.p0 + SS_PAGES * s + pg) * kPageSize + (tid & 15);
+            const int pg = kss >> 4;
+            const int npg = min(G::SSP, x.np - G::SSP * s);
+            const bool present = key_lane && pg < npg && !((flags[slot] >> pg) & 1u);
+            const int32_t kj = (x.p0 + G::SSP * s + pg) * kPageSize + (kss & 15);
             float sc[NV];
             bool grow = false;
 #pragma unroll
@@ -607,7 +644,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                     if (!wait_all(B_PVDONE + (int)(mp % NPB), (mp / NPB) & 1)) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < G::NCH; ++c) {
                         uint32_t o[16];
                         tmem_ld16(to + 16 * c, o);
                         tmem_ld_wait();
@@ -634,22 +671,24 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 split_e4m3x2(p0 * PSCALE, p1 * PSCALE, hb[f / 2], lb[f / 2]);
             }
             uint8_t* pb = pbuf + pbi * PBUF_BYTES;
-            const int kc = tid >> 4, kb = tid & 15;
+            const int kc = kss >> 4, kb = kss & 15;
+            if (key_lane) {
 #pragma unroll
-            for (int f = 0; f < NV; ++f) {
-                const int sh = 8 * (f & 1);
-                pb[f * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(hb[f / 2] >> sh);
-                pb[(8 + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[f / 2] >> sh);
+                for (int f = 0; f < NV; ++f) {
+                    const int sh = 8 * (f & 1);
+                    pb[f * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(hb[f / 2] >> sh);
+                    pb[(8 + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[f / 2] >> sh);
+                }
             }
             // V rows inside the PV's 32-key steps that no query of the row
             // attends (window edges, a flagged page, the page after an odd
             // last one) may hold anything, NaN included: zero them
             const int nks = (npg + 1) / 2;
-            if (tid < 32 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
+            if (key_lane && kss < 32 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint4* vr = reinterpret_cast<uint4*>(ring + OFF_VRING + slot * SLOT_BYTES +
-                                                         c * CHUNK_BYTES + tid * 128);
+                for (int c = 0; c < G::NCH; ++c) {
+                    uint4* vr = reinterpret_cast<uint4*>(ring + G::OFF_VRING + slot * G::SLOT_BYTES +
+                                                         c * G::CHUNK_BYTES + kss * 128);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -679,38 +718,39 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             Lt[f] = f < x.nvalid ? ((r[0] + r[kHeadTile]) + (r[2 * kHeadTile] + r[3 * kHeadTile]))
                                  : 0.f;
         }
+        // only an exactly empty sum means "no keys"; NaN in attended K / V
+        // reaches the output as in the definition
+        float fac[NV];
+#pragma unroll
+        for (int f = 0; f < NV; ++f) fac[f] = (Lt[f] == 0.f) ? 0.f : __fdividef(vsc, Lt[f] * PSCALE);
+        const int64_t r0 = (int64_t)x.b * p.Hq + x.h0;          // output row of column 0
+        bool bad_store = false;
         tc_fence_after();
-        uint32_t o0[16], o1[16];
-        tmem_ld16(to, o0);
-        tmem_ld16(to + 16, o1);
-        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < G::NCH; ++c) {
+            uint32_t o[16];
+            tmem_ld16(to + 16 * c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int f = 0; f < NV; ++f) {
+                if (f >= x.nvalid) continue;
+                const float v = (Lt[f] == 0.f)
+                                    ? 0.f
+                                    : (__uint_as_float(o[f]) + __uint_as_float(o[8 + f])) * fac[f];
+                if (single) {
+                    if (GA_CHK((r0 + f + 1) * D <= p.out_elems))
+                        p.out[(r0 + f) * D + 128 * c + tid] = __float2bfloat16_rn(v);
+                    else
+                        bad_store = true;
+                } else if (GA_CHK(x.rc < p.rc_capacity && p.partial_o != nullptr)) {
+                    p.partial_o[(x.rc * p.Hq + x.h0 + f) * (int64_t)D + 128 * c + tid] = v;
+                }
+            }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bars, B_OFREE + (int)ob));
-#pragma unroll
-        for (int f = 0; f < NV; ++f) {
-            if (f >= x.nvalid) continue;
-            // only an exactly empty sum means "no keys"; NaN in attended K / V
-            // reaches the output as in the definition
-            const float L = Lt[f];
-            const float fac = (L == 0.f) ? 0.f : __fdividef(vsc, L * PSCALE);
-            const float v0 = (L == 0.f) ? 0.f : (__uint_as_float(o0[f]) + __uint_as_float(o0[8 + f])) * fac;
-            const float v1 = (L == 0.f) ? 0.f : (__uint_as_float(o1[f]) + __uint_as_float(o1[8 + f])) * fac;
-            const int64_t h = x.h0 + f;
-            if (single) {
-                const int64_t r = (int64_t)x.b * p.Hq + h;
-                if (GA_CHK((r + 1) * D <= p.out_elems)) {
-                    p.out[r * D + tid] = __float2bfloat16_rn(v0);
-                    p.out[r * D + 128 + tid] = __float2bfloat16_rn(v1);
-                } else {
-                    report(p.err_word, kErrSelfCheck);
-                }
-            } else if (GA_CHK(x.rc < p.rc_capacity && p.partial_o != nullptr)) {
-                float* po = p.partial_o + (x.rc * p.Hq + h) * (int64_t)D;
-                po[tid] = v0;
-                po[128 + tid] = v1;
-            }
-        }
+        if (bad_store) report(p.err_word, kErrSelfCheck);
         if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity)) {
             float mm = -CUDART_INF_F, LL = 0.f;      // natural-log LSE of column tid
 #pragma unroll
@@ -729,7 +769,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
 
 // ------------------------------------------------------------------ kernel
 
-template <int NV>
+template <int D, int NV>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -738,11 +778,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __shared__ uint32_t tmem_slot;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    using G = Geo<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* pre = reinterpret_cast<int32_t*>(smem + OFF_PREFIX);
-    volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + OFF_FLAGS);
-    const uint32_t ring = smem_addr(smem + OFF_RING);
-    const uint32_t bars = smem_addr(smem + OFF_BARS);
+    int32_t* pre = reinterpret_cast<int32_t*>(smem + G::OFF_PREFIX);
+    volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_FLAGS);
+    const uint32_t ring = smem_addr(smem + G::OFF_RING);
+    const uint32_t bars = smem_addr(smem + G::OFF_BARS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NKS; ++s) {
@@ -775,19 +816,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int64_t total_rc = 0;
     if (!build_row_prefix(p, pre, NTHREADS, &total_rc)) return;
     const int64_t U = total_rc * p.Hkv * p.HG;
-    if (warp == MMA_WARP) tmem_alloc(smem_addr(&tmem_slot), TMEM_COLS);
+    if (warp == MMA_WARP) tmem_alloc(smem_addr(&tmem_slot), G::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     if (warp < NSW) {
-        softmax_warps<NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag);
+        softmax_warps<G, NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag);
     } else if (warp == MMA_WARP || warp == PV_WARP) {
         if (lane == 0) {
             if (warp == MMA_WARP)
-                qk_issuer(p, pre, U, ring, smem_addr(smem + OFF_Q), bars, tmem, &abort_flag);
+                qk_issuer<G>(p, pre, U, ring, smem_addr(smem + G::OFF_Q), bars, tmem, &abort_flag);
             else
-                pv_issuer(p, pre, U, ring, smem_addr(smem + OFF_P), bars, tmem, &abort_flag);
+                pv_issuer<G>(p, pre, U, ring, smem_addr(smem + G::OFF_P), bars, tmem, &abort_flag);
             // every MMA this thread issued has completed before TMEM is freed
             tc_commit(bar(bars, B_FIN));
             if (!mbar_wait(bar(bars, B_FIN), 0)) {
@@ -797,33 +838,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncwarp();
     } else if (warp == PROD_WARP) {
-        producer(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
+        producer<G>(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
     } else if (warp == Q_WARP) {
-        q_warp(p, pre, U, smem, bars, &abort_flag);
+        q_warp<G>(p, pre, U, smem, bars, &abort_flag);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == MMA_WARP) tmem_dealloc(tmem, G::TMEM_COLS);
 }
 
 }  // namespace tc
 
 // ------------------------------------------------------------------ host
 
-int launch_decode_tc(const DecodeArgs& a) {
+template <int D>
+static int run_tc(const DecodeArgs& a) {
     const ga_plan& pl = *a.plan;
     const int32_t S = pl.q_len;
     // (query, head) columns of a kv head, at most 8 per unit
     const int32_t cols = a.num_q_heads / a.num_kv_heads * S;
     const int nv = cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
-    auto kern = nv == 2 ? &tc::decode_tc_kernel<2>
-              : nv == 4 ? &tc::decode_tc_kernel<4> : &tc::decode_tc_kernel<8>;
-    int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), tc::SMEM_BYTES,
-                              nv == 2 ? 8 : nv == 4 ? 9 : 10);
+    auto kern = nv == 2 ? &tc::decode_tc_kernel<D, 2>
+              : nv == 4 ? &tc::decode_tc_kernel<D, 4> : &tc::decode_tc_kernel<D, 8>;
+    constexpr int kSmem = tc::Geo<D>::SMEM_BYTES;
+    int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmem,
+                              (D == 256 ? 8 : 11) + (nv == 2 ? 0 : nv == 4 ? 1 : 2));
     if (rc != GA_OK) return rc;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
-    // one box = one 128-dim half of a page-head block: [16 keys][128 B]
+    // one box = one 128-dim region of a page-head block: [16 keys][128 B]
     CUtensorMap tmK, tmV;
     rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
     if (rc != GA_OK) return rc;
@@ -866,12 +909,18 @@ int launch_decode_tc(const DecodeArgs& a) {
     p.pool_rows = rows;
     p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, tc::NTHREADS, tc::SMEM_BYTES, a.stream>>>(tmK, tmV, p);
+    kern<<<grid, tc::NTHREADS, kSmem, a.stream>>>(tmK, tmV, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
     if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
                               a.pt_stride, a.stream);
     return GA_OK;
+}
+
+int launch_decode_tc(const DecodeArgs& a) {
+    if (a.head_dim == 256) return run_tc<256>(a);
+    if (a.head_dim == 512) return run_tc<512>(a);
+    return GA_ERR_UNSUPPORTED;
 }
 
 }  // namespace ga

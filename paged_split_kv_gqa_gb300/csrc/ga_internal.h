@@ -44,7 +44,8 @@ int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_
 
 int launch_decode(const DecodeArgs& a);
 
-// Sliding-window hd256 decode over an E4M3 pool on tcgen05 tensor cores.
+// Decode over an E4M3 pool (hd256 sliding window, hd512 global with two
+// pools) on tcgen05 tensor cores.
 int launch_decode_tc(const DecodeArgs& a);
 
 int launch_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,

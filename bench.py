@@ -178,8 +178,26 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1):
         keys=int(M.attended_keys(wl.seq_lens, M.union_window(fam.window, S)).sum()))
 
 
+def workload_config(workload, seed, fp8="none"):
+    """The named workload; fp8 ("local", "global", "both") stores those
+    families' KV pools as E4M3 with per-head scales instead of bf16."""
+    import dataclasses
+
+    from paged_split_kv_gqa_gb300 import workloads as W
+    wl = W.config(WORKLOADS[workload], seed=seed)
+    if fp8 == "none":
+        return wl
+    loc, glo = wl.local, wl.global_
+    if fp8 in ("local", "both"):
+        loc = dataclasses.replace(loc, kv_dtype=W.KV_E4M3)
+    if fp8 in ("global", "both"):
+        glo = dataclasses.replace(glo, kv_dtype=W.KV_E4M3)
+    return W.Workload(wl.name, wl.seq_lens, wl.page_size, loc, glo, wl.local_layers,
+                      wl.global_layers)
+
+
 def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
-               q_len=1):
+               q_len=1, fp8="none"):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -187,7 +205,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
     import torch
     from paged_split_kv_gqa_gb300 import workloads as W
 
-    wl = W.config(WORKLOADS[workload], seed=seed)
+    wl = workload_config(workload, seed, fp8)
     if rows:
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
@@ -251,12 +269,12 @@ def oracle_sample(fams_cpu):
     return time.perf_counter() - t0
 
 
-def cpu_sample_inputs(seed, nrows, workload):
+def cpu_sample_inputs(seed, nrows, workload, fp8="none"):
     """CPU copies of a bounded sample of the same workload: its first nrows
     rows (same lengths), one layer per family, drawn on the host."""
     from paged_split_kv_gqa_gb300 import metrics as M
     from paged_split_kv_gqa_gb300 import workloads as W
-    wl = W.config(WORKLOADS[workload], seed=seed)
+    wl = workload_config(workload, seed, fp8)
     sub = W.Workload(wl.name, wl.seq_lens[:nrows].copy(), wl.page_size, wl.local, wl.global_)
     fams = [W.make_family_inputs(sub, fam, device="cpu", seed=seed,
                                  release_old=(fam.window > 0)) for fam in sub.families()]
@@ -332,7 +350,7 @@ def run_reference(args):
         return
     from oracle import oracle as O
     nrows = 2
-    fams, nbytes = cpu_sample_inputs(args.seed, nrows, args.workload)
+    fams, nbytes = cpu_sample_inputs(args.seed, nrows, args.workload, args.fp8)
     for _ in range(args.warmup):
         oracle_sample(fams)
     times = [oracle_sample(fams) for _ in range(args.steps)]
@@ -378,7 +396,8 @@ def run_ga(args):
         dist.init_process_group("nccl", device_id=device)
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
-                                         args.pools, args.kv_alias, args.splits, args.q_len)
+                                         args.pools, args.kv_alias, args.splits, args.q_len,
+                                         args.fp8)
 
     def step(evs=None):
         n = 0
@@ -464,7 +483,7 @@ def run_ga(args):
     kname = "decode_global_hd512" if dominant == "global" else "decode_local_hd256"
     # the committed counters cover the default 31B step (planner's splits, two pools)
     default_step = (args.workload == "31b" and not args.rows and not args.splits
-                    and not args.kv_alias and args.q_len == 1)
+                    and not args.kv_alias and args.q_len == 1 and args.fp8 == "none")
     traffic = committed_traffic(kname) if default_step else None
 
     # ---- end to end through host buffers: H2D inputs, the C-ABI calls, D2H outputs
@@ -530,6 +549,8 @@ def run_ga(args):
             text += f"; {args.pools} distinct pools per family rotated over the layers"
         if args.kv_alias:
             text += "; global family with K == V (one pool, read once)"
+        if args.fp8 != "none":
+            text += f"; {args.fp8} family KV stored as fp8-e4m3 with per-head scales"
         if args.splits:
             text += f"; split-KV count fixed at {args.splits} chunks per row"
         if args.q_len > 1:
@@ -588,6 +609,8 @@ def main():
                     help="split-KV chunks per row for every plan (0 = planner's choice)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per row (> 1: a multi-query / speculative-verify step)")
+    ap.add_argument("--fp8", default="none", choices=["none", "local", "global", "both"],
+                    help="store these families' KV pools as fp8-e4m3 with per-head scales")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -69,7 +69,7 @@ int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_
 }
 
 int ensure_smem_attr(const void* func, int bytes, int slot) {
-    static std::atomic<uint64_t> done[16];
+    static std::atomic<uint64_t> done[32];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GA_ERR_CUDA;
     const uint64_t bit = 1ull << (dev & 63);

@@ -1059,9 +1059,13 @@ int launch_decode(const DecodeArgs& a) {
 #endif
         return a.kv_dtype == GA_KV_BF16 ? run<CfgLocalBf16>(a, 0) : run<CfgLocalE4m3>(a, 1);
     }
-    if (a.head_dim == 512 && a.k_pool == a.v_pool)
+    if (a.head_dim == 512 && a.k_pool == a.v_pool) {
+#ifndef GA_E4M3_GLOBAL_MMA_SYNC
+        if (a.kv_dtype == GA_KV_E4M3) return launch_decode_tc(a);
+#endif
         return a.kv_dtype == GA_KV_BF16 ? run<CfgGlobalBf16Alias>(a, 4)
                                         : run<CfgGlobalE4m3Alias>(a, 5);
+    }
     if (a.head_dim == 512) {
 #ifndef GA_E4M3_GLOBAL_MMA_SYNC
         if (a.kv_dtype == GA_KV_E4M3) return launch_decode_tc(a);

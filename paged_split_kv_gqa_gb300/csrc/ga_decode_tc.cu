@@ -73,20 +73,25 @@ constexpr float PSCALE = 64.0f;                   // P scale: with slack 2^2, P 
 constexpr float MAX_SLACK = 2.0f;
 
 constexpr int al(int x) { return (x + 127) / 128 * 128; }
-// barriers: k_full / k_empty [NKS], v_full / v_empty [NVS], two each of
+// barriers: k_full / k_empty [NKS], v_full / v_empty [NVMAX], two each of
 // s_full, s_free, NPB each of p_full, pv_done, two each of o_free, q_full,
 // q_free, and fin
-constexpr int B_KFULL = 0, B_KEMPTY = NKS, B_VFULL = 2 * NKS, B_VEMPTY = 2 * NKS + NVS,
-              B_SFULL = 2 * NKS + 2 * NVS, B_SFREE = B_SFULL + 2,
+constexpr int NVMAX = NKS + NVS;                  // V slots when K == V (no K ring)
+constexpr int B_KFULL = 0, B_KEMPTY = NKS, B_VFULL = 2 * NKS, B_VEMPTY = 2 * NKS + NVMAX,
+              B_SFULL = 2 * NKS + 2 * NVMAX, B_SFREE = B_SFULL + 2,
               B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + NPB, B_OFREE = B_PVDONE + NPB,
               B_QFULL = B_OFREE + 2, B_QFREE = B_QFULL + 2, B_FIN = B_QFREE + 2,
               NBARS = B_FIN + 1;
 static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
 
-// Geometry per head dim.  Both give 32 KB K and V slots.
-template <int D_>
+// Geometry per head dim.  Both give 32 KB K and V slots.  ALIAS: K and V
+// are one pool; each block is fetched once into a V slot that serves both
+// products, and the K ring's memory becomes V slots too.
+template <int D_, bool ALIAS_ = false>
 struct Geo {
     static constexpr int D = D_;
+    static constexpr bool ALIAS = ALIAS_;
+    static constexpr int NVE = ALIAS ? NKS + NVS : NVS;   // V slots in use
     static constexpr int NCH = D / 128;                  // 128-dim regions (128 B of E4M3)
     static constexpr int SSP = D == 256 ? 8 : 4;          // pages per superstage
     static constexpr int MQ = SSP * kPageSize;            // keys per superstage = QK's M
@@ -97,14 +102,14 @@ struct Geo {
     static constexpr int O_COLS = 16 * NCH;               // TMEM columns of one O buffer
     static constexpr int TMEM_COLS = TM_O + 2 * O_COLS <= 128 ? 128 : 256;
     static constexpr int OFF_RING = 0;                    // K slots, then V slots
-    static constexpr int OFF_VRING = OFF_RING + NKS * SLOT_BYTES;
-    static constexpr int OFF_Q = OFF_VRING + NVS * SLOT_BYTES;
+    static constexpr int OFF_VRING = ALIAS ? OFF_RING : OFF_RING + NKS * SLOT_BYTES;
+    static constexpr int OFF_Q = OFF_RING + (NKS + NVS) * SLOT_BYTES;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
     static constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;              // [2][4 warps][8]
     static constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4); // [2][8] q scales
     static constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
     static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
-    static constexpr int OFF_BARS = al(OFF_FLAGS + NVS * 4);
+    static constexpr int OFF_BARS = al(OFF_FLAGS + NVMAX * 4);
     static constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -163,10 +168,10 @@ struct UnitCursor {
 // ------------------------------------------------------------------ producer
 
 // Warp 5.  For each superstage m of each unit: wait until K slot m % NKS and
-// V slot m % NVS are free, arm their "full" barriers with the bytes of the
+// V slot m % NVE are free, arm their "full" barriers with the bytes of the
 // good pages, and let lanes 0..SSP-1 each copy one page, K (every 128-dim
-// region) before V.  Pages with an invalid id are flagged (bit i of
-// flags[m % NVS]) and not copied.
+// region) before V (K == V: only the V slot, once).  Pages with an invalid id
+// are flagged (bit i of flags[m % NVE]) and not copied.
 template <class G>
 __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
                          const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
@@ -224,12 +229,13 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                 const int nb = 32 * (s / SPB + 1) + lane;
                 ids_nxt = (nb < x.np) ? __ldg(tbl + nb) : -1;
             }
-            const uint32_t n = seq, kslot = n % NKS, vslot = n % NVS;
+            const uint32_t n = seq, kslot = n % NKS, vslot = n % G::NVE;
             bool ok = true;
             if (lane == 0)
                 ok = !*abort_flag &&
-                     wait_or_abort(bar(bars, B_KEMPTY + kslot), ((n / NKS) & 1) ^ 1, abort_flag) &&
-                     wait_or_abort(bar(bars, B_VEMPTY + vslot), ((n / NVS) & 1) ^ 1, abort_flag);
+                     (G::ALIAS ||
+                      wait_or_abort(bar(bars, B_KEMPTY + kslot), ((n / NKS) & 1) ^ 1, abort_flag)) &&
+                     wait_or_abort(bar(bars, B_VEMPTY + vslot), ((n / G::NVE) & 1) ^ 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) {
                 if (lane == 0) {
@@ -251,7 +257,7 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             const uint32_t kfull = bar(bars, B_KFULL + kslot), vfull = bar(bars, B_VFULL + vslot);
             if (lane == 0) {
                 flags[vslot] = pm & ~gm;
-                mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
+                if (!G::ALIAS) mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
                 mbar_arrive_expect_tx(vfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
             }
             __syncwarp();
@@ -259,9 +265,11 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
                 const uint32_t kd = ring + kslot * G::SLOT_BYTES + (uint32_t)lane * (kPageSize * 128);
                 const uint32_t vd = ring + (uint32_t)G::OFF_VRING + vslot * G::SLOT_BYTES +
                                     (uint32_t)lane * (kPageSize * 128);
+                if (!G::ALIAS) {
 #pragma unroll
-                for (int c = 0; c < G::NCH; ++c)
-                    tma_load_3d(kd + c * G::CHUNK_BYTES, tmK, kfull, 0, y, c, policy);
+                    for (int c = 0; c < G::NCH; ++c)
+                        tma_load_3d(kd + c * G::CHUNK_BYTES, tmK, kfull, 0, y, c, policy);
+                }
 #pragma unroll
                 for (int c = 0; c < G::NCH; ++c)
                     tma_load_3d(vd + c * G::CHUNK_BYTES, tmV, vfull, 0, y, c, policy);
@@ -290,8 +298,8 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             }
         }
     };
-    drain(B_KFULL, NKS);
-    drain(B_VFULL, NVS);
+    if (!G::ALIAS) drain(B_KFULL, NKS);
+    drain(B_VFULL, G::NVE);
 }
 
 // ------------------------------------------------------------------ MMA issuers
@@ -323,14 +331,18 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
         const uint32_t qb = k & 1;
         if (!issuer_wait(p, bar(bars, B_QFULL + (int)qb), (k >> 1) & 1, abort_flag)) break;
         for (int s = 0; s < nss; ++s, ++m) {
-            const uint32_t slot = m % NKS, sb = m & 1;
-            if (!issuer_wait(p, bar(bars, B_KFULL + (int)slot), (m / NKS) & 1, abort_flag) ||
+            // K == V: S reads the V slot the block was fetched into
+            const uint32_t slot = G::ALIAS ? m % G::NVE : m % NKS, sb = m & 1;
+            if (!issuer_wait(p, bar(bars, (G::ALIAS ? B_VFULL : B_KFULL) + (int)slot),
+                             (m / (G::ALIAS ? G::NVE : NKS)) & 1, abort_flag) ||
                 !issuer_wait(p, bar(bars, B_SFREE + (int)sb), ((m >> 1) & 1) ^ 1, abort_flag)) {
                 stop = true;
                 break;
             }
             tc_fence_after();
-            const uint32_t ka = ring + slot * G::SLOT_BYTES, qa = qbuf + qb * G::QBUF_BYTES;
+            const uint32_t ka = ring + (uint32_t)(G::ALIAS ? G::OFF_VRING : G::OFF_RING) +
+                                slot * G::SLOT_BYTES,
+                           qa = qbuf + qb * G::QBUF_BYTES;
 #pragma unroll
             for (int c = 0; c < G::NCH; ++c)
 #pragma unroll
@@ -340,7 +352,7 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                                 smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
                                 (c | kk) != 0 ? 1u : 0u);
             tc_commit(bar(bars, B_SFULL + (int)sb));
-            tc_commit(bar(bars, B_KEMPTY + (int)slot));  // the K slot may be refilled
+            if (!G::ALIAS) tc_commit(bar(bars, B_KEMPTY + (int)slot));  // the K slot may be refilled
         }
         ++k;
     }
@@ -363,11 +375,11 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
         if (nss == 0) continue;
         const uint32_t ob = k & 1;
         for (int s = 0; s < nss; ++s, ++m) {
-            const uint32_t slot = m % NVS, pb = m % NPB;
+            const uint32_t slot = m % G::NVE, pb = m % NPB;
             if ((s == 0 &&
                  !issuer_wait(p, bar(bars, B_OFREE + (int)ob), ((k >> 1) & 1) ^ 1, abort_flag)) ||
                 !issuer_wait(p, bar(bars, B_PFULL + (int)pb), (m / NPB) & 1, abort_flag) ||
-                !issuer_wait(p, bar(bars, B_VFULL + (int)slot), (m / NVS) & 1, abort_flag)) {
+                !issuer_wait(p, bar(bars, B_VFULL + (int)slot), (m / G::NVE) & 1, abort_flag)) {
                 stop = true;
                 break;
             }
@@ -587,14 +599,14 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         const uint32_t ob = k & 1;
         const uint32_t to = tl + TM_O + G::O_COLS * ob;   // this unit's O^T columns
         for (int s = 0; s < nss; ++s) {
-            const uint32_t ms = n + (uint32_t)s, slot = ms % NVS, sb = ms & 1, pbi = ms % NPB;
+            const uint32_t ms = n + (uint32_t)s, slot = ms % G::NVE, sb = ms & 1, pbi = ms % NPB;
             // S of this superstage, the stage's V copies (they carry the
             // flags, and V rows may be zeroed below) and the P buffer's
             // previous PV
             bool ok = true;
             if (lane == 0)
                 ok = wait_or_abort(bar(bars, B_SFULL + (int)sb), (ms >> 1) & 1, abort_flag) &&
-                     wait_or_abort(bar(bars, B_VFULL + (int)slot), (ms / NVS) & 1, abort_flag) &&
+                     wait_or_abort(bar(bars, B_VFULL + (int)slot), (ms / G::NVE) & 1, abort_flag) &&
                      (ms < NPB || wait_or_abort(bar(bars, B_PVDONE + (int)pbi),
                                                 ((ms - NPB) / NPB) & 1, abort_flag));
             if (!settle(__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0)) break;
@@ -769,7 +781,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, int NV>
+template <int D, int NV, bool ALIAS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -778,7 +790,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __shared__ uint32_t tmem_slot;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    using G = Geo<D>;
+    using G = Geo<D, ALIAS>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t* pre = reinterpret_cast<int32_t*>(smem + G::OFF_PREFIX);
     volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_FLAGS);
@@ -790,7 +802,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar(bars, B_KFULL + s), 1);      // producer's arm (+ copied K bytes)
             mbar_init(bar(bars, B_KEMPTY + s), 1);     // QK commit
         }
-        for (int s = 0; s < NVS; ++s) {
+        for (int s = 0; s < NVMAX; ++s) {
             mbar_init(bar(bars, B_VFULL + s), 1);      // producer's arm (+ copied V bytes)
             mbar_init(bar(bars, B_VEMPTY + s), 1);     // PV commit
         }
@@ -852,18 +864,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-template <int D>
+template <int D, bool ALIAS>
 static int run_tc(const DecodeArgs& a) {
     const ga_plan& pl = *a.plan;
     const int32_t S = pl.q_len;
     // (query, head) columns of a kv head, at most 8 per unit
     const int32_t cols = a.num_q_heads / a.num_kv_heads * S;
     const int nv = cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
-    auto kern = nv == 2 ? &tc::decode_tc_kernel<D, 2>
-              : nv == 4 ? &tc::decode_tc_kernel<D, 4> : &tc::decode_tc_kernel<D, 8>;
-    constexpr int kSmem = tc::Geo<D>::SMEM_BYTES;
+    auto kern = nv == 2 ? &tc::decode_tc_kernel<D, 2, ALIAS>
+              : nv == 4 ? &tc::decode_tc_kernel<D, 4, ALIAS> : &tc::decode_tc_kernel<D, 8, ALIAS>;
+    constexpr int kSmem = tc::Geo<D, ALIAS>::SMEM_BYTES;
+    // attribute slots 8..19: (head dim, alias, column count)
     int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmem,
-                              (D == 256 ? 8 : 11) + (nv == 2 ? 0 : nv == 4 ? 1 : 2));
+                              8 + (D == 256 ? 0 : 6) + (ALIAS ? 3 : 0) +
+                                  (nv == 2 ? 0 : nv == 4 ? 1 : 2));
     if (rc != GA_OK) return rc;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
     // one box = one 128-dim region of a page-head block: [16 keys][128 B]
@@ -918,8 +932,10 @@ static int run_tc(const DecodeArgs& a) {
 }
 
 int launch_decode_tc(const DecodeArgs& a) {
-    if (a.head_dim == 256) return run_tc<256>(a);
-    if (a.head_dim == 512) return run_tc<512>(a);
+    // one pool for K and V (same pointer): fetch each block once
+    const bool alias = a.k_pool == a.v_pool;
+    if (a.head_dim == 256) return alias ? run_tc<256, true>(a) : run_tc<256, false>(a);
+    if (a.head_dim == 512) return alias ? run_tc<512, true>(a) : run_tc<512, false>(a);
     return GA_ERR_UNSUPPORTED;
 }
 

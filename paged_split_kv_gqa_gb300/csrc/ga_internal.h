@@ -52,7 +52,7 @@ int launch_combine(const float* partial_o, const float* partial_lse, const ga_pl
                    const int32_t* seq_lens, void* out, int32_t* err_word, int64_t pt_stride,
                    cudaStream_t stream);
 
-// Sets the dynamic shared-memory limit of `func` once per device (slot < 16
+// Sets the dynamic shared-memory limit of `func` once per device (slot < 32
 // identifies the kernel).
 int ensure_smem_attr(const void* func, int bytes, int slot);
 

@@ -415,13 +415,15 @@ def test_nan_in_attended_kv_propagates(ga, err, split):
     assert_close(out[ok], ref[ok], what="finite part")
 
 
-@pytest.mark.parametrize("kv", [0, 1])
-def test_kv_alias_one_pool(ga, err, kv):
+@pytest.mark.parametrize("D,window,kv", [(512, 0, 0), (512, 0, 1), (256, 1024, 1)])
+def test_kv_alias_one_pool(ga, err, D, window, kv):
     """k_pool is v_pool (K == V): the one-fetch kernel matches the two-pool
     kernel on a copy and the oracle with V = K.  The two kernels may split a
     chunk's pages over different numbers of consumer warps, so their merge
-    order (and the last bit) can differ; both are held to the oracle's bar."""
-    fam = _fam(32, 4, 512, 0, kv=kv)
+    order (and the last bit) can differ; both are held to the oracle's bar.
+    (E4M3 pools of either family run the tensor-core kernel, which fetches
+    each block once into a slot that serves both products.)"""
+    fam = _fam(32 if D == 512 else 16, 4 if D == 512 else 8, D, window, kv=kv)
     fi = _inputs([700, 33, 1500, 1], fam, seed=17)
     fi.v_pool = fi.k_pool
     if kv:

@@ -206,7 +206,8 @@ int ga_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_poo
  *   q [batch, num_q_heads, 256] bf16; num_q_heads % num_kv_heads == 0.
  *   kv_dtype GA_KV_BF16 or GA_KV_E4M3 (with k_scale, v_scale [Hkv] fp32;
  *       with E4M3 the products run on E4M3 tensor cores: q is scaled per head
- *       and split into two E4M3 parts, P likewise, about bf16 precision).
+ *       and split into two E4M3 parts, P likewise, about bf16 precision; an
+ *       E4M3 pool passed as both k_pool and v_pool is read once).
  *   seq_lens [batch] int32 device; window >= 1.
  *   scale: softmax scale (e.g. 1/sqrt(256), or 1.0 for the Gemma convention).
  *   plan: from ga_plan_splits with the same batch, heads, head_dim, window

@@ -20,10 +20,12 @@
 // with the 128-byte swizzle.  Page i of the superstage fills rows 16i ..
 // 16i+15 of each region (one 2 KB bulk tensor copy per page and region), so
 // the key rows of the superstage's pages sit at one uniform stride and a
-// single MMA descriptor spans them.  K and V slots are separate rings: a K slot is free
-// again as soon as its QK product has run, a V slot only after the softmax
-// and the PV product, so V gets more slots (2 K + 4 V in 192 KB keep the
-// copy engine busy).
+// single MMA descriptor spans them.  K and V slots are separate rings: a K
+// slot is free again as soon as its QK product has run, a V slot only after
+// the softmax and the PV product, so V gets more slots (2 K + 4 V in 192 KB
+// keep the copy engine busy).  With one pool for K and V (same pointer) each
+// block is fetched once into a V slot that serves both products, and all six
+// slots are V slots.
 //
 // Products (N = 16, K = 32 per instruction, fp32 accumulate):
 //   S   [keys x 16]  = K [keys x dims]  . Qs^T   (A K-major, B K-major; M = keys
@@ -42,8 +44,8 @@
 // (an MMA issue holds its thread for ~100 cycles, so one thread for both
 // made each product wait behind the other), warp 5 streams pages with bulk
 // tensor copies, warp 6 turns each unit's q rows into the E4M3 operand one
-// unit ahead.  Every role reads the next unit's length (and the producer its page
-// ids) while it works on the current one, so a unit boundary waits on no
+// unit ahead.  Every role reads the next unit's length (and the producer its
+// page ids) while it works on the current one, so a unit boundary waits on no
 // global load.  Hand-offs are mbarriers; every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>

@@ -368,15 +368,19 @@ def test_peaked_softmax_scale_one(ga, err):
     assert_close(out.float().cpu().numpy(), ref, what="scale 1.0", extra_abs=half_ulp)
 
 
-def test_max_batch_short_rows(ga, err):
-    fam = _fam(8, 8, 256, 32)
+@pytest.mark.parametrize("D,window,kv", [(256, 32, 0), (256, 32, 1), (512, 0, 1)])
+def test_max_batch_short_rows(ga, err, D, window, kv):
+    """2048 rows (the per-call maximum: each CTA keeps the row prefix in
+    shared memory), short and empty rows; bf16 and both E4M3 kernels."""
+    fam = _fam(8, 8 if D == 256 else 2, D, window, kv=kv)
     lens = (np.arange(2048) % 50).astype(np.int32)
     fi = _inputs(lens, fam, seed=11, poison=False)
     out = run_decode(ga, fi, _plan(ga, fi), err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     rows = list(range(0, 2048, 97))
-    assert_close(out[rows].float().cpu().numpy(), oracle_decode(fi, rows=rows), what="B=2048")
+    assert_close(out[rows].float().cpu().numpy(), oracle_decode(fi, rows=rows), kv_dtype=kv,
+                 what=f"B=2048 D={D} kv={kv}")
 
 
 def test_bad_page_id_and_length_report_without_nan(ga, err):

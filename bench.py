@@ -603,6 +603,10 @@ def run_ga(args):
         e2.record()
         torch.cuda.synchronize()
         t_e2e = s2.elapsed_time(e2) / 1e3
+        # every read-back must equal its device output (deterministic kernels,
+        # same inputs each step): a read-back that raced its decode would not
+        outputs_match = all(torch.equal(host[id(layer)]["out"], layer["out"].cpu())
+                            for layer in {id(layer): layer for layer in schedule}.values())
         if pg:
             t = torch.tensor([t_e2e], device=device)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -610,6 +614,7 @@ def run_ga(args):
         e2e = {"value": step_bytes * args.steps * world / t_e2e / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": t_e2e / args.steps * 1e3,
+               "read_back_matches_device": bool(outputs_match),
                "copies": "pinned host buffers; H2D and D2H on two side streams overlapping "
                          "other layers' decode; a step reads back the previous step's last "
                          "output first and copies in the next step's first inputs last "

@@ -195,10 +195,12 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
         if (seq_lens_host[b] < 0) return GA_ERR_INVALID_ARG;
 
     const int32_t weff = effective_window(window, q_len);
-    // more than 8 (query, head) columns per kv head: column-parallel units of
+    // more than 8 (query, head) columns per kv head: units of 64 columns for
+    // the tensor-core kernel from kTcMinCols on, else column-parallel units of
     // 4 tiles of 8 (every page read once for all of them)
     const int32_t cols = num_q_heads / num_kv_heads * q_len;
-    const int32_t tw = cols > kHeadTile ? 4 * kHeadTile : kHeadTile;
+    const int32_t tw = cols <= kHeadTile ? kHeadTile
+                       : cols >= kTcMinCols ? kTcColTile : 4 * kHeadTile;
     PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len,
                  tw};
     Candidate best;
@@ -299,7 +301,8 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
     if (plan->batch != batch || plan->num_q_heads != num_q_heads ||
         plan->num_kv_heads != num_kv_heads || plan->head_dim != head_dim ||
         plan->window != window || plan->page_size != page_size || plan->q_len < 1 ||
-        plan->q_len > kMaxQLen || (plan->col_tile != kHeadTile && plan->col_tile != 4 * kHeadTile))
+        plan->q_len > kMaxQLen || (plan->col_tile != kHeadTile && plan->col_tile != 4 * kHeadTile &&
+         plan->col_tile != kTcColTile))
         return GA_ERR_INVALID_ARG;
     if (batch == 0) return GA_OK;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return GA_ERR_INVALID_ARG;

@@ -1047,8 +1047,14 @@ using CfgGlobalBf16Col = DecodeCfg<512, GA_KV_BF16, 4, GA_CG_NS, false, true>;
 using CfgGlobalE4m3Alias = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, 2 * GA_GE_NS, true>;
 
 int launch_decode(const DecodeArgs& a) {
-    // more than one tile of (query, head) columns per kv head (multi-query
-    // decode, wide groups) and a plan made for column-parallel units
+    // many (query, head) columns per kv head (multi-query decode) and a plan
+    // made for 64-column units: the tensor-core kernel
+#ifndef GA_MQ_MMA_SYNC
+    if (a.plan->col_tile == kTcColTile && a.kv_dtype == GA_KV_BF16 && a.k_pool != a.v_pool)
+        return launch_mq_tc(a);
+#endif
+    // more than one tile of (query, head) columns per kv head and a plan made
+    // for wider units: column-parallel mma.sync units of 4 x 8 columns
     const bool colpar = a.plan->col_tile > kHeadTile && a.kv_dtype == GA_KV_BF16 &&
                         a.k_pool != a.v_pool;
     if (colpar)

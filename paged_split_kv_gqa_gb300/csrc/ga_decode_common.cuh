@@ -156,4 +156,53 @@ __device__ __forceinline__ bool build_row_prefix(const DecodeParams& p, int32_t*
     return true;
 }
 
+// ---- pieces of the warp-specialised tcgen05 kernels
+
+__device__ __forceinline__ uint32_t bar(uint32_t bars, int i) { return bars + 8u * (uint32_t)i; }
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t b, uint32_t parity,
+                                              volatile int* abort_flag) {
+    if (mbar_try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, parity)) {
+        if (*abort_flag || clock64() - t0 > kWaitBudgetCycles) return false;
+    }
+    return true;
+}
+
+// Walks a CTA's units (blockIdx.x, + gridDim.x, ...) with the next unit's
+// length load in flight while the current one is processed.
+struct UnitCursor {
+    int64_t u, U;
+    UnitLoc nl;
+    int32_t nlen;
+    __device__ __forceinline__ UnitCursor(const DecodeParams& p, const int32_t* pre, int64_t U_)
+        : u(blockIdx.x), U(U_), nl(), nlen(0) {
+        if (u < U) fetch(p, pre);
+    }
+    __device__ __forceinline__ void fetch(const DecodeParams& p, const int32_t* pre) {
+        nl = locate_unit(p, pre, u);
+        nlen = __ldg(p.seq_lens + nl.b);
+    }
+    // The current unit's geometry; starts the next unit's length load.
+    __device__ __forceinline__ UnitInfo take(const DecodeParams& p, const int32_t* pre) {
+        const UnitInfo x = finish_unit(p, pre, nl, nlen);
+        u += gridDim.x;
+        if (u < U) fetch(p, pre);
+        return x;
+    }
+    __device__ __forceinline__ bool more() const { return u < U; }
+};
+
+// Bounded wait of one issuing thread; on a timeout or an abort elsewhere it
+// reports, raises the abort flag and returns false.
+__device__ __forceinline__ bool issuer_wait(const DecodeParams& p, uint32_t b, uint32_t parity,
+                                            volatile int* abort_flag) {
+    if (!*abort_flag && wait_or_abort(b, parity, abort_flag)) return true;
+    report(p.err_word, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+}
+
 }  // namespace ga

@@ -121,19 +121,6 @@ struct Geo {
     static_assert(TM_O + 2 * O_COLS <= TMEM_COLS, "tensor memory");
 };
 
-__device__ __forceinline__ uint32_t bar(uint32_t bars, int i) { return bars + 8u * (uint32_t)i; }
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t b, uint32_t parity,
-                                              volatile int* abort_flag) {
-    if (mbar_try_wait(b, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(b, parity)) {
-        if (*abort_flag || clock64() - t0 > kWaitBudgetCycles) return false;
-    }
-    return true;
-}
-
 // Two values -> two E4M3 codes (hi) and the E4M3 codes of their remainders
 // (lo), low byte first: hi + lo carries ~8 bits of the value.
 __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -142,30 +129,6 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
     const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&h));
     lo = f32x2_to_e4m3x2(a - r.x, b - r.y);
 }
-
-// Walks a CTA's units (blockIdx.x, + gridDim.x, ...) with the next unit's
-// length load in flight while the current one is processed.
-struct UnitCursor {
-    int64_t u, U;
-    UnitLoc nl;
-    int32_t nlen;
-    __device__ __forceinline__ UnitCursor(const DecodeParams& p, const int32_t* pre, int64_t U_)
-        : u(blockIdx.x), U(U_), nl(), nlen(0) {
-        if (u < U) fetch(p, pre);
-    }
-    __device__ __forceinline__ void fetch(const DecodeParams& p, const int32_t* pre) {
-        nl = locate_unit(p, pre, u);
-        nlen = __ldg(p.seq_lens + nl.b);
-    }
-    // The current unit's geometry; starts the next unit's length load.
-    __device__ __forceinline__ UnitInfo take(const DecodeParams& p, const int32_t* pre) {
-        const UnitInfo x = finish_unit(p, pre, nl, nlen);
-        u += gridDim.x;
-        if (u < U) fetch(p, pre);
-        return x;
-    }
-    __device__ __forceinline__ bool more() const { return u < U; }
-};
 
 // ------------------------------------------------------------------ producer
 
@@ -305,16 +268,6 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
 }
 
 // ------------------------------------------------------------------ MMA issuers
-
-// Bounded wait of one issuing thread; on a timeout or an abort elsewhere it
-// reports, raises the abort flag and returns false.
-__device__ __forceinline__ bool issuer_wait(const DecodeParams& p, uint32_t b, uint32_t parity,
-                                            volatile int* abort_flag) {
-    if (!*abort_flag && wait_or_abort(b, parity, abort_flag)) return true;
-    report(p.err_word, kErrTimeout);
-    *abort_flag = 1;
-    return false;
-}
 
 // Warp 4, lane 0: S(m) = K q^T for the CTA's superstages in order, once the
 // stage's K half has landed, the S buffer is free and the unit's q operand

@@ -21,6 +21,12 @@ constexpr int kPageSize = 16;     // keys per page; one page = one 16-key MMA ti
 constexpr int kHeadTile = 8;      // query heads per unit (MMA N)
 constexpr int kMaxBatch = 2048;   // rows per call (decode keeps a row prefix in smem)
 constexpr int kMaxQLen = 64;      // query tokens per row of a multi-query decode
+constexpr int kTcColTile = 64;    // (query, head) columns per unit of the tensor-core
+                                  // multi-query kernel (N of its products)
+#ifndef GA_TC_MIN_COLS
+#define GA_TC_MIN_COLS 16
+#endif
+constexpr int kTcMinCols = GA_TC_MIN_COLS;   // columns per kv head from which plans use it
 
 enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
 

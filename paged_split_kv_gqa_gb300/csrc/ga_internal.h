@@ -48,6 +48,10 @@ int launch_decode(const DecodeArgs& a);
 // pools) on tcgen05 tensor cores.
 int launch_decode_tc(const DecodeArgs& a);
 
+// Multi-query decode over two bf16 pools (64 (query, head) columns per unit)
+// on tcgen05 tensor cores.
+int launch_mq_tc(const DecodeArgs& a);
+
 int launch_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
                    const int32_t* seq_lens, void* out, int32_t* err_word, int64_t pt_stride,
                    cudaStream_t stream);

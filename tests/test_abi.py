@@ -72,11 +72,14 @@ def test_multi_query_plan(ga):
     # 4 queries x group 2 = 8 columns: still one head group per kv head
     assert four.units == one.units
     assert one.col_tile == four.col_tile == 8
-    # 8 queries x group 2 = 16 columns: one column-parallel unit of 4 tiles of 8
+    # 5 queries x group 2 = 10 columns: one column-parallel unit of 4 tiles of 8
+    five = ga.ga_plan_splits_mq([40, 33], q_len=5, **kw)
+    assert five.col_tile == 32 and five.units == one.units
+    # 8 queries x group 2 = 16 columns and more: tensor-core units of 64 columns
     eight = ga.ga_plan_splits_mq([40, 33], q_len=8, **kw)
-    assert eight.col_tile == 32 and eight.units == one.units
-    wide = ga.ga_plan_splits_mq([40, 33], q_len=40, **kw)        # 80 columns: 3 units
-    assert wide.units == 3 * one.units
+    assert eight.col_tile == 64 and eight.units == one.units
+    wide = ga.ga_plan_splits_mq([40, 33], q_len=40, **kw)        # 80 columns: 2 units
+    assert wide.col_tile == 64 and wide.units == 2 * one.units
     # union window, row of length 33, W = 16: one query reads keys 17..32
     # (pages 1..2); four queries (positions 29..32) read keys 14..32 (pages 0..2)
     w1 = ga.ga_plan_splits([33], num_q_heads=2, num_kv_heads=2, head_dim=256, window=16,

@@ -150,8 +150,12 @@ def test_mq_chunk_parity_with_one_query_decodes(ga, err, family):
         one = _decode(ga, fi1, q1, fam, one_plan, err).float().cpu()
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        assert_close(out[:, :, i].numpy(), one.numpy().astype(np.float64),
-                     what=f"{family} query {i} vs one-query decode")
+        # both sides are rounded to bf16 on their own: a value near a rounding
+        # boundary may land one ulp (of the largest |o|) apart
+        ref = one.numpy().astype(np.float64)
+        ulp = 2.0 ** (math.floor(math.log2(max(np.abs(ref).max(), 1e-30))) - 7)
+        assert_close(out[:, :, i].numpy(), ref, what=f"{family} query {i} vs one-query decode",
+                     extra_abs=ulp)
 
 
 @pytest.mark.parametrize("family", ["local", "global"])

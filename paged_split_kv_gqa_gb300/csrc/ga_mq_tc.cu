@@ -18,31 +18,34 @@
 // One unit = (row chunk, kv head, tile of 64 columns).  Per stage of 128 keys
 // (8 pages), N = 64 columns, K = 16 per instruction, fp32 accumulate:
 //   S^T [128 keys x 64]  = K [keys x D] . q^T       A = K (K-major), B = q (K-major)
-//   O^T [128 dims x 64] += V^T [dims x keys] . P^T  A = V^T (MN-major, two 64-dim
-//                                                   swizzle atoms), B = P^T (K-major)
+//   O^T [128 dims x 64] += V^T [dims x keys] . P^T  A = V^T (MN-major), B = P^T (K-major)
+//   l   [128 x 64]      += 1 [128 x keys] . P^T     every row: the column sums of P
 // S^T sits in TMEM lanes = keys, so softmax thread t owns key t of every stage
-// and dim t of every 128-dim block of O^T.  TMEM holds two S buffers (2 x 64
-// columns) and O^T (D / 128 blocks of 64 columns): 384 of 512 columns at
-// hd512.  Columns as M would need O = 128 x 512 fp32, all of TMEM, at hd512.
+// and dim t of every 128-dim block of O^T.  TMEM holds two S buffers, O^T
+// (D / 128 blocks) and the sums, 64 columns each: 448 of 512 at hd512.
+// Columns as M would need O = 128 x 512 fp32, all of TMEM, at hd512.
 //
-// Shared memory: K and V rings of 32 KB slots, each one 128-dim block of a
-// stage as two [128 keys][128 B] regions (one 2 KB bulk tensor copy per page
-// and region, so the stage's 8 pages sit at one uniform row stride); the
-// unit's q rows as [D / 64][64 rows][128 B] (one bulk tensor copy per
-// region; two buffers at hd256); P^T as two [64 columns][128 B] regions.  All
-// operand tiles carry the 128-byte swizzle.
+// Shared memory.  K: a ring of 32 KB slots, each one 128-dim block of a stage
+// as two [128 keys][128 B] regions, filled by one 2 KB bulk tensor copy per
+// page and region (the QK product wants the stage's 128 keys at one row
+// stride).  V: a ring of 32 KB slots of whole page-head blocks
+// ([page][D / 64 regions][16 keys][128 B]), one copy per page: the PV product
+// takes one page per instruction, so a block's layout serves it as it lands.
+// q of the unit as [D / 64][64 rows][128 B] (one copy per region; two
+// buffers at hd256), P^T as two [64 columns][128 B] regions, and a constant
+// all-ones tile for the sums.  Operand tiles carry the 128-byte swizzle.
 //
 // Softmax in base 2 with a lazily raised running max: a column's max moves
-// only when a score exceeds it by more than SLACK (so P <= 2^16), and O^T is
-// then rescaled in TMEM.  P is rounded to bf16 and the row sums add the
-// rounded values, so numerator and denominator see the same weights.
+// only when a score exceeds it by more than SLACK (so P <= 2^16), then O^T and
+// the sums are rescaled in TMEM.  P is rounded to bf16 once and feeds both the
+// output and the sums, so numerator and denominator see the same weights.
 //
 // Roles (256 threads): warps 0-3 softmax and output; warp 4 streams K pages
 // and the unit's q rows, warp 5 streams V pages; warp 6 allocates TMEM and its
 // lane 0 issues QK; warp 7 zeroes V rows that no query attends (below the
 // window, past the row's end, pages with an invalid id: P is 0 there but
-// 0 x NaN is not 0) and its lane 0 issues PV.  Hand-offs are mbarriers; every
-// wait is bounded.
+// 0 x NaN is not 0) and its lane 0 issues PV and the sums.  Hand-offs are
+// mbarriers; every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,56 +57,66 @@ namespace ga {
 
 namespace mq {
 
-constexpr int NC = kTcColTile;                    // columns per unit: N of both products
+constexpr int NC = kTcColTile;                    // columns per unit: N of every product
 constexpr int KEYS = 128;                         // keys per stage: M of the QK product
 constexpr int SPG = KEYS / kPageSize;             // pages per stage
-constexpr int REGION_BYTES = KEYS * 128;          // [128 keys][64 dims] bf16
-constexpr int SLOT_BYTES = 2 * REGION_BYTES;      // one 128-dim block of a stage
+constexpr int REGION_BYTES = KEYS * 128;          // K: [128 keys][64 dims] bf16
+constexpr int SLOT_BYTES = 2 * REGION_BYTES;      // a K or V slot
 constexpr int QREG_BYTES = NC * 128;              // [64 columns][64 dims] bf16
 constexpr int PREG_BYTES = NC * 128;              // [64 columns][64 keys] bf16
 constexpr int P_BYTES = 2 * PREG_BYTES;           // P^T of a stage
+constexpr int ONES_BYTES = 4096;                  // [16 keys][128 rows] bf16 ones
 constexpr int NKS = 2, NVS = 2;                   // K and V slots
 constexpr int NSW = 4;                            // softmax warps
 constexpr int KP_WARP = 4, VP_WARP = 5, QK_WARP = 6, PV_WARP = 7;
 constexpr int NTHREADS = 256;
-constexpr int TM_S = 0, TM_O = 2 * NC;            // two S buffers, then O^T
+constexpr int TM_S = 0, TM_O = 2 * NC;            // two S buffers, then O^T, then the sums
 constexpr float SLACK = 16.0f;
 constexpr uint32_t FULL = 0xffffffffu;
 
 // barriers: k_full / k_empty [NKS], v_full / v_empty [NVS], s_full / s_free
-// [2], p_full, pv_done, o_free, q_full / q_free [2], fin
+// [2], p_full, p_half (the products on keys 0..63 ran), pv_done, o_free,
+// q_full / q_free [2], fin
 constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + NKS, B_VFULL = B_KEMPTY + NKS,
               B_VEMPTY = B_VFULL + NVS, B_SFULL = B_VEMPTY + NVS, B_SFREE = B_SFULL + 2,
-              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 1, B_OFREE = B_PVDONE + 1,
+              B_PFULL = B_SFREE + 2, B_PHALF = B_PFULL + 1, B_PVDONE = B_PHALF + 1,
+              B_OFREE = B_PVDONE + 1,
               B_QFULL = B_OFREE + 1, B_QFREE = B_QFULL + 2, B_FIN = B_QFREE + 2,
               NBARS = B_FIN + 1;
 
 template <int D_>
 struct Geo {
     static constexpr int D = D_;
-    static constexpr int NDC = D / 128;            // 128-dim blocks: slots per stage, O^T blocks
-    static constexpr int NQR = D / 64;             // 64-dim regions of q
+    static constexpr int NDC = D / 128;            // 128-dim blocks: K slots per stage, O^T blocks
+    static constexpr int NR = D / 64;              // 64-dim regions (128 B of bf16)
     static constexpr int NQB = D == 256 ? 2 : 1;   // q buffers
-    static constexpr int Q_BYTES = NQR * QREG_BYTES;
-    static constexpr int TMEM_COLS = TM_O + NDC * NC <= 256 ? 256 : 512;
+    static constexpr int Q_BYTES = NR * QREG_BYTES;
+    static constexpr int BLOCK_BYTES = kPageSize * D * 2;       // one page-head block
+    static constexpr int PPS = SLOT_BYTES / BLOCK_BYTES;        // pages per V slot
+    static constexpr int VSPS = SPG / PPS;                      // V slots per stage
+    static constexpr int TM_L = TM_O + NDC * NC;                // the column sums
+    static constexpr int TMEM_COLS = TM_L + NC <= 256 ? 256 : 512;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NKS * SLOT_BYTES;
     static constexpr int OFF_Q = OFF_V + NVS * SLOT_BYTES;
     static constexpr int OFF_P = OFF_Q + NQB * Q_BYTES;
-    static constexpr int OFF_RED = OFF_P + P_BYTES;              // [NC][NSW] column maxima
-    static constexpr int OFF_REDL = OFF_RED + NC * NSW * 4;      // [NC][NSW] column sums
-    static constexpr int OFF_ALPHA = OFF_REDL + NC * NSW * 4;    // [NC] rescale factors
+    static constexpr int OFF_ONES = OFF_P + P_BYTES;
+    static constexpr int OFF_RED = OFF_ONES + ONES_BYTES;        // [NC][NSW] column maxima
+    static constexpr int OFF_ALPHA = OFF_RED + NC * NSW * 4;     // [NC] rescale factors
     static constexpr int OFF_MAX = OFF_ALPHA + NC * 4;           // [NC] running maxima
-    static constexpr int OFF_COLQ = OFF_MAX + NC * 4;            // [NC] query index of a column
+    static constexpr int OFF_MSAFE = OFF_MAX + NC * 4;           // [NC] max, 0 for -inf
+    static constexpr int OFF_MTH = OFF_MSAFE + NC * 4;           // [NC] max + SLACK
+    static constexpr int OFF_COLQ = OFF_MTH + NC * 4;            // [NC] query index of a column
     static constexpr int OFF_PREFIX = OFF_COLQ + NC * 4;
     static constexpr int OFF_BARS = (OFF_PREFIX + (kMaxBatch + 1) * 4 + 7) / 8 * 8;
     static constexpr int SMEM_USED = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;          // slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 &&
-                      Q_BYTES % 1024 == 0,
+                      OFF_ONES % 1024 == 0 && Q_BYTES % 1024 == 0 && BLOCK_BYTES % 1024 == 0,
                   "swizzle-128B operands need 1024-byte aligned tiles");
-    static_assert(TM_O + NDC * NC <= TMEM_COLS, "tensor memory");
+    static_assert(PPS * BLOCK_BYTES == SLOT_BYTES && VSPS * PPS == SPG, "V slots");
+    static_assert(TM_L + NC <= TMEM_COLS, "tensor memory");
 };
 
 // Page ids of pages 32 j .. 32 j + 31 of a unit (one per lane), -1 past its end.
@@ -114,11 +127,12 @@ __device__ __forceinline__ int32_t page_ids32(const int32_t* tbl, int np, int j,
 
 // ------------------------------------------------------------------ producers
 
-// Warps 4 (K, plus each unit's q rows) and 5 (V).  For each stage of each
-// unit and each 128-dim block: wait until the ring slot is free, arm its
-// "full" barrier with the bytes of the stage's good pages, and let lanes 0..7
-// each copy one page (two 64-dim regions).  Pages with an invalid id are
-// reported by the K warp and copied by neither.
+// Warps 4 (K, plus each unit's q rows) and 5 (V).  Lanes 0..7 hold the pages
+// of a stage.  K: for each 128-dim block of each stage, wait until the ring
+// slot is free, arm its "full" barrier with the bytes of the good pages, and
+// copy each page's two 64-dim regions.  V: for each slot of PPS pages, the
+// same with one copy of each whole page-head block.  Pages with an invalid id
+// are reported by the K warp and copied by neither.
 template <class G, bool IS_K>
 __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const DecodeParams& p,
                          const int32_t* pre, int64_t U, uint32_t base, uint32_t bars,
@@ -130,6 +144,7 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
     constexpr int NS = IS_K ? NKS : NVS;
     constexpr int B_FULLB = IS_K ? B_KFULL : B_VFULL, B_EMPTYB = IS_K ? B_KEMPTY : B_VEMPTY;
     constexpr uint32_t OFF = IS_K ? G::OFF_K : G::OFF_V;
+    constexpr int SLOTS_PER_STAGE = IS_K ? G::NDC : G::VSPS;
     // Pages of K and V are read by every column tile of a kv head: keep them
     // in L2 at normal priority.
     const uint64_t pol = l2_evict_normal_policy();
@@ -164,7 +179,7 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
                 mbar_arrive_expect_tx(qf, (uint32_t)G::Q_BYTES);
                 const int32_t r0 = x.b * p.Hq + x.h0;             // first q row of the unit
 #pragma unroll
-                for (int r = 0; r < G::NQR; ++r)
+                for (int r = 0; r < G::NR; ++r)
                     tma_load_3d(base + G::OFF_Q + qb * G::Q_BYTES + r * QREG_BYTES, tmQ, qf, 0, r0,
                                 r, pol);
             }
@@ -193,7 +208,7 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
                     p.touch_log[x.rc * p.touch_stride + pi] = pid;
             }
 #pragma unroll 1
-            for (int c = 0; c < G::NDC; ++c) {
+            for (int j = 0; j < SLOTS_PER_STAGE; ++j) {
                 const uint32_t slot = seq % NS;
                 bool ok = true;
                 if (lane == 0)
@@ -204,12 +219,24 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
                     break;
                 }
                 const uint32_t fb = bar(bars, B_FULLB + (int)slot);
-                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(gm) * 2u * 2048u);
-                __syncwarp();
-                if (good) {
-                    const uint32_t dst = base + OFF + slot * SLOT_BYTES + (uint32_t)pl * 2048u;
-                    tma_load_3d(dst, tm, fb, 0, y, 2 * c, pol);
-                    tma_load_3d(dst + REGION_BYTES, tm, fb, 0, y, 2 * c + 1, pol);
+                const uint32_t dst0 = base + OFF + slot * SLOT_BYTES;
+                if (IS_K) {
+                    // 128-dim block j of every page: regions 2j, 2j + 1
+                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(gm) * 2u * 2048u);
+                    __syncwarp();
+                    if (good) {
+                        const uint32_t dst = dst0 + (uint32_t)pl * 2048u;
+                        tma_load_3d(dst, tm, fb, 0, y, 2 * j, pol);
+                        tma_load_3d(dst + REGION_BYTES, tm, fb, 0, y, 2 * j + 1, pol);
+                    }
+                } else {
+                    // pages PPS j .. PPS j + PPS - 1, whole page-head blocks
+                    const uint32_t sm = (gm >> (G::PPS * j)) & ((1u << G::PPS) - 1u);
+                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(sm) * G::BLOCK_BYTES);
+                    __syncwarp();
+                    if (good && pl / G::PPS == j)
+                        tma_load_3d(dst0 + (uint32_t)(pl % G::PPS) * G::BLOCK_BYTES, tm, fb, 0, y, 0,
+                                    pol);
                 }
                 ++seq;
             }
@@ -286,15 +313,14 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
     }
 }
 
-// Warp 7: O^T += V^T P^T for the CTA's stages in order, block by block as the
-// V slots land, once the softmax warps have written P(m).  Before a block's
-// products the warp zeroes the slot's V rows that no query of the row
-// attends: keys below the window or past the row's end in a copied page, and
-// every row of a page with an invalid id (never copied).  Lane 0 issues the
-// products (16 keys = one page per instruction, only the stage's pages) and
-// commits; each block's commit frees its V slot, the stage's last one the P
-// buffer.  A unit's first product overwrites O^T (accumulate off) once the
-// previous unit's epilogue has read it.
+// Warp 7: for each stage, once the softmax warps have written P(m), the
+// column sums l += 1 . P^T (one product per page), then for each V slot as it
+// lands: zero the slot's V rows that no query of the row attends (keys below
+// the window or past the row's end in a copied page, every row of a page with
+// an invalid id, never copied), then O^T += V^T P^T, one product per page and
+// 128-dim block.  Lane 0 issues and commits: a slot's commit frees it, the
+// stage's last one the P buffer.  A unit's first products overwrite O^T and
+// the sums (accumulate off) once the previous unit's epilogue has read them.
 template <class G>
 __device__ void pv_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                         uint32_t base, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
@@ -311,6 +337,10 @@ __device__ void pv_warp(const DecodeParams& p, const int32_t* pre, int64_t U, ui
             *abort_flag = 1;
         }
         return ok;
+    };
+    // P^T operand of the product for page kp of a stage (16 keys)
+    auto pdesc = [&](int kp) {
+        return smem_desc_sw128(base + G::OFF_P + (kp >> 2) * PREG_BYTES + 32 * (kp & 3), 16, 1024);
     };
     UnitCursor cur(p, pre, U);
     while (cur.more() && !stop) {
@@ -333,33 +363,29 @@ __device__ void pv_warp(const DecodeParams& p, const int32_t* pre, int64_t U, ui
                     zmask = ((1u << lo_in) - 1u) | (0xFFFFu & ~((1u << hi_in) - 1u));
                 }
             }
-            const bool any_zero = __any_sync(FULL, zmask != 0);
             const int npg = min(SPG, x.np - SPG * s);
-            for (int c = 0; c < G::NDC; ++c, ++vseq) {
+            const bool any_zero = __any_sync(FULL, zmask != 0);
+            if ((s == 0 && k > 0 && !wait1(B_OFREE, (k - 1) & 1)) || !wait1(B_PFULL, m & 1)) {
+                stop = true;
+                break;
+            }
+            for (int j = 0; j < G::VSPS; ++j, ++vseq) {
                 const uint32_t slot = vseq % NVS;
-                if (c == 0) {
-                    if ((s == 0 && k > 0 && !wait1(B_OFREE, (k - 1) & 1)) || !wait1(B_PFULL, m & 1)) {
-                        stop = true;
-                        break;
-                    }
-                }
                 if (!wait1(B_VFULL + (int)slot, (vseq / NVS) & 1)) {
                     stop = true;
                     break;
                 }
-                if (any_zero) {
-                    uint8_t* vs = smem + G::OFF_V + slot * SLOT_BYTES;
-                    for (int i = 0; i < SPG; ++i) {
-                        const uint32_t zm = __shfl_sync(FULL, zmask, i);
-                        if (zm == 0) continue;
-                        // 16 rows x 16 pieces of 16 bytes (two 128-byte regions)
-                        for (int e = lane; e < 256; e += 32) {
-                            const int j = e >> 4, part = e & 15;
-                            if ((zm >> j) & 1u)
-                                *reinterpret_cast<uint4*>(vs + (part >> 3) * REGION_BYTES +
-                                                          (kPageSize * i + j) * 128 + (part & 7) * 16) =
-                                    make_uint4(0u, 0u, 0u, 0u);
-                        }
+                uint8_t* vs = smem + G::OFF_V + slot * SLOT_BYTES;
+                for (int i = 0; any_zero && i < G::PPS; ++i) {
+                    const uint32_t zm = __shfl_sync(FULL, zmask, G::PPS * j + i);
+                    if (zm == 0) continue;
+                    // each zeroed row: 128 bytes in each of the NR regions
+                    for (int e = lane; e < kPageSize * G::NR * 8; e += 32) {
+                        const int row = e / (G::NR * 8), rest = e % (G::NR * 8);
+                        if ((zm >> row) & 1u)
+                            *reinterpret_cast<uint4*>(vs + i * G::BLOCK_BYTES + (rest >> 3) * 2048 +
+                                                      row * 128 + (rest & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_shared();
                 }
@@ -367,18 +393,26 @@ __device__ void pv_warp(const DecodeParams& p, const int32_t* pre, int64_t U, ui
                 if (lane == 0) {
                     tc_fence_after();
                     const uint32_t va = base + G::OFF_V + slot * SLOT_BYTES;
-                    const uint32_t pa = base + G::OFF_P;
-                    for (int ks = 0; ks < npg; ++ks)
-                        tc_mma_bf16(tmem + TM_O + NC * c,
-                                    smem_desc_sw128(va + 2048 * ks, REGION_BYTES, 1024),
-                                    smem_desc_sw128(pa + (ks >> 2) * PREG_BYTES + 32 * (ks & 3), 16, 1024),
-                                    IPV, (s == 0 && ks == 0) ? 0u : 1u);
+                    const uint64_t ones = smem_desc_sw128(base + G::OFF_ONES, 2048, 1024);
+                    for (int i = 0; i < G::PPS; ++i) {
+                        const int kp = G::PPS * j + i;          // page of the stage
+                        if (kp >= npg) break;
+                        const uint32_t acc = (s == 0 && kp == 0) ? 0u : 1u;
+                        tc_mma_bf16(tmem + G::TM_L, ones, pdesc(kp), IPV, acc);
+#pragma unroll
+                        for (int c = 0; c < G::NDC; ++c)
+                            tc_mma_bf16(tmem + TM_O + NC * c,
+                                        smem_desc_sw128(va + i * G::BLOCK_BYTES + 2 * c * 2048, 2048, 1024),
+                                        pdesc(kp), IPV, acc);
+                    }
                     tc_commit(bar(bars, B_VEMPTY + (int)slot));   // the V slot may be refilled
+                    // P^T keys 0..63 (region 0) are read by the products so far
+                    if (j == G::VSPS / 2 - 1) tc_commit(bar(bars, B_PHALF));
                 }
                 __syncwarp();
             }
             if (stop) break;
-            if (lane == 0) tc_commit(bar(bars, B_PVDONE));        // P buffer free, O^T current
+            if (lane == 0) tc_commit(bar(bars, B_PVDONE));        // P buffer free, O^T and l current
         }
         ++k;
     }
@@ -386,13 +420,37 @@ __device__ void pv_warp(const DecodeParams& p, const int32_t* pre, int64_t U, ui
 
 // ------------------------------------------------------------------ softmax warps
 
+// Column maxima of v[64] over the warp's 32 lanes by recursive halving: after
+// five exchange steps (62 shuffles) lane l holds the maxima of columns 2l and
+// 2l + 1 in t[0], t[1].
+__device__ __forceinline__ void warp_colmax64(const float (&v)[NC], int lane, float (&t)[32]) {
+    const bool b4 = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float keep = b4 ? v[i + 32] : v[i], send = b4 ? v[i] : v[i + 32];
+        t[i] = fmaxf(keep, __shfl_xor_sync(FULL, send, 16));
+    }
+    // n values left: pairs (i, i + n / 2) across lanes l, l ^ (n / 4)
+#pragma unroll
+    for (int n = 32; n >= 4; n >>= 1) {
+        const bool b = lane & (n / 4);
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = b ? t[i + n / 2] : t[i], send = b ? t[i] : t[i + n / 2];
+            t[i] = fmaxf(keep, __shfl_xor_sync(FULL, send, n / 4));
+        }
+    }
+}
+
 // Warps 0-3.  Thread t owns key t of every stage (TMEM lane t of S^T) and dim
 // t of each 128-dim block of O^T.  Per stage: read the 64 scores, mask each
 // column (query i = column % S sits at position L - S + i and attends keys j
-// with 0 <= (L - S + i) - j < window), raise a column's max only past SLACK
-// (then O^T is rescaled once the previous stage's PV has run), write P^T in
-// bf16 for the PV product.  At the end of a unit: the column sums, then O^T
-// from TMEM to the output (or a split partial and its LSE).
+// with 0 <= (L - S + i) - j < window; keys inside every column's range skip
+// the per-column test), raise a column's max only past SLACK (then O^T and the
+// sums are rescaled once the previous stage's products have run), write P^T
+// in bf16.  At the end of a unit: O^T scaled by 1 / l to the output (or a
+// split partial and its LSE).  The running maxima live in shared memory, one
+// writer per column between barriers.
 template <class G>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
@@ -401,17 +459,19 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
     const int w = tid >> 5, lane = tid & 31;
     const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);     // this warp's TMEM lanes
     float* red = reinterpret_cast<float*>(smem + G::OFF_RED);  // [NC][NSW] maxima
-    float* redl = reinterpret_cast<float*>(smem + G::OFF_REDL);
     float* alpha_sm = reinterpret_cast<float*>(smem + G::OFF_ALPHA);
-    // a column's running max is the same for every thread: one copy in shared
-    // memory, written by thread f only (column f), between barriers
     float* m_sm = reinterpret_cast<float*>(smem + G::OFF_MAX);
-    const float4* m4 = reinterpret_cast<const float4*>(m_sm);
+    float* msafe_sm = reinterpret_cast<float*>(smem + G::OFF_MSAFE);
+    float* mth_sm = reinterpret_cast<float*>(smem + G::OFF_MTH);
     int32_t* colq = reinterpret_cast<int32_t*>(smem + G::OFF_COLQ);
+    const float4* msafe4 = reinterpret_cast<const float4*>(msafe_sm);
+    const float4* mth4 = reinterpret_cast<const float4*>(mth_sm);
     const int4* colq4 = reinterpret_cast<const int4*>(colq);
-    uint8_t* pbuf = smem + G::OFF_P;
     const uint32_t wmask = p.mask_window > 0 ? (uint32_t)p.mask_window : 0x7fffffffu;
     bool stop = false;
+    // a wait of one warp that failed, reported at the next 128-thread barrier
+    // (every warp keeps the same sequence of named barriers)
+    bool late_fail = false;
 
     auto poll = [&](int b, uint32_t parity) -> bool {
         bool ok = true;
@@ -419,7 +479,9 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         return __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
     };
     auto settle = [&](bool ok) -> bool {
-        if (named_barrier_or(1, 128, !ok)) {
+        const bool bad = !ok || late_fail;
+        late_fail = false;
+        if (named_barrier_or(1, 128, bad)) {
             if (tid == 0) {
                 report(p.err_word, kErrTimeout);
                 *abort_flag = 1;
@@ -452,9 +514,13 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] = -CUDART_INF_F;
     };
 
-    // this thread's byte in a 128-byte P^T row: key tid, region tid / 64
-    uint8_t* prow = pbuf + (tid >> 6) * PREG_BYTES;
-    const int pkb = (tid & 63) * 2, pch = pkb >> 4, pin = pkb & 15;
+    // This thread's P^T bytes: key tid is byte 2 (tid % 64) of the 128-byte
+    // rows of region tid / 64; row f's 16-byte chunk is swizzled by f % 8.
+    uint16_t* prow = reinterpret_cast<uint16_t*>(smem + G::OFF_P + (tid >> 6) * PREG_BYTES);
+    const int pch = (tid & 63) >> 3, pin = tid & 7;
+    int poff[8];                                // element offset of row f (f % 8 = i) in row 0
+#pragma unroll
+    for (int i = 0; i < 8; ++i) poff[i] = ((pch ^ i) << 3) | pin;
 
     uint32_t n = 0;                             // stages so far
     UnitCursor cur(p, pre, U);
@@ -466,11 +532,10 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             write_empty(x, single);
             continue;
         }
-        float l[NC];
-#pragma unroll
-        for (int f = 0; f < NC; ++f) l[f] = 0.f;
         if (tid < NC) {
             m_sm[tid] = -CUDART_INF_F;
+            msafe_sm[tid] = 0.f;
+            mth_sm[tid] = -CUDART_INF_F;
             colq[tid] = (x.hg * NC + tid) % p.S;   // column tid is query i of its head
         }
         named_barrier(1, 128);                  // before anyone reads them
@@ -498,31 +563,41 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             const bool present = (tid >> 4) < npg && page_ok(pid, p.num_pages);
             const int32_t kj = (x.p0 + SPG * s) * kPageSize + tid;
             const int32_t dbase = x.g.len - p.S - kj;  // (position of query i) - kj = dbase + i
+            // key inside every column's window: no per-column test
+            const bool inside = present && x.nvalid == NC && dbase >= 0 &&
+                                (uint32_t)(dbase + p.S - 1) < wmask;
             float sc[NC];
+            if (inside) {
+#pragma unroll
+                for (int f = 0; f < NC; ++f) sc[f] = __uint_as_float(sr[f]) * p.scale_log2;
+            } else {
+#pragma unroll
+                for (int f4 = 0; f4 < NC / 4; ++f4) {
+                    const int4 qv = colq4[f4];
+                    const int qf[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int f = 4 * f4 + e;
+                        const bool valid = present && f < x.nvalid && (uint32_t)(dbase + qf[e]) < wmask;
+                        sc[f] = valid ? __uint_as_float(sr[f]) * p.scale_log2 : -CUDART_INF_F;
+                    }
+                }
+            }
             bool grow = false;
 #pragma unroll
             for (int f4 = 0; f4 < NC / 4; ++f4) {
-                const float4 mv = m4[f4];
-                const int4 qv = colq4[f4];
-                const float mf[4] = {mv.x, mv.y, mv.z, mv.w};
-                const int qf[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int f = 4 * f4 + e;
-                    const bool valid = present && f < x.nvalid && (uint32_t)(dbase + qf[e]) < wmask;
-                    sc[f] = valid ? __uint_as_float(sr[f]) * p.scale_log2 : -CUDART_INF_F;
-                    grow |= sc[f] > mf[e] + SLACK;
-                }
+                const float4 t4 = mth4[f4];
+                grow |= (sc[4 * f4] > t4.x) | (sc[4 * f4 + 1] > t4.y) | (sc[4 * f4 + 2] > t4.z) |
+                        (sc[4 * f4 + 3] > t4.w);
             }
             bool rescale = false;
             if (named_barrier_or(1, 128, grow)) {
                 // this stage's column maxima over the 128 keys
-#pragma unroll
-                for (int f = 0; f < NC; ++f) {
-                    float v = sc[f];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, off));
-                    if (lane == 0) red[f * NSW + w] = v;
+                {
+                    float t[32];
+                    warp_colmax64(sc, lane, t);
+                    red[(2 * lane) * NSW + w] = t[0];
+                    red[(2 * lane + 1) * NSW + w] = t[1];
                 }
                 named_barrier(1, 128);
                 float a = 1.f;
@@ -531,37 +606,40 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                     const float4 r4 = *reinterpret_cast<const float4*>(red + tid * NSW);
                     const float M = fmaxf(mo, fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w)));
                     // O^T and l hold this column's weights at the old max: scale them
-                    a = (mo == -CUDART_INF_F || M == mo) ? 1.f : exp2f(mo - M);
+                    a = (mo == -CUDART_INF_F || M == mo) ? 1.f : ex2_approx(mo - M);
                     alpha_sm[tid] = a;
                     m_sm[tid] = M;
+                    msafe_sm[tid] = (M == -CUDART_INF_F) ? 0.f : M;
+                    mth_sm[tid] = M + SLACK;
                 }
-                rescale = named_barrier_or(1, 128, a != 1.f);   // also publishes maxima, factors
-#pragma unroll
-                for (int f = 0; f < NC; ++f) l[f] *= alpha_sm[f];
+                rescale = named_barrier_or(1, 128, a != 1.f);   // also publishes the maxima
             }
-            // the P buffer is free once the previous stage's PV has run
-            if (ms > 0 && !wait_all(B_PVDONE, (ms - 1) & 1)) break;
-            // P^T row f, key tid: 2^(s - m) in bf16
+            // P^T row f, key tid: 2^(s - m) in bf16, two columns per conversion,
+            // computed before the wait for the P buffer
+            uint32_t pk[NC / 2];
 #pragma unroll
             for (int f4 = 0; f4 < NC / 4; ++f4) {
-                const float4 mv = m4[f4];
-                const float mq[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int f = 4 * f4 + e;
-                    const float mf = (mq[e] == -CUDART_INF_F) ? 0.f : mq[e];
-                    const __nv_bfloat16 pb = __float2bfloat16_rn(exp2f(sc[f] - mf));
-                    l[f] += __bfloat162float(pb);
-                    *reinterpret_cast<__nv_bfloat16*>(prow + f * 128 + (((pch ^ (f & 7)) << 4) | pin)) =
-                        pb;
-                }
+                const float4 mv = msafe4[f4];
+                pk[2 * f4] = pack_bf16x2(ex2_approx(sc[4 * f4] - mv.x), ex2_approx(sc[4 * f4 + 1] - mv.y));
+                pk[2 * f4 + 1] =
+                    pack_bf16x2(ex2_approx(sc[4 * f4 + 2] - mv.z), ex2_approx(sc[4 * f4 + 3] - mv.w));
             }
-            // O^T holds the earlier stages at the old maxima (the PV of stage
-            // ms - 1 has run, the one of stage ms waits for P): rescale it
+            // this warp's half of the P buffer (keys 0..63: warps 0-1, region 0)
+            // is free once the previous stage's products on it have run
+            if (ms > 0 && !poll(w < 2 ? B_PHALF : B_PVDONE, (ms - 1) & 1)) late_fail = true;
+#pragma unroll
+            for (int f = 0; f < NC; f += 2) {
+                prow[f * 64 + poff[f & 7]] = (uint16_t)pk[f / 2];
+                prow[(f + 1) * 64 + poff[(f + 1) & 7]] = (uint16_t)(pk[f / 2] >> 16);
+            }
+            // O^T and the sums hold the earlier stages at the old maxima (the
+            // products of stage ms - 1 have run, those of stage ms wait for P)
             if (rescale && s > 0) {
+                // every product of the previous stage (warps 0-1 waited for half)
+                if (!poll(B_PVDONE, (ms - 1) & 1)) late_fail = true;
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < G::NDC; ++c) {
+                for (int c = 0; c <= G::NDC; ++c) {     // O^T blocks, then the sums
 #pragma unroll
                     for (int q4 = 0; q4 < NC / 16; ++q4) {
                         uint32_t o[16];
@@ -583,19 +661,27 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         }
         if (stop) break;
 
-        // ---- epilogue: column sums, then O^T from TMEM
+        // ---- epilogue: 1 / l per column, then O^T from TMEM
+        const uint32_t ml = n + (uint32_t)nst - 1;
+        if (!wait_all(B_PVDONE, ml & 1)) break;
+        tc_fence_after();
+        uint32_t lr[NC];
+#pragma unroll
+        for (int q4 = 0; q4 < NC / 16; ++q4)
+            tmem_ld16(tl + G::TM_L + 16 * q4, *reinterpret_cast<uint32_t(*)[16]>(&lr[16 * q4]));
+        tmem_ld_wait();
+        float inv[NC];
+        float Lt = 0.f;                             // column tid's sum, for the LSE
 #pragma unroll
         for (int f = 0; f < NC; ++f) {
-            float v = l[f];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(FULL, v, off);
-            if (lane == 0) redl[f * NSW + w] = v;
+            const float L = __uint_as_float(lr[f]);
+            if (f == tid) Lt = L;
+            // only an exactly empty sum means "no keys"; NaN in attended K / V
+            // reaches the output as in the definition
+            inv[f] = (L == 0.f) ? 0.f : __frcp_rn(L);
         }
-        const uint32_t ml = n + (uint32_t)nst - 1;
-        if (!wait_all(B_PVDONE, ml & 1)) break;      // also publishes redl
         const int64_t r0 = (int64_t)x.b * p.Hq + x.h0;          // output row of column 0
         bool bad_store = false;
-        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < G::NDC; ++c) {
 #pragma unroll
@@ -607,11 +693,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 for (int j = 0; j < 16; ++j) {
                     const int f = 16 * q4 + j;
                     if (f >= x.nvalid) continue;
-                    const float4 L4 = *reinterpret_cast<const float4*>(redl + f * NSW);
-                    const float L = (L4.x + L4.y) + (L4.z + L4.w);
-                    // only an exactly empty sum means "no keys"; NaN in
-                    // attended K / V reaches the output as in the definition
-                    const float v = (L == 0.f) ? 0.f : __uint_as_float(o[j]) / L;
+                    const float v = __uint_as_float(o[j]) * inv[f];
                     if (single) {
                         if (GA_CHK((r0 + f + 1) * D <= p.out_elems))
                             p.out[(r0 + f) * D + 128 * c + tid] = __float2bfloat16_rn(v);
@@ -629,10 +711,8 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         if (bad_store) report(p.err_word, kErrSelfCheck);
         if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity)) {
             const float mm = m_sm[tid];            // natural-log LSE of column tid
-            const float4 L4 = *reinterpret_cast<const float4*>(redl + tid * NSW);
-            const float LL = (L4.x + L4.y) + (L4.z + L4.w);
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
-                (LL == 0.f) ? -CUDART_INF_F : (mm + log2f(LL)) * CUDART_LN2_F;
+                (Lt == 0.f) ? -CUDART_INF_F : (mm + log2f(Lt)) * CUDART_LN2_F;
         }
         n += (uint32_t)nst;
     }
@@ -671,12 +751,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar(bars, B_QFREE + i), 1);      // QK commit
         }
         mbar_init(bar(bars, B_PFULL), NSW);            // each softmax warp wrote P
+        mbar_init(bar(bars, B_PHALF), 1);              // PV commit after pages 0..3
         mbar_init(bar(bars, B_PVDONE), 1);             // PV commit
         mbar_init(bar(bars, B_OFREE), NSW);            // each softmax warp read O^T
         mbar_init(bar(bars, B_FIN), 2);                // both issuers' last commits
         mbar_init_fence();
         abort_flag = 0;
     }
+    // the all-ones operand of the sums (bf16 1.0 = 0x3F80)
+    for (int i = threadIdx.x; i < ONES_BYTES / 16; i += NTHREADS)
+        reinterpret_cast<uint4*>(smem + G::OFF_ONES)[i] =
+            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_shared();
     if (warp == KP_WARP && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmQ);
@@ -731,12 +817,13 @@ static int run_mq(const DecodeArgs& a) {
     int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmem, D == 256 ? 20 : 21);
     if (rc != GA_OK) return rc;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
-    // one box = one 64-dim region of a page-head block ([16 keys][128 B]) or
-    // of a unit's 64 q rows ([64 rows][128 B])
+    // K: one box = one 64-dim region of a page-head block ([16 keys][128 B]);
+    // V: one box = a whole page-head block; q: one 64-dim region of a unit's
+    // 64 rows
     CUtensorMap tmK, tmV, tmQ;
     rc = encode_rows_map(&tmK, a.k_pool, GA_KV_BF16, rows, D, kPageSize, 1);
     if (rc != GA_OK) return rc;
-    rc = encode_rows_map(&tmV, a.v_pool, GA_KV_BF16, rows, D, kPageSize, 1);
+    rc = encode_rows_map(&tmV, a.v_pool, GA_KV_BF16, rows, D, kPageSize, 0);
     if (rc != GA_OK) return rc;
     const int64_t qrows = (int64_t)a.batch * a.num_q_heads * S;
     rc = encode_rows_map(&tmQ, a.q, GA_KV_BF16, qrows, D, mq::NC, 1);

@@ -96,10 +96,16 @@ enum {
     GA_PLAN_TOUCH_LOG = 1,        /* decode records every physical page it reads (tests) */
     GA_PLAN_EXTERNAL_COMBINE = 2, /* a split decode call leaves the partials in the
                                      workspace; the caller runs ga_splitkv_combine */
-    GA_PLAN_TEST_WAIT_TIMEOUT = 4 /* test hook: CTA 0 of the decode launch issues no page, so
-                                     its consumers' bounded waits run out (~2 s) and the
+    GA_PLAN_TEST_WAIT_TIMEOUT = 4, /* test hook: CTA 0 of the decode launch issues no page,
+                                     so its consumers' bounded waits run out (~2 s) and the
                                      call reports GA_DEVERR_TIMEOUT; CTA 0's rows are then
                                      undefined.  Never set outside tests. */
+    GA_PLAN_TENSOR_CORE_UNITS = 8, /* more than 8 (query, head) columns per kv head: always
+                                      units of 64 columns (tensor-core kernel on bf16 pools) */
+    GA_PLAN_COLUMN_PARALLEL_UNITS = 16 /* ... always column-parallel units of 32 columns.
+                                      Neither flag: 64-column units from 32 columns per kv
+                                      head at head_dim 512 and from 64 at head_dim 256
+                                      (where each is the faster on GB300), else 32. */
 };
 
 /*
@@ -120,8 +126,10 @@ typedef struct ga_plan {
     int32_t flags;           /* GA_PLAN_* */
     int32_t touch_stride;    /* touch-log entries per row-chunk (flag set) */
     int32_t q_len;           /* query tokens per row S (1 = one-query decode) */
-    int32_t col_tile;        /* (query, head) columns per work unit: 8, or 32 when a kv
-                                head has more than 8 (column-parallel units) */
+    int32_t col_tile;        /* (query, head) columns per work unit: 8; when a kv head has
+                                more than 8, 32 (column-parallel mma.sync units) or 64
+                                (tcgen05 units; bf16 pools with K and V apart, other
+                                pools run 8-column units) */
     int64_t row_chunks;      /* (row, chunk) pairs the workspace holds */
     int64_t units;           /* work units (row-chunk x kv head x head group) planned */
     int64_t workspace_bytes; /* device workspace the decode call needs (0 if none) */

@@ -183,9 +183,13 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
         return GA_ERR_INVALID_ARG;
     if (q_len < 1) return GA_ERR_INVALID_ARG;
     if (q_len > kMaxQLen) return GA_ERR_UNSUPPORTED;
+    const int32_t known_flags = GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE |
+                                GA_PLAN_TEST_WAIT_TIMEOUT | GA_PLAN_TENSOR_CORE_UNITS |
+                                GA_PLAN_COLUMN_PARALLEL_UNITS;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || window < 0 ||
         num_sms < 1 || requested_splits < 0 || fixed_chunk_tokens < 0 ||
-        (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~(GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE | GA_PLAN_TEST_WAIT_TIMEOUT)))
+        (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~known_flags) ||
+        ((flags & GA_PLAN_TENSOR_CORE_UNITS) && (flags & GA_PLAN_COLUMN_PARALLEL_UNITS)))
         return GA_ERR_INVALID_ARG;
     if (batch > kMaxBatch) return GA_ERR_UNSUPPORTED;
     if (head_dim != 256 && head_dim != 512) return GA_ERR_UNSUPPORTED;
@@ -196,11 +200,12 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
 
     const int32_t weff = effective_window(window, q_len);
     // more than 8 (query, head) columns per kv head: units of 64 columns for
-    // the tensor-core kernel from kTcMinCols on, else column-parallel units of
-    // 4 tiles of 8 (every page read once for all of them)
+    // the tensor-core kernel, or column-parallel units of 4 tiles of 8 (every
+    // page read once for all of them)
     const int32_t cols = num_q_heads / num_kv_heads * q_len;
-    const int32_t tw = cols <= kHeadTile ? kHeadTile
-                       : cols >= kTcMinCols ? kTcColTile : 4 * kHeadTile;
+    const bool tc = (flags & GA_PLAN_TENSOR_CORE_UNITS) ||
+                    (!(flags & GA_PLAN_COLUMN_PARALLEL_UNITS) && cols >= tc_min_cols(head_dim));
+    const int32_t tw = cols <= kHeadTile ? kHeadTile : tc ? kTcColTile : 4 * kHeadTile;
     PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len,
                  tw};
     Candidate best;

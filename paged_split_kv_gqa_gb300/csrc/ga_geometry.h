@@ -23,10 +23,11 @@ constexpr int kMaxBatch = 2048;   // rows per call (decode keeps a row prefix in
 constexpr int kMaxQLen = 64;      // query tokens per row of a multi-query decode
 constexpr int kTcColTile = 64;    // (query, head) columns per unit of the tensor-core
                                   // multi-query kernel (N of its products)
-#ifndef GA_TC_MIN_COLS
-#define GA_TC_MIN_COLS 16
-#endif
-constexpr int kTcMinCols = GA_TC_MIN_COLS;   // columns per kv head from which plans use it
+
+// Columns per kv head from which a plan uses tensor-core units by default
+// (measured on the 31B-shaped batch: at hd512 32 columns already run faster
+// on tcgen05, at hd256 the column-parallel kernel stays ahead up to 32).
+GA_HD int32_t tc_min_cols(int32_t head_dim) { return head_dim == 512 ? 32 : 64; }
 
 enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
 

@@ -41,6 +41,8 @@ GA_SPLIT_CHUNK = 2
 GA_PLAN_TOUCH_LOG = 1
 GA_PLAN_EXTERNAL_COMBINE = 2
 GA_PLAN_TEST_WAIT_TIMEOUT = 4
+GA_PLAN_TENSOR_CORE_UNITS = 8
+GA_PLAN_COLUMN_PARALLEL_UNITS = 16
 PAGE_SIZE = 16
 MAX_Q_LEN = 64
 

@@ -75,11 +75,24 @@ def test_multi_query_plan(ga):
     # 5 queries x group 2 = 10 columns: one column-parallel unit of 4 tiles of 8
     five = ga.ga_plan_splits_mq([40, 33], q_len=5, **kw)
     assert five.col_tile == 32 and five.units == one.units
-    # 8 queries x group 2 = 16 columns and more: tensor-core units of 64 columns
-    eight = ga.ga_plan_splits_mq([40, 33], q_len=8, **kw)
-    assert eight.col_tile == 64 and eight.units == one.units
-    wide = ga.ga_plan_splits_mq([40, 33], q_len=40, **kw)        # 80 columns: 2 units
+    # hd256 below 64 columns: column-parallel units unless tensor-core units
+    # are asked for
+    eight = ga.ga_plan_splits_mq([40, 33], q_len=8, **kw)           # 16 columns
+    assert eight.col_tile == 32 and eight.units == one.units
+    eight_tc = ga.ga_plan_splits_mq([40, 33], q_len=8, flags=ga.GA_PLAN_TENSOR_CORE_UNITS, **kw)
+    assert eight_tc.col_tile == 64 and eight_tc.units == one.units
+    wide = ga.ga_plan_splits_mq([40, 33], q_len=40, **kw)        # 80 columns: 2 units of 64
     assert wide.col_tile == 64 and wide.units == 2 * one.units
+    wide_cp = ga.ga_plan_splits_mq([40, 33], q_len=40, flags=ga.GA_PLAN_COLUMN_PARALLEL_UNITS,
+                                   **kw)
+    assert wide_cp.col_tile == 32 and wide_cp.units == 3 * one.units
+    # hd512: tensor-core units from 32 columns (4 queries x group 8)
+    g8 = dict(num_q_heads=16, num_kv_heads=2, head_dim=512, window=0, num_sms=8)
+    assert ga.ga_plan_splits_mq([40, 33], q_len=2, **g8).col_tile == 32
+    assert ga.ga_plan_splits_mq([40, 33], q_len=4, **g8).col_tile == 64
+    with pytest.raises(ga.GAError):
+        ga.ga_plan_splits_mq([40, 33], q_len=4, flags=ga.GA_PLAN_TENSOR_CORE_UNITS |
+                             ga.GA_PLAN_COLUMN_PARALLEL_UNITS, **g8)
     # union window, row of length 33, W = 16: one query reads keys 17..32
     # (pages 1..2); four queries (positions 29..32) read keys 14..32 (pages 0..2)
     w1 = ga.ga_plan_splits([33], num_q_heads=2, num_kv_heads=2, head_dim=256, window=16,

@@ -24,7 +24,7 @@ CASES = {
     "global_e4m3": (W.Family("global", 16, 2, 512, 0, 1), 1),      # tensor-core kernel, hd512
     "local_bf16_5_queries": (W.Family("local", 4, 2, 256, 32), 5),     # column-parallel units
     "global_bf16_4_queries": (W.Family("global", 16, 2, 512, 0), 4),   # tensor-core mq, hd512
-    "local_bf16_16_queries": (W.Family("local", 4, 2, 256, 32), 16),   # tensor-core mq, hd256
+    "local_bf16_32_queries": (W.Family("local", 4, 2, 256, 32), 32),   # tensor-core mq, hd256
 }
 
 

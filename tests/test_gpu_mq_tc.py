@@ -1,8 +1,9 @@
 """GPU parity of the tensor-core multi-query decode against the fp64 oracle.
 
-Plans for 16 and more (query, head) columns per kv head run on bf16 pools in
-units of 64 columns whose products run on tcgen05, 128 keys (8 pages) per
-stage.  That kernel's own edge cases are:
+Plans with units of 64 (query, head) columns (the default from 32 columns
+per kv head at hd512 and 64 at hd256, or any count above 8 with
+GA_PLAN_TENSOR_CORE_UNITS) run on bf16 pools in a kernel whose products run
+on tcgen05, 128 keys (8 pages) per stage.  That kernel's own edge cases are:
 - lengths around 128-key stages and 16-key pages;
 - rows shorter than S (queries at negative positions);
 - column tiles that are partly empty (g * S not a multiple of 64);
@@ -57,6 +58,11 @@ def err():
     return torch.zeros(1, dtype=torch.int32, device=DEV)
 
 
+def _tc_plan(ga, lens, fam, S, **kw):
+    """A plan with 64-column tensor-core units whatever the column count."""
+    return _plan(ga, lens, fam, S, flags=ga.GA_PLAN_TENSOR_CORE_UNITS, **kw)
+
+
 def _check(ga, err, fi, q, fam, plan, ref, what, scale=None, extra_abs=None):
     assert plan.col_tile == 64, "plan does not use the tensor-core units"
     out = _decode(ga, fi, q, fam, plan, err, scale=scale)
@@ -76,7 +82,7 @@ def test_tc_edge_lengths_every_split(ga, err, S, family):
     fi, q = _inputs(EDGE_TC, fam, S, seed=400 + S)
     ref = _oracle(fi, q, fam)
     for name, split in SPLITS.items():
-        got = _check(ga, err, fi, q, fam, _plan(ga, EDGE_TC, fam, S, **split), ref,
+        got = _check(ga, err, fi, q, fam, _tc_plan(ga, EDGE_TC, fam, S, **split), ref,
                      f"S={S} {family} {name}")
         for b, L in enumerate(EDGE_TC):
             for i in range(S):
@@ -97,7 +103,7 @@ def test_tc_partial_and_multiple_tiles(ga, err, Hq, Hkv, D, window, S):
     fi, q = _inputs(lens, fam, S, seed=11 + S)
     ref = _oracle(fi, q, fam)
     for split in (dict(requested_splits=1), dict(requested_splits=2)):
-        _check(ga, err, fi, q, fam, _plan(ga, lens, fam, S, **split), ref,
+        _check(ga, err, fi, q, fam, _tc_plan(ga, lens, fam, S, **split), ref,
                f"Hq={Hq} Hkv={Hkv} D={D} W={window} S={S} {split}")
 
 
@@ -113,7 +119,7 @@ def test_tc_flagged_page_mid_stage(ga, err, family):
     first = int(fi.seq_lens[0].item() - 1) // P
     bad = first - 4
     fi.page_table[0, bad] = 1 << 30
-    out = _decode(ga, fi, q, fam, _plan(ga, lens, fam, S, requested_splits=1), err)
+    out = _decode(ga, fi, q, fam, _tc_plan(ga, lens, fam, S, requested_splits=1), err)
     torch.cuda.synchronize()
     assert int(err.item()) & ga.GA_DEVERR_PAGE_ID
     got = out.float().cpu().numpy()
@@ -132,7 +138,7 @@ def test_tc_scale_one_peaked_softmax(ga, err, family):
     ref = _oracle(fi, q, fam, scale=1.0)
     # bf16 output: half an ulp of the largest |o| on top of the bf16 bound
     extra = 0.5 * 2.0 ** (math.floor(math.log2(max(np.abs(ref).max(), 1e-30))) - 7)
-    _check(ga, err, fi, q, fam, _plan(ga, EDGE_TC, fam, S), ref, f"{family} scale 1.0",
+    _check(ga, err, fi, q, fam, _tc_plan(ga, EDGE_TC, fam, S), ref, f"{family} scale 1.0",
            scale=1.0, extra_abs=extra)
 
 

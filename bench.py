@@ -130,7 +130,10 @@ class ClockSampler:
 WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 
 
-def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1):
+MQ_UNIT_FLAGS = {"auto": 0, "tc": "GA_PLAN_TENSOR_CORE_UNITS", "cp": "GA_PLAN_COLUMN_PARALLEL_UNITS"}
+
+
+def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto"):
     """One layer's inputs.  q_len > 1: a multi-query step (q_len new tokens
     per row at its last positions, e.g. a speculative-decoding verify): the
     pools keep the union of the queries' windows, q / out are
@@ -159,10 +162,12 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1):
     if alias:                      # K == V: one pool serves both (global family)
         fi.v_pool = fi.k_pool
         fi.v_scale = fi.k_scale
+    unit_flag = MQ_UNIT_FLAGS[mq_units]
     plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                              window=fam.window, requested_splits=splits,
-                             flags=ga.GA_PLAN_EXTERNAL_COMBINE, q_len=S)
+                             flags=ga.GA_PLAN_EXTERNAL_COMBINE |
+                             (getattr(ga, unit_flag) if unit_flag else 0), q_len=S)
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
     esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
@@ -197,7 +202,7 @@ def workload_config(workload, seed, fp8="none"):
 
 
 def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
-               q_len=1, fp8="none"):
+               q_len=1, fp8="none", mq_units="auto"):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -210,7 +215,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
-    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len)
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units)
                        for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
@@ -397,7 +402,7 @@ def run_ga(args):
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
                                          args.pools, args.kv_alias, args.splits, args.q_len,
-                                         args.fp8)
+                                         args.fp8, args.mq_units)
 
     def step(evs=None):
         n = 0
@@ -629,7 +634,7 @@ def run_ga(args):
     if rank == 0:
         def plan_desc(p):
             return {"mode": ["none", "count", "chunk"][p.mode], "splits": p.splits,
-                    "chunk_pages": p.chunk_pages,
+                    "chunk_pages": p.chunk_pages, "col_tile": p.col_tile,
                     "units": p.units, "grid": p.grid}
 
         text = WORKLOAD_TEXT[args.workload]
@@ -646,6 +651,9 @@ def run_ga(args):
         if args.q_len > 1:
             text += (f"; {args.q_len} query tokens per row at its last positions (causal "
                      f"within the chunk), {args.q_len} appends per row and layer")
+        if args.mq_units != "auto":
+            text += {"tc": "; tcgen05 units of 64 columns forced",
+                     "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
@@ -701,6 +709,10 @@ def main():
                     help="query tokens per row (> 1: a multi-query / speculative-verify step)")
     ap.add_argument("--fp8", default="none", choices=["none", "local", "global", "both"],
                     help="store these families' KV pools as fp8-e4m3 with per-head scales")
+    ap.add_argument("--mq-units", default="auto", choices=sorted(MQ_UNIT_FLAGS),
+                    help="multi-query units for more than 8 (query, head) columns per kv head: "
+                         "the planner's choice, tcgen05 units of 64 columns, or column-parallel "
+                         "mma.sync units of 32")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

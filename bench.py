@@ -261,8 +261,9 @@ def launch_layer(ga, f, err, events=None):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(fams_cpu):
-    """Run the oracle on every row of the sampled inputs; returns seconds."""
+def oracle_sample(fams_cpu, nthreads=0):
+    """Run the oracle on every row of the sampled inputs (nthreads 0: all
+    host cores); returns seconds."""
     from oracle import oracle as O
     t0 = time.perf_counter()
     for f in fams_cpu:
@@ -270,7 +271,7 @@ def oracle_sample(fams_cpu):
         fn(f.q, f.k_pool, f.v_pool, f.page_table, f.seq_lens,
            num_kv_heads=f.family.num_kv_heads, window=f.family.window,
            scale=1.0 / math.sqrt(f.family.head_dim), kv_dtype=f.family.kv_dtype,
-           k_scale=f.k_scale, v_scale=f.v_scale)
+           k_scale=f.k_scale, v_scale=f.v_scale, nthreads=nthreads)
     return time.perf_counter() - t0
 
 
@@ -329,16 +330,23 @@ def run_cpu_baseline(sets, batch, target_s=10.0):
         if t >= target_s / 2 or nrows >= batch:
             break
         nrows = min(batch, max(nrows + 1, int(nrows * min(8.0, 0.75 * target_s / max(t, 1e-3)))))
-    lens = fams[0].seq_lens.numpy()
-    nbytes = sum(M.decode_bytes(lens, num_q_heads=f.family.num_q_heads,
-                                num_kv_heads=f.family.num_kv_heads, head_dim=f.family.head_dim,
-                                window=f.family.window, page_size=16,
-                                kv_bytes_per_elem=1 if f.family.kv_dtype == W.KV_E4M3 else 2,
-                                q_len=f.q.shape[2] if f.q.dim() == 4 else 1)
-                 for f in fams)
+    def sample_bytes(fs):
+        lens = fs[0].seq_lens.numpy()
+        return sum(M.decode_bytes(lens, num_q_heads=f.family.num_q_heads,
+                                  num_kv_heads=f.family.num_kv_heads, head_dim=f.family.head_dim,
+                                  window=f.family.window, page_size=16,
+                                  kv_bytes_per_elem=1 if f.family.kv_dtype == W.KV_E4M3 else 2,
+                                  q_len=f.q.shape[2] if f.q.dim() == 4 else 1)
+                   for f in fs)
+    nbytes = sample_bytes(fams)
+    # the same oracle on one core, on the first row only (a few seconds)
+    one = [gather_rows_to_host(layers[0], 1) for layers in sets.values()]
+    t1 = oracle_sample(one, nthreads=1)
     return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": O.max_threads(), "kind": "oracle",
             "sample": f"first {nrows} of {batch} rows of the bench batch, one layer per family, "
-                      f"fp64 C oracle with OpenMP on all cores, {t:.2f} s"}
+                      f"fp64 C oracle with OpenMP on all cores, {t:.2f} s",
+            "single_thread": {"value": sample_bytes(one) / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"first row, one layer per family, {t1:.2f} s"}}
 
 
 # ------------------------------------------------------------------ arms

@@ -71,6 +71,17 @@
 #define ORACLE_KV_BF16 0
 #define ORACLE_KV_E4M3 1
 
+/* Threads of one call: nthreads > 0 as asked, else the process default.
+ * Passed per parallel region, so one call never changes the next one's. */
+static int oracle_threads(int nthreads) {
+#ifdef _OPENMP
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
 /* ---------------------------------------------------------------- numbers */
 
 double oracle_bf16_to_double(uint16_t bits) {
@@ -232,10 +243,8 @@ int oracle_decode(const uint16_t* q, const void* k_pool, const void* v_pool, int
     const int32_t g = Hq / Hkv;
     const int32_t nr = rows ? nrows : B;
     int status = 0;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#endif
-#pragma omp parallel for schedule(dynamic, 1)
+    const int nt = oracle_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (int64_t unit = 0; unit < (int64_t)nr * Hkv; ++unit) {
         int32_t r = (int32_t)(unit / Hkv);
         int32_t c = (int32_t)(unit % Hkv);
@@ -324,10 +333,8 @@ int oracle_decode_mq(const uint16_t* q, const void* k_pool, const void* v_pool, 
                     Hkv, D, P, num_pages};
     const int32_t g = Hq / Hkv;
     int status = 0;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#endif
-#pragma omp parallel for schedule(dynamic, 1)
+    const int nt = oracle_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (int64_t unit = 0; unit < (int64_t)B * Hkv; ++unit) {
         int32_t b = (int32_t)(unit / Hkv);
         int32_t c = (int32_t)(unit % Hkv);

@@ -639,6 +639,23 @@ def run_ga(args):
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = run_cpu_baseline(sets, wl.batch)
 
+    # The practical HBM read ceiling on this GPU (own read-only stream kernel,
+    # 4 GiB > L2, after the timed region): the decode kernels' second denominator
+    ceiling = None
+    if rank == 0 and not args.rows:
+        buf = torch.empty(4 << 30, dtype=torch.uint8, device=device)
+        sink = torch.zeros(1, dtype=torch.int64, device=device)
+        for _ in range(2):
+            ga.ga_read_stream(buf, sink)
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record()
+        for _ in range(10):
+            ga.ga_read_stream(buf, sink)
+        e3.record()
+        torch.cuda.synchronize()
+        ceiling = buf.numel() * 10 / (s3.elapsed_time(e3) / 1e3) / 1e9
+        del buf
+
     if rank == 0:
         def plan_desc(p):
             return {"mode": ["none", "count", "chunk"][p.mode], "splits": p.splits,
@@ -681,6 +698,10 @@ def run_ga(args):
                          "bound": "hbm", "achieved": dom_ach, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_ach / peak,
                          "frac_of_nominal_8TBs": dom_ach / NOMINAL_HBM_GBS,
+                         "read_ceiling_gbs": ceiling,
+                         "frac_of_read_ceiling": (dom_ach / ceiling) if ceiling else None,
+                         "read_ceiling_kernel": "ga_read_stream: own read-only stream, 16-byte "
+                                                "loads, 4 GiB, 10 passes",
                          "traffic": traffic},
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -315,6 +315,19 @@ int ga_decode_global_hd512_noalloc(const void* q, const void* k_pool, const void
                                    float scale, const ga_plan* plan, void* out,
                                    int32_t* err_word, ga_stream_t stream);
 
+/*
+ * ga_read_stream -- measurement helper, not part of the decode path: reads
+ * `bytes` of device memory at src once with 16-byte non-allocating loads
+ * (every SM, a grid of 8 CTAs per SM) and folds them into one word, so that
+ * a caller can time the practical HBM read ceiling the decode kernels stream
+ * against ("Gemma 4 31B on vLLM -- operating-point reference", Three
+ * load-bearing facts: decode throughput saturates on HBM bandwidth).
+ *   src: device memory, 16-byte aligned; bytes a multiple of 16 (> 0).
+ *   sink: one device uint64, written only if the fold hits a fixed value.
+ * Errors: GA_ERR_INVALID_ARG for a null / unaligned pointer or bad size.
+ */
+int ga_read_stream(const void* src, int64_t bytes, void* sink, ga_stream_t stream);
+
 /* Name of a GA_* status code (static string). */
 const char* ga_strerror(int status);
 

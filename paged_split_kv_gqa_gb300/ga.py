@@ -84,8 +84,9 @@ def _load():
                                                    i32, i64, f32, P, p, p, p]
     for fn in ("ga_plan_splits", "ga_plan_splits_mq", "ga_kv_append", "ga_decode_local_hd256",
                "ga_decode_global_hd512", "ga_splitkv_combine", "ga_check_error_word",
-               "ga_decode_global_hd512_noalloc"):
+               "ga_decode_global_hd512_noalloc", "ga_read_stream"):
         getattr(lib, fn).restype = ctypes.c_int
+    lib.ga_read_stream.argtypes = [p, i64, p, p]
     lib.ga_check_error_word.argtypes = [i32]
     lib.ga_strerror.argtypes = [ctypes.c_int]
     lib.ga_strerror.restype = ctypes.c_char_p
@@ -255,6 +256,13 @@ def ga_splitkv_combine(partial_o, partial_lse, plan, seq_lens, pt_stride, out, *
 
 def ga_check_error_word(word: int) -> int:
     return int(_lib.ga_check_error_word(int(word)))
+
+
+def ga_read_stream(src: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """One read of every byte of src (measurement helper: the HBM read
+    ceiling); sink is a device int64 tensor of one element."""
+    _check(_lib.ga_read_stream(_ptr(src), src.numel() * src.element_size(), _ptr(sink),
+                               _stream(stream)), "ga_read_stream")
 
 
 def workspace_views(plan: ga_plan, workspace: torch.Tensor):

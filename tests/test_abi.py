@@ -186,6 +186,15 @@ def test_combine_rejects_before_launch(ga):
     assert f(None, None, ctypes.byref(none), None, 3, None, None, None) == ga.GA_OK
 
 
+def test_read_stream_rejects_before_launch(ga):
+    f = ga.lib.ga_read_stream
+    assert f(None, 1 << 20, FAKE, None) == ga.GA_ERR_INVALID_ARG      # no source
+    assert f(FAKE, 1 << 20, None, None) == ga.GA_ERR_INVALID_ARG      # no sink
+    assert f(MIS, 1 << 20, FAKE, None) == ga.GA_ERR_INVALID_ARG       # unaligned source
+    assert f(FAKE, 24, FAKE, None) == ga.GA_ERR_INVALID_ARG           # not a multiple of 16
+    assert f(FAKE, 0, FAKE, None) == ga.GA_ERR_INVALID_ARG            # empty
+
+
 def test_oracle_and_library_share_no_code():
     """The oracle sources never include or import the CUDA path and vice versa."""
     orc = open(os.path.join(ROOT, "oracle", "ga_oracle.c")).read() + \

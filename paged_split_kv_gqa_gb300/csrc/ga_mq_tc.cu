@@ -313,14 +313,15 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
     }
 }
 
-// Warp 7: for each stage, once the softmax warps have written P(m), the
-// column sums l += 1 . P^T (one product per page), then for each V slot as it
-// lands: zero the slot's V rows that no query of the row attends (keys below
-// the window or past the row's end in a copied page, every row of a page with
-// an invalid id, never copied), then O^T += V^T P^T, one product per page and
-// 128-dim block.  Lane 0 issues and commits: a slot's commit frees it, the
-// stage's last one the P buffer.  A unit's first products overwrite O^T and
-// the sums (accumulate off) once the previous unit's epilogue has read them.
+// Warp 7: for each stage, once the softmax warps have written P(m), for each
+// V slot as it lands: zero the slot's V rows that no query of the row attends
+// (keys below the window or past the row's end in a copied page, every row of
+// a page with an invalid id, never copied), then per page of the slot the
+// column sums l += 1 . P^T and O^T += V^T P^T per 128-dim block.  Lane 0
+// issues and commits: a slot's commit frees it; the commit after pages 0..3
+// releases the first half of P^T (keys 0..63), the stage's last one the whole
+// P buffer.  A unit's first products overwrite O^T and the sums (accumulate
+// off) once the previous unit's epilogue has read them.
 template <class G>
 __device__ void pv_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                         uint32_t base, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
@@ -447,10 +448,11 @@ __device__ __forceinline__ void warp_colmax64(const float (&v)[NC], int lane, fl
 // column (query i = column % S sits at position L - S + i and attends keys j
 // with 0 <= (L - S + i) - j < window; keys inside every column's range skip
 // the per-column test), raise a column's max only past SLACK (then O^T and the
-// sums are rescaled once the previous stage's products have run), write P^T
-// in bf16.  At the end of a unit: O^T scaled by 1 / l to the output (or a
-// split partial and its LSE).  The running maxima live in shared memory, one
-// writer per column between barriers.
+// sums are rescaled once the previous stage's products have run), compute P
+// in bf16 and write P^T once this warp's half of the buffer is free (keys
+// 0..63 are released before 64..127).  At the end of a unit: O^T scaled by
+// 1 / l to the output (or a split partial and its LSE).  The running maxima
+// live in shared memory, one writer per column between barriers.
 template <class G>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile int* abort_flag) {

@@ -7,8 +7,10 @@
 // 1025 boundaries, full-context hd512 layers), with the S queries of a row as
 // extra (query, head) columns of each kv head: g query heads give g * S
 // columns, each with its own causal and window mask ("Gemma 4 31B on vLLM --
-// operating-point reference": EAGLE3 verify of 3 draft tokens; "Gemma 4 on
-// Apple Silicon with Core AI": prefill chunks of 64 tokens).
+// operating-point reference", Operating-point recipes, LIGHT: EAGLE3 verify of
+// 3 speculative tokens; "visible-cx/Gemma-4-31B-CoreAI" model card,
+// hybrid-pf64/ bundles: prefill chunks of 64 tokens with a query axis and an
+// intra-chunk causal mask).
 //
 // Why a separate kernel.  From a few dozen columns per kv head on, the work
 // is a dense contraction (4 D flops per key and column), and the mma.sync

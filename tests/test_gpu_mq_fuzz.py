@@ -5,9 +5,10 @@ force the tcgen05 units of 64 columns, odd seeds the column-parallel mma.sync
 units (with E4M3 pools both plans run the 8-column tensor-core kernel), so
 both kinds see the same distribution of shapes.  The method: the paged
 attention of both families with the S queries of a row at its last S
-positions, causal inside the chunk ("Gemma 4 on Apple Silicon with Core AI",
-prefill chunks; "Gemma 4 31B on vLLM -- operating-point reference",
-speculative verify)."""
+positions, causal inside the chunk ("visible-cx/Gemma-4-31B-CoreAI" model
+card, hybrid-pf64/ bundles: prefill chunks; "Gemma 4 31B on vLLM --
+operating-point reference", Operating-point recipes, LIGHT: speculative
+verify)."""
 import math
 
 import numpy as np

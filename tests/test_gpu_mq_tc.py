@@ -17,9 +17,10 @@ on tcgen05, 128 keys (8 pages) per stage.  That kernel's own edge cases are:
   rescales O in tensor memory, many times.
 
 The method is the paged attention of both families with the S queries of a
-row as extra columns, each with its causal and window mask ("Gemma 4 on Apple
-Silicon with Core AI": prefill chunks of 64 tokens; "Gemma 4 31B on vLLM --
-operating-point reference": speculative verify).
+row as extra columns, each with its causal and window mask
+("visible-cx/Gemma-4-31B-CoreAI" model card, hybrid-pf64/ bundles: prefill
+chunks of 64 tokens; "Gemma 4 31B on vLLM -- operating-point reference",
+Operating-point recipes, LIGHT: speculative verify).
 """
 import dataclasses
 import math

@@ -100,3 +100,53 @@ def test_invalid(ga):
         ga.ga_plan_splits(np.ones(4097, dtype=np.int32), **base)
     p = ga.ga_plan_splits([], **base)
     assert p.units == 0 and p.grid == 1
+
+
+def _chunks(L, Wn, mode, s=0, cp=0):
+    n = _pages(L, Wn)
+    if n == 0 or mode == "none":
+        return 1
+    per = -(-n // s) if mode == "count" else cp
+    return -(-n // per)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_multi_query_plan_properties(ga, seed):
+    """Seeded random multi-query plans: the column tile follows the unit rule
+    (8 up to 8 columns per kv head; 64 from 32 columns at hd512 / 64 at hd256 or
+    when tensor-core units are asked for; else 32), and units, grid, row chunks
+    (union window W + S - 1) and the partials' workspace follow from it."""
+    rng = np.random.default_rng(500 + seed)
+    D = int(rng.choice([256, 512]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 3, 8]))
+    S = int(rng.choice([1, 2, 4, 5, 8, 16, 33, 64]))
+    Wn = int(rng.choice([0, 32, 1024])) if D == 256 else 0
+    lens = [int(x) for x in rng.integers(0, 3000, size=int(rng.integers(1, 12)))]
+    flags = int(rng.choice([0, ga.GA_PLAN_TENSOR_CORE_UNITS, ga.GA_PLAN_COLUMN_PARALLEL_UNITS]))
+    split = [dict(requested_splits=1), dict(requested_splits=3), dict(fixed_chunk_tokens=64)][
+        seed % 3]
+    p = ga.ga_plan_splits_mq(lens, q_len=S, num_q_heads=g * Hkv, num_kv_heads=Hkv, head_dim=D,
+                             window=Wn, num_sms=152, flags=flags, **split)
+    cols = g * S
+    if cols <= 8:
+        tile = 8
+    elif flags == ga.GA_PLAN_TENSOR_CORE_UNITS:
+        tile = 64
+    elif flags == ga.GA_PLAN_COLUMN_PARALLEL_UNITS:
+        tile = 32
+    else:
+        tile = 64 if cols >= (32 if D == 512 else 64) else 32
+    assert p.col_tile == tile and p.q_len == S
+    w_union = Wn + S - 1 if Wn else 0
+    mode = "none" if "requested_splits" in split and split["requested_splits"] == 1 else \
+        ("count" if "requested_splits" in split else "chunk")
+    rc = sum(_chunks(L, w_union, mode, s=split.get("requested_splits", 0),
+                     cp=split.get("fixed_chunk_tokens", 0) // 16) for L in lens)
+    assert p.row_chunks == rc
+    assert p.units == rc * Hkv * -(-cols // tile)
+    assert p.grid == max(1, min(p.units, 152))
+    if p.mode != ga.GA_SPLIT_NONE:
+        assert p.partial_lse_offset >= p.partial_o_offset + rc * g * Hkv * S * D * 4
+        assert p.partial_o_offset % 256 == 0 and p.partial_lse_offset % 256 == 0
+        assert p.workspace_bytes >= p.partial_lse_offset + rc * g * Hkv * S * 4

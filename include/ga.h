@@ -298,8 +298,13 @@ int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const g
  *   - plan->workspace_bytes > GA_NOALLOC_SCRATCH_BYTES is rejected with
  *     GA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it together with the current context;
+ *     make that first call before any stream capture.  A call made in another
+ *     context of the device (after cudaDeviceReset, or a driver-API context
+ *     made current) looks the address up again: the first call there should
+ *     also come before any capture.
+ *   - A plan built with GA_PLAN_TOUCH_LOG is rejected (GA_ERR_INVALID_ARG):
+ *     the log would land in the built-in array, out of the caller's reach.
  *   - Every call shares the one array: calls whose kernels overlap on the GPU
  *     (other streams, unordered threads) race on it and give wrong results.
  *     The array keeps the last call's contents; nothing in it needs to start

@@ -150,7 +150,7 @@ using namespace ga;
 
 extern "C" {
 
-int32_t ga_version(void) { return 0x000200; }
+int32_t ga_version(void) { return 0x000300; }
 
 const char* ga_strerror(int status) {
     switch (status) {
@@ -254,6 +254,15 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
         off += (bytes + 255) / 256 * 256;
         return at;
     };
+    // every non-empty workspace starts with the same ticket region, so that
+    // no plan's partials ever land on another plan's tickets
+    if (p.mode != kSplitNone || (flags & GA_PLAN_TOUCH_LOG)) {
+        static_assert(GA_TICKETS_PER_ROW == kTicketsPerRow &&
+                          GA_TICKET_REGION_BYTES == (int64_t)kMaxBatch * kTicketsPerRow * 4,
+                      "ticket region");
+        p.ticket_offset = take(GA_TICKET_REGION_BYTES);
+        p.ticket_bytes = GA_TICKET_REGION_BYTES;
+    }
     if (p.mode != kSplitNone) {
         p.partial_o_offset = take(p.row_chunks * num_q_heads * (int64_t)q_len * head_dim * 4);
         p.partial_lse_offset = take(p.row_chunks * num_q_heads * (int64_t)q_len * 4);
@@ -318,6 +327,12 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
         if (!workspace || !aligned16(workspace)) return GA_ERR_INVALID_ARG;
         if ((int64_t)workspace_bytes < plan->workspace_bytes) return GA_ERR_WORKSPACE_TOO_SMALL;
     }
+    // the ticket region, when the plan has one, lies inside its workspace
+    if (plan->ticket_bytes != 0 &&
+        (plan->ticket_bytes != GA_TICKET_REGION_BYTES || plan->ticket_offset < 0 ||
+         plan->ticket_offset % 256 != 0 ||
+         plan->ticket_offset + plan->ticket_bytes > plan->workspace_bytes))
+        return GA_ERR_INVALID_ARG;
     DecodeArgs a{q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride, seq_lens,
                  batch, num_q_heads, num_kv_heads, head_dim, window, num_pages, scale, plan,
                  workspace, out, err_word, reinterpret_cast<cudaStream_t>(stream)};

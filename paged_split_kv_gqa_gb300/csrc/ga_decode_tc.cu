@@ -458,7 +458,7 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
 template <class G, int NV>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile uint32_t* flags,
-                              volatile int* abort_flag) {
+                              volatile int* abort_flag, volatile int* s_last) {
     constexpr int D = G::D;
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
@@ -524,6 +524,9 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         nks = __ldg(p.k_scale + cur.nl.c);
         nvs = __ldg(p.v_scale + cur.nl.c);
     }
+    // a split unit whose partials are being made: it owes its ticket arrival
+    UnitInfo owed{};
+    bool owe = false;
     while (cur.more() && !stop) {
         const UnitInfo x = cur.take(p, pre);
         const float ksc = nks, vsc = nvs;
@@ -532,9 +535,13 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             nvs = __ldg(p.v_scale + cur.nl.c);
         }
         const bool single = (x.g.chunks == 1);
+        owed = x;
+        owe = !single && p.tickets != nullptr;
         const int nss = (x.np + G::SSP - 1) / G::SSP;
         if (nss == 0) {
             write_empty(x, single);
+            if (owe) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
+            owe = false;
             continue;
         }
         const uint32_t qb = k & 1;
@@ -729,8 +736,20 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
                 (LL == 0.f) ? -CUDART_INF_F : (mm + log2f(LL)) * CUDART_LN2_F;
         }
+        if (owe) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
+        owe = false;
         n += (uint32_t)nss;
         ++k;
+    }
+    // After an abort every remaining split unit of this CTA still arrives
+    // (its partials are undefined; the error word says so), so that the
+    // tickets return to zero.
+    if (p.tickets != nullptr) {
+        if (owe) split_arrive(p, pre, owed, D, tid, 128, 1, s_last);
+        while (cur.more()) {
+            const UnitInfo x = cur.take(p, pre);
+            if (x.g.chunks > 1) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
+        }
     }
 }
 
@@ -742,6 +761,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
+    __shared__ int s_last;            // the fused combine's "this arrival was the last"
     __shared__ uint32_t tmem_slot;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -789,7 +809,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     if (warp < NSW) {
-        softmax_warps<G, NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag);
+        softmax_warps<G, NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag, &s_last);
     } else if (warp == MMA_WARP || warp == PV_WARP) {
         if (lane == 0) {
             if (warp == MMA_WARP)
@@ -866,6 +886,7 @@ static int run_tc(const DecodeArgs& a) {
     p.group = a.num_q_heads / a.num_kv_heads * S;
     p.TW = kHeadTile;
     p.HG = (p.group + kHeadTile - 1) / kHeadTile;
+    p.tickets = fused_tickets(pl, a.workspace, p.Hkv, p.HG);
     p.window = effective_window(a.window, S);
     p.S = S;
     p.mask_window = a.window;
@@ -880,7 +901,7 @@ static int run_tc(const DecodeArgs& a) {
     const int grid = pl.grid > 0 ? pl.grid : 1;
     kern<<<grid, tc::NTHREADS, kSmem, a.stream>>>(tmK, tmV, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
-    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
+    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE) && p.tickets == nullptr)
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
                               a.pt_stride, a.stream);
     return GA_OK;

@@ -21,6 +21,7 @@ constexpr int kPageSize = 16;     // keys per page; one page = one 16-key MMA ti
 constexpr int kHeadTile = 8;      // query heads per unit (MMA N)
 constexpr int kMaxBatch = 2048;   // rows per call (decode keeps a row prefix in smem)
 constexpr int kMaxQLen = 64;      // query tokens per row of a multi-query decode
+constexpr int kTicketsPerRow = 64;   // split-KV tickets per row (fused combine)
 constexpr int kTcColTile = 64;    // (query, head) columns per unit of the tensor-core
                                   // multi-query kernel (N of its products)
 

@@ -1,8 +1,8 @@
 """The C-ABI library builds, loads without a GPU, exports every symbol the
 header declares, and rejects bad arguments on the host before any launch."""
 import ctypes
-import re
 import os
+import re
 
 import numpy as np
 import pytest
@@ -47,15 +47,34 @@ def test_strerror_and_version(ga):
     assert ga.strerror(0) == "GA_OK"
     assert "WORKSPACE" in ga.strerror(3)
     assert "unknown" in ga.strerror(99)
-    assert ga.ga_version() == 0x000200
+    assert ga.ga_version() == 0x000300
     assert ga.ga_check_error_word(0) == ga.GA_OK
     assert ga.ga_check_error_word(ga.GA_DEVERR_PAGE_ID) == ga.GA_ERR_DEVICE_CHECK
 
 
-def test_plan_struct_layout_matches_header(ga):
-    # 14 int32 (the last two: q_len, reserved) then 6 int64, no padding surprises
-    assert ctypes.sizeof(ga.ga_plan) == 14 * 4 + 6 * 8
-    assert ga.ga_plan.q_len.offset == 12 * 4 and ga.ga_plan.row_chunks.offset == 14 * 4
+def test_plan_struct_layout_matches_header(ga, tmp_path):
+    """The ctypes mirror of ga_plan against the C compiler's own layout of the
+    header's struct (size and every field offset)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [n for n, _ in ga.ga_plan._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stdio.h>\n#include <stddef.h>\n#include \"ga.h\"\nint main(void) {\n"
+        '  printf("%zu\\n", sizeof(ga_plan));\n'
+        + "".join(f'  printf("%zu\\n", offsetof(ga_plan, {n}));\n' for n in names)
+        + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([cc, "-I", os.path.join(root, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(ga.ga_plan)
+    assert got[1:] == [getattr(ga.ga_plan, n).offset for n in names]
 
 
 def test_multi_query_plan(ga):
@@ -66,9 +85,13 @@ def test_multi_query_plan(ga):
     one = ga.ga_plan_splits([40, 33], **kw)
     four = ga.ga_plan_splits_mq([40, 33], q_len=4, **kw)
     assert one.q_len == 1 and four.q_len == 4
-    assert four.partial_o_offset == one.partial_o_offset == 0
-    # partial O: row_chunks x (Hq * S) x D fp32, 256-byte aligned regions
-    assert four.partial_lse_offset >= four.row_chunks * 4 * 4 * 256 * 4
+    # the fixed ticket region first, then partial O: row_chunks x (Hq * S) x D
+    # fp32, 256-byte aligned regions
+    assert four.ticket_offset == one.ticket_offset == 0
+    assert four.ticket_bytes == one.ticket_bytes == ga.TICKET_REGION_BYTES
+    assert four.partial_o_offset == one.partial_o_offset == ga.TICKET_REGION_BYTES
+    assert four.partial_lse_offset >= (four.partial_o_offset
+                                       + four.row_chunks * 4 * 4 * 256 * 4)
     # 4 queries x group 2 = 8 columns: still one head group per kv head
     assert four.units == one.units
     assert one.col_tile == four.col_tile == 8

@@ -53,18 +53,23 @@ def test_wait_runs_out_reports_and_context_survives(ga, case):
     stall = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_TEST_WAIT_TIMEOUT, **kw)
     assert stall.grid > 1                      # other CTAs still run
     fi_run = dataclasses.replace(fi, family=fam)
+    ws = ga.workspace_for(stall, DEV)
     t0 = time.time()
-    run_decode(ga, fi_run, stall, err=err, out=torch.empty_like(fi.q))
+    run_decode(ga, fi_run, stall, err=err, out=torch.empty_like(fi.q), workspace=ws)
     torch.cuda.synchronize()
     elapsed = time.time() - t0
     word = int(err.item())
     assert word & ga.GA_DEVERR_TIMEOUT, hex(word)
     assert ga.ga_check_error_word(word) == ga.GA_ERR_DEVICE_CHECK
     assert elapsed < 30.0
-    # the context is intact: the same call without the hook is correct
+    # every chunk still arrived on its split-KV ticket: the region is zero again
+    assert not bool(ws[:ga.TICKET_REGION_BYTES].any())
+    # the context is intact: the same call without the hook, on the same
+    # workspace, is correct
     err.zero_()
     plan = ga.ga_plan_splits(lens, **kw)
-    out = run_decode(ga, fi_run, plan, err=err, out=torch.empty_like(fi.q))
+    assert plan.workspace_bytes <= ws.numel()
+    out = run_decode(ga, fi_run, plan, err=err, out=torch.empty_like(fi.q), workspace=ws)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     scale = 1.0 / math.sqrt(fam.head_dim)

@@ -3,10 +3,8 @@
 A step on the 31B-shaped decode batch (the default workload: B 64, L ~
 U[8192, 32768], 32 query heads; local 16 KV heads hd256 window 1024; global 4
 KV heads hd512) is: KV append (local) -> local decode (+ split-KV combine if
-planned) -> KV append (global) -> global decode (+ combine).  A split
-decode merges its own partials (the last chunk of a row and kv head does it
-inside the decode kernel); --external-combine launches the combine kernel
-after it instead.  All of it runs in libga's CUDA kernels through the C ABI.  --workload ragged runs
+planned) -> KV append (global) -> global decode -> split-KV combine.  All of
+it runs in libga's CUDA kernels through the C ABI.  --workload ragged runs
 the 50-local (fp8) + 10-global layer sweep instead.
 
 Printed: one JSON line with the metric (algorithmic HBM GB/s of the step),
@@ -135,8 +133,7 @@ WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 MQ_UNIT_FLAGS = {"auto": 0, "tc": "GA_PLAN_TENSOR_CORE_UNITS", "cp": "GA_PLAN_COLUMN_PARALLEL_UNITS"}
 
 
-def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto",
-               external_combine=False):
+def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto"):
     """One layer's inputs.  q_len > 1: a multi-query step (q_len new tokens
     per row at its last positions, e.g. a speculative-decoding verify): the
     pools keep the union of the queries' windows, q / out are
@@ -169,7 +166,8 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, 
     plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                              window=fam.window, requested_splits=splits,
-                             flags=(ga.GA_PLAN_EXTERNAL_COMBINE if external_combine else 0) |
+                             flags=ga.GA_PLAN_EXTERNAL_COMBINE |
+                             (ga.GA_PLAN_KV_E4M3 if fam.kv_dtype == W.KV_E4M3 else 0) |
                              (getattr(ga, unit_flag) if unit_flag else 0), q_len=S)
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
@@ -205,7 +203,7 @@ def workload_config(workload, seed, fp8="none"):
 
 
 def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
-               q_len=1, fp8="none", mq_units="auto", external_combine=False):
+               q_len=1, fp8="none", mq_units="auto"):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -218,8 +216,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
-    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units,
-                                  external_combine)
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units)
                        for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
@@ -235,26 +232,9 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
     return wl, schedule, sets, err
 
 
-def decode_kernels(ga, f):
-    """Kernels one decode call of this layer launches: the decode kernel, plus
-    the combine kernel for a split plan whose merge is not fused (external
-    combine asked for, or more unit columns per row than a row's tickets)."""
-    plan, fam, fi = f["plan"], f["fam"], f["fi"]
-    if plan.mode == ga.GA_SPLIT_NONE:
-        return 1
-    if plan.flags & ga.GA_PLAN_EXTERNAL_COMBINE:
-        return 2                   # the caller's ga_splitkv_combine
-    cols = fam.num_q_heads // fam.num_kv_heads * plan.q_len
-    two_bf16_pools = fam.kv_dtype == 0 and fi.k_pool.data_ptr() != fi.v_pool.data_ptr()
-    width = plan.col_tile if two_bf16_pools else 8
-    units_per_row = fam.num_kv_heads * -(-cols // width)
-    return 1 if units_per_row <= ga.TICKETS_PER_ROW else 2
-
-
 def launch_layer(ga, f, err, events=None):
     """append + decode (+ combine) of one layer on the current stream.
     Returns the number of kernels launched."""
-    n = f["kn"].shape[0] + decode_kernels(ga, f)
     fi, fam, plan = f["fi"], f["fam"], f["plan"]
     S = f["kn"].shape[0]
     for i in range(S):                 # this step's new token(s) of every row
@@ -272,9 +252,11 @@ def launch_layer(ga, f, err, events=None):
                                   **kw)
     if events is not None:
         events[1].record()
-    if plan.mode != ga.GA_SPLIT_NONE and plan.flags & ga.GA_PLAN_EXTERNAL_COMBINE:
+    n = S + 1
+    if plan.mode != ga.GA_SPLIT_NONE:
         ga.ga_splitkv_combine(f["po"], f["plse"], plan, fi.seq_lens, fi.page_table.shape[1],
                               f["out"], err_word=err)
+        n += 1
     return n
 
 
@@ -454,7 +436,7 @@ def run_ga(args):
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
                                          args.pools, args.kv_alias, args.splits, args.q_len,
-                                         args.fp8, args.mq_units, args.external_combine)
+                                         args.fp8, args.mq_units)
 
     def step(evs=None):
         n = 0
@@ -756,9 +738,7 @@ def run_ga(args):
             },
             "pct_of_peak": {"measured": value / peak, "nominal_8TBs": value / NOMINAL_HBM_GBS},
             "families": families,
-            "roofline": {"kernel": f"{kname} (decode kernel"
-                                   + (", combine excluded)" if args.external_combine else
-                                      " with its fused split-KV combine)"),
+            "roofline": {"kernel": f"{kname} (decode kernel, combine excluded)",
                          "bound": "hbm", "achieved": dom_ach, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_ach / peak,
                          "frac_of_nominal_8TBs": dom_ach / NOMINAL_HBM_GBS,
@@ -802,9 +782,6 @@ def main():
                     help="query tokens per row (> 1: a multi-query / speculative-verify step)")
     ap.add_argument("--fp8", default="none", choices=["none", "local", "global", "both"],
                     help="store these families' KV pools as fp8-e4m3 with per-head scales")
-    ap.add_argument("--external-combine", action="store_true",
-                    help="split plans leave the merge to a separate combine kernel launch "
-                         "(the decode kernel is then timed alone)")
     ap.add_argument("--mq-units", default="auto", choices=sorted(MQ_UNIT_FLAGS),
                     help="multi-query units for more than 8 (query, head) columns per kv head: "
                          "the planner's choice, tcgen05 units of 64 columns, or column-parallel "

@@ -102,10 +102,19 @@ enum {
                                      undefined.  Never set outside tests. */
     GA_PLAN_TENSOR_CORE_UNITS = 8, /* more than 8 (query, head) columns per kv head: always
                                       units of 64 columns (tensor-core kernel on bf16 pools) */
-    GA_PLAN_COLUMN_PARALLEL_UNITS = 16 /* ... always column-parallel units of 32 columns.
+    GA_PLAN_COLUMN_PARALLEL_UNITS = 16, /* ... always column-parallel units of 32 columns.
                                       Neither flag: 64-column units from 32 columns per kv
                                       head at head_dim 512 and from 64 at head_dim 256
                                       (where each is the faster on GB300), else 32. */
+    GA_PLAN_KV_E4M3 = 32          /* the plan is for E4M3 pools.  On the sliding family
+                                      (head_dim 256, one query per row) with 2 or 4 query
+                                      heads per kv head and Hkv a multiple of 8 / group, a
+                                      work unit then spans 8 / group kv heads: the decode
+                                      copies a page's blocks of those heads as one box per
+                                      128-dim region, and the planner's cost model counts
+                                      such units.  Results do not depend on it; a plan made
+                                      without it also serves E4M3 pools (one kv head per
+                                      unit), and the flag is ignored for bf16 pools. */
 };
 
 /*
@@ -136,26 +145,7 @@ typedef struct ga_plan {
     int64_t partial_o_offset;    /* byte offsets inside the workspace */
     int64_t partial_lse_offset;
     int64_t touch_log_offset;
-    int64_t ticket_offset;       /* split-KV tickets of the fused combine: always 0 */
-    int64_t ticket_bytes;        /* GA_TICKET_REGION_BYTES when the workspace is non-empty */
 } ga_plan;
-
-/*
- * Workspace tickets.  Every non-empty workspace starts with a fixed region of
- * GA_TICKET_REGION_BYTES (one int32 counter per (row, kv head x head group),
- * GA_TICKETS_PER_ROW per row): the split decode's chunks of a (row, kv head)
- * count their arrivals there, and the chunk that arrives last merges the
- * partials itself (no second kernel).  The region's size and place are the
- * same for every plan, so one workspace can serve plans of any shape.
- *   - It must hold zeros before the first decode call that uses the
- *     workspace (allocate it zeroed, or clear it once).
- *   - Every decode call leaves it zeros when the call's kernel completes,
- *     also after a device-reported error (every chunk still arrives).
- *   - Calls that use the same workspace must not overlap on the GPU (their
- *     partials race anyway).
- */
-#define GA_TICKETS_PER_ROW 64
-#define GA_TICKET_REGION_BYTES ((int64_t)2048 * GA_TICKETS_PER_ROW * 4)
 
 /*
  * ga_plan_splits -- choose how each row's attended pages are cut into split-KV
@@ -239,15 +229,10 @@ int ga_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_poo
  *   scale: softmax scale (e.g. 1/sqrt(256), or 1.0 for the Gemma convention).
  *   plan: from ga_plan_splits with the same batch, heads, head_dim, window
  *       and page_size.  If plan->mode != GA_SPLIT_NONE the call needs
- *       workspace (>= plan->workspace_bytes, 16-byte aligned, its ticket
- *       region zeroed before first use: see "Workspace tickets").  The chunk
- *       of a (row, kv head) that finishes last merges that row's partials
- *       inside the decode kernel, with the same arithmetic as
- *       ga_splitkv_combine (bit-identical outputs); when a kv head has more
- *       unit columns than GA_TICKETS_PER_ROW / Hkv allows, the call launches
- *       ga_splitkv_combine's kernel after the decode instead.  With
- *       GA_PLAN_EXTERNAL_COMBINE the partials are left for the caller's
- *       ga_splitkv_combine.
+ *       workspace (>= plan->workspace_bytes, 16-byte aligned) and runs the
+ *       decode kernel then ga_splitkv_combine's kernel on `stream` (the
+ *       latter is left to the caller when the plan has
+ *       GA_PLAN_EXTERNAL_COMBINE).
  *   out [batch, num_q_heads, 256] bf16.
  * Rows with L_b = 0 produce zeros.
  * Multi-query decode (plan from ga_plan_splits_mq with q_len = S > 1): q and
@@ -300,10 +285,8 @@ int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool
  *   decode call got (a length beyond pt_stride * page_size counts as 0).
  *   Rows whose chunk count is 1 are left untouched (the decode call wrote
  *   them).  out [plan->batch, Hq, S, D] bf16.
- * The decode calls merge their own partials when split (fused, or with this
- * kernel when the tickets do not cover the plan); it is exported for plans
- * with GA_PLAN_EXTERNAL_COMBINE, testing and callers that write their own
- * partials.
+ * The decode calls invoke this themselves when split; it is exported for
+ * testing and for callers that write their own partials.
  */
 int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
                        const int32_t* seq_lens, int64_t pt_stride, void* out,

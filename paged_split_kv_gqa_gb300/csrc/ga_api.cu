@@ -68,6 +68,30 @@ int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_
     return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
 }
 
+// An E4M3 pool [num_pages, Hkv, 16, D] seen, for one 128-byte region of the
+// head dim (bytes 128 * region .. + 127 of every key row), as the 5-D tensor
+// (byte e < 128, key % 8, kv head, key / 8, page) with byte strides
+// (1, D, 16 D, 8 D, Hkv 16 D).  One box {128, 8, hp, 2, 1} holds that region
+// of hp consecutive kv heads of one page and lands as [key / 8][head][key % 8]
+// rows of 128 bytes (128-byte swizzle): each head's keys in groups of 8 rows,
+// the groups of one head 8 * hp rows apart.
+int encode_heads_map(CUtensorMap* map, const void* pool, int32_t region, int32_t num_kv_heads,
+                     int64_t num_pages, int32_t head_dim, int32_t hp) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return GA_ERR_CUDA;
+    const cuuint64_t D = (cuuint64_t)head_dim;
+    const cuuint64_t dims[5] = {128, 8, (cuuint64_t)num_kv_heads, 2, (cuuint64_t)num_pages};
+    const cuuint64_t strides[4] = {D, 16 * D, 8 * D, (cuuint64_t)num_kv_heads * 16 * D};
+    const cuuint32_t box[5] = {128, 8, (cuuint32_t)hp, 2, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                           const_cast<uint8_t*>(static_cast<const uint8_t*>(pool)) + 128 * region,
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
+}
+
 int ensure_smem_attr(const void* func, int bytes, int slot) {
     static std::atomic<uint64_t> done[32];
     int dev = 0;
@@ -89,6 +113,8 @@ struct PlanInput {
     const int32_t* lens;
     int32_t B, Hq, Hkv, D, W, num_sms, S;    // W: the window of the union of S queries
     int32_t TW;                              // columns per work unit
+    int32_t HP;                              // kv heads per work unit
+    double page_weight;                      // a page-head's bytes relative to bf16
 };
 
 // Row-chunk count and per-unit page counts of a candidate chunking.
@@ -101,7 +127,7 @@ struct Candidate {
 
 void evaluate(const PlanInput& in, Candidate& cand) {
     const int32_t HG = ceil_div(in.Hq / in.Hkv * in.S, in.TW);
-    const int64_t per_rc = (int64_t)in.Hkv * HG;
+    const int64_t per_rc = (int64_t)(in.Hkv / in.HP) * HG;
     std::vector<int32_t> rc_pages;
     rc_pages.reserve(in.B * 4);
     int64_t split_rows_rc = 0;
@@ -119,7 +145,8 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     cand.row_chunks = (int64_t)rc_pages.size();
     cand.units = cand.row_chunks * per_rc;
     // Static round-robin schedule of the persistent grid: unit u -> CTA u % G.
-    // Cost in "page loads per SM": each unit costs its pages plus a fixed
+    // Cost in "page loads per SM" (bf16 page-head blocks): each unit costs its
+    // pages (times its kv heads, weighted by the KV element size) plus a fixed
     // overhead (warp merge, pipeline refill: ~3.5K cycles, about 4 pages of
     // stream time); a split adds the partial round trip spread over all SMs
     // plus one extra launch.  (With 2 pages the ragged 256-row global family
@@ -129,7 +156,7 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     std::vector<double> load((size_t)G, 0.0);
     for (int64_t u = 0; u < cand.units; ++u) {
         const int64_t rc = u / per_rc;
-        load[(size_t)(u % G)] += rc_pages[(size_t)rc] + unit_ovh;
+        load[(size_t)(u % G)] += rc_pages[(size_t)rc] * in.HP * in.page_weight + unit_ovh;
     }
     double makespan = 0;
     for (double v : load) makespan = std::max(makespan, v);
@@ -183,9 +210,10 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
         return GA_ERR_INVALID_ARG;
     if (q_len < 1) return GA_ERR_INVALID_ARG;
     if (q_len > kMaxQLen) return GA_ERR_UNSUPPORTED;
+    static_assert(GA_PLAN_KV_E4M3 == kPlanKvE4m3, "plan flag");
     const int32_t known_flags = GA_PLAN_TOUCH_LOG | GA_PLAN_EXTERNAL_COMBINE |
                                 GA_PLAN_TEST_WAIT_TIMEOUT | GA_PLAN_TENSOR_CORE_UNITS |
-                                GA_PLAN_COLUMN_PARALLEL_UNITS;
+                                GA_PLAN_COLUMN_PARALLEL_UNITS | GA_PLAN_KV_E4M3;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || window < 0 ||
         num_sms < 1 || requested_splits < 0 || fixed_chunk_tokens < 0 ||
         (requested_splits > 0 && fixed_chunk_tokens > 0) || (flags & ~known_flags) ||
@@ -206,8 +234,10 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     const bool tc = (flags & GA_PLAN_TENSOR_CORE_UNITS) ||
                     (!(flags & GA_PLAN_COLUMN_PARALLEL_UNITS) && cols >= tc_min_cols(head_dim));
     const int32_t tw = cols <= kHeadTile ? kHeadTile : tc ? kTcColTile : 4 * kHeadTile;
+    const int32_t hp = tc_heads_per_unit(flags, head_dim, q_len, num_q_heads / num_kv_heads,
+                                         num_kv_heads);
     PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len,
-                 tw};
+                 hp > 1 ? kHeadTile : tw, hp, (flags & GA_PLAN_KV_E4M3) ? 0.5 : 1.0};
     Candidate best;
     if (requested_splits == 1) {
         best = Candidate{kSplitNone, 0, 0};
@@ -254,15 +284,6 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
         off += (bytes + 255) / 256 * 256;
         return at;
     };
-    // every non-empty workspace starts with the same ticket region, so that
-    // no plan's partials ever land on another plan's tickets
-    if (p.mode != kSplitNone || (flags & GA_PLAN_TOUCH_LOG)) {
-        static_assert(GA_TICKETS_PER_ROW == kTicketsPerRow &&
-                          GA_TICKET_REGION_BYTES == (int64_t)kMaxBatch * kTicketsPerRow * 4,
-                      "ticket region");
-        p.ticket_offset = take(GA_TICKET_REGION_BYTES);
-        p.ticket_bytes = GA_TICKET_REGION_BYTES;
-    }
     if (p.mode != kSplitNone) {
         p.partial_o_offset = take(p.row_chunks * num_q_heads * (int64_t)q_len * head_dim * 4);
         p.partial_lse_offset = take(p.row_chunks * num_q_heads * (int64_t)q_len * 4);
@@ -327,12 +348,6 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
         if (!workspace || !aligned16(workspace)) return GA_ERR_INVALID_ARG;
         if ((int64_t)workspace_bytes < plan->workspace_bytes) return GA_ERR_WORKSPACE_TOO_SMALL;
     }
-    // the ticket region, when the plan has one, lies inside its workspace
-    if (plan->ticket_bytes != 0 &&
-        (plan->ticket_bytes != GA_TICKET_REGION_BYTES || plan->ticket_offset < 0 ||
-         plan->ticket_offset % 256 != 0 ||
-         plan->ticket_offset + plan->ticket_bytes > plan->workspace_bytes))
-        return GA_ERR_INVALID_ARG;
     DecodeArgs a{q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride, seq_lens,
                  batch, num_q_heads, num_kv_heads, head_dim, window, num_pages, scale, plan,
                  workspace, out, err_word, reinterpret_cast<cudaStream_t>(stream)};

@@ -1,7 +1,9 @@
-// ga_combine.cu -- the standalone log-sum-exp merge of split-KV partials
-// (ga_splitkv_combine, and the decode calls' fallback when a plan's units do
-// not fit the fused tail's tickets).  The arithmetic lives in ga_combine.cuh,
-// shared with the fused tail of the decode kernels.
+// ga_combine.cu -- the log-sum-exp merge of split-KV partials
+// (ga_splitkv_combine; the decode calls launch it after a split decode).
+// For row b, column h and the row's chunks s:
+//     M = max_s lse_s,  out = sum_s e^{lse_s - M} o_s / sum_s e^{lse_s - M}
+// ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is mandatory here":
+// flash-decode with split factor 8); the arithmetic is in ga_combine.cuh.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
     const int t = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (t >= p.Hq * nb) return;
     const int h = t / nb, d0 = (t % nb) * 128;
-    const uint2 o = merge_warp128<false>(p.po, p.plse, rc0, S, p.Hq, p.D, h, d0);
+    const uint2 o = merge_warp128(p.po, p.plse, rc0, S, p.Hq, p.D, h, d0);
     *reinterpret_cast<uint2*>(p.out + ((int64_t)b * p.Hq + h) * p.D + d0 +
                               4 * (threadIdx.x & 31)) = o;
 }

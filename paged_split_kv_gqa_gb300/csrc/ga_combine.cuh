@@ -1,6 +1,7 @@
-// ga_combine.cuh -- the log-sum-exp merge of split-KV partials, one home for
-// the standalone combine kernel and the fused tail of the decode kernels, so
-// both give bit-identical outputs.
+// ga_combine.cuh -- the log-sum-exp merge of split-KV partials: the
+// arithmetic, written once with every rounding step spelled out, in a
+// latency-friendly warp form and a plain per-thread form that give the same
+// bits.
 //
 // For row b, (query, head) column h and the row's chunks s = 0 .. S-1:
 //     M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s
@@ -17,37 +18,27 @@
 
 namespace ga {
 
-// kCoherent: the partials were written by other CTAs of the running kernel
-// (fused tail), so they are read through L2 only (no stale L1 lines); the
-// standalone kernel reads them through the read-only path.
-template <bool kCoherent>
-__device__ __forceinline__ float ld_part(const float* a) {
-    if constexpr (kCoherent) return __ldcg(a);
-    else return __ldg(a);
-}
-template <bool kCoherent>
+__device__ __forceinline__ float ld_part(const float* a) { return __ldg(a); }
 __device__ __forceinline__ float4 ld_part4(const float* a) {
-    if constexpr (kCoherent) return __ldcg(reinterpret_cast<const float4*>(a));
-    else return __ldg(reinterpret_cast<const float4*>(a));
+    return __ldg(reinterpret_cast<const float4*>(a));
 }
 
 // Dims d .. d+3 of column h: partial o at po[(rc0 + s) * Hq + h][D], lse at
 // plse[(rc0 + s) * Hq + h].  Returns the four outputs packed as bf16.  Every
-// rounding step is spelled out so that both callers compute the same bits.
-template <bool kCoherent>
+// rounding step is spelled out so that merge_warp128 computes the same bits.
 __device__ __forceinline__ uint2 merge_chunks4(const float* po, const float* plse, int64_t rc0,
                                                int S, int64_t Hq, int D, int64_t h, int d) {
     const float* lse = plse + rc0 * Hq + h;
     float M = -CUDART_INF_F;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ld_part<kCoherent>(lse + (int64_t)s * Hq));
+    for (int s = 0; s < S; ++s) M = fmaxf(M, ld_part(lse + (int64_t)s * Hq));
     const float Ms = (M == -CUDART_INF_F) ? 0.f : M;
     float ax = 0.f, ay = 0.f, az = 0.f, aw = 0.f, den = 0.f;
     for (int s = 0; s < S; ++s) {
-        const float ls = ld_part<kCoherent>(lse + (int64_t)s * Hq);
+        const float ls = ld_part(lse + (int64_t)s * Hq);
         if (ls == -CUDART_INF_F) continue;                 // empty chunk (NaN is kept)
         const float wgt = expf(__fsub_rn(ls, Ms));
         den = __fadd_rn(den, wgt);
-        const float4 v = ld_part4<kCoherent>(po + ((rc0 + s) * Hq + h) * (int64_t)D + d);
+        const float4 v = ld_part4(po + ((rc0 + s) * Hq + h) * (int64_t)D + d);
         ax = __fmaf_rn(wgt, v.x, ax);
         ay = __fmaf_rn(wgt, v.y, ay);
         az = __fmaf_rn(wgt, v.z, az);
@@ -74,16 +65,15 @@ constexpr float kSkipChunk = -1.0f;
 // are shared by shuffles, and the partials are read 8 chunks at a time with
 // independent loads.  Rows with more than kMergeWarpMaxChunks chunks take
 // merge_chunks4 itself.
-template <bool kCoherent>
 __device__ __forceinline__ uint2 merge_warp128(const float* po, const float* plse, int64_t rc0,
                                                int S, int64_t Hq, int D, int64_t h, int d0) {
     const int lane = threadIdx.x & 31;
     if (S > kMergeWarpMaxChunks)
-        return merge_chunks4<kCoherent>(po, plse, rc0, S, Hq, D, h, d0 + 4 * lane);
+        return merge_chunks4(po, plse, rc0, S, Hq, D, h, d0 + 4 * lane);
     const float* lse = plse + rc0 * Hq + h;
-    const float l0 = lane < S ? ld_part<kCoherent>(lse + (int64_t)lane * Hq) : -CUDART_INF_F;
+    const float l0 = lane < S ? ld_part(lse + (int64_t)lane * Hq) : -CUDART_INF_F;
     const float l1 =
-        lane + 32 < S ? ld_part<kCoherent>(lse + (int64_t)(lane + 32) * Hq) : -CUDART_INF_F;
+        lane + 32 < S ? ld_part(lse + (int64_t)(lane + 32) * Hq) : -CUDART_INF_F;
     // the maximum ignores NaN (fmaxf), like merge_chunks4's running maximum
     float M = fmaxf(fmaxf(-CUDART_INF_F, l0), l1);
 #pragma unroll
@@ -107,7 +97,7 @@ __device__ __forceinline__ uint2 merge_warp128(const float* po, const float* pls
         float4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            if (s0 + j < S) v[j] = ld_part4<kCoherent>(base + (int64_t)(s0 + j) * step);
+            if (s0 + j < S) v[j] = ld_part4(base + (int64_t)(s0 + j) * step);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (s0 + j < S) {

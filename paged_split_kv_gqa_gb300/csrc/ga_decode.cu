@@ -324,7 +324,7 @@ template <class C>
 __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const int32_t* pre,
                          int64_t U, uint8_t* smem, uint32_t ring, uint32_t bars,
                          volatile uint32_t* flags, volatile int* abort_flag,
-                         volatile int* q_issued, volatile int* s_last) {
+                         volatile int* q_issued) {
     const int tid = threadIdx.x;            // 0 .. NCT-1
     const int w = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, t = lane & 3;
@@ -740,8 +740,6 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
                     p.partial_lse[x.rc * p.Hq + h + 1] =
                         (l1 == 0.f) ? -CUDART_INF_F : (m1 + log2f(l1)) * CUDART_LN2_F;
             }
-            // (every unit arrives, also after an abort: see split_arrive)
-            if (!single && p.tickets) split_arrive(p, pre, x, C::D, tid, C::NCT, 1, s_last);
             continue;
         }
         if (gid == 0) {
@@ -895,8 +893,6 @@ __device__ void consumer(const CUtensorMap* tmQ, const DecodeParams& p, const in
         }
         if (!single && tid < x.nvalid && GA_CHK(x.rc < p.rc_capacity))
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] = lse;
-        // every unit arrives, also after an abort (the loop visits all units)
-        if (!single && p.tickets) split_arrive(p, pre, x, C::D, tid, C::NCT, 1, s_last);
     }
 }
 
@@ -909,7 +905,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     __shared__ int q_issued;          // the q tile of the next unit was requested
-    __shared__ int s_last;            // the fused combine's "this arrival was the last"
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -944,7 +939,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     if (warp == C::NCW)
         producer<C>(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
     else
-        consumer<C>(&tmQ, p, pre, U, smem, ring, bars, flags, &abort_flag, &q_issued, &s_last);
+        consumer<C>(&tmQ, p, pre, U, smem, ring, bars, flags, &abort_flag, &q_issued);
 }
 
 // ------------------------------------------------------------------ host
@@ -968,7 +963,7 @@ static int run(const DecodeArgs& a, int slot) {
                          C::TW);
     if (rc != GA_OK) return rc;
 
-    DecodeParams p{};
+    DecodeParams p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.page_table = a.page_table;
     p.seq_lens = a.seq_lens;
@@ -992,7 +987,6 @@ static int run(const DecodeArgs& a, int slot) {
     p.group = a.num_q_heads / a.num_kv_heads * S;
     p.TW = C::TW;
     p.HG = (p.group + C::TW - 1) / C::TW;
-    p.tickets = fused_tickets(pl, a.workspace, p.Hkv, p.HG);
     p.window = effective_window(a.window, S);
     p.S = S;
     p.mask_window = a.window;
@@ -1007,7 +1001,7 @@ static int run(const DecodeArgs& a, int slot) {
     const int grid = pl.grid > 0 ? pl.grid : 1;
     decode_kernel<C><<<grid, C::NTHREADS, C::SMEM_BYTES, a.stream>>>(tmK, tmV, tmQ, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
-    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE) && p.tickets == nullptr)
+    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
                               a.pt_stride, a.stream);
     return GA_OK;

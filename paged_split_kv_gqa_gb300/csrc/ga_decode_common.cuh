@@ -6,7 +6,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "ga_combine.cuh"
 #include "ga_device.cuh"
 #include "ga_internal.h"
 
@@ -22,8 +21,6 @@ struct DecodeParams {
     float* partial_o;             // [rc_capacity, Hq, D]
     float* partial_lse;           // [rc_capacity, Hq]
     int32_t* touch_log;           // [rc_capacity, touch_stride] or null
-    int32_t* tickets;             // [kMaxBatch, kTicketsPerRow] arrival counters of the
-                                  // fused combine, or null (no split, or merged apart)
     int32_t* err_word;
     int64_t pt_stride;
     int64_t num_pages;
@@ -157,50 +154,6 @@ __device__ __forceinline__ bool build_row_prefix(const DecodeParams& p, int32_t*
         return false;
     }
     return true;
-}
-
-// ---- fused split-KV combine
-//
-// Called by the nthr threads (named barrier bar_id, tid in [0, nthr)) that
-// stored unit x's partials and LSEs, once per unit of a split row (chunks > 1),
-// including units skipped after an abort: the unit's ticket counts the
-// arrivals of the row's chunks for this (kv head, head group), and the
-// arrival that completes the count merges the row's partials of the unit's
-// columns into out with the standalone combine's arithmetic, then resets the
-// ticket to zero for the next call.  No CTA waits for another.
-// Kept out of line: the merge's registers must not weigh on the decode loop's
-// allocation (it runs once per split unit, with little live state around it).
-static __device__ __noinline__ void split_arrive(const DecodeParams& p, const int32_t* pre,
-                                          const UnitInfo& x, int D, int tid, int nthr,
-                                          int bar_id, volatile int* s_last) {
-    __threadfence();                  // this thread's partial stores, device-wide
-    named_barrier(bar_id, nthr);
-    if (tid == 0) {
-        int32_t* tk = p.tickets + (int64_t)x.b * kTicketsPerRow + (x.c * p.HG + x.hg);
-        const int32_t old = atomicAdd(tk, 1);
-        const int last = (old == x.g.chunks - 1) ? 1 : 0;
-        if (last) atomicExch(tk, 0);
-        *s_last = last;
-    }
-    named_barrier(bar_id, nthr);
-    if (!*s_last) return;
-    __threadfence();                  // the other chunks' partials are visible
-    const int64_t rc0 = pre[x.b];
-    const int nb = D / 128, nw = nthr / 32;
-    for (int t = tid >> 5; t < x.nvalid * nb; t += nw) {       // one warp per task
-        const int n = t / nb, d0 = (t % nb) * 128;
-        const int64_t h = x.h0 + n;
-        const int64_t blk = ((int64_t)x.b * p.Hq + h) * D + d0;   // the warp's 128 dims
-        // warp-uniform check (the merge shuffles across the warp)
-        if (!GA_CHK(blk + 128 <= p.out_elems && rc0 + x.g.chunks <= p.rc_capacity)) {
-            report(p.err_word, kErrSelfCheck);
-            continue;
-        }
-        const int64_t at = blk + 4 * (tid & 31);
-        const uint2 v = merge_warp128<true>(p.partial_o, p.partial_lse, rc0, x.g.chunks, p.Hq,
-                                            D, h, d0);
-        *reinterpret_cast<uint2*>(p.out + at) = v;
-    }
 }
 
 // ---- pieces of the warp-specialised tcgen05 kernels

@@ -89,20 +89,37 @@ static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
 // Geometry per head dim.  Both give 32 KB K and V slots.  ALIAS: K and V
 // are one pool; each block is fetched once into a V slot that serves both
 // products, and the K ring's memory becomes V slots too.
-template <int D_, bool ALIAS_ = false>
+//
+// HP > 1 (head_dim 256, two pools): a unit spans HP kv heads (its 8 columns
+// are their query heads).  A superstage is 8 / HP pages of all HP heads, and
+// page i fills rows 16 HP i .. 16 HP i + 16 HP - 1 of each region as
+// [key / 8][head][key % 8] (one 5-D box of 2 HP KB per page and region), so
+// a head's keys lie in groups of 8 rows, 8 HP rows apart: the QK product runs
+// over all 128 rows at once (a row only counts for its own head's columns),
+// the PV product runs per head (its own accumulator, K = 32 keys per
+// instruction at a group stride of 1 KB x HP), so a NaN in one head's V never
+// meets another head's P.
+template <int D_, bool ALIAS_ = false, int HP_ = 1>
 struct Geo {
     static constexpr int D = D_;
     static constexpr bool ALIAS = ALIAS_;
+    static constexpr int HP = HP_;                        // kv heads per unit
     static constexpr int NVE = ALIAS ? NKS + NVS : NVS;   // V slots in use
     static constexpr int NCH = D / 128;                  // 128-dim regions (128 B of E4M3)
-    static constexpr int SSP = D == 256 ? 8 : 4;          // pages per superstage
-    static constexpr int MQ = SSP * kPageSize;            // keys per superstage = QK's M
-    static constexpr int CHUNK_BYTES = MQ * 128;          // one region: [MQ keys][128 B]
+    static constexpr int SSP = HP > 1 ? 8 / HP : (D == 256 ? 8 : 4);   // pages per superstage
+    static constexpr int PAGE_ROWS = kPageSize * HP;      // rows a page adds to a region tile
+    static constexpr int MQ = SSP * PAGE_ROWS;            // rows per superstage = QK's M
+    static constexpr int CHUNK_BYTES = MQ * 128;          // one region: [MQ rows][128 B]
     static constexpr int SLOT_BYTES = NCH * CHUNK_BYTES;  // K or V of a superstage
     static constexpr int BLOCK_BYTES = kPageSize * D;     // K or V of one page-head block
     static constexpr int QBUF_BYTES = NCH * 16 * 128;     // [region][16 rows][128 B]
-    static constexpr int O_COLS = 16 * NCH;               // TMEM columns of one O buffer
-    static constexpr int TMEM_COLS = TM_O + 2 * O_COLS <= 128 ? 128 : 256;
+    static constexpr int O_HEAD = 16 * NCH;               // TMEM columns of one head's O
+    static constexpr int O_COLS = HP * O_HEAD;            // TMEM columns of one O buffer
+    static constexpr int TMEM_COLS = TM_O + 2 * O_COLS <= 128   ? 128
+                                     : TM_O + 2 * O_COLS <= 256 ? 256
+                                                                : 512;
+    static constexpr int PV_STEPS = HP > 1 ? 4 / HP : 0;  // K = 32 products per head and region
+    static_assert(HP == 1 || (D == 256 && !ALIAS && (HP == 2 || HP == 4)), "heads per unit");
     static constexpr int OFF_RING = 0;                    // K slots, then V slots
     static constexpr int OFF_VRING = ALIAS ? OFF_RING : OFF_RING + NKS * SLOT_BYTES;
     static constexpr int OFF_Q = OFF_RING + (NKS + NVS) * SLOT_BYTES;
@@ -118,7 +135,7 @@ struct Geo {
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && CHUNK_BYTES % 1024 == 0,
                   "swizzle-128B operands need 1024-byte aligned tiles");
     static_assert((MQ == 128 || MQ == 64) && SSP * NCH <= 32, "superstage shape");
-    static_assert(TM_O + 2 * O_COLS <= TMEM_COLS, "tensor memory");
+    static_assert(TM_O + 2 * O_COLS <= TMEM_COLS && TMEM_COLS <= 512, "tensor memory");
 };
 
 // Two values -> two E4M3 codes (hi) and the E4M3 codes of their remainders
@@ -138,9 +155,10 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
 // region) before V (K == V: only the V slot, once).  Pages with an invalid id
 // are flagged (bit i of flags[m % NVE]) and not copied.
 template <class G>
-__device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const DecodeParams& p,
-                         const int32_t* pre, int64_t U, uint32_t ring, uint32_t bars,
-                         volatile uint32_t* flags, volatile int* abort_flag) {
+__device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmK1,
+                         const CUtensorMap* tmV1, const DecodeParams& p, const int32_t* pre,
+                         int64_t U, uint32_t ring, uint32_t bars, volatile uint32_t* flags,
+                         volatile int* abort_flag) {
     const int lane = threadIdx.x & 31;
     // Test hook: nothing is armed or copied for CTA 0, so the other roles'
     // bounded waits run out and report GA_DEVERR_TIMEOUT.
@@ -215,29 +233,42 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             const int32_t pid = __shfl_sync(0xffffffffu, ids, (G::SSP * (s % SPB) + pl) & 31);
             const bool present = lane < G::SSP && pi < x.np;
             const bool valid_id = present && page_ok(pid, p.num_pages);
-            const int32_t y = valid_id ? page_block_row(pid, x.c, p.Hkv) : 0;
-            const bool good = valid_id && GA_CHK(y >= 0 && (int64_t)y + kPageSize <= p.pool_rows);
+            // first row of the unit's (first) kv head in the [pages * Hkv * 16, D] view
+            const int32_t y = valid_id ? page_block_row(pid, x.c * G::HP, p.Hkv * G::HP) : 0;
+            const bool good =
+                valid_id && GA_CHK(y >= 0 && (int64_t)y + G::PAGE_ROWS <= p.pool_rows);
             const uint32_t gm = __ballot_sync(0xffffffffu, good);
             const uint32_t pm = __ballot_sync(0xffffffffu, present);
             const uint32_t kfull = bar(bars, B_KFULL + kslot), vfull = bar(bars, B_VFULL + vslot);
+            constexpr uint32_t kPageBytes = (uint32_t)(G::HP * G::BLOCK_BYTES);
             if (lane == 0) {
                 flags[vslot] = pm & ~gm;
-                if (!G::ALIAS) mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
-                mbar_arrive_expect_tx(vfull, (uint32_t)__popc(gm) * G::BLOCK_BYTES);
+                if (!G::ALIAS) mbar_arrive_expect_tx(kfull, (uint32_t)__popc(gm) * kPageBytes);
+                mbar_arrive_expect_tx(vfull, (uint32_t)__popc(gm) * kPageBytes);
             }
             __syncwarp();
             if (good) {
-                const uint32_t kd = ring + kslot * G::SLOT_BYTES + (uint32_t)lane * (kPageSize * 128);
+                const uint32_t kd = ring + kslot * G::SLOT_BYTES + (uint32_t)lane * (G::PAGE_ROWS * 128);
                 const uint32_t vd = ring + (uint32_t)G::OFF_VRING + vslot * G::SLOT_BYTES +
-                                    (uint32_t)lane * (kPageSize * 128);
-                if (!G::ALIAS) {
+                                    (uint32_t)lane * (G::PAGE_ROWS * 128);
+                if constexpr (G::HP > 1) {
+                    // one box per region: the page's rows of the unit's HP kv heads
+                    static_assert(G::NCH == 2, "one 5-D map per 128-byte region");
+                    const int32_t h0 = x.c * G::HP;
+                    tma_load_5d(kd, tmK, kfull, 0, 0, h0, 0, pid, policy);
+                    tma_load_5d(kd + G::CHUNK_BYTES, tmK1, kfull, 0, 0, h0, 0, pid, policy);
+                    tma_load_5d(vd, tmV, vfull, 0, 0, h0, 0, pid, policy);
+                    tma_load_5d(vd + G::CHUNK_BYTES, tmV1, vfull, 0, 0, h0, 0, pid, policy);
+                } else {
+                    if (!G::ALIAS) {
+#pragma unroll
+                        for (int c = 0; c < G::NCH; ++c)
+                            tma_load_3d(kd + c * G::CHUNK_BYTES, tmK, kfull, 0, y, c, policy);
+                    }
 #pragma unroll
                     for (int c = 0; c < G::NCH; ++c)
-                        tma_load_3d(kd + c * G::CHUNK_BYTES, tmK, kfull, 0, y, c, policy);
+                        tma_load_3d(vd + c * G::CHUNK_BYTES, tmV, vfull, 0, y, c, policy);
                 }
-#pragma unroll
-                for (int c = 0; c < G::NCH; ++c)
-                    tma_load_3d(vd + c * G::CHUNK_BYTES, tmV, vfull, 0, y, c, policy);
             } else if (present) {
                 report(p.err_word, valid_id ? kErrSelfCheck : kErrPageId);
             }
@@ -340,15 +371,38 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
             }
             tc_fence_after();
             const int nks = (min(G::SSP, x.np - G::SSP * s) + 1) / 2;   // 32 keys per MMA
+            if constexpr (G::HP > 1) {
+                // per head h: its 32-key steps j (pages 2j, 2j + 1), groups of 8
+                // keys 8 HP rows apart, into its own accumulator; P^T holds head
+                // h's keys at 128 / HP h .. in the same order
 #pragma unroll
-            for (int c = 0; c < G::NCH; ++c) {
-                const uint32_t d = tmem + TM_O + G::O_COLS * ob + 16 * c;
-                const uint32_t va =
-                    ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::CHUNK_BYTES;
-                for (int ks = 0; ks < nks; ++ks)
-                    tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, G::CHUNK_BYTES, 1024),
-                                smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024), IPV,
-                                (s == 0 && ks == 0) ? 0u : 1u);
+                for (int c = 0; c < G::NCH; ++c) {
+                    const uint32_t va =
+                        ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::CHUNK_BYTES;
+#pragma unroll
+                    for (int h = 0; h < G::HP; ++h) {
+                        const uint32_t d = tmem + TM_O + G::O_COLS * ob + G::O_HEAD * h + 16 * c;
+                        for (int j = 0; j < G::PV_STEPS && j < nks; ++j)
+                            tc_mma_e4m3(
+                                d,
+                                smem_desc_sw128(va + 1024 * h + j * 4 * (1024 * G::HP),
+                                                G::CHUNK_BYTES, 1024 * G::HP),
+                                smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * (h * G::PV_STEPS + j),
+                                                16, 1024),
+                                IPV, (s == 0 && j == 0) ? 0u : 1u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < G::NCH; ++c) {
+                    const uint32_t d = tmem + TM_O + G::O_COLS * ob + 16 * c;
+                    const uint32_t va =
+                        ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::CHUNK_BYTES;
+                    for (int ks = 0; ks < nks; ++ks)
+                        tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, G::CHUNK_BYTES, 1024),
+                                    smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024),
+                                    IPV, (s == 0 && ks == 0) ? 0u : 1u);
+                }
             }
             tc_commit(bar(bars, B_VEMPTY + (int)slot));  // the V slot may be refilled
             tc_commit(bar(bars, B_PVDONE + (int)pb));    // P buffer free, O up to date
@@ -458,7 +512,7 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
 template <class G, int NV>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile uint32_t* flags,
-                              volatile int* abort_flag, volatile int* s_last) {
+                              volatile int* abort_flag) {
     constexpr int D = G::D;
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
@@ -517,31 +571,33 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] = -CUDART_INF_F;
     };
 
+    constexpr int GQ = NV / G::HP;              // (query, head) columns per kv head of a unit
     uint32_t n = 0, k = 0;                      // superstages, active units so far
     UnitCursor cur(p, pre, U);
-    float nks = 1.f, nvs = 1.f;                 // the pending unit's K / V scales
-    if (cur.more()) {
-        nks = __ldg(p.k_scale + cur.nl.c);
-        nvs = __ldg(p.v_scale + cur.nl.c);
-    }
-    // a split unit whose partials are being made: it owes its ticket arrival
-    UnitInfo owed{};
-    bool owe = false;
+    float nks[G::HP], nvs[G::HP];               // the pending unit's K / V scales, per kv head
+    auto load_scales = [&]() {
+#pragma unroll
+        for (int h = 0; h < G::HP; ++h) {
+            nks[h] = __ldg(p.k_scale + cur.nl.c * G::HP + h);
+            nvs[h] = __ldg(p.v_scale + cur.nl.c * G::HP + h);
+        }
+    };
+#pragma unroll
+    for (int h = 0; h < G::HP; ++h) nks[h] = nvs[h] = 1.f;
+    if (cur.more()) load_scales();
     while (cur.more() && !stop) {
         const UnitInfo x = cur.take(p, pre);
-        const float ksc = nks, vsc = nvs;
-        if (cur.more()) {
-            nks = __ldg(p.k_scale + cur.nl.c);
-            nvs = __ldg(p.v_scale + cur.nl.c);
+        float ksc[G::HP], vsc[G::HP];
+#pragma unroll
+        for (int h = 0; h < G::HP; ++h) {
+            ksc[h] = nks[h];
+            vsc[h] = nvs[h];
         }
+        if (cur.more()) load_scales();
         const bool single = (x.g.chunks == 1);
-        owed = x;
-        owe = !single && p.tickets != nullptr;
         const int nss = (x.np + G::SSP - 1) / G::SSP;
         if (nss == 0) {
             write_empty(x, single);
-            if (owe) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
-            owe = false;
             continue;
         }
         const uint32_t qb = k & 1;
@@ -550,7 +606,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         int32_t clo[NV], chi[NV];
 #pragma unroll
         for (int f = 0; f < NV; ++f) {
-            kf[f] = p.scale_log2 * ksc * qsc[qb * kHeadTile + f];
+            kf[f] = p.scale_log2 * ksc[f / GQ] * qsc[qb * kHeadTile + f];
             // query i = column % S sits at position L - S + i: keys [clo, chi)
             const int32_t pos = x.g.len - p.S + (x.hg * kHeadTile + f) % p.S;
             chi[f] = f < x.nvalid ? pos + 1 : 0;
@@ -579,15 +635,22 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bars, B_SFREE + (int)sb));
-            const int pg = kss >> 4;
+            // this thread's row: page pg of the superstage, key of that page,
+            // and (HP > 1) which of the unit's kv heads it belongs to
+            const int pg = kss / G::PAGE_ROWS;
+            const int rr = kss % G::PAGE_ROWS;
+            const int khi = G::HP > 1 ? rr / (8 * G::HP) : 0;
+            const int key = G::HP > 1 ? 8 * khi + (kss & 7) : (kss & 15);
+            const int hrow = G::HP > 1 ? (rr >> 3) % G::HP : 0;
             const int npg = min(G::SSP, x.np - G::SSP * s);
             const bool present = key_lane && pg < npg && !((flags[slot] >> pg) & 1u);
-            const int32_t kj = (x.p0 + G::SSP * s + pg) * kPageSize + (kss & 15);
+            const int32_t kj = (x.p0 + G::SSP * s + pg) * kPageSize + key;
             float sc[NV];
             bool grow = false;
 #pragma unroll
             for (int f = 0; f < NV; ++f) {
-                const bool valid = present && kj >= clo[f] && kj < chi[f];
+                const bool valid =
+                    present && (G::HP == 1 || f / GQ == hrow) && kj >= clo[f] && kj < chi[f];
                 sc[f] = valid ? (__uint_as_float(sr[f]) + __uint_as_float(sr[8 + f])) * kf[f]
                               : -CUDART_INF_F;
                 grow |= sc[f] > m[f] + MAX_SLACK;
@@ -617,17 +680,21 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                     const uint32_t mp = ms - 1;
                     if (!wait_all(B_PVDONE + (int)(mp % NPB), (mp / NPB) & 1)) break;
                     tc_fence_after();
+                    // (HP > 1: every head's accumulator; a head's columns of the
+                    // other heads hold nothing used)
+#pragma unroll
+                    for (int h = 0; h < G::HP; ++h)
 #pragma unroll
                     for (int c = 0; c < G::NCH; ++c) {
                         uint32_t o[16];
-                        tmem_ld16(to + 16 * c, o);
+                        tmem_ld16(to + G::O_HEAD * h + 16 * c, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int f = 0; f < NV; ++f) {
                             o[f] = __float_as_uint(__uint_as_float(o[f]) * alpha[f]);
                             o[8 + f] = __float_as_uint(__uint_as_float(o[8 + f]) * alpha[f]);
                         }
-                        tmem_st16(to + 16 * c, o);
+                        tmem_st16(to + G::O_HEAD * h + 16 * c, o);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -645,7 +712,11 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 split_e4m3x2(p0 * PSCALE, p1 * PSCALE, hb[f / 2], lb[f / 2]);
             }
             uint8_t* pb = pbuf + pbi * PBUF_BYTES;
-            const int kc = kss >> 4, kb = kss & 15;
+            // P^T position of this key: its head's keys together, in the
+            // order the head's PV product reads them (HP > 1)
+            const int kpos =
+                G::HP > 1 ? (128 / G::HP) * hrow + 8 * (2 * pg + khi) + (kss & 7) : kss;
+            const int kc = kpos >> 4, kb = kpos & 15;
             if (key_lane) {
 #pragma unroll
                 for (int f = 0; f < NV; ++f) {
@@ -658,7 +729,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             // attends (window edges, a flagged page, the page after an odd
             // last one) may hold anything, NaN included: zero them
             const int nks = (npg + 1) / 2;
-            if (key_lane && kss < 32 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
+            if (key_lane && pg < 2 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
 #pragma unroll
                 for (int c = 0; c < G::NCH; ++c) {
                     uint4* vr = reinterpret_cast<uint4*>(ring + G::OFF_VRING + slot * G::SLOT_BYTES +
@@ -696,18 +767,21 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         // reaches the output as in the definition
         float fac[NV];
 #pragma unroll
-        for (int f = 0; f < NV; ++f) fac[f] = (Lt[f] == 0.f) ? 0.f : __fdividef(vsc, Lt[f] * PSCALE);
+        for (int f = 0; f < NV; ++f)
+            fac[f] = (Lt[f] == 0.f) ? 0.f : __fdividef(vsc[f / GQ], Lt[f] * PSCALE);
         const int64_t r0 = (int64_t)x.b * p.Hq + x.h0;          // output row of column 0
         bool bad_store = false;
         tc_fence_after();
 #pragma unroll
+        for (int h = 0; h < G::HP; ++h)         // HP > 1: head h's columns from its accumulator
+#pragma unroll
         for (int c = 0; c < G::NCH; ++c) {
             uint32_t o[16];
-            tmem_ld16(to + 16 * c, o);
+            tmem_ld16(to + G::O_HEAD * h + 16 * c, o);
             tmem_ld_wait();
 #pragma unroll
             for (int f = 0; f < NV; ++f) {
-                if (f >= x.nvalid) continue;
+                if (f >= x.nvalid || f / GQ != h) continue;
                 const float v = (Lt[f] == 0.f)
                                     ? 0.f
                                     : (__uint_as_float(o[f]) + __uint_as_float(o[8 + f])) * fac[f];
@@ -736,36 +810,27 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
                 (LL == 0.f) ? -CUDART_INF_F : (mm + log2f(LL)) * CUDART_LN2_F;
         }
-        if (owe) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
-        owe = false;
         n += (uint32_t)nss;
         ++k;
-    }
-    // After an abort every remaining split unit of this CTA still arrives
-    // (its partials are undefined; the error word says so), so that the
-    // tickets return to zero.
-    if (p.tickets != nullptr) {
-        if (owe) split_arrive(p, pre, owed, D, tid, 128, 1, s_last);
-        while (cur.more()) {
-            const UnitInfo x = cur.take(p, pre);
-            if (x.g.chunks > 1) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
-        }
     }
 }
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, int NV, bool ALIAS>
+// tmK / tmV: the pools' 3-D maps (HP = 1), or their 5-D maps of region 0 and
+// tmK1 / tmV1 those of region 1 (HP > 1; unused otherwise).
+template <int D, int NV, bool ALIAS, int HP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmK1,
+                     const __grid_constant__ CUtensorMap tmV1, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
-    __shared__ int s_last;            // the fused combine's "this arrival was the last"
     __shared__ uint32_t tmem_slot;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    using G = Geo<D, ALIAS>;
+    using G = Geo<D, ALIAS, HP>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t* pre = reinterpret_cast<int32_t*>(smem + G::OFF_PREFIX);
     volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_FLAGS);
@@ -799,6 +864,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == PROD_WARP && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
+        if (HP > 1) {
+            prefetch_tensormap(&tmK1);
+            prefetch_tensormap(&tmV1);
+        }
     }
     int64_t total_rc = 0;
     if (!build_row_prefix(p, pre, NTHREADS, &total_rc)) return;
@@ -809,7 +878,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     if (warp < NSW) {
-        softmax_warps<G, NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag, &s_last);
+        softmax_warps<G, NV>(p, pre, U, smem, bars, tmem, flags, &abort_flag);
     } else if (warp == MMA_WARP || warp == PV_WARP) {
         if (lane == 0) {
             if (warp == MMA_WARP)
@@ -825,7 +894,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncwarp();
     } else if (warp == PROD_WARP) {
-        producer<G>(&tmK, &tmV, p, pre, U, ring, bars, flags, &abort_flag);
+        producer<G>(&tmK, &tmV, &tmK1, &tmV1, p, pre, U, ring, bars, flags, &abort_flag);
     } else if (warp == Q_WARP) {
         q_warp<G>(p, pre, U, smem, bars, &abort_flag);
     }
@@ -839,28 +908,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-template <int D, bool ALIAS>
+template <int D, bool ALIAS, int HP = 1>
 static int run_tc(const DecodeArgs& a) {
     const ga_plan& pl = *a.plan;
     const int32_t S = pl.q_len;
-    // (query, head) columns of a kv head, at most 8 per unit
+    // (query, head) columns of a kv head, at most 8 per unit; HP > 1: the
+    // unit's 8 columns are the query heads of HP kv heads
     const int32_t cols = a.num_q_heads / a.num_kv_heads * S;
-    const int nv = cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
-    auto kern = nv == 2 ? &tc::decode_tc_kernel<D, 2, ALIAS>
-              : nv == 4 ? &tc::decode_tc_kernel<D, 4, ALIAS> : &tc::decode_tc_kernel<D, 8, ALIAS>;
-    constexpr int kSmem = tc::Geo<D, ALIAS>::SMEM_BYTES;
-    // attribute slots 8..19: (head dim, alias, column count)
+    const int nv = HP > 1 ? 8 : cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
+    auto pick = [nv]() {
+        if constexpr (HP > 1) {
+            (void)nv;
+            return &tc::decode_tc_kernel<D, 8, ALIAS, HP>;
+        } else {
+            return nv == 2   ? &tc::decode_tc_kernel<D, 2, ALIAS, 1>
+                   : nv == 4 ? &tc::decode_tc_kernel<D, 4, ALIAS, 1>
+                             : &tc::decode_tc_kernel<D, 8, ALIAS, 1>;
+        }
+    };
+    auto kern = pick();
+    constexpr int kSmem = tc::Geo<D, ALIAS, HP>::SMEM_BYTES;
+    // attribute slots 8..19: (head dim, alias, column count); 22, 23: HP = 2, 4
     int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmem,
-                              8 + (D == 256 ? 0 : 6) + (ALIAS ? 3 : 0) +
-                                  (nv == 2 ? 0 : nv == 4 ? 1 : 2));
+                              HP > 1 ? (HP == 2 ? 22 : 23)
+                                     : 8 + (D == 256 ? 0 : 6) + (ALIAS ? 3 : 0) +
+                                           (nv == 2 ? 0 : nv == 4 ? 1 : 2));
     if (rc != GA_OK) return rc;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
-    // one box = one 128-dim region of a page-head block: [16 keys][128 B]
-    CUtensorMap tmK, tmV;
-    rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
-    if (rc != GA_OK) return rc;
-    rc = encode_rows_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
-    if (rc != GA_OK) return rc;
+    CUtensorMap tmK, tmV, tmK1, tmV1;
+    if constexpr (HP > 1) {
+        // one box = one 128-dim region of a page's blocks of HP kv heads
+        rc = encode_heads_map(&tmK, a.k_pool, 0, a.num_kv_heads, a.num_pages, a.head_dim, HP);
+        if (rc == GA_OK)
+            rc = encode_heads_map(&tmK1, a.k_pool, 1, a.num_kv_heads, a.num_pages, a.head_dim, HP);
+        if (rc == GA_OK)
+            rc = encode_heads_map(&tmV, a.v_pool, 0, a.num_kv_heads, a.num_pages, a.head_dim, HP);
+        if (rc == GA_OK)
+            rc = encode_heads_map(&tmV1, a.v_pool, 1, a.num_kv_heads, a.num_pages, a.head_dim, HP);
+        if (rc != GA_OK) return rc;
+    } else {
+        // one box = one 128-dim region of a page-head block: [16 keys][128 B]
+        rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
+        if (rc != GA_OK) return rc;
+        rc = encode_rows_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
+        if (rc != GA_OK) return rc;
+        tmK1 = tmK;
+        tmV1 = tmV;
+    }
 
     DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -882,11 +976,11 @@ static int run_tc(const DecodeArgs& a) {
     p.rc_capacity = pl.row_chunks;
     p.B = a.batch;
     p.Hq = a.num_q_heads * S;
-    p.Hkv = a.num_kv_heads;
-    p.group = a.num_q_heads / a.num_kv_heads * S;
+    // units over groups of HP kv heads (columns: their query heads)
+    p.Hkv = a.num_kv_heads / HP;
+    p.group = a.num_q_heads / a.num_kv_heads * S * HP;
     p.TW = kHeadTile;
     p.HG = (p.group + kHeadTile - 1) / kHeadTile;
-    p.tickets = fused_tickets(pl, a.workspace, p.Hkv, p.HG);
     p.window = effective_window(a.window, S);
     p.S = S;
     p.mask_window = a.window;
@@ -899,9 +993,9 @@ static int run_tc(const DecodeArgs& a) {
     p.pool_rows = rows;
     p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, tc::NTHREADS, kSmem, a.stream>>>(tmK, tmV, p);
+    kern<<<grid, tc::NTHREADS, kSmem, a.stream>>>(tmK, tmV, tmK1, tmV1, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
-    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE) && p.tickets == nullptr)
+    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
                               a.pt_stride, a.stream);
     return GA_OK;
@@ -910,6 +1004,12 @@ static int run_tc(const DecodeArgs& a) {
 int launch_decode_tc(const DecodeArgs& a) {
     // one pool for K and V (same pointer): fetch each block once
     const bool alias = a.k_pool == a.v_pool;
+    if (a.head_dim == 256 && !alias) {
+        const int32_t hp = tc_heads_per_unit(a.plan->flags, a.head_dim, a.plan->q_len,
+                                             a.num_q_heads / a.num_kv_heads, a.num_kv_heads);
+        if (hp == 4) return run_tc<256, false, 4>(a);
+        if (hp == 2) return run_tc<256, false, 2>(a);
+    }
     if (a.head_dim == 256) return alias ? run_tc<256, true>(a) : run_tc<256, false>(a);
     if (a.head_dim == 512) return alias ? run_tc<512, true>(a) : run_tc<512, false>(a);
     return GA_ERR_UNSUPPORTED;

@@ -21,7 +21,6 @@ constexpr int kPageSize = 16;     // keys per page; one page = one 16-key MMA ti
 constexpr int kHeadTile = 8;      // query heads per unit (MMA N)
 constexpr int kMaxBatch = 2048;   // rows per call (decode keeps a row prefix in smem)
 constexpr int kMaxQLen = 64;      // query tokens per row of a multi-query decode
-constexpr int kTicketsPerRow = 64;   // split-KV tickets per row (fused combine)
 constexpr int kTcColTile = 64;    // (query, head) columns per unit of the tensor-core
                                   // multi-query kernel (N of its products)
 
@@ -29,6 +28,21 @@ constexpr int kTcColTile = 64;    // (query, head) columns per unit of the tenso
 // (measured on the 31B-shaped batch: at hd512 32 columns already run faster
 // on tcgen05, at hd256 the column-parallel kernel stays ahead up to 32).
 GA_HD int32_t tc_min_cols(int32_t head_dim) { return head_dim == 512 ? 32 : 64; }
+
+// Plan flag: the plan is for E4M3 pools (GA_PLAN_KV_E4M3).
+constexpr int32_t kPlanKvE4m3 = 32;
+
+// KV heads per work unit of the E4M3 tensor-core decode: 8 / group for the
+// sliding family (head_dim 256, one query per row, GQA group 2 or 4, Hkv a
+// multiple of it) when the plan was made for E4M3 pools; else 1.  The unit's
+// 8 (query, head) columns are then the query heads of those kv heads.
+GA_HD int32_t tc_heads_per_unit(int32_t plan_flags, int32_t head_dim, int32_t q_len,
+                                int32_t group, int32_t num_kv_heads) {
+    if (!(plan_flags & kPlanKvE4m3) || head_dim != 256 || q_len != 1) return 1;
+    if (group != 2 && group != 4) return 1;
+    const int32_t hp = 8 / group;
+    return num_kv_heads % hp == 0 ? hp : 1;
+}
 
 enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
 

@@ -42,16 +42,10 @@ struct DecodeArgs {
 int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_t rows,
                     int32_t head_dim, int32_t box_rows, int32_t box_cols = 0);
 
-// The ticket region of the fused split-KV combine for a decode launch whose
-// units have HG head groups per kv head, or null when the launch must leave
-// the merge to the standalone combine kernel (no split, an external combine
-// asked for, or more unit columns per row than a row has tickets).
-inline int32_t* fused_tickets(const ga_plan& pl, void* workspace, int32_t Hkv, int32_t HG) {
-    if (pl.mode == GA_SPLIT_NONE || (pl.flags & GA_PLAN_EXTERNAL_COMBINE)) return nullptr;
-    if (pl.ticket_bytes < GA_TICKET_REGION_BYTES || (int64_t)Hkv * HG > kTicketsPerRow)
-        return nullptr;
-    return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + pl.ticket_offset);
-}
+// Builds the 5-D tensor map of one 128-byte region of an E4M3 pool whose box
+// is one page of hp consecutive kv heads ([key / 8][head][key % 8] rows).
+int encode_heads_map(CUtensorMap* map, const void* pool, int32_t region, int32_t num_kv_heads,
+                     int64_t num_pages, int32_t head_dim, int32_t hp);
 
 int launch_decode(const DecodeArgs& a);
 

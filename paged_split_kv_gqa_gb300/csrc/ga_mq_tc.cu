@@ -457,8 +457,7 @@ __device__ __forceinline__ void warp_colmax64(const float (&v)[NC], int lane, fl
 // live in shared memory, one writer per column between barriers.
 template <class G>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
-                              uint32_t bars, uint32_t tmem, volatile int* abort_flag,
-                              volatile int* s_last) {
+                              uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
     constexpr int D = G::D;
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
@@ -529,19 +528,12 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
 
     uint32_t n = 0;                             // stages so far
     UnitCursor cur(p, pre, U);
-    // a split unit whose partials are being made: it owes its ticket arrival
-    UnitInfo owed{};
-    bool owe = false;
     while (cur.more() && !stop) {
         const UnitInfo x = cur.take(p, pre);
         const bool single = (x.g.chunks == 1);
-        owed = x;
-        owe = !single && p.tickets != nullptr;
         const int nst = (x.np + SPG - 1) / SPG;
         if (nst == 0) {
             write_empty(x, single);
-            if (owe) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
-            owe = false;
             continue;
         }
         if (tid < NC) {
@@ -726,19 +718,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             p.partial_lse[x.rc * p.Hq + x.h0 + tid] =
                 (Lt == 0.f) ? -CUDART_INF_F : (mm + log2f(Lt)) * CUDART_LN2_F;
         }
-        if (owe) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
-        owe = false;
         n += (uint32_t)nst;
-    }
-    // After an abort every remaining split unit of this CTA still arrives
-    // (its partials are undefined; the error word says so), so that the
-    // tickets return to zero.
-    if (p.tickets != nullptr) {
-        if (owe) split_arrive(p, pre, owed, D, tid, 128, 1, s_last);
-        while (cur.more()) {
-            const UnitInfo x = cur.take(p, pre);
-            if (x.g.chunks > 1) split_arrive(p, pre, x, D, tid, 128, 1, s_last);
-        }
     }
 }
 
@@ -750,7 +730,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  const __grid_constant__ CUtensorMap tmQ, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
-    __shared__ int s_last;            // the fused combine's "this arrival was the last"
     __shared__ uint32_t tmem_slot;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -802,7 +781,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     if (warp < NSW) {
-        softmax_warps<G>(p, pre, U, smem, bars, tmem, &abort_flag, &s_last);
+        softmax_warps<G>(p, pre, U, smem, bars, tmem, &abort_flag);
     } else if (warp == QK_WARP || warp == PV_WARP) {
         if (warp == QK_WARP) {
             if (lane == 0) qk_issuer<G>(p, pre, U, base, bars, tmem, &abort_flag);
@@ -876,7 +855,6 @@ static int run_mq(const DecodeArgs& a) {
     p.group = a.num_q_heads / a.num_kv_heads * S;
     p.TW = mq::NC;
     p.HG = (p.group + mq::NC - 1) / mq::NC;
-    p.tickets = fused_tickets(pl, a.workspace, p.Hkv, p.HG);
     p.window = effective_window(a.window, S);
     p.S = S;
     p.mask_window = a.window;
@@ -891,7 +869,7 @@ static int run_mq(const DecodeArgs& a) {
     const int grid = pl.grid > 0 ? pl.grid : 1;
     kern<<<grid, mq::NTHREADS, kSmem, a.stream>>>(tmK, tmV, tmQ, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
-    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE) && p.tickets == nullptr)
+    if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,
                               a.pt_stride, a.stream);
     return GA_OK;

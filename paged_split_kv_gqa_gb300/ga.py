@@ -43,10 +43,9 @@ GA_PLAN_EXTERNAL_COMBINE = 2
 GA_PLAN_TEST_WAIT_TIMEOUT = 4
 GA_PLAN_TENSOR_CORE_UNITS = 8
 GA_PLAN_COLUMN_PARALLEL_UNITS = 16
+GA_PLAN_KV_E4M3 = 32
 PAGE_SIZE = 16
 MAX_Q_LEN = 64
-TICKETS_PER_ROW = 64
-TICKET_REGION_BYTES = 2048 * TICKETS_PER_ROW * 4
 
 
 class GAError(RuntimeError):
@@ -61,7 +60,7 @@ class ga_plan(ctypes.Structure):
         "window", "page_size", "grid", "flags", "touch_stride", "q_len", "col_tile")] + [
         (n, ctypes.c_int64) for n in ("row_chunks", "units", "workspace_bytes",
                                        "partial_o_offset", "partial_lse_offset",
-                                       "touch_log_offset", "ticket_offset", "ticket_bytes")]
+                                       "touch_log_offset")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -169,12 +168,10 @@ def ga_plan_splits(seq_lens_host: Sequence[int], *, num_q_heads: int, num_kv_hea
 
 
 def workspace_for(plan: ga_plan, device=None) -> Optional[torch.Tensor]:
-    """A caller-side workspace buffer of plan.workspace_bytes (None if 0),
-    zero-filled: its leading ticket region must hold zeros before first use
-    (every decode call leaves it zeros again)."""
+    """A caller-side workspace buffer of plan.workspace_bytes (None if 0)."""
     if plan.workspace_bytes == 0:
         return None
-    return torch.zeros(int(plan.workspace_bytes), dtype=torch.uint8, device=device or "cuda")
+    return torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=device or "cuda")
 
 
 def ga_kv_append(k_new, v_new, k_pool, v_pool, page_table, positions, *, k_scale=None,

@@ -85,13 +85,9 @@ def test_multi_query_plan(ga):
     one = ga.ga_plan_splits([40, 33], **kw)
     four = ga.ga_plan_splits_mq([40, 33], q_len=4, **kw)
     assert one.q_len == 1 and four.q_len == 4
-    # the fixed ticket region first, then partial O: row_chunks x (Hq * S) x D
-    # fp32, 256-byte aligned regions
-    assert four.ticket_offset == one.ticket_offset == 0
-    assert four.ticket_bytes == one.ticket_bytes == ga.TICKET_REGION_BYTES
-    assert four.partial_o_offset == one.partial_o_offset == ga.TICKET_REGION_BYTES
-    assert four.partial_lse_offset >= (four.partial_o_offset
-                                       + four.row_chunks * 4 * 4 * 256 * 4)
+    assert four.partial_o_offset == one.partial_o_offset == 0
+    # partial O: row_chunks x (Hq * S) x D fp32, 256-byte aligned regions
+    assert four.partial_lse_offset >= four.row_chunks * 4 * 4 * 256 * 4
     # 4 queries x group 2 = 8 columns: still one head group per kv head
     assert four.units == one.units
     assert one.col_tile == four.col_tile == 8

@@ -1,12 +1,10 @@
-"""The split-KV combine fused into the decode kernels: the chunk of a (row,
-kv head) that finishes last merges the row's partials itself.  For every
-decode kernel (page-parallel bf16, E4M3 on tcgen05 at both head dims,
-column-parallel units, the tcgen05 multi-query kernel) the fused output must be
-bit-identical to the decode with an external combine plus ga_splitkv_combine
-(one arithmetic, shared), the ticket region must be zero again after the call,
-and repeated calls on one workspace must keep giving the same bits.  A plan
-whose units outnumber a row's tickets falls back to the combine kernel and
-still matches the oracle.  ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is
+"""The split-KV merge behind every decode kernel (page-parallel bf16, E4M3 on
+tcgen05 at both head dims, K == V, column-parallel units, the tcgen05
+multi-query kernel): the decode call's own merge must give the same bits as a
+decode with an external combine followed by ga_splitkv_combine, repeat calls
+must give the same bits, and both must match the oracle.  Rows with more than
+64 chunks take the merge's per-thread form; a workspace may serve plans of
+different shapes in turn.  ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is
 mandatory here": flash-decode split and merge.)"""
 import dataclasses
 import math
@@ -45,7 +43,7 @@ def _setup(case, seed=11):
     fam, S = CASES[case]
     lens = np.array([1500, 3000, 40, 1025, 16, 0, 2222, 700], dtype=np.int32)
     alloc = dataclasses.replace(fam, window=fam.window + S - 1 if fam.window else 0)
-    wl = W.Workload("fused", lens, 16, alloc, alloc)
+    wl = W.Workload("merge", lens, 16, alloc, alloc)
     fi = W.make_family_inputs(wl, alloc, device=DEV, seed=seed, poison=True,
                               release_old=fam.window > 0)
     if case.endswith("kv_alias"):
@@ -73,21 +71,17 @@ def _call(ga, fi, plan, ws, out, err):
 @pytest.mark.parametrize("split", [dict(requested_splits=3), dict(fixed_chunk_tokens=64)],
                          ids=["s3", "c64"])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_fused_equals_external_combine(ga, case, split):
+def test_internal_equals_external_combine(ga, case, split):
     fam, S, lens, fi = _setup(case)
     kw = dict(num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
               head_dim=fam.head_dim, window=fam.window, q_len=S, **split)
-    fused = ga.ga_plan_splits(lens, **kw)
+    inner = ga.ga_plan_splits(lens, **kw)
     outer = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_EXTERNAL_COMBINE, **kw)
-    assert fused.mode != ga.GA_SPLIT_NONE
+    assert inner.mode != ga.GA_SPLIT_NONE
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ws = ga.workspace_for(fused, DEV)
-    a = _call(ga, fi, fused, ws, torch.full_like(fi.q, float("nan")), err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    assert not bool(ws[:ga.TICKET_REGION_BYTES].any()), "tickets not reset"
-    # again on the same workspace (tickets reused): the same bits
-    a2 = _call(ga, fi, fused, ws, torch.full_like(fi.q, float("nan")), err)
+    ws = ga.workspace_for(inner, DEV)
+    a = _call(ga, fi, inner, ws, torch.full_like(fi.q, float("nan")), err)
+    a2 = _call(ga, fi, inner, ws, torch.full_like(fi.q, float("nan")), err)
     ws2 = ga.workspace_for(outer, DEV)
     b = _call(ga, fi, outer, ws2, torch.full_like(fi.q, float("nan")), err)
     po, plse, _ = ga.workspace_views(outer, ws2)
@@ -95,7 +89,7 @@ def test_fused_equals_external_combine(ga, case, split):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(a, a2)
-    assert torch.equal(a, b), f"{case}: fused combine differs from the external one"
+    assert torch.equal(a, b), f"{case}: the call's merge differs from the external one"
     scale = 1.0 / math.sqrt(fam.head_dim)
     if S == 1:
         ref = oracle_decode(fi)
@@ -108,10 +102,28 @@ def test_fused_equals_external_combine(ga, case, split):
     assert_close(a.float().cpu().numpy(), ref, kv_dtype=fam.kv_dtype, what=case)
 
 
+@pytest.mark.parametrize("case", ["local_bf16", "global_bf16"])
+def test_more_than_64_chunks_per_row(ga, case):
+    """16-token chunks: rows with more than 64 attended pages (up to 188 here)
+    have more chunks than the warp merge's 64 and take the per-thread merge."""
+    fam, S, lens, fi = _setup(case)
+    plan = ga.ga_plan_splits(lens, num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
+                             head_dim=fam.head_dim, window=fam.window, fixed_chunk_tokens=16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _call(ga, fi, plan, ga.workspace_for(plan, DEV), torch.full_like(fi.q, float("nan")),
+                err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    def pages(L):              # logical pages holding the attended keys of a row
+        lo = max(0, L - fam.window) if fam.window else 0
+        return (L - 1) // 16 - lo // 16 + 1 if L > 0 else 0
+    assert max(pages(int(L)) for L in lens) > 64
+    assert_close(out.float().cpu().numpy(), oracle_decode(fi), what=case)
+
+
 def test_workspace_shared_by_plans_of_different_shapes(ga):
     """One workspace serves a local and a global plan in turn (different
-    batch sizes and head counts): the tickets sit in the same fixed region,
-    no plan's partials land on them, and every call matches the oracle."""
+    batch sizes and head counts); every call matches the oracle."""
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     cases = []
     for case, lens in (("local_bf16", [1500, 3000, 40, 1025]),
@@ -125,7 +137,7 @@ def test_workspace_shared_by_plans_of_different_shapes(ga):
                                  num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                                  window=fam.window, requested_splits=4)
         cases.append((fi, plan))
-    ws = torch.zeros(max(p.workspace_bytes for _, p in cases), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(max(p.workspace_bytes for _, p in cases), dtype=torch.uint8, device=DEV)
     for rnd in range(2):
         for fi, plan in cases:
             out = _call(ga, fi, plan, ws, torch.full_like(fi.q, float("nan")), err)
@@ -133,23 +145,3 @@ def test_workspace_shared_by_plans_of_different_shapes(ga):
             assert int(err.item()) == 0
             assert_close(out.float().cpu().numpy(), oracle_decode(fi),
                          what=f"{fi.family.name} round {rnd}")
-    assert not bool(ws[:ga.TICKET_REGION_BYTES].any())
-
-
-def test_more_unit_columns_than_tickets_falls_back(ga):
-    """128 kv heads (group 1): 128 unit columns per row exceed the 64 tickets
-    of a row, so the call merges with the combine kernel instead."""
-    fam = W.Family("local", 128, 128, 256, 64)
-    lens = np.array([200, 77, 130], dtype=np.int32)
-    wl = W.Workload("wide", lens, 16, fam, fam)
-    fi = W.make_family_inputs(wl, fam, device=DEV, seed=4, poison=True)
-    plan = ga.ga_plan_splits(lens, num_q_heads=128, num_kv_heads=128, head_dim=256, window=64,
-                             requested_splits=2)
-    assert plan.num_kv_heads * 1 > ga.TICKETS_PER_ROW
-    err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ws = ga.workspace_for(plan, DEV)
-    out = _call(ga, fi, plan, ws, torch.full_like(fi.q, float("nan")), err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    assert not bool(ws[:ga.TICKET_REGION_BYTES].any())
-    assert_close(out.float().cpu().numpy(), oracle_decode(fi), what="fallback")

@@ -150,3 +150,17 @@ def test_multi_query_plan_properties(ga, seed):
         assert p.partial_lse_offset >= p.partial_o_offset + rc * g * Hkv * S * D * 4
         assert p.partial_o_offset % 256 == 0 and p.partial_lse_offset % 256 == 0
         assert p.workspace_bytes >= p.partial_lse_offset + rc * g * Hkv * S * 4
+
+
+def test_units_span_several_kv_heads(ga):
+    """The planner counts units of 8 / group kv heads with the flag."""
+    lens = [3000] * 8
+    kw = dict(num_q_heads=32, num_kv_heads=16, head_dim=256, window=1024, num_sms=152,
+              requested_splits=1)
+    one = ga.ga_plan_splits(lens, **kw)
+    four = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw)
+    assert one.units == 8 * 16 and four.units == 8 * 4
+    kw.update(num_q_heads=64)                                   # group 4: two kv heads
+    assert ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw).units == 8 * 8
+    kw.update(num_q_heads=16)                                   # group 1: one
+    assert ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw).units == 8 * 16

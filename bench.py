@@ -44,10 +44,17 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+# The sources a bf16 decode launch's DRAM traffic depends on: the kernel, the
+# headers it includes, and the host code that encodes its tensor maps and
+# makes its plan.
+DECODE_SOURCES = ("ga_api.cu", "ga_decode.cu", "ga_decode_common.cuh", "ga_device.cuh",
+                  "ga_geometry.h")
+
+
+def kernel_source_hash(files=DECODE_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_split_kv_gqa_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(files):
         with open(os.path.join(csrc, fn), "rb") as fh:
             h.update(fn.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -422,6 +429,48 @@ def l2_claim(schedule):
             f"reads (< {L2_BYTES / 1e6:.0f} MB L2); L2 hits possible")
 
 
+def one_page_rows_ms(ga, layer, err, device, reps=21):
+    """The fixed part of a decode launch of this family: the same decode call
+    (batch, heads, pools, table, a plan made the same way; the combine is
+    timed apart, as for the family's own figure) with every row cut to one
+    page (16 keys), median of `reps` launches timed with CUDA events.  The
+    family's launch time minus this is the time spent streaming its KV."""
+    import torch
+    fi, fam, plan = layer["fi"], layer["fam"], layer["plan"]
+    B = fi.seq_lens.numel()
+    S = plan.q_len
+    lens = torch.full((B,), max(16, S), dtype=torch.int32, device=device)
+    p16 = ga.ga_plan_splits([max(16, S)] * B, num_q_heads=fam.num_q_heads,
+                            num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
+                            window=fam.window, flags=plan.flags, q_len=S)
+    ws = ga.workspace_for(p16, device)
+    out = torch.empty_like(layer["out"])
+    kw = dict(scale=layer["scale"], plan=p16, workspace=ws, out=out, k_scale=fi.k_scale,
+              v_scale=fi.v_scale, err_word=err)
+
+    def call():
+        if fam.window > 0:
+            ga.ga_decode_local_hd256(layer["q"], fi.k_pool, fi.v_pool, fi.page_table, lens,
+                                     window=fam.window, **kw)
+        else:
+            ga.ga_decode_global_hd512(layer["q"], fi.k_pool, fi.v_pool, fi.page_table, lens,
+                                      **kw)
+
+    for _ in range(3):
+        call()
+    ts = []
+    for _ in range(reps):
+        if hasattr(torch.cuda, "_sleep"):     # the host enqueues ahead of the GPU
+            torch.cuda._sleep(1_000_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sorted(ts)[len(ts) // 2]
+
+
 def run_ga(args):
     import torch
     from paged_split_kv_gqa_gb300 import ga
@@ -514,6 +563,8 @@ def run_ga(args):
             "algorithmic_bytes_per_launch": fam_bytes[name] // fam_n[name],
             "attended_kv_tokens_per_s_per_layer": fam_keys[name] / t,
             "kv_dtype": "e4m3" if sets[name][0]["fam"].kv_dtype else "bf16"}
+    for name in families:
+        families[name]["one_page_rows_ms"] = one_page_rows_ms(ga, sets[name][0], err, device)
     dominant = max(fam_ms, key=fam_ms.get)
     step_bytes = sum(layer["bytes"] + layer["append_bytes"] for layer in schedule)
     value = step_bytes * args.steps * world / elapsed / 1e9

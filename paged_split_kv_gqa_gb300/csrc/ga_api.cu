@@ -92,6 +92,27 @@ int encode_heads_map(CUtensorMap* map, const void* pool, int32_t region, int32_t
     return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
 }
 
+// A bf16 pool [num_pages, Hkv, 16, D] seen as the 5-D tensor (element e < 64
+// of a 128-byte row chunk, key % 8, 64-dim region, key / 8, page-head block)
+// with byte strides (2, 2 D, 128, 16 D, 32 D).  One box {64, 8, 2, 2, 1} is a
+// 128-dim block (two 64-dim regions) of one page-head block, 4 KB, and lands
+// as [key / 8][region][key % 8] rows of 128 bytes (128-byte swizzle): each
+// region's keys in groups of 8 rows, 16 rows apart.
+int encode_kblock_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int32_t head_dim) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return GA_ERR_CUDA;
+    const cuuint64_t D = (cuuint64_t)head_dim;
+    const cuuint64_t dims[5] = {64, 8, D / 64, 2, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[4] = {2 * D, 128, 16 * D, 32 * D};
+    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
+}
+
 int ensure_smem_attr(const void* func, int bytes, int slot) {
     static std::atomic<uint64_t> done[32];
     int dev = 0;

@@ -27,10 +27,12 @@
 // (D / 128 blocks) and the sums, 64 columns each: 448 of 512 at hd512.
 // Columns as M would need O = 128 x 512 fp32, all of TMEM, at hd512.
 //
-// Shared memory.  K: a ring of 32 KB slots, each one 128-dim block of a stage
-// as two [128 keys][128 B] regions, filled by one 2 KB bulk tensor copy per
-// page and region (the QK product wants the stage's 128 keys at one row
-// stride).  V: a ring of 32 KB slots of whole page-head blocks
+// Shared memory.  K: a ring of 32 KB slots, each one 128-dim block of a stage,
+// filled by one 4 KB bulk tensor copy per page that lands as [key / 8][64-dim
+// region][key % 8] rows: each region's 8-key groups then sit 2 KB apart in
+// key order over the stage's 8 pages, the uniform stride the QK product's
+// operand needs (two copies per page and region with [128 keys][128 B]
+// regions cost the producer twice the copies).  V: a ring of 32 KB slots of whole page-head blocks
 // ([page][D / 64 regions][16 keys][128 B]), one copy per page: the PV product
 // takes one page per instruction, so a block's layout serves it as it lands.
 // q of the unit as [D / 64][64 rows][128 B] (one copy per region; two
@@ -62,8 +64,7 @@ namespace mq {
 constexpr int NC = kTcColTile;                    // columns per unit: N of every product
 constexpr int KEYS = 128;                         // keys per stage: M of the QK product
 constexpr int SPG = KEYS / kPageSize;             // pages per stage
-constexpr int REGION_BYTES = KEYS * 128;          // K: [128 keys][64 dims] bf16
-constexpr int SLOT_BYTES = 2 * REGION_BYTES;      // a K or V slot
+constexpr int SLOT_BYTES = 2 * KEYS * 128;        // a K or V slot: 128 keys x 128 dims bf16
 constexpr int QREG_BYTES = NC * 128;              // [64 columns][64 dims] bf16
 constexpr int PREG_BYTES = NC * 128;              // [64 columns][64 keys] bf16
 constexpr int P_BYTES = 2 * PREG_BYTES;           // P^T of a stage
@@ -223,14 +224,13 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
                 const uint32_t fb = bar(bars, B_FULLB + (int)slot);
                 const uint32_t dst0 = base + OFF + slot * SLOT_BYTES;
                 if (IS_K) {
-                    // 128-dim block j of every page: regions 2j, 2j + 1
+                    // 128-dim block j of every page (regions 2j, 2j + 1) as one
+                    // 4 KB box: page pl fills rows 32 pl .. 32 pl + 31 of the slot
                     if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(gm) * 2u * 2048u);
                     __syncwarp();
-                    if (good) {
-                        const uint32_t dst = dst0 + (uint32_t)pl * 2048u;
-                        tma_load_3d(dst, tm, fb, 0, y, 2 * j, pol);
-                        tma_load_3d(dst + REGION_BYTES, tm, fb, 0, y, 2 * j + 1, pol);
-                    }
+                    if (good)
+                        tma_load_5d(dst0 + (uint32_t)pl * 4096u, tm, fb, 0, 0, 2 * j, 0,
+                                    y / kPageSize, pol);
                 } else {
                     // pages PPS j .. PPS j + PPS - 1, whole page-head blocks
                     const uint32_t sm = (gm >> (G::PPS * j)) & ((1u << G::PPS) - 1u);
@@ -296,12 +296,13 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                 }
                 tc_fence_after();
                 const uint32_t ka = base + G::OFF_K + slot * SLOT_BYTES;
+                // region r of the slot: 8-key groups 2 KB apart, starting at r KB
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_bf16(tmem + TM_S + NC * sb,
-                                    smem_desc_sw128(ka + r * REGION_BYTES + 32 * kk, 16, 1024),
+                                    smem_desc_sw128(ka + r * 1024 + 32 * kk, 16, 2048),
                                     smem_desc_sw128(qa + (2 * c + r) * QREG_BYTES + 32 * kk, 16, 1024),
                                     IQK, (c | r | kk) != 0 ? 1u : 0u);
                 tc_commit(bar(bars, B_KEMPTY + (int)slot));     // the K slot may be refilled
@@ -821,11 +822,11 @@ static int run_mq(const DecodeArgs& a) {
     int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmem, D == 256 ? 20 : 21);
     if (rc != GA_OK) return rc;
     const int64_t rows = a.num_pages * a.num_kv_heads * (int64_t)kPageSize;
-    // K: one box = one 64-dim region of a page-head block ([16 keys][128 B]);
-    // V: one box = a whole page-head block; q: one 64-dim region of a unit's
-    // 64 rows
+    // K: one box = one 128-dim block of a page-head block ([key / 8][64-dim
+    // region][key % 8], 4 KB); V: one box = a whole page-head block; q: one
+    // 64-dim region of a unit's 64 rows
     CUtensorMap tmK, tmV, tmQ;
-    rc = encode_rows_map(&tmK, a.k_pool, GA_KV_BF16, rows, D, kPageSize, 1);
+    rc = encode_kblock_map(&tmK, a.k_pool, a.num_pages * a.num_kv_heads, D);
     if (rc != GA_OK) return rc;
     rc = encode_rows_map(&tmV, a.v_pool, GA_KV_BF16, rows, D, kPageSize, 0);
     if (rc != GA_OK) return rc;

@@ -24,9 +24,12 @@ struct CombineParams {
     int32_t B, Hq, D, window, mode, splits, chunk_pages;
 };
 
-// One CTA of 4 warps per (4 merge tasks, row); a task is one column's
-// 128-dim block, taken by one warp (merge_warp128).
-constexpr int kCombineWarps = 4;
+// One CTA of 8 warps per (16 merge tasks, row); a task is one column's
+// 128-dim block, taken by one warp (merge_warp128).  Every CTA finds its row's
+// first row-chunk from the lengths of the rows before it (a strided sum over
+// the CTA's 256 threads), so wider CTAs repeat that O(B) work less often.
+constexpr int kCombineWarps = 8;
+constexpr int kTasksPerCta = 16;
 
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const CombineParams p) {
     const int b = blockIdx.y;
@@ -51,12 +54,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
         return;
     }
     const int nb = p.D / 128;
-    const int t = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-    if (t >= p.Hq * nb) return;
-    const int h = t / nb, d0 = (t % nb) * 128;
-    const uint2 o = merge_warp128(p.po, p.plse, rc0, S, p.Hq, p.D, h, d0);
-    *reinterpret_cast<uint2*>(p.out + ((int64_t)b * p.Hq + h) * p.D + d0 +
-                              4 * (threadIdx.x & 31)) = o;
+    for (int t = blockIdx.x * kTasksPerCta + (threadIdx.x >> 5);
+         t < min(p.Hq * nb, (int)(blockIdx.x + 1) * kTasksPerCta); t += kCombineWarps) {
+        const int h = t / nb, d0 = (t % nb) * 128;
+        const uint2 o = merge_warp128(p.po, p.plse, rc0, S, p.Hq, p.D, h, d0);
+        *reinterpret_cast<uint2*>(p.out + ((int64_t)b * p.Hq + h) * p.D + d0 +
+                                  4 * (threadIdx.x & 31)) = o;
+    }
 }
 
 int launch_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,
@@ -81,7 +85,7 @@ int launch_combine(const float* partial_o, const float* partial_lse, const ga_pl
     p.chunk_pages = plan->chunk_pages;
     if (p.B == 0) return GA_OK;
     const int tasks = p.Hq * (p.D / 128);
-    dim3 grid((tasks + kCombineWarps - 1) / kCombineWarps, p.B);
+    dim3 grid((tasks + kTasksPerCta - 1) / kTasksPerCta, p.B);
     combine_kernel<<<grid, 32 * kCombineWarps, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? GA_OK : GA_ERR_CUDA;
 }

@@ -364,6 +364,65 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def workload_text(args):
+    text = WORKLOAD_TEXT[args.workload]
+    if args.rows:
+        text += f" -- PROFILING SUBSET: first {args.rows} rows"
+    if args.workload == "ragged":
+        text += f"; {args.pools} distinct pools per family rotated over the layers"
+    if args.kv_alias:
+        text += "; global family with K == V (one pool, read once)"
+    if args.fp8 != "none":
+        text += f"; {args.fp8} family KV stored as fp8-e4m3 with per-head scales"
+    if args.splits:
+        text += f"; split-KV count fixed at {args.splits} chunks per row"
+    if args.q_len > 1:
+        text += (f"; {args.q_len} query tokens per row at its last positions (causal "
+                 f"within the chunk), {args.q_len} appends per row and layer")
+    if args.mq_units != "auto":
+        text += {"tc": "; tcgen05 units of 64 columns forced",
+                 "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
+    return text
+
+
+def host_schedule(args, wl):
+    """The step's layers as the bench runs them, with each layer's algorithmic
+    decode bytes, computed on the host (the same object for a layer that is
+    repeated, as the bench's rotated pools are)."""
+    from paged_split_kv_gqa_gb300 import metrics as M
+    from paged_split_kv_gqa_gb300 import workloads as W
+
+    def layer(fam):
+        esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
+        return {"bytes": M.decode_bytes(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                                        num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
+                                        window=fam.window, page_size=wl.page_size,
+                                        kv_bytes_per_elem=esz,
+                                        kv_alias=args.kv_alias and fam.window == 0,
+                                        q_len=args.q_len)}
+    if args.workload != "ragged":
+        return [layer(wl.local), layer(wl.global_)]
+    loc = [layer(wl.local) for _ in range(args.pools)]
+    glo = [layer(wl.global_) for _ in range(args.pools)]
+    schedule, nl, ng = [], 0, 0
+    per = wl.local_layers // wl.global_layers
+    for _ in range(wl.global_layers):
+        for _ in range(per):
+            schedule.append(loc[nl % args.pools])
+            nl += 1
+        schedule.append(glo[ng % args.pools])
+        ng += 1
+    return schedule
+
+
+def line_config(args, wl, world):
+    """The `config` of the JSON line, the same for the GPU arm and the
+    reference arm: the workload, the whole-job batch and what keeps each timed
+    repetition reading from HBM."""
+    return {"workload": workload_text(args), "global_batch": wl.batch * world,
+            "l2": l2_claim(host_schedule(args, wl))}
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle as it stands on the host cores."""
     rank, _, world = dist_env()
@@ -371,6 +430,11 @@ def run_reference(args):
         return
     from oracle import oracle as O
     nrows = 2
+    wl = workload_config(args.workload, args.seed, args.fp8)
+    if args.rows:
+        from paged_split_kv_gqa_gb300 import workloads as W
+        wl = W.Workload(wl.name, wl.seq_lens[:args.rows].copy(), wl.page_size, wl.local,
+                        wl.global_, wl.local_layers, wl.global_layers)
     fams, nbytes = cpu_sample_inputs(args.seed, nrows, args.workload, args.fp8)
     for _ in range(args.warmup):
         oracle_sample(fams)
@@ -384,7 +448,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload} decode, sampled rows", "batch": nrows},
+            "config": line_config(args, wl, world),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -757,36 +821,15 @@ def run_ga(args):
                     "chunk_pages": p.chunk_pages, "col_tile": p.col_tile,
                     "units": p.units, "grid": p.grid}
 
-        text = WORKLOAD_TEXT[args.workload]
-        if args.rows:
-            text += f" -- PROFILING SUBSET: first {args.rows} rows"
-        if args.workload == "ragged":
-            text += f"; {args.pools} distinct pools per family rotated over the layers"
-        if args.kv_alias:
-            text += "; global family with K == V (one pool, read once)"
-        if args.fp8 != "none":
-            text += f"; {args.fp8} family KV stored as fp8-e4m3 with per-head scales"
-        if args.splits:
-            text += f"; split-KV count fixed at {args.splits} chunks per row"
-        if args.q_len > 1:
-            text += (f"; {args.q_len} query tokens per row at its last positions (causal "
-                     f"within the chunk), {args.q_len} appends per row and layer")
-        if args.mq_units != "auto":
-            text += {"tc": "; tcgen05 units of 64 columns forced",
-                     "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": text,
-                "global_batch": wl.batch * world,
-                "step": f"{len(schedule)} layers, each append+decode(+combine)"
-                        + ("" if args.eager else "; captured in one CUDA graph, replayed"),
-                "l2": l2_claim(schedule),
-                "plans": {n: plan_desc(layers[0]["plan"]) for n, layers in sets.items()},
-            },
+            "config": line_config(args, wl, world),
+            "step": f"{len(schedule)} layers, each append+decode(+combine)"
+                    + ("" if args.eager else "; captured in one CUDA graph, replayed"),
+            "plans": {n: plan_desc(layers[0]["plan"]) for n, layers in sets.items()},
             "pct_of_peak": {"measured": value / peak, "nominal_8TBs": value / NOMINAL_HBM_GBS},
             "families": families,
             "roofline": {"kernel": f"{kname} (decode kernel, combine excluded)",

@@ -24,12 +24,14 @@ struct CombineParams {
     int32_t B, Hq, D, window, mode, splits, chunk_pages;
 };
 
-// One CTA of 8 warps per (16 merge tasks, row); a task is one column's
-// 128-dim block, taken by one warp (merge_warp128).  Every CTA finds its row's
-// first row-chunk from the lengths of the rows before it (a strided sum over
-// the CTA's 256 threads), so wider CTAs repeat that O(B) work less often.
-constexpr int kCombineWarps = 8;
-constexpr int kTasksPerCta = 16;
+// One CTA of 4 warps per (4 merge tasks, row); a task is one column's 128-dim
+// block, taken by one warp (merge_warp128).  Every CTA finds its row's first
+// row-chunk from the lengths of the rows before it (a strided sum over its 128
+// threads).  Wider CTAs (8 warps, 16 tasks) repeat that O(B) sum less often
+// but serialise the merges of small batches: the ragged 60-layer step at
+// B = 1 took 1.108 ms with them against 0.834 ms with these.
+constexpr int kCombineWarps = 4;
+constexpr int kTasksPerCta = 4;
 
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const CombineParams p) {
     const int b = blockIdx.y;

@@ -131,3 +131,21 @@ def test_31b_sampled(ga, err, split):
                  kv_dtype=1, what=f"31B local E4M3 4-head units {split}")
     del fi
     torch.cuda.empty_cache()
+
+
+def test_ragged_sampled(ga, err):
+    """The ragged 256-row batch (lognormal lengths, E4M3 sliding family) in the
+    launch configuration the bench times: a plan made with GA_PLAN_KV_E4M3."""
+    wl = W.config(5)
+    fam = wl.local
+    assert fam.kv_dtype == W.KV_E4M3
+    fi = W.make_family_inputs(wl, fam, device=DEV, poison=True, release_old=True)
+    plan = _plan(ga, fi)
+    out = run_decode(ga, fi, plan, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = W.sample_rows(wl.batch, 16)
+    assert_close(out[rows].float().cpu().numpy(), oracle_decode_rows_gathered(fi, rows),
+                 kv_dtype=1, what="ragged local E4M3 4-head units")
+    del fi
+    torch.cuda.empty_cache()

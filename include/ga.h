@@ -106,15 +106,18 @@ enum {
                                       Neither flag: 64-column units from 32 columns per kv
                                       head at head_dim 512 and from 64 at head_dim 256
                                       (where each is the faster on GB300), else 32. */
-    GA_PLAN_KV_E4M3 = 32          /* the plan is for E4M3 pools.  On the sliding family
-                                      (head_dim 256, one query per row) with 2 or 4 query
-                                      heads per kv head and Hkv a multiple of 8 / group, a
-                                      work unit then spans 8 / group kv heads: the decode
-                                      copies a page's blocks of those heads as one box per
-                                      128-dim region, and the planner's cost model counts
-                                      such units.  Results do not depend on it; a plan made
-                                      without it also serves E4M3 pools (one kv head per
-                                      unit), and the flag is ignored for bf16 pools. */
+    GA_PLAN_KV_E4M3 = 32          /* the plan is for E4M3 pools: the cost model weighs an
+                                      E4M3 page at half a bf16 one, and on the sliding family
+                                      (head_dim 256, one query per row, 2 or 4 query heads per
+                                      kv head, Hkv a multiple of 8 / group) the planner may
+                                      give a work unit 8 / group kv heads (kv_heads_per_unit),
+                                      whose pages the decode then copies as one box per
+                                      128-dim region for all of them: it does so when the
+                                      one-head plan needs no split and the wider units alone
+                                      fill at least four rounds of the SMs (fewer, larger units
+                                      measured slower below that).  Results do not depend on
+                                      it; a plan made without it also serves E4M3 pools, and
+                                      bf16 pools ignore it. */
 };
 
 /*
@@ -145,6 +148,11 @@ typedef struct ga_plan {
     int64_t partial_o_offset;    /* byte offsets inside the workspace */
     int64_t partial_lse_offset;
     int64_t touch_log_offset;
+    int32_t kv_heads_per_unit;   /* kv heads per work unit of the E4M3 sliding-family decode:
+                                    1, or 8 / group when the plan has GA_PLAN_KV_E4M3 and the
+                                    planner found such units better (see that flag).  A caller
+                                    may set it to 1 or to that value; other kernels ignore it. */
+    int32_t reserved;            /* 0 */
 } ga_plan;
 
 /*

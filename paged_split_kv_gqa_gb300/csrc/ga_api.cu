@@ -92,24 +92,29 @@ int encode_heads_map(CUtensorMap* map, const void* pool, int32_t region, int32_t
     return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
 }
 
-// A bf16 pool [num_pages, Hkv, 16, D] seen as the 5-D tensor (element e < 64
-// of a 128-byte row chunk, key % 8, 64-dim region, key / 8, page-head block)
-// with byte strides (2, 2 D, 128, 16 D, 32 D).  One box {64, 8, 2, 2, 1} is a
-// 128-dim block (two 64-dim regions) of one page-head block, 4 KB, and lands
-// as [key / 8][region][key % 8] rows of 128 bytes (128-byte swizzle): each
-// region's keys in groups of 8 rows, 16 rows apart.
-int encode_kblock_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int32_t head_dim) {
+// A pool [num_pages, Hkv, 16, D] (bf16 or E4M3 codes) seen as the 5-D tensor
+// (element e of a 128-byte row chunk, key % 8, 128-byte region of the head
+// dim, key / 8, page-head block) with byte strides (esize, D esize, 128,
+// 8 D esize, 16 D esize).  One box {128 / esize, 8, box_regions, 2, 1} covers
+// box_regions consecutive regions of one page-head block and lands as
+// [key / 8][region][key % 8] rows of 128 bytes (128-byte swizzle): each
+// region's keys in groups of 8 rows, 8 box_regions rows apart.
+int encode_region_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_t num_blocks,
+                      int32_t head_dim, int32_t box_regions) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return GA_ERR_CUDA;
-    const cuuint64_t D = (cuuint64_t)head_dim;
-    const cuuint64_t dims[5] = {64, 8, D / 64, 2, (cuuint64_t)num_blocks};
-    const cuuint64_t strides[4] = {2 * D, 128, 16 * D, 32 * D};
-    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    const cuuint64_t esz = kv_dtype == GA_KV_BF16 ? 2 : 1;
+    const cuuint64_t row = (cuuint64_t)head_dim * esz;        // bytes per key row
+    const cuuint64_t dims[5] = {128 / esz, 8, row / 128, 2, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[4] = {row, 128, 8 * row, 16 * row};
+    const cuuint32_t box[5] = {(cuuint32_t)(128 / esz), 8, (cuuint32_t)box_regions, 2, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool),
-                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = enc(map,
+                           kv_dtype == GA_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                           5, const_cast<void*>(pool), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GA_OK : GA_ERR_CUDA;
 }
 
@@ -255,10 +260,8 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     const bool tc = (flags & GA_PLAN_TENSOR_CORE_UNITS) ||
                     (!(flags & GA_PLAN_COLUMN_PARALLEL_UNITS) && cols >= tc_min_cols(head_dim));
     const int32_t tw = cols <= kHeadTile ? kHeadTile : tc ? kTcColTile : 4 * kHeadTile;
-    const int32_t hp = tc_heads_per_unit(flags, head_dim, q_len, num_q_heads / num_kv_heads,
-                                         num_kv_heads);
     PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len,
-                 hp > 1 ? kHeadTile : tw, hp, (flags & GA_PLAN_KV_E4M3) ? 0.5 : 1.0};
+                 tw, 1, (flags & GA_PLAN_KV_E4M3) ? 0.5 : 1.0};
     Candidate best;
     if (requested_splits == 1) {
         best = Candidate{kSplitNone, 0, 0};
@@ -283,7 +286,23 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
             if (c.cost < best.cost * 0.98) best = c;
         }
     }
+    // E4M3 sliding family: units of several kv heads when the one-head plan
+    // needs no split and the wider units alone fill at least four rounds of
+    // the SMs (measured on the ragged 256-row batch: 4-head units 5884 vs 5580
+    // GB/s; on 128 rows, 31B or 12B batches, or whenever they forced a split,
+    // they were slower)
+    int32_t hp = 1;
+    const int32_t hp_rule = tc_heads_per_unit(flags, head_dim, q_len,
+                                              num_q_heads / num_kv_heads, num_kv_heads);
+    if (hp_rule > 1 && best.mode == kSplitNone &&
+        best.row_chunks * (num_kv_heads / hp_rule) >= 4 * (int64_t)num_sms) {
+        hp = hp_rule;
+        in.HP = hp;
+        in.TW = kHeadTile;
+        evaluate(in, best);
+    }
     ga_plan p{};
+    p.kv_heads_per_unit = hp;
     p.mode = best.mode;
     p.splits = best.splits;
     p.chunk_pages = best.chunk_pages;
@@ -369,6 +388,12 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
         if (!workspace || !aligned16(workspace)) return GA_ERR_INVALID_ARG;
         if ((int64_t)workspace_bytes < plan->workspace_bytes) return GA_ERR_WORKSPACE_TOO_SMALL;
     }
+    // kv heads per unit: 0 or 1, or the wider units the geometry allows
+    if (plan->kv_heads_per_unit > 1 &&
+        plan->kv_heads_per_unit != tc_heads_per_unit(plan->flags, head_dim, plan->q_len,
+                                                     num_q_heads / num_kv_heads, num_kv_heads))
+        return GA_ERR_INVALID_ARG;
+    if (plan->kv_heads_per_unit < 0) return GA_ERR_INVALID_ARG;
     DecodeArgs a{q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride, seq_lens,
                  batch, num_q_heads, num_kv_heads, head_dim, window, num_pages, scale, plan,
                  workspace, out, err_word, reinterpret_cast<cudaStream_t>(stream)};

@@ -15,12 +15,13 @@
 // pool ("Gemma 4 31B on vLLM -- operating-point reference": an FP8 KV cache
 // covers every layer).
 //
-// Layout of one superstage in shared memory: a K slot and a V slot of 32 KB,
-// each D/128 regions (one per 128 dims), each a dense [keys][128 bytes] tile
-// with the 128-byte swizzle.  Page i of the superstage fills rows 16i ..
-// 16i+15 of each region (one 2 KB bulk tensor copy per page and region), so
-// the key rows of the superstage's pages sit at one uniform stride and a
-// single MMA descriptor spans them.  K and V slots are separate rings: a K
+// Layout of one superstage in shared memory: a K slot and a V slot of 32 KB.
+// Each page-head block arrives as one bulk tensor copy (a 5-D box over all of
+// its 128-byte regions) that lands as [key / 8][region][key % 8] rows of 128
+// bytes with the 128-byte swizzle, page i of the superstage at 16 D i bytes:
+// every region's 8-key groups then sit at one uniform stride (1 KB x D/128) in
+// key order, so a single MMA descriptor per region spans the superstage's
+// scattered pages.  K and V slots are separate rings: a K
 // slot is free again as soon as its QK product has run, a V slot only after
 // the softmax and the PV product, so V gets more slots (2 K + 4 V in 192 KB
 // keep the copy engine busy).  With one pool for K and V (same pointer) each
@@ -120,6 +121,23 @@ struct Geo {
                                                                 : 512;
     static constexpr int PV_STEPS = HP > 1 ? 4 / HP : 0;  // K = 32 products per head and region
     static_assert(HP == 1 || (D == 256 && !ALIAS && (HP == 2 || HP == 4)), "heads per unit");
+    // HP == 1: a page-head block arrives as one box over all its regions and
+    // lands as [key / 8][region][key % 8] rows, page i at BLOCK_BYTES i: each
+    // region's 8-key groups then sit 1 KB x NCH apart, in key order, starting
+    // 1 KB x region into the slot.  HP > 1: region tiles CHUNK_BYTES apart, 8-row
+    // groups 1 KB apart (rows in [key / 8][head][key % 8] order).
+    static constexpr bool ILV = HP == 1;
+    // where page i of a superstage starts in a slot: a whole block (HP == 1) or
+    // its 16 HP rows of each region tile (HP > 1)
+    static constexpr uint32_t PAGE_OFF = ILV ? BLOCK_BYTES : PAGE_ROWS * 128;
+    static_assert(SSP * PAGE_OFF == (ILV ? SLOT_BYTES : CHUNK_BYTES), "pages fill a slot");
+    static constexpr uint32_t REGION_OFF = ILV ? 1024 : CHUNK_BYTES;   // region c at c x this
+    static constexpr uint32_t GROUP_STRIDE = ILV ? 1024 * NCH : 1024;  // QK operand SBO
+    // byte offset in a slot of operand row r (the superstage's key r, HP == 1) of region c
+    static __device__ __forceinline__ uint32_t row_off(int c, int r) {
+        return (uint32_t)c * REGION_OFF + (uint32_t)(r >> 3) * GROUP_STRIDE +
+               (uint32_t)(r & 7) * 128u;
+    }
     static constexpr int OFF_RING = 0;                    // K slots, then V slots
     static constexpr int OFF_VRING = ALIAS ? OFF_RING : OFF_RING + NKS * SLOT_BYTES;
     static constexpr int OFF_Q = OFF_RING + (NKS + NVS) * SLOT_BYTES;
@@ -248,9 +266,9 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
             }
             __syncwarp();
             if (good) {
-                const uint32_t kd = ring + kslot * G::SLOT_BYTES + (uint32_t)lane * (G::PAGE_ROWS * 128);
+                const uint32_t kd = ring + kslot * G::SLOT_BYTES + (uint32_t)lane * G::PAGE_OFF;
                 const uint32_t vd = ring + (uint32_t)G::OFF_VRING + vslot * G::SLOT_BYTES +
-                                    (uint32_t)lane * (G::PAGE_ROWS * 128);
+                                    (uint32_t)lane * G::PAGE_OFF;
                 if constexpr (G::HP > 1) {
                     // one box per region: the page's rows of the unit's HP kv heads
                     static_assert(G::NCH == 2, "one 5-D map per 128-byte region");
@@ -260,14 +278,10 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
                     tma_load_5d(vd, tmV, vfull, 0, 0, h0, 0, pid, policy);
                     tma_load_5d(vd + G::CHUNK_BYTES, tmV1, vfull, 0, 0, h0, 0, pid, policy);
                 } else {
-                    if (!G::ALIAS) {
-#pragma unroll
-                        for (int c = 0; c < G::NCH; ++c)
-                            tma_load_3d(kd + c * G::CHUNK_BYTES, tmK, kfull, 0, y, c, policy);
-                    }
-#pragma unroll
-                    for (int c = 0; c < G::NCH; ++c)
-                        tma_load_3d(vd + c * G::CHUNK_BYTES, tmV, vfull, 0, y, c, policy);
+                    // one box per page-head block over all its regions
+                    const int32_t blk = y / kPageSize;
+                    if (!G::ALIAS) tma_load_5d(kd, tmK, kfull, 0, 0, 0, 0, blk, policy);
+                    tma_load_5d(vd, tmV, vfull, 0, 0, 0, 0, blk, policy);
                 }
             } else if (present) {
                 report(p.err_word, valid_id ? kErrSelfCheck : kErrPageId);
@@ -334,7 +348,8 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_e4m3(tmem + TM_S + 16 * sb,
-                                smem_desc_sw128(ka + c * G::CHUNK_BYTES + 32 * kk, 16, 1024),
+                                smem_desc_sw128(ka + c * G::REGION_OFF + 32 * kk, 16,
+                                                G::GROUP_STRIDE),
                                 smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
                                 (c | kk) != 0 ? 1u : 0u);
             tc_commit(bar(bars, B_SFULL + (int)sb));
@@ -397,9 +412,12 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                 for (int c = 0; c < G::NCH; ++c) {
                     const uint32_t d = tmem + TM_O + G::O_COLS * ob + 16 * c;
                     const uint32_t va =
-                        ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::CHUNK_BYTES;
+                        ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::REGION_OFF;
+                    // 32 keys per product: 4 groups of 8, GROUP_STRIDE apart
                     for (int ks = 0; ks < nks; ++ks)
-                        tc_mma_e4m3(d, smem_desc_sw128(va + 4096 * ks, G::CHUNK_BYTES, 1024),
+                        tc_mma_e4m3(d,
+                                    smem_desc_sw128(va + 4 * G::GROUP_STRIDE * ks, G::CHUNK_BYTES,
+                                                    G::GROUP_STRIDE),
                                     smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024),
                                     IPV, (s == 0 && ks == 0) ? 0u : 1u);
                 }
@@ -733,7 +751,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
 #pragma unroll
                 for (int c = 0; c < G::NCH; ++c) {
                     uint4* vr = reinterpret_cast<uint4*>(ring + G::OFF_VRING + slot * G::SLOT_BYTES +
-                                                         c * G::CHUNK_BYTES + kss * 128);
+                                                         G::row_off(c, kss));
 #pragma unroll
                     for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -947,10 +965,11 @@ static int run_tc(const DecodeArgs& a) {
             rc = encode_heads_map(&tmV1, a.v_pool, 1, a.num_kv_heads, a.num_pages, a.head_dim, HP);
         if (rc != GA_OK) return rc;
     } else {
-        // one box = one 128-dim region of a page-head block: [16 keys][128 B]
-        rc = encode_rows_map(&tmK, a.k_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
+        // one box = a whole page-head block, [key / 8][128-dim region][key % 8]
+        const int64_t blocks = a.num_pages * a.num_kv_heads;
+        rc = encode_region_map(&tmK, a.k_pool, a.kv_dtype, blocks, a.head_dim, D / 128);
         if (rc != GA_OK) return rc;
-        rc = encode_rows_map(&tmV, a.v_pool, a.kv_dtype, rows, a.head_dim, kPageSize, 1);
+        rc = encode_region_map(&tmV, a.v_pool, a.kv_dtype, blocks, a.head_dim, D / 128);
         if (rc != GA_OK) return rc;
         tmK1 = tmK;
         tmV1 = tmV;
@@ -1005,8 +1024,8 @@ int launch_decode_tc(const DecodeArgs& a) {
     // one pool for K and V (same pointer): fetch each block once
     const bool alias = a.k_pool == a.v_pool;
     if (a.head_dim == 256 && !alias) {
-        const int32_t hp = tc_heads_per_unit(a.plan->flags, a.head_dim, a.plan->q_len,
-                                             a.num_q_heads / a.num_kv_heads, a.num_kv_heads);
+        // the plan's unit width (checked against the geometry at the entry)
+        const int32_t hp = a.plan->kv_heads_per_unit;
         if (hp == 4) return run_tc<256, false, 4>(a);
         if (hp == 2) return run_tc<256, false, 2>(a);
     }

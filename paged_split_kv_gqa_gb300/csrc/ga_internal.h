@@ -47,9 +47,11 @@ int encode_rows_map(CUtensorMap* map, const void* base, int32_t kv_dtype, int64_
 int encode_heads_map(CUtensorMap* map, const void* pool, int32_t region, int32_t num_kv_heads,
                      int64_t num_pages, int32_t head_dim, int32_t hp);
 
-// Builds the 5-D tensor map of a bf16 pool whose box is one 128-dim block of
-// one page-head block ([key / 8][64-dim region][key % 8] rows, 4 KB).
-int encode_kblock_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int32_t head_dim);
+// Builds the 5-D tensor map of a pool whose box is box_regions consecutive
+// 128-byte regions of one page-head block, landing as [key / 8][region]
+// [key % 8] rows of 128 bytes.
+int encode_region_map(CUtensorMap* map, const void* pool, int32_t kv_dtype, int64_t num_blocks,
+                      int32_t head_dim, int32_t box_regions);
 
 int launch_decode(const DecodeArgs& a);
 

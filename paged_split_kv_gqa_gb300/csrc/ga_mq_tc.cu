@@ -27,12 +27,11 @@
 // (D / 128 blocks) and the sums, 64 columns each: 448 of 512 at hd512.
 // Columns as M would need O = 128 x 512 fp32, all of TMEM, at hd512.
 //
-// Shared memory.  K: a ring of 32 KB slots, each one 128-dim block of a stage,
-// filled by one 4 KB bulk tensor copy per page that lands as [key / 8][64-dim
-// region][key % 8] rows: each region's 8-key groups then sit 2 KB apart in
-// key order over the stage's 8 pages, the uniform stride the QK product's
-// operand needs (two copies per page and region with [128 keys][128 B]
-// regions cost the producer twice the copies).  V: a ring of 32 KB slots of whole page-head blocks
+// Shared memory.  K: a ring of 64 KB in slots of one (or two) 64-dim regions
+// of a stage, filled by one bulk tensor copy per page that lands as
+// [key / 8][region][key % 8] rows: each region's 8-key groups sit at a uniform
+// stride in key order over the stage's 8 pages, as the QK product's operand
+// needs.  V: a ring of 64 KB in slots of whole page-head blocks
 // ([page][D / 64 regions][16 keys][128 B]), one copy per page: the PV product
 // takes one page per instruction, so a block's layout serves it as it lands.
 // q of the unit as [D / 64][64 rows][128 B] (one copy per region; two
@@ -64,12 +63,22 @@ namespace mq {
 constexpr int NC = kTcColTile;                    // columns per unit: N of every product
 constexpr int KEYS = 128;                         // keys per stage: M of the QK product
 constexpr int SPG = KEYS / kPageSize;             // pages per stage
-constexpr int SLOT_BYTES = 2 * KEYS * 128;        // a K or V slot: 128 keys x 128 dims bf16
+// K and V rings of 64 KB each, in slots of GA_MQ_SLOT_KB: 32 KB (2 slots: a K
+// slot is a 128-dim block of a stage, a V slot two hd512 pages) or, as a
+// build option, 16 KB (4 slots of one 64-dim region / one page: more of each
+// ring in flight, but more barriers and commits per stage; measured slower,
+// S = 64 global 10.95 vs 9.69 ms).
+#ifndef GA_MQ_SLOT_KB
+#define GA_MQ_SLOT_KB 32
+#endif
+constexpr int SLOT_BYTES = GA_MQ_SLOT_KB * 1024;    // a K or V slot
+constexpr int K_REGIONS = SLOT_BYTES / (KEYS * 128); // 64-dim regions of a stage per K slot
+static_assert(K_REGIONS == 1 || K_REGIONS == 2, "K slot: one or two 64-dim regions");
 constexpr int QREG_BYTES = NC * 128;              // [64 columns][64 dims] bf16
 constexpr int PREG_BYTES = NC * 128;              // [64 columns][64 keys] bf16
 constexpr int P_BYTES = 2 * PREG_BYTES;           // P^T of a stage
 constexpr int ONES_BYTES = 4096;                  // [16 keys][128 rows] bf16 ones
-constexpr int NKS = 2, NVS = 2;                   // K and V slots
+constexpr int NKS = 65536 / SLOT_BYTES, NVS = NKS; // K and V slots
 constexpr int NSW = 4;                            // softmax warps
 constexpr int KP_WARP = 4, VP_WARP = 5, QK_WARP = 6, PV_WARP = 7;
 constexpr int NTHREADS = 256;
@@ -90,11 +99,12 @@ constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + NKS, B_VFULL = B_KEMPTY + NKS,
 template <int D_>
 struct Geo {
     static constexpr int D = D_;
-    static constexpr int NDC = D / 128;            // 128-dim blocks: K slots per stage, O^T blocks
+    static constexpr int NDC = D / 128;            // 128-dim blocks: O^T blocks
     static constexpr int NR = D / 64;              // 64-dim regions (128 B of bf16)
     static constexpr int NQB = D == 256 ? 2 : 1;   // q buffers
     static constexpr int Q_BYTES = NR * QREG_BYTES;
     static constexpr int BLOCK_BYTES = kPageSize * D * 2;       // one page-head block
+    static constexpr int KSPS = NR / K_REGIONS;                 // K slots per stage
     static constexpr int PPS = SLOT_BYTES / BLOCK_BYTES;        // pages per V slot
     static constexpr int VSPS = SPG / PPS;                      // V slots per stage
     static constexpr int TM_L = TM_O + NDC * NC;                // the column sums
@@ -147,7 +157,7 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
     constexpr int NS = IS_K ? NKS : NVS;
     constexpr int B_FULLB = IS_K ? B_KFULL : B_VFULL, B_EMPTYB = IS_K ? B_KEMPTY : B_VEMPTY;
     constexpr uint32_t OFF = IS_K ? G::OFF_K : G::OFF_V;
-    constexpr int SLOTS_PER_STAGE = IS_K ? G::NDC : G::VSPS;
+    constexpr int SLOTS_PER_STAGE = IS_K ? G::KSPS : G::VSPS;
     // Pages of K and V are read by every column tile of a kv head: keep them
     // in L2 at normal priority.
     const uint64_t pol = l2_evict_normal_policy();
@@ -224,13 +234,14 @@ __device__ void producer(const CUtensorMap* tm, const CUtensorMap* tmQ, const De
                 const uint32_t fb = bar(bars, B_FULLB + (int)slot);
                 const uint32_t dst0 = base + OFF + slot * SLOT_BYTES;
                 if (IS_K) {
-                    // 128-dim block j of every page (regions 2j, 2j + 1) as one
-                    // 4 KB box: page pl fills rows 32 pl .. 32 pl + 31 of the slot
-                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(gm) * 2u * 2048u);
+                    // regions K_REGIONS j .. of every page as one box of 2 KB per
+                    // region: page pl fills rows 16 K_REGIONS pl .. of the slot
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(fb, (uint32_t)__popc(gm) * (uint32_t)K_REGIONS * 2048u);
                     __syncwarp();
                     if (good)
-                        tma_load_5d(dst0 + (uint32_t)pl * 4096u, tm, fb, 0, 0, 2 * j, 0,
-                                    y / kPageSize, pol);
+                        tma_load_5d(dst0 + (uint32_t)pl * (uint32_t)(K_REGIONS * 2048), tm, fb, 0, 0,
+                                    K_REGIONS * j, 0, y / kPageSize, pol);
                 } else {
                     // pages PPS j .. PPS j + PPS - 1, whole page-head blocks
                     const uint32_t sm = (gm >> (G::PPS * j)) & ((1u << G::PPS) - 1u);
@@ -288,7 +299,7 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                 stop = true;
                 break;
             }
-            for (int c = 0; c < G::NDC; ++c, ++kseq) {
+            for (int c = 0; c < G::KSPS; ++c, ++kseq) {
                 const uint32_t slot = kseq % NKS;
                 if (!issuer_wait(p, bar(bars, B_KFULL + (int)slot), (kseq / NKS) & 1, abort_flag)) {
                     stop = true;
@@ -296,14 +307,15 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                 }
                 tc_fence_after();
                 const uint32_t ka = base + G::OFF_K + slot * SLOT_BYTES;
-                // region r of the slot: 8-key groups 2 KB apart, starting at r KB
+                // region r of the slot: 8-key groups K_REGIONS KB apart, from r KB
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < K_REGIONS; ++r)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_bf16(tmem + TM_S + NC * sb,
-                                    smem_desc_sw128(ka + r * 1024 + 32 * kk, 16, 2048),
-                                    smem_desc_sw128(qa + (2 * c + r) * QREG_BYTES + 32 * kk, 16, 1024),
+                                    smem_desc_sw128(ka + r * 1024 + 32 * kk, 16, K_REGIONS * 1024),
+                                    smem_desc_sw128(qa + (K_REGIONS * c + r) * QREG_BYTES + 32 * kk,
+                                                    16, 1024),
                                     IQK, (c | r | kk) != 0 ? 1u : 0u);
                 tc_commit(bar(bars, B_KEMPTY + (int)slot));     // the K slot may be refilled
             }
@@ -826,7 +838,8 @@ static int run_mq(const DecodeArgs& a) {
     // region][key % 8], 4 KB); V: one box = a whole page-head block; q: one
     // 64-dim region of a unit's 64 rows
     CUtensorMap tmK, tmV, tmQ;
-    rc = encode_kblock_map(&tmK, a.k_pool, a.num_pages * a.num_kv_heads, D);
+    rc = encode_region_map(&tmK, a.k_pool, GA_KV_BF16, a.num_pages * a.num_kv_heads, D,
+                           mq::K_REGIONS);
     if (rc != GA_OK) return rc;
     rc = encode_rows_map(&tmV, a.v_pool, GA_KV_BF16, rows, D, kPageSize, 0);
     if (rc != GA_OK) return rc;

@@ -60,7 +60,8 @@ class ga_plan(ctypes.Structure):
         "window", "page_size", "grid", "flags", "touch_stride", "q_len", "col_tile")] + [
         (n, ctypes.c_int64) for n in ("row_chunks", "units", "workspace_bytes",
                                        "partial_o_offset", "partial_lse_offset",
-                                       "touch_log_offset")]
+                                       "touch_log_offset")] + [
+        (n, ctypes.c_int32) for n in ("kv_heads_per_unit", "reserved")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -45,10 +45,14 @@ def _inputs(lens, fam, seed, **kw):
 
 
 def _plan(ga, fi, flags=0, **kw):
+    """A plan for E4M3 pools with units of 8 / group kv heads set explicitly
+    (the planner picks them only for large batches)."""
     fam = fi.family
-    return ga.ga_plan_splits(fi.seq_lens.cpu().numpy(), num_q_heads=fam.num_q_heads,
+    plan = ga.ga_plan_splits(fi.seq_lens.cpu().numpy(), num_q_heads=fam.num_q_heads,
                              num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
                              window=fam.window, flags=ga.GA_PLAN_KV_E4M3 | flags, **kw)
+    plan.kv_heads_per_unit = 8 // (fam.num_q_heads // fam.num_kv_heads)
+    return plan
 
 
 @pytest.mark.parametrize("split", SPLITS, ids=lambda s: str(s))
@@ -135,12 +139,16 @@ def test_31b_sampled(ga, err, split):
 
 def test_ragged_sampled(ga, err):
     """The ragged 256-row batch (lognormal lengths, E4M3 sliding family) in the
-    launch configuration the bench times: a plan made with GA_PLAN_KV_E4M3."""
+    launch configuration the bench times: a plan made with GA_PLAN_KV_E4M3,
+    whose units the planner makes 4 kv heads wide."""
     wl = W.config(5)
     fam = wl.local
     assert fam.kv_dtype == W.KV_E4M3
     fi = W.make_family_inputs(wl, fam, device=DEV, poison=True, release_old=True)
-    plan = _plan(ga, fi)
+    plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                             num_kv_heads=fam.num_kv_heads, head_dim=256, window=fam.window,
+                             flags=ga.GA_PLAN_KV_E4M3)
+    assert plan.kv_heads_per_unit == 4                    # the planner's own choice here
     out = run_decode(ga, fi, plan, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0

@@ -55,6 +55,8 @@ def test_wait_runs_out_reports_and_context_survives(ga, case):
     extra = getattr(ga, FLAGS[case]) if case in FLAGS else 0
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     stall = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_TEST_WAIT_TIMEOUT | extra, **kw)
+    if extra:                                  # units of 4 kv heads (set explicitly)
+        stall.kv_heads_per_unit = 4
     assert stall.grid > 1                      # other CTAs still run
     fi_run = dataclasses.replace(fi, family=fam)
     t0 = time.time()
@@ -68,6 +70,8 @@ def test_wait_runs_out_reports_and_context_survives(ga, case):
     # the context is intact: the same call without the hook is correct
     err.zero_()
     plan = ga.ga_plan_splits(lens, flags=extra, **kw)
+    if extra:
+        plan.kv_heads_per_unit = 4
     out = run_decode(ga, fi_run, plan, err=err, out=torch.empty_like(fi.q))
     torch.cuda.synchronize()
     assert int(err.item()) == 0

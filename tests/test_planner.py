@@ -153,14 +153,24 @@ def test_multi_query_plan_properties(ga, seed):
 
 
 def test_units_span_several_kv_heads(ga):
-    """The planner counts units of 8 / group kv heads with the flag."""
-    lens = [3000] * 8
-    kw = dict(num_q_heads=32, num_kv_heads=16, head_dim=256, window=1024, num_sms=152,
-              requested_splits=1)
-    one = ga.ga_plan_splits(lens, **kw)
-    four = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw)
-    assert one.units == 8 * 16 and four.units == 8 * 4
-    kw.update(num_q_heads=64)                                   # group 4: two kv heads
-    assert ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw).units == 8 * 8
-    kw.update(num_q_heads=16)                                   # group 1: one
-    assert ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw).units == 8 * 16
+    """With GA_PLAN_KV_E4M3 the planner gives the E4M3 sliding family units of
+    8 / group kv heads only when the one-head plan needs no split and the wider
+    units fill at least four rounds of the SMs; otherwise one kv head."""
+    kw = dict(num_q_heads=32, num_kv_heads=16, head_dim=256, window=1024, num_sms=152)
+    few = [3000] * 8                              # 32 four-head units: too few
+    one = ga.ga_plan_splits(few, **kw)
+    p = ga.ga_plan_splits(few, flags=ga.GA_PLAN_KV_E4M3, **kw)
+    assert one.kv_heads_per_unit == 1 and p.kv_heads_per_unit == 1 and p.units == one.units
+    many = W.config(5).seq_lens                   # 256 rows: 1024 four-head units
+    p = ga.ga_plan_splits(many, flags=ga.GA_PLAN_KV_E4M3, **kw)
+    assert p.mode == ga.GA_SPLIT_NONE and p.kv_heads_per_unit == 4 and p.units == 256 * 4
+    assert ga.ga_plan_splits(many, **kw).kv_heads_per_unit == 1     # bf16 plan
+    # group 4: two kv heads per unit; group 1: never
+    p = ga.ga_plan_splits(many, flags=ga.GA_PLAN_KV_E4M3,
+                          **dict(kw, num_q_heads=64))
+    assert p.kv_heads_per_unit == 2 and p.units == 256 * 8
+    p = ga.ga_plan_splits(many, flags=ga.GA_PLAN_KV_E4M3, **dict(kw, num_q_heads=16))
+    assert p.kv_heads_per_unit == 1
+    # the global family (head_dim 512) and multi-query plans keep one kv head
+    assert ga.ga_plan_splits(many, flags=ga.GA_PLAN_KV_E4M3,
+                             **dict(kw, head_dim=512, window=0)).kv_heads_per_unit == 1

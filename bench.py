@@ -140,7 +140,8 @@ WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 MQ_UNIT_FLAGS = {"auto": 0, "tc": "GA_PLAN_TENSOR_CORE_UNITS", "cp": "GA_PLAN_COLUMN_PARALLEL_UNITS"}
 
 
-def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto"):
+def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto",
+               fp8_units=0):
     """One layer's inputs.  q_len > 1: a multi-query step (q_len new tokens
     per row at its last positions, e.g. a speculative-decoding verify): the
     pools keep the union of the queries' windows, q / out are
@@ -176,6 +177,8 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, 
                              flags=ga.GA_PLAN_EXTERNAL_COMBINE |
                              (ga.GA_PLAN_KV_E4M3 if fam.kv_dtype == W.KV_E4M3 else 0) |
                              (getattr(ga, unit_flag) if unit_flag else 0), q_len=S)
+    if fp8_units and fam.kv_dtype == W.KV_E4M3 and fam.window > 0:
+        plan.kv_heads_per_unit = fp8_units        # A/B: force the E4M3 unit width
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
     esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
@@ -210,7 +213,7 @@ def workload_config(workload, seed, fp8="none"):
 
 
 def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
-               q_len=1, fp8="none", mq_units="auto"):
+               q_len=1, fp8="none", mq_units="auto", fp8_units=0):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -223,7 +226,8 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
         wl = W.Workload(wl.name + f" (first {rows} rows)", wl.seq_lens[:rows].copy(),
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
-    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units)
+    sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units,
+                                  fp8_units)
                        for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
@@ -379,6 +383,8 @@ def workload_text(args):
     if args.q_len > 1:
         text += (f"; {args.q_len} query tokens per row at its last positions (causal "
                  f"within the chunk), {args.q_len} appends per row and layer")
+    if args.fp8_units:
+        text += f"; E4M3 sliding-family units of {args.fp8_units} kv heads forced"
     if args.mq_units != "auto":
         text += {"tc": "; tcgen05 units of 64 columns forced",
                  "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
@@ -549,7 +555,7 @@ def run_ga(args):
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
                                          args.pools, args.kv_alias, args.splits, args.q_len,
-                                         args.fp8, args.mq_units)
+                                         args.fp8, args.mq_units, args.fp8_units)
 
     def step(evs=None):
         n = 0
@@ -876,6 +882,9 @@ def main():
                     help="query tokens per row (> 1: a multi-query / speculative-verify step)")
     ap.add_argument("--fp8", default="none", choices=["none", "local", "global", "both"],
                     help="store these families' KV pools as fp8-e4m3 with per-head scales")
+    ap.add_argument("--fp8-units", type=int, default=0,
+                    help="kv heads per unit of the E4M3 sliding-family decode (1, or 8 / group): "
+                         "forces the width the planner would otherwise choose (A/B)")
     ap.add_argument("--mq-units", default="auto", choices=sorted(MQ_UNIT_FLAGS),
                     help="multi-query units for more than 8 (query, head) columns per kv head: "
                          "the planner's choice, tcgen05 units of 64 columns, or column-parallel "

@@ -3,8 +3,9 @@
 A step on the 31B-shaped decode batch (the default workload: B 64, L ~
 U[8192, 32768], 32 query heads; local 16 KV heads hd256 window 1024; global 4
 KV heads hd512) is: KV append (local) -> local decode (+ split-KV combine if
-planned) -> KV append (global) -> global decode -> split-KV combine.  All of
-it runs in libga's CUDA kernels through the C ABI.  --workload ragged runs
+planned) -> KV append (global) -> global decode -> split-KV combine, each
+append inside its decode launch (`--separate-append` launches it apart).
+All of it runs in libga's CUDA kernels through the C ABI.  --workload ragged runs
 the 50-local (fp8) + 10-global layer sweep instead.
 
 Printed: one JSON line with the metric (algorithmic HBM GB/s of the step),
@@ -141,7 +142,7 @@ MQ_UNIT_FLAGS = {"auto": 0, "tc": "GA_PLAN_TENSOR_CORE_UNITS", "cp": "GA_PLAN_CO
 
 
 def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto",
-               fp8_units=0):
+               fp8_units=0, separate_append=False):
     """One layer's inputs.  q_len > 1: a multi-query step (q_len new tokens
     per row at its last positions, e.g. a speculative-decoding verify): the
     pools keep the union of the queries' windows, q / out are
@@ -183,6 +184,7 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, 
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
     esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
     return dict(
+        separate_append=separate_append,
         fam=fam, fi=fi, plan=plan, ws=ws, po=po, plse=plse, q=q, kn=kn, vn=vn, pos=pos,
         out=torch.empty_like(q), scale=1.0 / math.sqrt(fam.head_dim),
         bytes=M.decode_bytes(wl.seq_lens, num_q_heads=fam.num_q_heads,
@@ -213,7 +215,7 @@ def workload_config(workload, seed, fp8="none"):
 
 
 def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
-               q_len=1, fp8="none", mq_units="auto", fp8_units=0):
+               q_len=1, fp8="none", mq_units="auto", fp8_units=0, separate_append=False):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -227,7 +229,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
     sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units,
-                                  fp8_units)
+                                  fp8_units, separate_append)
                        for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
@@ -244,18 +246,28 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
 
 
 def launch_layer(ga, f, err, events=None):
-    """append + decode (+ combine) of one layer on the current stream.
-    Returns the number of kernels launched."""
+    """append + decode (+ combine) of one layer on the current stream.  A
+    one-query step appends inside the decode launch (the decode call with the
+    append fused) unless the layer asks for the append kernel first
+    (`separate_append`).  Returns the number of kernels launched."""
     fi, fam, plan = f["fi"], f["fam"], f["plan"]
     S = f["kn"].shape[0]
-    for i in range(S):                 # this step's new token(s) of every row
-        ga.ga_kv_append(f["kn"][i], f["vn"][i], fi.k_pool, fi.v_pool, fi.page_table, f["pos"][i],
-                        k_scale=fi.k_scale, v_scale=fi.v_scale, err_word=err)
+    fused = S == 1 and not f["separate_append"]
+    if not fused:
+        for i in range(S):             # this step's new token(s) of every row
+            ga.ga_kv_append(f["kn"][i], f["vn"][i], fi.k_pool, fi.v_pool, fi.page_table,
+                            f["pos"][i], k_scale=fi.k_scale, v_scale=fi.v_scale, err_word=err)
     kw = dict(scale=f["scale"], plan=plan, workspace=f["ws"], out=f["out"], k_scale=fi.k_scale,
               v_scale=fi.v_scale, err_word=err)
     if events is not None:
         events[0].record()
-    if fam.window > 0:
+    if fused and fam.window > 0:
+        ga.ga_decode_local_hd256_append(f["kn"][0], f["vn"][0], f["q"], fi.k_pool, fi.v_pool,
+                                        fi.page_table, fi.seq_lens, window=fam.window, **kw)
+    elif fused:
+        ga.ga_decode_global_hd512_append(f["kn"][0], f["vn"][0], f["q"], fi.k_pool, fi.v_pool,
+                                         fi.page_table, fi.seq_lens, **kw)
+    elif fam.window > 0:
         ga.ga_decode_local_hd256(f["q"], fi.k_pool, fi.v_pool, fi.page_table, fi.seq_lens,
                                  window=fam.window, **kw)
     else:
@@ -263,7 +275,9 @@ def launch_layer(ga, f, err, events=None):
                                   **kw)
     if events is not None:
         events[1].record()
-    n = S + 1
+    # the decode launch, plus the append kernel(s) when not fused (or when a
+    # kv head's query heads span several units: the call appends first)
+    n = 1 + (S if not fused else (1 if fam.num_q_heads // fam.num_kv_heads > 8 else 0))
     if plan.mode != ga.GA_SPLIT_NONE:
         ga.ga_splitkv_combine(f["po"], f["plse"], plan, fi.seq_lens, fi.page_table.shape[1],
                               f["out"], err_word=err)
@@ -385,6 +399,8 @@ def workload_text(args):
                  f"within the chunk), {args.q_len} appends per row and layer")
     if args.fp8_units:
         text += f"; E4M3 sliding-family units of {args.fp8_units} kv heads forced"
+    if args.separate_append:
+        text += "; append kernel launched before each decode (not fused)"
     if args.mq_units != "auto":
         text += {"tc": "; tcgen05 units of 64 columns forced",
                  "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
@@ -555,7 +571,8 @@ def run_ga(args):
         pg = dist
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
                                          args.pools, args.kv_alias, args.splits, args.q_len,
-                                         args.fp8, args.mq_units, args.fp8_units)
+                                         args.fp8, args.mq_units, args.fp8_units,
+                                         args.separate_append)
 
     def step(evs=None):
         n = 0
@@ -653,7 +670,11 @@ def run_ga(args):
         uniq = [layer for fam_layers in sets.values() for layer in fam_layers]
         for layer in uniq:
             fi = layer["fi"]
-            h = {k: layer[k].cpu().pin_memory() for k in ("q", "kn", "vn", "pos")}
+            # positions only where an append kernel reads them (the fused
+            # append takes L - 1 from seq_lens)
+            keys = ("q", "kn", "vn") if (layer["kn"].shape[0] == 1 and
+                                         not layer["separate_append"]) else ("q", "kn", "vn", "pos")
+            h = {k: layer[k].cpu().pin_memory() for k in keys}
             h["seq_lens"] = fi.seq_lens.cpu().pin_memory()
             h["out"] = torch.empty_like(layer["out"], device="cpu").pin_memory()
             host[id(layer)] = h
@@ -681,7 +702,8 @@ def run_ga(args):
         def copy_inputs(layer):
             h = host[id(layer)]
             for k in ("q", "kn", "vn", "pos"):
-                layer[k].copy_(h[k], non_blocking=True)
+                if k in h:
+                    layer[k].copy_(h[k], non_blocking=True)
             layer["fi"].seq_lens.copy_(h["seq_lens"], non_blocking=True)
 
         def read_back(layer):
@@ -882,6 +904,9 @@ def main():
                     help="query tokens per row (> 1: a multi-query / speculative-verify step)")
     ap.add_argument("--fp8", default="none", choices=["none", "local", "global", "both"],
                     help="store these families' KV pools as fp8-e4m3 with per-head scales")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="one-query steps launch the append kernel before the decode instead "
+                         "of the decode call with the append fused (A/B)")
     ap.add_argument("--fp8-units", type=int, default=0,
                     help="kv heads per unit of the E4M3 sliding-family decode (1, or 8 / group): "
                          "forces the width the planner would otherwise choose (A/B)")

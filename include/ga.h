@@ -277,6 +277,45 @@ int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool
                            void* out, int32_t* err_word, ga_stream_t stream);
 
 /*
+ * ga_decode_local_hd256_append, ga_decode_global_hd512_append -- one decode
+ * step with the KV page append fused in: the same result as
+ *     ga_kv_append(k_new, v_new, k_pool, v_pool, ..., positions = seq_lens - 1)
+ * followed by ga_decode_local_hd256 / ga_decode_global_hd512 on the same
+ * stream (pools bit-identical, outputs bit-identical), in one launch ("[Model]
+ * Gemma 4 M1 12B", Description: paged prefill and decode; a decode step's
+ * token is appended at position L - 1 and then attended).  The unit of the
+ * decode that reads a row's last page writes the row's token into it first.
+ *   k_new, v_new [batch, num_kv_heads, D] bf16, 16-byte aligned: this step's
+ *       token of every row, written at seq_lens[b] - 1 (rows of length 0
+ *       write nothing; E4M3 pools get the quantisation ga_kv_append uses).
+ *   plan->q_len must be 1.  Other arguments as for the decode call, with the
+ *       pools writable.
+ * When a kv head's query heads span several units (more than 8 query heads
+ * per kv head), or the plan is one for 64-column multi-query units, the call
+ * launches the append kernel before the decode: the
+ * same result in two launches.  Device errors: those of both calls
+ * (GA_DEVERR_POSITION for an invalid page id at the token's slot).
+ */
+int ga_decode_local_hd256_append(const void* k_new, const void* v_new, const void* q,
+                                 void* k_pool, void* v_pool, int32_t kv_dtype,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* page_table, int64_t pt_stride,
+                                 const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t window, int32_t page_size,
+                                 int64_t num_pages, float scale, const ga_plan* plan,
+                                 void* workspace, size_t workspace_bytes, void* out,
+                                 int32_t* err_word, ga_stream_t stream);
+int ga_decode_global_hd512_append(const void* k_new, const void* v_new, const void* q,
+                                  void* k_pool, void* v_pool, int32_t kv_dtype,
+                                  const float* k_scale, const float* v_scale,
+                                  const int32_t* page_table, int64_t pt_stride,
+                                  const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t page_size, int64_t num_pages,
+                                  float scale, const ga_plan* plan, void* workspace,
+                                  size_t workspace_bytes, void* out, int32_t* err_word,
+                                  ga_stream_t stream);
+
+/*
  * ga_splitkv_combine -- merge split-KV partials by log-sum-exp
  * ("visible-cx/Gemma-4-31B-CoreAI", "--metal-sdpa is mandatory here":
  * flash-decode with split factor 8):

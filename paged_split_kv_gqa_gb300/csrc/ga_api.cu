@@ -12,11 +12,13 @@
 
 namespace ga {
 
+// positions null: each row's token goes to seq_lens[b] - 1 (rows of length 0,
+// or longer than the table holds, append nothing)
 int launch_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                   int32_t kv_dtype, const float* k_scale, const float* v_scale,
                   const int32_t* page_table, int64_t pt_stride, const int32_t* positions,
                   int32_t batch, int32_t num_kv_heads, int32_t head_dim, int64_t num_pages,
-                  int32_t* err_word, cudaStream_t stream);
+                  int32_t* err_word, cudaStream_t stream, const int32_t* seq_lens = nullptr);
 
 // ------------------------------------------------------------------ tensor maps
 
@@ -363,7 +365,8 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                         int32_t window, int32_t page_size, int64_t num_pages, float scale,
                         const ga_plan* plan, void* workspace, size_t workspace_bytes, void* out,
-                        int32_t* err_word, ga_stream_t stream) {
+                        int32_t* err_word, ga_stream_t stream, const void* k_new = nullptr,
+                        const void* v_new = nullptr) {
     if (plan == nullptr || batch < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || pt_stride < 1 || num_pages < 1 ||
         !std::isfinite(scale))
@@ -394,9 +397,28 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
                                                      num_q_heads / num_kv_heads, num_kv_heads))
         return GA_ERR_INVALID_ARG;
     if (plan->kv_heads_per_unit < 0) return GA_ERR_INVALID_ARG;
+    const bool append = k_new != nullptr || v_new != nullptr;
+    if (append && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new) ||
+                   plan->q_len != 1))
+        return GA_ERR_INVALID_ARG;
     DecodeArgs a{q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride, seq_lens,
                  batch, num_q_heads, num_kv_heads, head_dim, window, num_pages, scale, plan,
                  workspace, out, err_word, reinterpret_cast<cudaStream_t>(stream)};
+    if (append) {
+        if (num_q_heads / num_kv_heads <= kHeadTile && plan->col_tile != kTcColTile) {
+            // every kv head of a row chunk is one unit of a kernel that
+            // appends: the decode appends
+            a.k_new = k_new;
+            a.v_new = v_new;
+        } else {
+            // a kv head spans several units: append first, then decode
+            const int rc = launch_append(k_new, v_new, const_cast<void*>(k_pool),
+                                         const_cast<void*>(v_pool), kv_dtype, k_scale, v_scale,
+                                         page_table, pt_stride, nullptr, batch, num_kv_heads,
+                                         head_dim, num_pages, err_word, a.stream, seq_lens);
+            if (rc != GA_OK) return rc;
+        }
+    }
     return launch_decode(a);
 }
 
@@ -425,6 +447,38 @@ int ga_decode_global_hd512(const void* q, const void* k_pool, const void* v_pool
                         seq_lens, batch, num_q_heads, num_kv_heads, 512, 0, page_size,
                         num_pages, scale, plan, workspace, workspace_bytes, out, err_word,
                         stream);
+}
+
+int ga_decode_local_hd256_append(const void* k_new, const void* v_new, const void* q,
+                                 void* k_pool, void* v_pool, int32_t kv_dtype,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* page_table, int64_t pt_stride,
+                                 const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t window, int32_t page_size,
+                                 int64_t num_pages, float scale, const ga_plan* plan,
+                                 void* workspace, size_t workspace_bytes, void* out,
+                                 int32_t* err_word, ga_stream_t stream) {
+    if (window < 1 || !k_new || !v_new) return GA_ERR_INVALID_ARG;
+    return decode_entry(q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride,
+                        seq_lens, batch, num_q_heads, num_kv_heads, 256, window, page_size,
+                        num_pages, scale, plan, workspace, workspace_bytes, out, err_word,
+                        stream, k_new, v_new);
+}
+
+int ga_decode_global_hd512_append(const void* k_new, const void* v_new, const void* q,
+                                  void* k_pool, void* v_pool, int32_t kv_dtype,
+                                  const float* k_scale, const float* v_scale,
+                                  const int32_t* page_table, int64_t pt_stride,
+                                  const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t page_size, int64_t num_pages,
+                                  float scale, const ga_plan* plan, void* workspace,
+                                  size_t workspace_bytes, void* out, int32_t* err_word,
+                                  ga_stream_t stream) {
+    if (!k_new || !v_new) return GA_ERR_INVALID_ARG;
+    return decode_entry(q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, pt_stride,
+                        seq_lens, batch, num_q_heads, num_kv_heads, 512, 0, page_size,
+                        num_pages, scale, plan, workspace, workspace_bytes, out, err_word,
+                        stream, k_new, v_new);
 }
 
 int ga_splitkv_combine(const float* partial_o, const float* partial_lse, const ga_plan* plan,

@@ -21,28 +21,13 @@ struct AppendParams {
     const float* k_scale;
     const float* v_scale;
     const int32_t* page_table;
-    const int32_t* positions;
+    const int32_t* positions;   // or null: the position is seq_lens[b] - 1
+    const int32_t* seq_lens;
     int32_t* err_word;
     int64_t pt_stride;
     int64_t num_pages;
     int32_t B, Hkv, D, kv_dtype;
 };
-
-__device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t out[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float a = __fdiv_rn(bf16_lo(w[2 * i]), scale);
-        const float b = __fdiv_rn(bf16_hi(w[2 * i]), scale);
-        const float c = __fdiv_rn(bf16_lo(w[2 * i + 1]), scale);
-        const float d = __fdiv_rn(bf16_hi(w[2 * i + 1]), scale);
-        const uint32_t ab = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t cd = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-        out[i] = (ab & 0xFFFFu) | (cd << 16);
-    }
-    return make_uint2(out[0], out[1]);
-}
 
 // One thread per 8 consecutive elements of one (row, kv head).
 __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
@@ -52,7 +37,16 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     const int d8 = (int)(idx % per_head);
     const int c = (int)((idx / per_head) % p.Hkv);
     const int b = (int)(idx / ((int64_t)per_head * p.Hkv));
-    const int32_t pos = __ldg(p.positions + b);
+    int32_t pos;
+    if (p.positions != nullptr) {
+        pos = __ldg(p.positions + b);
+    } else {
+        // one-query decode step: the token at L - 1; an empty row appends
+        // nothing, and a length the table cannot hold is the decode's to report
+        const int32_t L = __ldg(p.seq_lens + b);
+        if ((int64_t)L > p.pt_stride * kPageSize) return;
+        pos = L - 1;
+    }
     if (pos < 0) return;
     const int64_t lp = pos / kPageSize;
     if (lp >= p.pt_stride) {
@@ -81,8 +75,9 @@ int launch_append(const void* k_new, const void* v_new, void* k_pool, void* v_po
                   int32_t kv_dtype, const float* k_scale, const float* v_scale,
                   const int32_t* page_table, int64_t pt_stride, const int32_t* positions,
                   int32_t batch, int32_t num_kv_heads, int32_t head_dim, int64_t num_pages,
-                  int32_t* err_word, cudaStream_t stream) {
+                  int32_t* err_word, cudaStream_t stream, const int32_t* seq_lens) {
     AppendParams p;
+    p.seq_lens = seq_lens;
     p.k_new = static_cast<const uint4*>(k_new);
     p.v_new = static_cast<const uint4*>(v_new);
     p.k_pool = k_pool;

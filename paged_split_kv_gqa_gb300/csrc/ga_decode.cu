@@ -149,6 +149,7 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
     int64_t u = blockIdx.x;
     UnitInfo x = {};
     int32_t id_cur = -1, id_nxt = -1;
+    TokenAppend<C::D, C::KV, 1> tok;
     if (u < U) {
         x = unit_info(p, pre, u);
         first_ids(x, id_cur, id_nxt);
@@ -180,10 +181,13 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const D
             for (int l = lane; l * 128 < x.nvalid * C::D * 2; l += 32) prefetch_l2(qrow + 128 * l);
         }
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
+        tok.start(p, x);               // this step's token, written before its page's copy
         // page ids of this unit, 32 at a time (the next batch loads one batch ahead)
         for (int i0 = 0; i0 < x.np && !stop; i0 += 32) {
             const int cnt = min(32, x.np - i0);
             for (int k = 0; k < cnt && !stop; k += kIssueLanes) {
+                if (i0 + k + kIssueLanes >= x.np)     // the group with the last page
+                    tok.finish(p, __shfl_sync(0xffffffffu, id_cur, (x.np - 1 - i0) & 31));
                 const int32_t pid = __shfl_sync(0xffffffffu, id_cur, (k + lane) & 31);
                 bool fail = false;
                 if (lane < kIssueLanes && k + lane < cnt) {
@@ -977,6 +981,10 @@ static int run(const DecodeArgs& a, int slot) {
     p.touch_log = (pl.flags & GA_PLAN_TOUCH_LOG)
                       ? reinterpret_cast<int32_t*>(ws + pl.touch_log_offset)
                       : nullptr;
+    p.k_new = static_cast<const uint4*>(a.k_new);
+    p.v_new = static_cast<const uint4*>(a.v_new);
+    p.k_pool = const_cast<void*>(a.k_pool);
+    p.v_pool = const_cast<void*>(a.v_pool);
     p.err_word = a.err_word;
     p.pt_stride = a.pt_stride;
     p.num_pages = a.num_pages;

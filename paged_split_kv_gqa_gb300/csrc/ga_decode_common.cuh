@@ -21,6 +21,12 @@ struct DecodeParams {
     float* partial_o;             // [rc_capacity, Hq, D]
     float* partial_lse;           // [rc_capacity, Hq]
     int32_t* touch_log;           // [rc_capacity, touch_stride] or null
+    // this step's new token, [B, Hkv, D] bf16, appended by the decode itself
+    // (one-query decode with the append fused), or null
+    const uint4* k_new;
+    const uint4* v_new;
+    void* k_pool;                 // the pools, for that append
+    void* v_pool;
     int32_t* err_word;
     int64_t pt_stride;
     int64_t num_pages;
@@ -155,6 +161,108 @@ __device__ __forceinline__ bool build_row_prefix(const DecodeParams& p, int32_t*
     }
     return true;
 }
+
+// ---- the KV page append fused into a one-query decode
+//
+// When the call carries this step's token (p.k_new), the unit that holds a
+// row's last page (its last chunk; the token's position is L - 1) writes the
+// token of its kv heads [x.c NH, x.c NH + NH) into that page's slot exactly
+// as ga_kv_append does (bf16 bits, or the E4M3 quantisation), and orders those
+// generic stores before the bulk tensor copy of that page.  Only this unit
+// reads those page-head blocks of the row, so no other CTA waits for it.
+template <int D, int KV, int NH>
+struct TokenAppend {
+    static constexpr int PER_HEAD = D / 8;                     // uint4 of bf16 per head
+    static constexpr int PER_LANE = (NH * PER_HEAD + 31) / 32;
+    static constexpr int LINES = NH * D * 2 / 128;             // 128-byte lines of k (or v)
+
+    __device__ __forceinline__ static bool due(const DecodeParams& p, const UnitInfo& x) {
+        return p.k_new != nullptr && x.hg == 0 && x.g.len > 0 && x.j == x.g.chunks - 1;
+    }
+
+    // The lanes of one warp write the token of row b, kv heads [c0, c0 + NH),
+    // at position pos into `page` (reported, and nothing written, if the id
+    // is not a page of the pool).  No fence.
+    __device__ __forceinline__ static void write(const DecodeParams& p, int32_t b, int32_t c0,
+                                                 int32_t pos, int32_t page) {
+        const int lane = threadIdx.x & 31;
+        if (!page_ok(page, p.num_pages)) {
+            if (lane == 0) report(p.err_word, kErrPosition);
+            return;
+        }
+        const int hkv = p.Hkv * NH;                            // kv heads of the pool
+        const int64_t src0 = ((int64_t)b * hkv + c0) * PER_HEAD;
+        const int64_t slot = (int64_t)(pos % kPageSize) * D;
+        uint4 k[PER_LANE], v[PER_LANE];
+        float ks[PER_LANE], vs[PER_LANE];
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+            const int e = lane + 32 * i;
+            if (e < NH * PER_HEAD) {
+                k[i] = __ldg(p.k_new + src0 + e);
+                v[i] = __ldg(p.v_new + src0 + e);
+                if constexpr (KV != GA_KV_BF16) {
+                    ks[i] = __ldg(p.k_scale + c0 + e / PER_HEAD);
+                    vs[i] = __ldg(p.v_scale + c0 + e / PER_HEAD);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+            const int e = lane + 32 * i;
+            if (e < NH * PER_HEAD) {
+                const int64_t elem = page_block_elem(page, c0 + e / PER_HEAD, hkv, D) + slot +
+                                     (int64_t)(e % PER_HEAD) * 8;
+                if constexpr (KV == GA_KV_BF16) {
+                    reinterpret_cast<uint4*>(p.k_pool)[elem / 8] = k[i];
+                    reinterpret_cast<uint4*>(p.v_pool)[elem / 8] = v[i];
+                } else {
+                    reinterpret_cast<uint2*>(p.k_pool)[elem / 8] = quantize8(k[i], ks[i]);
+                    reinterpret_cast<uint2*>(p.v_pool)[elem / 8] = quantize8(v[i], vs[i]);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ static const int32_t* page_entry(const DecodeParams& p,
+                                                                int32_t b, int32_t pos) {
+        return p.page_table + (int64_t)b * p.pt_stride + pos / kPageSize;
+    }
+
+    // The token's lines into L2 (lanes first, first + step, ...).
+    __device__ __forceinline__ static void prefetch(const DecodeParams& p, int32_t b, int32_t c0,
+                                                    int first, int step) {
+        const int64_t src0 = ((int64_t)b * (p.Hkv * NH) + c0) * PER_HEAD;
+        for (int l = first; l < LINES; l += step) {
+            prefetch_l2(reinterpret_cast<const char*>(p.k_new + src0) + 128 * l);
+            prefetch_l2(reinterpret_cast<const char*>(p.v_new + src0) + 128 * l);
+        }
+    }
+
+    // Used by a producer warp that writes its own unit's token: start() at
+    // the start of unit x, finish() right before it issues the copy of the
+    // unit's last page, with that page's id (the lines have been on their
+    // way to L2 since start()).
+    int32_t b, c0, pos;
+    bool pending;
+
+    __device__ __forceinline__ void start(const DecodeParams& p, const UnitInfo& x) {
+        pending = due(p, x);
+        if (!pending) return;
+        b = x.b;
+        c0 = x.c * NH;
+        pos = x.g.len - 1;
+        prefetch(p, b, c0, threadIdx.x & 31, 32);
+    }
+
+    __device__ __forceinline__ void finish(const DecodeParams& p, int32_t page) {
+        if (!pending) return;
+        pending = false;
+        write(p, b, c0, pos, page);
+        fence_proxy_async_global();
+        __syncwarp();
+    }
+};
 
 // ---- pieces of the warp-specialised tcgen05 kernels
 

@@ -78,13 +78,13 @@ constexpr float MAX_SLACK = 2.0f;
 constexpr int al(int x) { return (x + 127) / 128 * 128; }
 // barriers: k_full / k_empty [NKS], v_full / v_empty [NVMAX], two each of
 // s_full, s_free, NPB each of p_full, pv_done, two each of o_free, q_full,
-// q_free, and fin
+// q_free, fin, and tok
 constexpr int NVMAX = NKS + NVS;                  // V slots when K == V (no K ring)
 constexpr int B_KFULL = 0, B_KEMPTY = NKS, B_VFULL = 2 * NKS, B_VEMPTY = 2 * NKS + NVMAX,
               B_SFULL = 2 * NKS + 2 * NVMAX, B_SFREE = B_SFULL + 2,
               B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + NPB, B_OFREE = B_PVDONE + NPB,
               B_QFULL = B_OFREE + 2, B_QFREE = B_QFULL + 2, B_FIN = B_QFREE + 2,
-              NBARS = B_FIN + 1;
+              B_TOK = B_FIN + 1, NBARS = B_TOK + 1;
 static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
 
 // Geometry per head dim.  Both give 32 KB K and V slots.  ALIAS: K and V
@@ -167,6 +167,15 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
 
 // ------------------------------------------------------------------ producer
 
+// Who writes this step's token of a unit that holds its row's last page:
+// the producer itself for the CTA's first unit when that unit is short (its
+// last page is copied right away, before the q warp could have written the
+// token), the q warp for every other such unit.
+template <class G>
+__device__ __forceinline__ bool producer_writes_token(const UnitInfo& x, bool first_unit) {
+    return first_unit && (x.np + G::SSP - 1) / G::SSP <= 2;
+}
+
 // Warp 5.  For each superstage m of each unit: wait until K slot m % NKS and
 // V slot m % NVE are free, arm their "full" barriers with the bytes of the
 // good pages, and let lanes 0..SSP-1 each copy one page, K (every 128-dim
@@ -198,6 +207,10 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
     }
     uint32_t seq = 0;                 // superstages armed so far
     bool stop = false;
+    using Tok = TokenAppend<G::D, GA_KV_E4M3, G::HP>;
+    Tok tok;                          // a token this warp writes itself
+    bool tokens_written = false;      // the q warp's B_TOK arrival has been seen
+    bool first_unit = true;
     while (have && !stop) {
         // The next unit: its length is on its way; once it has arrived (after
         // this unit's first superstage) its first page ids are loaded too.
@@ -222,6 +235,10 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
         }
         const int32_t* tbl = p.page_table + (int64_t)x.b * p.pt_stride + x.p0;
         const bool log = p.touch_log != nullptr && x.c == 0 && x.hg == 0;
+        const bool own_token = producer_writes_token<G>(x, first_unit);
+        tok.pending = false;
+        if (own_token) tok.start(p, x);
+        first_unit = false;
         constexpr int SPB = 32 / G::SSP;  // superstages per batch of 32 page ids
         const int nss = (x.np + G::SSP - 1) / G::SSP;
         for (int s = 0; s < nss; ++s) {
@@ -230,10 +247,14 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
                 const int nb = 32 * (s / SPB + 1) + lane;
                 ids_nxt = (nb < x.np) ? __ldg(tbl + nb) : -1;
             }
+            // the superstage with the row's last page: after the step's token
+            if (s == nss - 1) tok.finish(p, __shfl_sync(0xffffffffu, ids, (x.np - 1) & 31));
+            const bool tok_wait =
+                !tokens_written && !own_token && s == nss - 1 && Tok::due(p, x);
             const uint32_t n = seq, kslot = n % NKS, vslot = n % G::NVE;
             bool ok = true;
             if (lane == 0)
-                ok = !*abort_flag &&
+                ok = !*abort_flag && (!tok_wait || wait_or_abort(bar(bars, B_TOK), 0, abort_flag)) &&
                      (G::ALIAS ||
                       wait_or_abort(bar(bars, B_KEMPTY + kslot), ((n / NKS) & 1) ^ 1, abort_flag)) &&
                      wait_or_abort(bar(bars, B_VEMPTY + vslot), ((n / G::NVE) & 1) ^ 1, abort_flag);
@@ -246,6 +267,7 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
                 stop = true;
                 break;
             }
+            tokens_written |= tok_wait;
             const int pl = lane % G::SSP;
             const int pi = G::SSP * s + pl;
             const int32_t pid = __shfl_sync(0xffffffffu, ids, (G::SSP * (s % SPB) + pl) & 31);
@@ -438,6 +460,41 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 // columns past the unit's valid ones are zero.  Lane l takes column l / 4,
 // dims D/4 (l % 4) .. +D/4-1.  Buffer k % 2 is rewritten once the softmax
 // warps are done with active unit k - 2 (its scales read, all its S consumed).
+// The q warp, once per launch: this step's token of every other unit of the
+// CTA that holds its row's last page, written into that page (the producer
+// waits on B_TOK before it copies such a page).  Lane i takes the CTA's
+// units i, i + 32, ...: their page-table entries and token lines are fetched
+// in parallel, then the warp writes one unit's token at a time.
+template <class G>
+__device__ void append_tokens(const DecodeParams& p, const int32_t* pre, int64_t U,
+                              uint32_t bars) {
+    using Tok = TokenAppend<G::D, GA_KV_E4M3, G::HP>;
+    const int lane = threadIdx.x & 31;
+    for (int64_t u0 = blockIdx.x; u0 < U; u0 += 32 * (int64_t)gridDim.x) {
+        const int64_t u = u0 + (int64_t)lane * gridDim.x;
+        UnitInfo x = {};
+        bool due = false;
+        if (u < U) {
+            x = unit_info(p, pre, u);
+            due = Tok::due(p, x) && !producer_writes_token<G>(x, u == blockIdx.x);
+        }
+        const int32_t pos = x.g.len - 1, c0 = x.c * G::HP;
+        int32_t page = -1;
+        if (due) {
+            Tok::prefetch(p, x.b, c0, 0, 1);
+            page = __ldg(Tok::page_entry(p, x.b, pos));
+        }
+        for (uint32_t m = __ballot_sync(0xffffffffu, due); m != 0; m &= m - 1) {
+            const int j = __ffs(m) - 1;
+            Tok::write(p, __shfl_sync(0xffffffffu, x.b, j), __shfl_sync(0xffffffffu, c0, j),
+                       __shfl_sync(0xffffffffu, pos, j), __shfl_sync(0xffffffffu, page, j));
+        }
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(bars, B_TOK));
+}
+
 template <class G>
 __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                        uint32_t bars, volatile int* abort_flag) {
@@ -448,7 +505,13 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
     const int f = lane >> 2, d0 = (G::D / 4) * (lane & 3);
     UnitCursor cur(p, pre, U);
     uint32_t k = 0;
+    // this step's tokens once the first unit's q is ready (or at the end)
+    bool tokens = p.k_new == nullptr;
     while (cur.more()) {
+        if (k == 1 && !tokens) {
+            append_tokens<G>(p, pre, U, bars);
+            tokens = true;
+        }
         const UnitInfo y = cur.take(p, pre);
         if (y.np == 0) continue;
         const uint32_t qb = k & 1;
@@ -513,6 +576,7 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
         if (lane == 0) mbar_arrive(bar(bars, B_QFULL + (int)qb));
         ++k;
     }
+    if (!tokens) append_tokens<G>(p, pre, U, bars);
 }
 
 // ------------------------------------------------------------------ softmax warps
@@ -876,6 +940,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar(bars, B_QFREE + i), NSW);    // each softmax warp is done with it
         }
         mbar_init(bar(bars, B_FIN), 2);                // both issuers' last commits
+        mbar_init(bar(bars, B_TOK), 1);                // the q warp wrote the step's tokens
         mbar_init_fence();
         abort_flag = 0;
     }
@@ -989,6 +1054,10 @@ static int run_tc(const DecodeArgs& a) {
     p.touch_log = (pl.flags & GA_PLAN_TOUCH_LOG)
                       ? reinterpret_cast<int32_t*>(ws + pl.touch_log_offset)
                       : nullptr;
+    p.k_new = static_cast<const uint4*>(a.k_new);
+    p.v_new = static_cast<const uint4*>(a.v_new);
+    p.k_pool = const_cast<void*>(a.k_pool);
+    p.v_pool = const_cast<void*>(a.v_pool);
     p.err_word = a.err_word;
     p.pt_stride = a.pt_stride;
     p.num_pages = a.num_pages;

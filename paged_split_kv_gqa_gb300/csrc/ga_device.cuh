@@ -90,6 +90,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for global memory: generic stores before a bulk tensor copy that
+// reads them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -348,5 +354,25 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Eight bf16 values (one uint4) as eight E4M3FN codes of fp32(x) / scale
+// (IEEE division, round to nearest even, saturating to +-448): the KV page
+// append's quantisation ("[Model] Gemma 4 M2 26B-A4B", Proposed Plan: opt-in
+// FP8 KV pool for the sliding family).
+__device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float a = __fdiv_rn(bf16_lo(w[2 * i]), scale);
+        const float b = __fdiv_rn(bf16_hi(w[2 * i]), scale);
+        const float c = __fdiv_rn(bf16_lo(w[2 * i + 1]), scale);
+        const float d = __fdiv_rn(bf16_hi(w[2 * i + 1]), scale);
+        const uint32_t ab = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t cd = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+        out[i] = (ab & 0xFFFFu) | (cd << 16);
+    }
+    return make_uint2(out[0], out[1]);
+}
 
 }  // namespace ga

@@ -33,6 +33,10 @@ struct DecodeArgs {
     void* out;
     int32_t* err_word;
     cudaStream_t stream;
+    // this step's token [B, Hkv, D] bf16, written by the decode kernel itself
+    // at position seq_lens[b] - 1 before it reads that page, or null
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
 };
 
 // Builds a 3-D tensor map over a row-major [rows, D] array (a KV pool as

@@ -81,12 +81,17 @@ def _load():
                                           i64, f32, P, p, sz, p, p, p]
     lib.ga_decode_global_hd512.argtypes = [p, p, p, i32, p, p, p, i64, p, i32, i32, i32, i32,
                                            i64, f32, P, p, sz, p, p, p]
+    lib.ga_decode_local_hd256_append.argtypes = [p, p, p, p, p, i32, p, p, p, i64, p, i32, i32,
+                                                 i32, i32, i32, i64, f32, P, p, sz, p, p, p]
+    lib.ga_decode_global_hd512_append.argtypes = [p, p, p, p, p, i32, p, p, p, i64, p, i32, i32,
+                                                  i32, i32, i64, f32, P, p, sz, p, p, p]
     lib.ga_splitkv_combine.argtypes = [p, p, P, p, i64, p, p, p]
     lib.ga_decode_global_hd512_noalloc.argtypes = [p, p, p, i32, p, p, p, i64, p, i32, i32, i32,
                                                    i32, i64, f32, P, p, p, p]
     for fn in ("ga_plan_splits", "ga_plan_splits_mq", "ga_kv_append", "ga_decode_local_hd256",
                "ga_decode_global_hd512", "ga_splitkv_combine", "ga_check_error_word",
-               "ga_decode_global_hd512_noalloc", "ga_read_stream"):
+               "ga_decode_global_hd512_noalloc", "ga_read_stream",
+               "ga_decode_local_hd256_append", "ga_decode_global_hd512_append"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.ga_read_stream.argtypes = [p, i64, p, p]
     lib.ga_check_error_word.argtypes = [i32]
@@ -226,6 +231,48 @@ def ga_decode_global_hd512(q, k_pool, v_pool, page_table, seq_lens, *, scale, pl
                    page_table, seq_lens, window=None, scale=scale, plan=plan,
                    workspace=workspace, out=out, k_scale=k_scale, v_scale=v_scale,
                    err_word=err_word, stream=stream)
+
+
+def _decode_append(fn, name, k_new, v_new, q, k_pool, v_pool, page_table, seq_lens, *, window,
+                   scale, plan, workspace, out, k_scale, v_scale, err_word, stream):
+    B, Hq, D = q.shape
+    if plan.q_len != 1 or out.shape != q.shape or k_new.shape != (B, k_pool.shape[1], D) \
+            or v_new.shape != k_new.shape:
+        raise GAError(GA_ERR_INVALID_ARG, f"{name}: q / out / k_new / v_new shapes")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = [_ptr(k_new), _ptr(v_new), _ptr(q), _ptr(k_pool), _ptr(v_pool), _kv_dtype(k_pool),
+            _ptr(k_scale), _ptr(v_scale), _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
+            B, Hq, k_pool.shape[1]]
+    if window is not None:
+        args.append(window)
+    args += [k_pool.shape[2], k_pool.shape[0], float(scale), ctypes.byref(plan), _ptr(workspace),
+             ws_bytes, _ptr(out), _ptr(err_word), _stream(stream)]
+    _check(fn(*args), name)
+    return out
+
+
+def ga_decode_local_hd256_append(k_new, v_new, q, k_pool, v_pool, page_table, seq_lens, *,
+                                 window, scale, plan, workspace=None, out=None, k_scale=None,
+                                 v_scale=None, err_word=None, stream=None):
+    """Append this step's token (at seq_lens - 1) and decode, in one launch."""
+    if out is None:
+        out = torch.empty_like(q)
+    return _decode_append(_lib.ga_decode_local_hd256_append, "ga_decode_local_hd256_append",
+                          k_new, v_new, q, k_pool, v_pool, page_table, seq_lens, window=window,
+                          scale=scale, plan=plan, workspace=workspace, out=out, k_scale=k_scale,
+                          v_scale=v_scale, err_word=err_word, stream=stream)
+
+
+def ga_decode_global_hd512_append(k_new, v_new, q, k_pool, v_pool, page_table, seq_lens, *,
+                                  scale, plan, workspace=None, out=None, k_scale=None,
+                                  v_scale=None, err_word=None, stream=None):
+    """Append this step's token (at seq_lens - 1) and decode, in one launch."""
+    if out is None:
+        out = torch.empty_like(q)
+    return _decode_append(_lib.ga_decode_global_hd512_append, "ga_decode_global_hd512_append",
+                          k_new, v_new, q, k_pool, v_pool, page_table, seq_lens, window=None,
+                          scale=scale, plan=plan, workspace=workspace, out=out, k_scale=k_scale,
+                          v_scale=v_scale, err_word=err_word, stream=stream)
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

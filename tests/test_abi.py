@@ -39,7 +39,8 @@ def test_every_declared_symbol_is_exported(ga):
 
 def test_python_binding_has_same_names(ga):
     for name in ("ga_kv_append", "ga_decode_local_hd256", "ga_decode_global_hd512",
-                 "ga_splitkv_combine", "ga_plan_splits", "ga_check_error_word", "ga_version"):
+                 "ga_splitkv_combine", "ga_plan_splits", "ga_check_error_word", "ga_version",
+                 "ga_decode_local_hd256_append", "ga_decode_global_hd512_append"):
         assert callable(getattr(ga, name)), name
 
 

@@ -83,3 +83,38 @@ def test_wait_runs_out_reports_and_context_survives(ga, case):
                           fi.seq_lens.cpu(), num_kv_heads=fam.num_kv_heads, window=fam.window,
                           scale=scale)
     assert_close(out.float().cpu().numpy(), ref, kv_dtype=fam.kv_dtype, what=case)
+
+
+@pytest.mark.parametrize("case", ["local_bf16", "global_e4m3", "local_e4m3_4_heads"])
+def test_fused_append_wait_runs_out(ga, case):
+    """The decode call with the KV append fused in, under the same hook: the
+    timeout is reported and the call returns; the same call without the hook
+    then appends (again: the token bits are the same) and decodes correctly."""
+    fam, _ = CASES[case]
+    lens = np.array([200, 77, 130, 40], dtype=np.int32)
+    fi = W.make_family_inputs(W.Workload("fail", lens, 16, fam, fam), fam, device=DEV, seed=7)
+    extra = getattr(ga, FLAGS[case]) if case in FLAGS else 0
+    kw = dict(num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
+              head_dim=fam.head_dim, window=fam.window, requested_splits=2)
+    fused = ga.ga_decode_local_hd256_append if fam.window else ga.ga_decode_global_hd512_append
+    call_kw = dict(scale=1.0 / math.sqrt(fam.head_dim), k_scale=fi.k_scale, v_scale=fi.v_scale)
+    if fam.window:
+        call_kw["window"] = fam.window
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for flags in (ga.GA_PLAN_TEST_WAIT_TIMEOUT | extra, extra):
+        plan = ga.ga_plan_splits(lens, flags=flags, **kw)
+        if extra:
+            plan.kv_heads_per_unit = 4
+        out = torch.empty_like(fi.q)
+        err.zero_()
+        t0 = time.time()
+        fused(fi.k_new, fi.v_new, fi.q, fi.k_pool, fi.v_pool, fi.page_table, fi.seq_lens,
+              plan=plan, workspace=ga.workspace_for(plan, DEV), out=out, err_word=err, **call_kw)
+        torch.cuda.synchronize()
+        assert time.time() - t0 < 30.0
+        word = int(err.item())
+        if flags & ga.GA_PLAN_TEST_WAIT_TIMEOUT:
+            assert word & ga.GA_DEVERR_TIMEOUT, hex(word)
+        else:
+            assert word == 0, hex(word)
+    assert_close(out.float().cpu().numpy(), oracle_decode(fi), kv_dtype=fam.kv_dtype, what=case)

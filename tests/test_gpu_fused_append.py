@@ -148,3 +148,56 @@ def test_fused_append_rejects_multi_query_plan(ga):
         ga.ga_decode_global_hd512_append(fi.k_new, fi.v_new, fi.q, fi.k_pool, fi.v_pool,
                                          fi.page_table, fi.seq_lens, scale=0.1, plan=plan)
     assert exc.value.status == ga.GA_ERR_INVALID_ARG
+
+
+FULL = {
+    # (workload index, family, plan flags): the launch configurations the bench times
+    "31b_local_bf16": (3, "local", 0),
+    "31b_global_bf16": (3, "global", 0),
+    "ragged_local_e4m3": (5, "local", "e4m3"),
+    "ragged_global_bf16": (5, "global", 0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FULL))
+def test_fused_append_full_size(ga, case):
+    """Full-size batches with the bench's plans (several units per CTA, so the
+    tcgen05 kernel's q warp writes the tokens of a CTA's later units): pools
+    and outputs bit-identical to the two-launch step, and sampled rows
+    against the oracle."""
+    from tests.helpers import oracle_decode_rows_gathered
+    idx, which, flags = FULL[case]
+    wl = W.config(idx)
+    fam = wl.local if which == "local" else wl.global_
+    fi = W.make_family_inputs(wl, fam, device=DEV, seed=5, poison=True,
+                              release_old=fam.window > 0)
+    plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                             num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
+                             window=fam.window,
+                             flags=ga.GA_PLAN_KV_E4M3 if flags == "e4m3" else 0)
+    if case == "ragged_local_e4m3":
+        assert plan.kv_heads_per_unit == 4
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = ga.workspace_for(plan, DEV)
+    k1, v1 = _pools(fi)
+    pos = (fi.seq_lens - 1).to(torch.int32)
+    ga.ga_kv_append(fi.k_new, fi.v_new, k1, v1, fi.page_table, pos, k_scale=fi.k_scale,
+                    v_scale=fi.v_scale, err_word=err)
+    out1 = torch.empty_like(fi.q)
+    dec = ga.ga_decode_local_hd256 if fam.window else ga.ga_decode_global_hd512
+    dec(fi.q, k1, v1, fi.page_table, fi.seq_lens, **_kw(fam, fi, plan, ws, out1, err, k1, v1))
+    k2, v2 = fi.k_pool, fi.v_pool            # appended in place by the fused call
+    out2 = torch.empty_like(fi.q)
+    fused = ga.ga_decode_local_hd256_append if fam.window else ga.ga_decode_global_hd512_append
+    fused(fi.k_new, fi.v_new, fi.q, k2, v2, fi.page_table, fi.seq_lens,
+          **_kw(fam, fi, plan, ws, out2, err, k2, v2))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _same(out1, out2), f"{case}: outputs differ"
+    assert _same(k1, k2) and _same(v1, v2), f"{case}: pools differ"
+    del k1, v1
+    rows = W.sample_rows(wl.batch, 8)
+    assert_close(out2[rows].float().cpu().numpy(), oracle_decode_rows_gathered(fi, rows),
+                 kv_dtype=fam.kv_dtype, what=case)
+    del fi
+    torch.cuda.empty_cache()

@@ -22,23 +22,30 @@ struct CombineParams {
     int64_t pt_stride;
     int64_t rc_capacity;
     int32_t B, Hq, D, window, mode, splits, chunk_pages;
+    int32_t rows_per_cta;   // consecutive rows of one CTA
 };
 
-// One CTA of 4 warps per (4 merge tasks, row); a task is one column's 128-dim
-// block, taken by one warp (merge_warp128).  Every CTA finds its row's first
-// row-chunk from the lengths of the rows before it (a strided sum over its 128
-// threads).  Wider CTAs (8 warps, 16 tasks) repeat that O(B) sum less often
-// but serialise the merges of small batches: the ragged 60-layer step at
-// B = 1 took 1.108 ms with them against 0.834 ms with these.
+// One CTA of 4 warps per (4 merge tasks, block of rows_per_cta consecutive
+// rows); a task is one column's 128-dim block, taken by one warp
+// (merge_warp128).  A CTA finds its first row's first row-chunk from the
+// lengths of the rows before it (a strided sum over its 128 threads) and
+// steps through its other rows from there.  The host makes row blocks of
+// ceil(B / 128) rows, so at most 128 row blocks sum their prefixes: O(B) per
+// CTA, O(B * tasks / 4 * 128) in all, at any batch.  Small batches keep one
+// row per CTA: wider CTAs (8 warps, 16 tasks) serialised the merges there
+// (the ragged 60-layer step at B = 1 took 1.108 ms with them against 0.834 ms
+// with these).
 constexpr int kCombineWarps = 4;
 constexpr int kTasksPerCta = 4;
+constexpr int kCombineRowBlocks = 128;
 
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const CombineParams p) {
-    const int b = blockIdx.y;
+    const int b0 = blockIdx.y * p.rows_per_cta;
+    const int b1 = min(p.B, b0 + p.rows_per_cta);
     __shared__ int32_t s_red[kCombineWarps];
-    // row-chunk offset of row b: chunks of all rows before it
+    // row-chunk offset of row b0: chunks of all rows before it
     int32_t part = 0;
-    for (int r = threadIdx.x; r < b; r += blockDim.x)
+    for (int r = threadIdx.x; r < b0; r += blockDim.x)
         part += row_geometry(__ldg(p.seq_lens + r), p.window, p.pt_stride, p.mode, p.splits,
                              p.chunk_pages).chunks;
 #pragma unroll
@@ -47,21 +54,25 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
     __syncthreads();
     int64_t rc0 = 0;
     for (int wv = 0; wv < kCombineWarps; ++wv) rc0 += s_red[wv];
-    const RowGeom g = row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride, p.mode,
-                                   p.splits, p.chunk_pages);
-    const int S = g.chunks;
-    if (S <= 1) return;                       // written by the decode kernel
-    if (rc0 + S > p.rc_capacity) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) report(p.err_word, kErrCapacity);
-        return;
-    }
     const int nb = p.D / 128;
-    for (int t = blockIdx.x * kTasksPerCta + (threadIdx.x >> 5);
-         t < min(p.Hq * nb, (int)(blockIdx.x + 1) * kTasksPerCta); t += kCombineWarps) {
-        const int h = t / nb, d0 = (t % nb) * 128;
-        const uint2 o = merge_warp128(p.po, p.plse, rc0, S, p.Hq, p.D, h, d0);
-        *reinterpret_cast<uint2*>(p.out + ((int64_t)b * p.Hq + h) * p.D + d0 +
-                                  4 * (threadIdx.x & 31)) = o;
+    for (int b = b0; b < b1; ++b) {
+        const RowGeom g = row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride, p.mode,
+                                       p.splits, p.chunk_pages);
+        const int S = g.chunks;
+        if (S > 1) {                          // (one chunk: written by the decode kernel)
+            if (rc0 + S > p.rc_capacity) {
+                if (threadIdx.x == 0 && blockIdx.x == 0) report(p.err_word, kErrCapacity);
+                return;
+            }
+            for (int t = blockIdx.x * kTasksPerCta + (threadIdx.x >> 5);
+                 t < min(p.Hq * nb, (int)(blockIdx.x + 1) * kTasksPerCta); t += kCombineWarps) {
+                const int h = t / nb, d0 = (t % nb) * 128;
+                const uint2 o = merge_warp128(p.po, p.plse, rc0, S, p.Hq, p.D, h, d0);
+                *reinterpret_cast<uint2*>(p.out + ((int64_t)b * p.Hq + h) * p.D + d0 +
+                                          4 * (threadIdx.x & 31)) = o;
+            }
+        }
+        rc0 += S;
     }
 }
 
@@ -86,8 +97,10 @@ int launch_combine(const float* partial_o, const float* partial_lse, const ga_pl
     p.splits = plan->splits;
     p.chunk_pages = plan->chunk_pages;
     if (p.B == 0) return GA_OK;
+    p.rows_per_cta = (p.B + kCombineRowBlocks - 1) / kCombineRowBlocks;
     const int tasks = p.Hq * (p.D / 128);
-    dim3 grid((tasks + kTasksPerCta - 1) / kTasksPerCta, p.B);
+    dim3 grid((tasks + kTasksPerCta - 1) / kTasksPerCta,
+              (p.B + p.rows_per_cta - 1) / p.rows_per_cta);
     combine_kernel<<<grid, 32 * kCombineWarps, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? GA_OK : GA_ERR_CUDA;
 }

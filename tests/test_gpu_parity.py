@@ -473,16 +473,20 @@ def test_e4m3_large_q_is_exact_enough_and_inf_q_reported(ga, err):
     assert int(err.item()) & ga.GA_DEVERR_Q_RANGE
 
 
-def test_combine_kernel_alone(ga, err):
-    """GPU combine on random fp32 partials vs the oracle's LSE merge."""
-    lens = [300, 17, 900, 0]
-    Hq, D = 8, 512
+_BIG_BATCH = [int(x) for x in np.random.default_rng(3).integers(0, 400, 700)]
+
+
+@pytest.mark.parametrize("lens", [[300, 17, 900, 0], _BIG_BATCH], ids=["4_rows", "700_rows"])
+def test_combine_kernel_alone(ga, err, lens):
+    """GPU combine on random fp32 partials vs the oracle's LSE merge (700 rows:
+    the combine takes blocks of several consecutive rows per CTA)."""
+    Hq, D = (8, 512) if len(lens) < 100 else (2, 256)
     plan = ga.ga_plan_splits(lens, num_q_heads=Hq, num_kv_heads=2, head_dim=D, window=0,
                              fixed_chunk_tokens=64)
     g = torch.Generator(device="cpu").manual_seed(15)
     po = torch.randn(plan.row_chunks, Hq, D, generator=g)
     pl = torch.randn(plan.row_chunks, Hq, generator=g) * 3
-    pl[1, 2] = -float("inf")
+    pl[1, Hq - 1] = -float("inf")
     seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
     out = torch.zeros(len(lens), Hq, D, dtype=torch.bfloat16, device=DEV)
     ga.ga_splitkv_combine(po.to(DEV), pl.to(DEV), plan, seq, 64, out, err_word=err)

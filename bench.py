@@ -565,7 +565,9 @@ def run_ga(args):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     pg = None
-    if world > 1:
+    # under torchrun (even with one rank) the barrier and the max over ranks
+    # run through the process group, as they do on N GPUs
+    if world > 1 or "LOCAL_WORLD_SIZE" in os.environ:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
         pg = dist
@@ -916,6 +918,9 @@ def main():
                          "mma.sync units of 32")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    world = dist_env()[2]
+    if "WORLD_SIZE" in os.environ and args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but {world} ranks were launched")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -442,6 +442,7 @@ def line_config(args, wl, world):
     reference arm: the workload, the whole-job batch and what keeps each timed
     repetition reading from HBM."""
     return {"workload": workload_text(args), "global_batch": wl.batch * world,
+            "parallelism": f"replicas x{world}: one independent batch per rank, no exchange",
             "l2": l2_claim(host_schedule(args, wl))}
 
 

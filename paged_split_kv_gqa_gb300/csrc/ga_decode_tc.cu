@@ -453,13 +453,6 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 
 // ------------------------------------------------------------------ q warp
 
-// Warp 6.  For each active unit (one with pages), in the order the MMA issuer
-// takes them: the unit's q rows as the QK operand in buffer k % 2 -- column f
-// scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row 8 + f
-// of each 128-dim region ([16 rows][128 B], 128-byte swizzle); rows of
-// columns past the unit's valid ones are zero.  Lane l takes column l / 4,
-// dims D/4 (l % 4) .. +D/4-1.  Buffer k % 2 is rewritten once the softmax
-// warps are done with active unit k - 2 (its scales read, all its S consumed).
 // The q warp, once per launch: this step's token of every other unit of the
 // CTA that holds its row's last page, written into that page (the producer
 // waits on B_TOK before it copies such a page).  Lane i takes the CTA's
@@ -495,6 +488,13 @@ __device__ void append_tokens(const DecodeParams& p, const int32_t* pre, int64_t
     if (lane == 0) mbar_arrive(bar(bars, B_TOK));
 }
 
+// Warp 6.  For each active unit (one with pages), in the order the MMA issuer
+// takes them: the unit's q rows as the QK operand in buffer k % 2 -- column f
+// scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row 8 + f
+// of each 128-dim region ([16 rows][128 B], 128-byte swizzle); rows of
+// columns past the unit's valid ones are zero.  Lane l takes column l / 4,
+// dims D/4 (l % 4) .. +D/4-1.  Buffer k % 2 is rewritten once the softmax
+// warps are done with active unit k - 2 (its scales read, all its S consumed).
 template <class G>
 __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                        uint32_t bars, volatile int* abort_flag) {

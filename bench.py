@@ -139,10 +139,11 @@ WORKLOADS = {"31b": 3, "12b": 2, "long": 4, "ragged": 5}
 
 
 MQ_UNIT_FLAGS = {"auto": 0, "tc": "GA_PLAN_TENSOR_CORE_UNITS", "cp": "GA_PLAN_COLUMN_PARALLEL_UNITS"}
+DEALS = {"round-robin": 0, "rows-by-size": 1}      # ga_plan.schedule
 
 
 def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, mq_units="auto",
-               fp8_units=0, separate_append=False):
+               fp8_units=0, separate_append=False, deal="auto"):
     """One layer's inputs.  q_len > 1: a multi-query step (q_len new tokens
     per row at its last positions, e.g. a speculative-decoding verify): the
     pools keep the union of the queries' windows, q / out are
@@ -180,6 +181,8 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, 
                              (getattr(ga, unit_flag) if unit_flag else 0), q_len=S)
     if fp8_units and fam.kv_dtype == W.KV_E4M3 and fam.window > 0:
         plan.kv_heads_per_unit = fp8_units        # A/B: force the E4M3 unit width
+    if deal != "auto" and plan.mode == ga.GA_SPLIT_NONE and S == 1:
+        plan.schedule = DEALS[deal]               # A/B: force how units are dealt to CTAs
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
     esz = 1 if fam.kv_dtype == W.KV_E4M3 else 2
@@ -215,7 +218,8 @@ def workload_config(workload, seed, fp8="none"):
 
 
 def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, splits=0,
-               q_len=1, fp8="none", mq_units="auto", fp8_units=0, separate_append=False):
+               q_len=1, fp8="none", mq_units="auto", fp8_units=0, separate_append=False,
+               deal="auto"):
     """The layers one step launches, in order.  31b / 12b / long: one local and
     one global layer.  ragged: 50 local + 10 global layers in 5:1 order, the
     layers of a family rotating over `pools` distinct KV pools (each > L2).
@@ -229,7 +233,7 @@ def build_step(device, seed, workload="31b", rows=0, pools=4, kv_alias=False, sp
                         wl.page_size, wl.local, wl.global_, wl.local_layers, wl.global_layers)
     npool = pools if workload == "ragged" else 1
     sets = {fam.name: [make_layer(device, wl, fam, seed, i, kv_alias, splits, q_len, mq_units,
-                                  fp8_units, separate_append)
+                                  fp8_units, separate_append, deal)
                        for i in range(npool)]
             for fam in wl.families()}
     if workload == "ragged":
@@ -401,6 +405,8 @@ def workload_text(args):
         text += f"; E4M3 sliding-family units of {args.fp8_units} kv heads forced"
     if args.separate_append:
         text += "; append kernel launched before each decode (not fused)"
+    if args.deal != "auto":
+        text += f"; one-chunk plans deal units {args.deal}"
     if args.mq_units != "auto":
         text += {"tc": "; tcgen05 units of 64 columns forced",
                  "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
@@ -575,7 +581,7 @@ def run_ga(args):
     wl, schedule, sets, err = build_step(device, args.seed + rank, args.workload, args.rows,
                                          args.pools, args.kv_alias, args.splits, args.q_len,
                                          args.fp8, args.mq_units, args.fp8_units,
-                                         args.separate_append)
+                                         args.separate_append, args.deal)
 
     def step(evs=None):
         n = 0
@@ -910,6 +916,9 @@ def main():
     ap.add_argument("--separate-append", action="store_true",
                     help="one-query steps launch the append kernel before the decode instead "
                          "of the decode call with the append fused (A/B)")
+    ap.add_argument("--deal", default="auto", choices=["auto"] + sorted(DEALS),
+                    help="how one-chunk one-query plans deal work units to the CTAs: the "
+                         "planner's choice, or forced (A/B)")
     ap.add_argument("--fp8-units", type=int, default=0,
                     help="kv heads per unit of the E4M3 sliding-family decode (1, or 8 / group): "
                          "forces the width the planner would otherwise choose (A/B)")

@@ -152,8 +152,19 @@ typedef struct ga_plan {
                                     1, or 8 / group when the plan has GA_PLAN_KV_E4M3 and the
                                     planner found such units better (see that flag).  A caller
                                     may set it to 1 or to that value; other kernels ignore it. */
-    int32_t reserved;            /* 0 */
+    int32_t schedule;            /* how the persistent CTAs deal out the units:
+                                    GA_SCHEDULE_ROUND_ROBIN (unit i to CTA i mod grid), or
+                                    GA_SCHEDULE_ROWS_BY_SIZE (one-chunk one-query plans of at
+                                    most 1791 rows: rows in descending order of attended
+                                    pages, every other pass over the CTAs reversed).  The
+                                    planner picks the second when it evens out CTA loads of
+                                    unequal rows.  Results do not depend on it. */
 } ga_plan;
+
+enum {
+    GA_SCHEDULE_ROUND_ROBIN = 0,
+    GA_SCHEDULE_ROWS_BY_SIZE = 1
+};
 
 /*
  * ga_plan_splits -- choose how each row's attended pages are cut into split-KV

@@ -150,6 +150,7 @@ struct Candidate {
     int32_t mode, splits, chunk_pages;
     int64_t row_chunks = 0, units = 0;
     int32_t max_cp = 0;
+    int32_t schedule = kScheduleRoundRobin;
     double cost = 0;
 };
 
@@ -188,6 +189,30 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     }
     double makespan = 0;
     for (double v : load) makespan = std::max(makespan, v);
+    // One chunk per row: the rows-by-size deal (longest rows first, every
+    // other pass reversed) when it evens the CTA loads out by more than 3 %
+    // (the ragged 256-row sliding family: 213 against 238 superstages on the
+    // busiest CTA).  It is simulated here exactly as the kernels deal it.
+    cand.schedule = kScheduleRoundRobin;
+    if (cand.mode == kSplitNone && in.S == 1 && sorted_schedule_fits(in.B) && cand.units > G) {
+        std::vector<int32_t> order((size_t)in.B);
+        for (int32_t b = 0; b < in.B; ++b) order[(size_t)b] = b;
+        std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+            return row_sort_key(rc_pages[(size_t)a]) < row_sort_key(rc_pages[(size_t)b]);
+        });
+        std::vector<double> sorted_load((size_t)G, 0.0);
+        for (int64_t u = 0; u < cand.units; ++u) {
+            const uint32_t pos = snake_position((uint32_t)u, (uint32_t)G, (uint32_t)cand.units);
+            const int32_t b = order[(size_t)(pos / per_rc)];
+            sorted_load[(size_t)(u % G)] += rc_pages[(size_t)b] * in.HP * in.page_weight + unit_ovh;
+        }
+        double sorted_span = 0;
+        for (double v : sorted_load) sorted_span = std::max(sorted_span, v);
+        if (sorted_span < 0.97 * makespan) {
+            makespan = sorted_span;
+            cand.schedule = kScheduleSorted;
+        }
+    }
     double combine = 0;
     if (split_rows_rc > 0) {
         const double page_bytes = 2.0 * kPageSize * in.D * 2.0;   // K + V page-head, bf16
@@ -305,6 +330,9 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     }
     ga_plan p{};
     p.kv_heads_per_unit = hp;
+    static_assert(GA_SCHEDULE_ROWS_BY_SIZE == kScheduleSorted &&
+                      GA_SCHEDULE_ROUND_ROBIN == kScheduleRoundRobin, "schedule ids");
+    p.schedule = best.schedule;
     p.mode = best.mode;
     p.splits = best.splits;
     p.chunk_pages = best.chunk_pages;

@@ -38,6 +38,7 @@ struct DecodeParams {
     int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
     int32_t S, mask_window;
     int32_t TW;                   // columns per work unit (8, or 8 x warps column-parallel)
+    int32_t schedule;             // kScheduleRoundRobin, or kScheduleSorted (pre = row order)
     int32_t test_wait_timeout;    // test hook: CTA 0's producer issues nothing
     float scale_log2;             // softmax scale * log2(e)
     int64_t out_elems;            // B * Hq * D
@@ -78,6 +79,19 @@ struct UnitLoc {
 __device__ __forceinline__ UnitLoc locate_unit(const DecodeParams& p, const int32_t* pre,
                                                int64_t u) {
     UnitLoc l;
+    if (p.schedule == kScheduleSorted) {
+        // slot u -> position in the rows-by-size order -> (row, kv head, head
+        // group); one chunk per row, so the row-chunk is the row
+        const uint32_t upr = (uint32_t)p.Hkv * (uint32_t)p.HG;
+        const uint32_t pos = snake_position((uint32_t)u, gridDim.x, (uint32_t)p.B * upr);
+        const uint32_t r = pos / upr, rem = pos - r * upr;
+        const uint32_t hg = (p.HG == 1) ? 0u : rem % (uint32_t)p.HG;
+        l.hg = (int32_t)hg;
+        l.c = (int32_t)((rem - hg) / (uint32_t)p.HG);
+        l.b = pre[r];
+        l.rc = l.b;
+        return l;
+    }
     if (u < (int64_t(1) << 31)) {      // unit_coords in 32 bits (64-bit division is slow)
         const uint32_t v = (uint32_t)u, hg = (uint32_t)p.HG, hkv = (uint32_t)p.Hkv;
         const uint32_t q1 = (hg == 1) ? v : v / hg;
@@ -104,7 +118,7 @@ __device__ __forceinline__ UnitInfo finish_unit(const DecodeParams& p, const int
     x.b = l.b;
     x.c = l.c;
     x.hg = l.hg;
-    x.j = (int32_t)(x.rc - pre[x.b]);
+    x.j = p.schedule == kScheduleSorted ? 0 : (int32_t)(x.rc - pre[x.b]);
     x.g = row_geometry(len, p.window, p.pt_stride, p.mode, p.splits, p.chunk_pages);
     chunk_pages_of(x.g, x.j, &x.p0, &x.np);
     x.h0 = x.c * p.group + x.hg * p.TW;
@@ -117,6 +131,62 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeParams& p, const int32
                                               int64_t u) {
     const UnitLoc l = locate_unit(p, pre, u);
     return finish_unit(p, pre, l, __ldg(p.seq_lens + l.b));
+}
+
+__device__ __forceinline__ int32_t row_key(const DecodeParams& p, int32_t b) {
+    return row_sort_key(row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride, p.mode,
+                                     p.splits, p.chunk_pages).npages);
+}
+
+// The rows-by-size schedule (one chunk per row, so pre[b] = b until now):
+// pre[0 .. B) becomes the rows in descending order of attended pages, ties
+// in row order -- the same order in every CTA (counts, then a stable scatter
+// by one warp); the kSortKeys ints after pre[B] are its counters.
+__device__ __forceinline__ void build_row_order(const DecodeParams& p, int32_t* pre,
+                                                int nthreads) {
+    int32_t* cnt = pre + p.B + 1;
+    for (int i = threadIdx.x; i < kSortKeys; i += nthreads) cnt[i] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < p.B; b += nthreads) atomicAdd(&cnt[row_key(p, b)], 1);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        constexpr int PER = (kSortKeys + 31) / 32;        // buckets per lane
+        int v[PER], run = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int k = lane * PER + i;
+            v[i] = k < kSortKeys ? cnt[k] : 0;
+            run += v[i];
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+        }
+        int start = incl - run;                           // first slot of bucket lane * PER
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int k = lane * PER + i;
+            if (k < kSortKeys) cnt[k] = start;
+            start += v[i];
+        }
+        __syncwarp();
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            const bool live = b < p.B;
+            const int key = live ? row_key(p, b) : kSortKeys + lane;   // dead lanes match none
+            const uint32_t peers = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int pos = live ? cnt[key] + rank : 0;
+            __syncwarp();
+            if (live && rank == __popc(peers) - 1) cnt[key] += __popc(peers);
+            __syncwarp();
+            if (live) pre[pos] = b;
+        }
+    }
+    __syncthreads();
 }
 
 // Every thread of the block: chunk count of every row, then an inclusive
@@ -155,6 +225,7 @@ __device__ __forceinline__ bool build_row_prefix(const DecodeParams& p, int32_t*
     __syncthreads();
     if (bad && blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrSeqLen);
     *total_rc = pre[p.B];
+    if (p.schedule == kScheduleSorted) build_row_order(p, pre, nthreads);
     if (p.mode != kSplitNone && *total_rc > p.rc_capacity) {
         if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrCapacity);
         return false;

@@ -46,6 +46,33 @@ GA_HD int32_t tc_heads_per_unit(int32_t plan_flags, int32_t head_dim, int32_t q_
 
 enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
 
+// How a persistent grid of G CTAs walks the U work units.  CTA i takes slots
+// i, i + G, i + 2G, ...  Round robin (kScheduleRoundRobin): slot = unit.
+// Rows by size (kScheduleSorted, one-chunk plans of one-query decodes): the
+// units are taken row by row in descending order of the row's attended
+// pages (ties in row order), and every odd pass over the G CTAs runs
+// backwards, so the CTA that took the largest unit of one pass takes the
+// smallest of the next (a longest-first, snake-order deal of unequal units).
+enum { kScheduleRoundRobin = 0, kScheduleSorted = 1 };
+constexpr int kSortKeys = 257;    // sort key = 256 - min(attended pages, 256)
+
+GA_HD int32_t row_sort_key(int32_t npages) {
+    return kSortKeys - 1 - (npages < kSortKeys - 1 ? npages : kSortKeys - 1);
+}
+
+// The sorted schedule keeps the row order and kSortKeys counters after the
+// row prefix in shared memory: batches up to kMaxBatch - kSortKeys rows.
+GA_HD bool sorted_schedule_fits(int32_t batch) { return batch + kSortKeys <= kMaxBatch; }
+
+// Slot s of a grid of G CTAs over U units -> its position in the sorted
+// order.  (Walking each CTA's passes from a different starting pass, so that
+// long and short rows would mix at any moment, measured slower.)
+GA_HD uint32_t snake_position(uint32_t s, uint32_t G, uint32_t U) {
+    const uint32_t r = s / G, q = s - r * G;
+    const uint32_t len = U - r * G < G ? U - r * G : G;      // CTAs in pass r
+    return r * G + ((r & 1u) ? len - 1u - q : q);
+}
+
 // Geometry of one row for one call: which keys it attends, which logical
 // pages hold them, and how those pages are cut into split-KV chunks.
 struct RowGeom {

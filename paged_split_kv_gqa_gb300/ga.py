@@ -38,6 +38,8 @@ GA_DEVERR_POSITION = 32
 GA_SPLIT_NONE = 0
 GA_SPLIT_COUNT = 1
 GA_SPLIT_CHUNK = 2
+GA_SCHEDULE_ROUND_ROBIN = 0
+GA_SCHEDULE_ROWS_BY_SIZE = 1
 GA_PLAN_TOUCH_LOG = 1
 GA_PLAN_EXTERNAL_COMBINE = 2
 GA_PLAN_TEST_WAIT_TIMEOUT = 4
@@ -61,7 +63,7 @@ class ga_plan(ctypes.Structure):
         (n, ctypes.c_int64) for n in ("row_chunks", "units", "workspace_bytes",
                                        "partial_o_offset", "partial_lse_offset",
                                        "touch_log_offset")] + [
-        (n, ctypes.c_int32) for n in ("kv_heads_per_unit", "reserved")]
+        (n, ctypes.c_int32) for n in ("kv_heads_per_unit", "schedule")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

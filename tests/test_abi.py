@@ -176,6 +176,12 @@ def test_decode_rejects_before_launch(ga):
     bad = _plan(ga)
     bad.col_tile = 16
     assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
+    bad = _plan(ga, requested_splits=2)
+    bad.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE                              # split plan
+    assert _decode_local(ga, bad, ws=FAKE, wsb=bad.workspace_bytes) == ga.GA_ERR_INVALID_ARG
+    bad = _plan(ga)
+    bad.schedule = 2                                                        # unknown
+    assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
 
 
 def test_append_rejects_before_launch(ga):

@@ -1,0 +1,157 @@
+"""The rows-by-size deal of work units (GA_SCHEDULE_ROWS_BY_SIZE: rows in
+descending order of attended pages, every other pass over the CTAs
+reversed) changes which CTA takes a unit, never what a unit computes: every
+decode kernel's outputs are bit-identical to the round-robin deal, the page
+sets read are the same, the fused append writes the same pools, and sampled
+rows match the oracle.  Batches with more units than CTAs (the plan made
+for 40 SMs) and unequal rows, including empty ones.  ("[Model] Gemma 4 M3
+31B", Proposed Plan: the split-KV / work policy re-checked per geometry.)"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from paged_split_kv_gqa_gb300 import workloads as W
+from tests.helpers import assert_close, oracle_decode_rows_gathered, run_decode
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+_rng = np.random.default_rng(11)
+LENS = [int(x) for x in np.clip(np.exp(_rng.normal(6.5, 1.2, 96)), 0, 4000).astype(int)]
+LENS[:6] = [0, 1, 16, 1023, 1024, 1025]
+
+CASES = {
+    "local_bf16": (W.Family("local", 16, 8, 256, 1024), {}),
+    "local_e4m3": (W.Family("local", 16, 8, 256, 1024, 1), {}),
+    "local_e4m3_4_heads": (W.Family("local", 16, 8, 256, 1024, 1), {"heads": 4}),
+    "local_e4m3_kv_alias": (W.Family("local", 16, 8, 256, 1024, 1), {"alias": True}),
+    "global_bf16_unsplit": (W.Family("global", 16, 2, 512, 0), {}),
+    "global_e4m3_unsplit": (W.Family("global", 16, 2, 512, 0, 1), {}),
+}
+
+
+@pytest.fixture(scope="module")
+def ga():
+    from paged_split_kv_gqa_gb300 import _build
+    _build.build()
+    from paged_split_kv_gqa_gb300 import ga as mod
+    return mod
+
+
+def _setup(case):
+    fam, opt = CASES[case]
+    wl = W.Workload("schedule", np.asarray(LENS, dtype=np.int32), 16, fam, fam)
+    fi = W.make_family_inputs(wl, fam, device=DEV, seed=23, poison=True,
+                              release_old=fam.window > 0)
+    if opt.get("alias"):
+        fi = dataclasses.replace(fi, v_pool=fi.k_pool, v_scale=fi.k_scale)
+    return fam, opt, fi
+
+
+def _plans(ga, fam, opt, flags=0):
+    kw = dict(num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
+              head_dim=fam.head_dim, window=fam.window, requested_splits=1, num_sms=40,
+              flags=flags | (ga.GA_PLAN_KV_E4M3 if fam.kv_dtype == W.KV_E4M3 else 0))
+    out = []
+    for sched in (ga.GA_SCHEDULE_ROUND_ROBIN, ga.GA_SCHEDULE_ROWS_BY_SIZE):
+        plan = ga.ga_plan_splits(LENS, **kw)
+        if opt.get("heads"):
+            plan.kv_heads_per_unit = opt["heads"]
+        plan.schedule = sched
+        assert plan.units > plan.grid
+        out.append(plan)
+    return out
+
+
+def _bits(t):
+    return t.contiguous().view(torch.uint8)
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_deal_changes_no_bit(ga, case):
+    fam, opt, fi = _setup(case)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = []
+    for plan in _plans(ga, fam, opt):
+        outs.append(run_decode(ga, fi, plan, err=err, out=torch.full_like(fi.q, float("nan"))))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(_bits(outs[0]), _bits(outs[1])), case
+    rows = sorted(set([0, 1, 3, 4, 5] + W.sample_rows(len(LENS), 6, seed=2).tolist()))
+    assert_close(outs[1][rows].float().cpu().numpy(), oracle_decode_rows_gathered(fi, rows),
+                 kv_dtype=fam.kv_dtype, what=case)
+
+
+@pytest.mark.parametrize("case", ["local_bf16", "local_e4m3_4_heads"])
+def test_deal_reads_the_same_pages(ga, case):
+    """Touch log (one row-chunk per row in an unsplit plan): the same physical
+    pages per row under both deals, equal to the oracle's window pages."""
+    fam, opt, fi = _setup(case)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    logs = []
+    for plan in _plans(ga, fam, opt, flags=ga.GA_PLAN_TOUCH_LOG):
+        if opt.get("heads"):
+            plan.kv_heads_per_unit = opt["heads"]
+        ws = ga.workspace_for(plan, DEV)
+        _, _, log = ga.workspace_views(plan, ws)
+        log.fill_(-1)
+        run_decode(ga, fi, plan, err=err, workspace=ws)
+        torch.cuda.synchronize()
+        logs.append(log.cpu().numpy().copy())
+    assert int(err.item()) == 0
+    assert np.array_equal(logs[0], logs[1])
+    table = fi.page_table.cpu().numpy()
+    for b, L in enumerate(LENS):
+        first, n = O.logical_pages(L, fam.window, 16)
+        assert [int(x) for x in logs[1][b] if x >= 0] == \
+            [int(table[b, p]) for p in range(first, first + n)], (b, L)
+
+
+@pytest.mark.parametrize("case", ["local_bf16", "local_e4m3", "local_e4m3_4_heads"])
+def test_deal_with_fused_append(ga, case):
+    """The decode call with the append fused in: same pools and outputs under
+    both deals (the unit that holds a row's last page writes its token)."""
+    fam, opt, fi = _setup(case)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    res = []
+    for plan in _plans(ga, fam, opt):
+        k, v = fi.k_pool.clone(), fi.v_pool.clone()
+        out = torch.empty_like(fi.q)
+        ga.ga_decode_local_hd256_append(fi.k_new, fi.v_new, fi.q, k, v, fi.page_table,
+                                        fi.seq_lens, window=fam.window,
+                                        scale=1 / math.sqrt(fam.head_dim), plan=plan,
+                                        workspace=ga.workspace_for(plan, DEV), out=out,
+                                        k_scale=fi.k_scale, v_scale=fi.v_scale, err_word=err)
+        torch.cuda.synchronize()
+        res.append((k, v, out))
+    assert int(err.item()) == 0
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(_bits(a), _bits(b)), case
+
+
+def test_ragged_batch_deal_sampled(ga):
+    """The ragged 256-row batch in the bench's launch configuration: the
+    planner deals rows by size, and sampled rows match the oracle."""
+    wl = W.config(5)
+    fam = wl.local
+    fi = W.make_family_inputs(wl, fam, device=DEV, poison=True, release_old=True, seed=3)
+    plan = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                             num_kv_heads=fam.num_kv_heads, head_dim=256, window=fam.window,
+                             flags=ga.GA_PLAN_KV_E4M3)
+    assert plan.schedule == ga.GA_SCHEDULE_ROWS_BY_SIZE and plan.kv_heads_per_unit == 4
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_decode(ga, fi, plan, err=err)
+    plan0 = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                              num_kv_heads=fam.num_kv_heads, head_dim=256, window=fam.window,
+                              flags=ga.GA_PLAN_KV_E4M3)
+    plan0.schedule = ga.GA_SCHEDULE_ROUND_ROBIN
+    out0 = run_decode(ga, fi, plan0, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(_bits(out), _bits(out0))
+    rows = W.sample_rows(wl.batch, 12, seed=4)
+    assert_close(out[rows].float().cpu().numpy(), oracle_decode_rows_gathered(fi, rows),
+                 kv_dtype=1, what="ragged rows-by-size")

@@ -174,3 +174,49 @@ def test_units_span_several_kv_heads(ga):
     # the global family (head_dim 512) and multi-query plans keep one kv head
     assert ga.ga_plan_splits(many, flags=ga.GA_PLAN_KV_E4M3,
                              **dict(kw, head_dim=512, window=0)).kv_heads_per_unit == 1
+
+
+def _snake(s, G, U):
+    """Slot s of G CTAs over U units -> position in the sorted order: every
+    odd pass over the CTAs runs backwards (the deal the header documents)."""
+    r, q = divmod(s, G)
+    n = min(G, U - r * G)
+    return r * G + (n - 1 - q if r % 2 else q)
+
+
+@pytest.mark.parametrize("G,U", [(152, 1024), (152, 152), (7, 50), (5, 3), (40, 512)])
+def test_snake_deal_is_a_permutation(G, U):
+    pos = [_snake(s, G, U) for s in range(U)]
+    assert sorted(pos) == list(range(U))
+    # CTA q takes slots q, q + G, ...: in a full odd pass it gets position G - 1 - q
+    if U >= 2 * G:
+        assert pos[G] == 2 * G - 1 and pos[2 * G - 1] == G
+
+
+def test_rows_by_size_schedule(ga):
+    """The planner deals one-chunk plans of unequal rows longest first (snake
+    order) when that evens out the CTA loads; equal rows, split plans and
+    multi-query plans keep round robin.  The choice is checked against the
+    same deal simulated here: the busiest CTA's pages drop."""
+    kw = dict(num_q_heads=32, num_kv_heads=16, head_dim=256, window=1024, num_sms=152)
+    lens = W.config(5).seq_lens
+    p = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, **kw)
+    assert p.mode == ga.GA_SPLIT_NONE and p.schedule == ga.GA_SCHEDULE_ROWS_BY_SIZE
+    upr = 16 // p.kv_heads_per_unit
+    pages = [_pages(int(L), 1024) for L in lens]
+    order = sorted(range(len(lens)), key=lambda b: (-min(pages[b], 256), b))
+    G, U = p.grid, p.units
+    rr, sn = np.zeros(G), np.zeros(G)
+    for s in range(U):
+        rr[s % G] += pages[s // upr]
+        sn[s % G] += pages[order[_snake(s, G, U) // upr]]
+    assert rr.sum() == sn.sum() and sn.max() < 0.97 * rr.max()
+    # equal rows: nothing to gain
+    q = ga.ga_plan_splits([20000] * 64, **kw)
+    assert q.mode == ga.GA_SPLIT_NONE and q.schedule == ga.GA_SCHEDULE_ROUND_ROBIN
+    # split plans and multi-query plans: round robin
+    assert ga.ga_plan_splits(lens, requested_splits=2, **kw).schedule == 0
+    assert ga.ga_plan_splits_mq(lens, q_len=4, **kw).schedule == 0
+    # the row order and its counters must fit after the row prefix
+    big = np.random.default_rng(0).integers(1, 3000, 1792)
+    assert ga.ga_plan_splits(big, requested_splits=1, **kw).schedule == 0

@@ -76,22 +76,28 @@ struct UnitLoc {
     int32_t b, c, hg;
 };
 
+// The rows-by-size deal: slot u -> position in the sorted order -> (row, kv
+// head, head group); one chunk per row, so the row-chunk is the row.  Kept
+// out of line: the decode kernels' hot loops are sensitive to the size of
+// the code inlined into them (their instruction fetch).
+static __device__ __noinline__ UnitLoc locate_sorted(const DecodeParams& p, const int32_t* pre,
+                                                     int64_t u) {
+    UnitLoc l;
+    const uint32_t upr = (uint32_t)p.Hkv * (uint32_t)p.HG;
+    const uint32_t pos = snake_position((uint32_t)u, gridDim.x, (uint32_t)p.B * upr);
+    const uint32_t r = pos / upr, rem = pos - r * upr;
+    const uint32_t hg = (p.HG == 1) ? 0u : rem % (uint32_t)p.HG;
+    l.hg = (int32_t)hg;
+    l.c = (int32_t)((rem - hg) / (uint32_t)p.HG);
+    l.b = pre[r];
+    l.rc = l.b;
+    return l;
+}
+
 __device__ __forceinline__ UnitLoc locate_unit(const DecodeParams& p, const int32_t* pre,
                                                int64_t u) {
+    if (p.schedule == kScheduleSorted) return locate_sorted(p, pre, u);
     UnitLoc l;
-    if (p.schedule == kScheduleSorted) {
-        // slot u -> position in the rows-by-size order -> (row, kv head, head
-        // group); one chunk per row, so the row-chunk is the row
-        const uint32_t upr = (uint32_t)p.Hkv * (uint32_t)p.HG;
-        const uint32_t pos = snake_position((uint32_t)u, gridDim.x, (uint32_t)p.B * upr);
-        const uint32_t r = pos / upr, rem = pos - r * upr;
-        const uint32_t hg = (p.HG == 1) ? 0u : rem % (uint32_t)p.HG;
-        l.hg = (int32_t)hg;
-        l.c = (int32_t)((rem - hg) / (uint32_t)p.HG);
-        l.b = pre[r];
-        l.rc = l.b;
-        return l;
-    }
     if (u < (int64_t(1) << 31)) {      // unit_coords in 32 bits (64-bit division is slow)
         const uint32_t v = (uint32_t)u, hg = (uint32_t)p.HG, hkv = (uint32_t)p.Hkv;
         const uint32_t q1 = (hg == 1) ? v : v / hg;
@@ -128,7 +134,7 @@ __device__ __forceinline__ UnitInfo finish_unit(const DecodeParams& p, const int
 }
 
 __device__ __forceinline__ UnitInfo unit_info(const DecodeParams& p, const int32_t* pre,
-                                              int64_t u) {
+                                                     int64_t u) {
     const UnitLoc l = locate_unit(p, pre, u);
     return finish_unit(p, pre, l, __ldg(p.seq_lens + l.b));
 }
@@ -142,8 +148,8 @@ __device__ __forceinline__ int32_t row_key(const DecodeParams& p, int32_t b) {
 // pre[0 .. B) becomes the rows in descending order of attended pages, ties
 // in row order -- the same order in every CTA (counts, then a stable scatter
 // by one warp); the kSortKeys ints after pre[B] are its counters.
-__device__ __forceinline__ void build_row_order(const DecodeParams& p, int32_t* pre,
-                                                int nthreads) {
+static __device__ __noinline__ void build_row_order(const DecodeParams& p, int32_t* pre,
+                                                    int nthreads) {
     int32_t* cnt = pre + p.B + 1;
     for (int i = threadIdx.x; i < kSortKeys; i += nthreads) cnt[i] = 0;
     __syncthreads();

@@ -155,3 +155,37 @@ def test_ragged_batch_deal_sampled(ga):
     rows = W.sample_rows(wl.batch, 12, seed=4)
     assert_close(out[rows].float().cpu().numpy(), oracle_decode_rows_gathered(fi, rows),
                  kv_dtype=1, what="ragged rows-by-size")
+
+
+def test_deal_at_the_batch_limit(ga):
+    """1791 rows, the most the rows-by-size deal takes (its row order and
+    counters fill the row-prefix array exactly): bit-identical to round robin
+    and sampled rows against the oracle; 1792 rows with the deal forced are
+    refused before any launch."""
+    fam = W.Family("local", 2, 1, 256, 64)
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(0, 200, 1791)]
+    wl = W.Workload("limit", np.asarray(lens, dtype=np.int32), 16, fam, fam)
+    fi = W.make_family_inputs(wl, fam, device=DEV, seed=9, poison=True, release_old=True)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = []
+    for sched in (ga.GA_SCHEDULE_ROUND_ROBIN, ga.GA_SCHEDULE_ROWS_BY_SIZE):
+        plan = ga.ga_plan_splits(lens, num_q_heads=2, num_kv_heads=1, head_dim=256, window=64,
+                                 requested_splits=1, num_sms=40)
+        plan.schedule = sched
+        outs.append(run_decode(ga, fi, plan, err=err, out=torch.full_like(fi.q, float("nan"))))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(_bits(outs[0]), _bits(outs[1]))
+    rows = W.sample_rows(len(lens), 10, seed=6)
+    assert_close(outs[1][rows].float().cpu().numpy(), oracle_decode_rows_gathered(fi, rows),
+                 kv_dtype=0, what="1791 rows")
+    lens2 = lens + [5]
+    wl2 = W.Workload("limit+1", np.asarray(lens2, dtype=np.int32), 16, fam, fam)
+    fi2 = W.make_family_inputs(wl2, fam, device=DEV, seed=9, release_old=True)
+    plan = ga.ga_plan_splits(lens2, num_q_heads=2, num_kv_heads=1, head_dim=256, window=64,
+                             requested_splits=1, num_sms=40)
+    plan.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE
+    with pytest.raises(ga.GAError) as exc:
+        run_decode(ga, fi2, plan, err=err)
+    assert exc.value.status == ga.GA_ERR_INVALID_ARG

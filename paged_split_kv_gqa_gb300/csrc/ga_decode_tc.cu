@@ -488,6 +488,72 @@ __device__ void append_tokens(const DecodeParams& p, const int32_t* pre, int64_t
     if (lane == 0) mbar_arrive(bar(bars, B_TOK));
 }
 
+// One unit's q rows into a q buffer (the layout q_warp describes) and their
+// scales, by the 32 lanes of the q warp: LPC lanes per column, each taking
+// D / LPC consecutive dims.  LPC = 4 covers all 8 columns (rows of columns
+// past the unit's valid ones written as zeros); LPC = 16 covers columns 0
+// and 1 only, for units of at most 2 valid columns whose other rows are
+// already zero.
+template <class G, int LPC>
+__device__ __forceinline__ void prep_q(const DecodeParams& p, const UnitInfo& y, uint8_t* qb_buf,
+                                       float* qsc_b) {
+    constexpr int DPL = G::D / LPC;                // dims per lane
+    constexpr int NW = DPL / 8;                    // 16-byte loads per lane (8 dims each)
+    static_assert(NW % 2 == 0, "16-dim pieces");
+    const int lane = threadIdx.x & 31;
+    const int f = lane / LPC, part = lane % LPC, d0 = DPL * part;
+    uint4 wv[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) wv[i] = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
+    if (f < y.nvalid) {
+        if (GA_CHK((row + 1) * G::D <= p.out_elems)) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + row * G::D + d0);
+#pragma unroll
+            for (int i = 0; i < NW; ++i) wv[i] = __ldg(src + i);
+        } else {
+            report(p.err_word, kErrSelfCheck);
+        }
+    }
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+        const uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            am = fmaxf(am, fmaxf(fabsf(bf16_lo(e[j])), fabsf(bf16_hi(e[j]))));
+    }
+#pragma unroll
+    for (int off = 1; off < LPC; off <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+    if (part == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
+    const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
+    const float inv = 1.0f / sc;
+    if (LPC == 4 || f < y.nvalid) {
+#pragma unroll
+        for (int i = 0; i < NW; i += 2) {         // 16 dims: elements of wv[i], wv[i + 1]
+            const uint32_t e[8] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w,
+                                   wv[i + 1].x, wv[i + 1].y, wv[i + 1].z, wv[i + 1].w};
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t h01, l01, h23, l23;
+                split_e4m3x2(bf16_lo(e[2 * j]) * inv, bf16_hi(e[2 * j]) * inv, h01, l01);
+                split_e4m3x2(bf16_lo(e[2 * j + 1]) * inv, bf16_hi(e[2 * j + 1]) * inv, h23, l23);
+                hw[j] = h01 | (h23 << 16);
+                lw[j] = l01 | (l23 << 16);
+            }
+            const int dd = d0 + 8 * i;                       // first dim of the piece
+            const int jj = (dd & 127) >> 4;                  // 16-byte chunk of the 128-byte row
+            uint8_t* half = qb_buf + (dd >> 7) * 2048;
+            *reinterpret_cast<uint4*>(half + f * 128 + ((jj ^ (f & 7)) << 4)) =
+                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(half + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        if (part == 0) qsc_b[f] = sc;
+    }
+}
+
 // Warp 6.  For each active unit (one with pages), in the order the MMA issuer
 // takes them: the unit's q rows as the QK operand in buffer k % 2 -- column f
 // scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row 8 + f
@@ -495,14 +561,21 @@ __device__ void append_tokens(const DecodeParams& p, const int32_t* pre, int64_t
 // columns past the unit's valid ones are zero.  Lane l takes column l / 4,
 // dims D/4 (l % 4) .. +D/4-1.  Buffer k % 2 is rewritten once the softmax
 // warps are done with active unit k - 2 (its scales read, all its S consumed).
-template <class G>
+template <class G, int NV>
 __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                        uint32_t bars, volatile int* abort_flag) {
-    constexpr int NW = G::D / 32;                  // 16-byte loads per lane (8 dims each)
     const int lane = threadIdx.x & 31;
     float* qsc = reinterpret_cast<float*>(smem + G::OFF_QSC);  // [2][8]
     uint8_t* qbuf = smem + G::OFF_Q;
-    const int f = lane >> 2, d0 = (G::D / 4) * (lane & 3);
+    // At most 2 valid columns per unit (NV = 2: one kv head of GQA group 1 or
+    // 2, the same for every unit of a launch): 16 lanes per column, and the
+    // rows of the other columns are zeroed once here instead of for every unit.
+    constexpr bool narrow = NV == 2;
+    if constexpr (narrow) {
+        for (int i = lane; i < 2 * G::QBUF_BYTES / 16; i += 32)
+            reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (lane < 2 * kHeadTile) qsc[lane] = 1.0f;
+    }
     UnitCursor cur(p, pre, U);
     uint32_t k = 0;
     // this step's tokens once the first unit's q is ready (or at the end)
@@ -523,54 +596,7 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
             }
             break;
         }
-        uint4 wv[NW];
-#pragma unroll
-        for (int i = 0; i < NW; ++i) wv[i] = make_uint4(0u, 0u, 0u, 0u);
-        const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
-        if (f < y.nvalid) {
-            if (GA_CHK((row + 1) * G::D <= p.out_elems)) {
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + row * G::D + d0);
-#pragma unroll
-                for (int i = 0; i < NW; ++i) wv[i] = __ldg(src + i);
-            } else {
-                report(p.err_word, kErrSelfCheck);
-            }
-        }
-        float am = 0.f;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            const uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                am = fmaxf(am, fmaxf(fabsf(bf16_lo(e[j])), fabsf(bf16_hi(e[j]))));
-        }
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-        if ((lane & 3) == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
-        const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
-        const float inv = 1.0f / sc;
-#pragma unroll
-        for (int i = 0; i < NW; i += 2) {         // 16 dims: elements of wv[i], wv[i + 1]
-            const uint32_t e[8] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w,
-                                   wv[i + 1].x, wv[i + 1].y, wv[i + 1].z, wv[i + 1].w};
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t h01, l01, h23, l23;
-                split_e4m3x2(bf16_lo(e[2 * j]) * inv, bf16_hi(e[2 * j]) * inv, h01, l01);
-                split_e4m3x2(bf16_lo(e[2 * j + 1]) * inv, bf16_hi(e[2 * j + 1]) * inv, h23, l23);
-                hw[j] = h01 | (h23 << 16);
-                lw[j] = l01 | (l23 << 16);
-            }
-            const int dd = d0 + 8 * i;                       // first dim of the piece
-            const int jj = (dd & 127) >> 4;                  // 16-byte chunk of the 128-byte row
-            uint8_t* half = qbuf + qb * G::QBUF_BYTES + (dd >> 7) * 2048;
-            *reinterpret_cast<uint4*>(half + f * 128 + ((jj ^ (f & 7)) << 4)) =
-                make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(half + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
-                make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-        if ((lane & 3) == 0) qsc[qb * kHeadTile + f] = sc;
+        prep_q<G, narrow ? 16 : 4>(p, y, qbuf + qb * G::QBUF_BYTES, qsc + qb * kHeadTile);
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bars, B_QFULL + (int)qb));
@@ -979,7 +1005,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == PROD_WARP) {
         producer<G>(&tmK, &tmV, &tmK1, &tmV1, p, pre, U, ring, bars, flags, &abort_flag);
     } else if (warp == Q_WARP) {
-        q_warp<G>(p, pre, U, smem, bars, &abort_flag);
+        q_warp<G, NV>(p, pre, U, smem, bars, &abort_flag);
     }
     tc_fence_before();
     __syncthreads();

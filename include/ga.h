@@ -158,7 +158,9 @@ typedef struct ga_plan {
                                     most 1791 rows: rows in descending order of attended
                                     pages, every other pass over the CTAs reversed).  The
                                     planner picks the second when it evens out CTA loads of
-                                    unequal rows.  Results do not depend on it. */
+                                    unequal rows.  Results do not depend on it.  The decode
+                                    calls refuse any other value, and the second on other
+                                    plans, with GA_ERR_INVALID_ARG before any launch. */
 } ga_plan;
 
 enum {

@@ -230,7 +230,7 @@ using namespace ga;
 
 extern "C" {
 
-int32_t ga_version(void) { return 0x000300; }
+int32_t ga_version(void) { return 0x000400; }
 
 const char* ga_strerror(int status) {
     switch (status) {

@@ -48,7 +48,7 @@ def test_strerror_and_version(ga):
     assert ga.strerror(0) == "GA_OK"
     assert "WORKSPACE" in ga.strerror(3)
     assert "unknown" in ga.strerror(99)
-    assert ga.ga_version() == 0x000300
+    assert ga.ga_version() == 0x000400
     assert ga.ga_check_error_word(0) == ga.GA_OK
     assert ga.ga_check_error_word(ga.GA_DEVERR_PAGE_ID) == ga.GA_ERR_DEVICE_CHECK
 

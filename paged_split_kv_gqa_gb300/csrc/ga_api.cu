@@ -143,6 +143,7 @@ struct PlanInput {
     int32_t TW;                              // columns per work unit
     int32_t HP;                              // kv heads per work unit
     double page_weight;                      // a page-head's bytes relative to bf16
+    double unit_ovh;                         // fixed cost of a work unit, in bf16 page-heads
 };
 
 // Row-chunk count and per-unit page counts of a candidate chunking.
@@ -176,12 +177,12 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     // Static round-robin schedule of the persistent grid: unit u -> CTA u % G.
     // Cost in "page loads per SM" (bf16 page-head blocks): each unit costs its
     // pages (times its kv heads, weighted by the KV element size) plus a fixed
-    // overhead (warp merge, pipeline refill: ~3.5K cycles, about 4 pages of
-    // stream time); a split adds the partial round trip spread over all SMs
-    // plus one extra launch.  (With 2 pages the ragged 256-row global family
-    // got 32-page chunks, 6411 GB/s; 64-page chunks measure 6559 GB/s.)
+    // overhead (in.unit_ovh); a split adds the partial round trip spread over
+    // all SMs plus one extra launch.  (With 2 pages of overhead the ragged
+    // 256-row global family got 32-page chunks, 6411 GB/s; 64-page chunks
+    // measure 6559 GB/s.)
     const int64_t G = std::max<int64_t>(1, std::min<int64_t>(cand.units, in.num_sms));
-    const double unit_ovh = 4.0;
+    const double unit_ovh = in.unit_ovh;
     std::vector<double> load((size_t)G, 0.0);
     for (int64_t u = 0; u < cand.units; ++u) {
         const int64_t rc = u / per_rc;
@@ -287,8 +288,15 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     const bool tc = (flags & GA_PLAN_TENSOR_CORE_UNITS) ||
                     (!(flags & GA_PLAN_COLUMN_PARALLEL_UNITS) && cols >= tc_min_cols(head_dim));
     const int32_t tw = cols <= kHeadTile ? kHeadTile : tc ? kTcColTile : 4 * kHeadTile;
+    // A unit's fixed cost: the page-parallel kernels' merge and pipeline
+    // refill (~3.5K cycles, about 4 pages of stream time); the tcgen05 E4M3
+    // kernels' unit start and drain (q preparation, the first superstage's
+    // products, the epilogue from tensor memory: one-page rows measure ~6 us
+    // a unit, about 18 bf16 pages; with 4 the ragged batch's first 4 rows got
+    // 16-page chunks, 19.2 us a layer with the combine, against 15.6 unsplit).
+    const bool e4m3 = (flags & GA_PLAN_KV_E4M3) != 0;
     PlanInput in{seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim, weff, num_sms, q_len,
-                 tw, 1, (flags & GA_PLAN_KV_E4M3) ? 0.5 : 1.0};
+                 tw, 1, e4m3 ? 0.5 : 1.0, e4m3 ? 18.0 : 4.0};
     Candidate best;
     if (requested_splits == 1) {
         best = Candidate{kSplitNone, 0, 0};

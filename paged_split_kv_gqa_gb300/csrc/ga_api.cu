@@ -287,7 +287,11 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     const int32_t cols = num_q_heads / num_kv_heads * q_len;
     const bool tc = (flags & GA_PLAN_TENSOR_CORE_UNITS) ||
                     (!(flags & GA_PLAN_COLUMN_PARALLEL_UNITS) && cols >= tc_min_cols(head_dim));
-    const int32_t tw = cols <= kHeadTile ? kHeadTile : tc ? kTcColTile : 4 * kHeadTile;
+    // (E4M3 pools run units of 8 columns whatever the tile: a plan made for
+    // them is costed with the units its kernels run)
+    const int32_t tw = (cols <= kHeadTile || (flags & GA_PLAN_KV_E4M3)) ? kHeadTile
+                       : tc                                           ? kTcColTile
+                                                                      : 4 * kHeadTile;
     // A unit's fixed cost: the page-parallel kernels' merge and pipeline
     // refill (~3.5K cycles, about 4 pages of stream time); the tcgen05 E4M3
     // kernels' unit start and drain (q preparation, the first superstage's

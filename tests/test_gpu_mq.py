@@ -158,22 +158,27 @@ def test_mq_chunk_parity_with_one_query_decodes(ga, err, family):
                      extra_abs=ulp)
 
 
+@pytest.mark.parametrize("kv", [0, 1], ids=["bf16", "e4m3"])
 @pytest.mark.parametrize("family", ["local", "global"])
-def test_mq_31b_eagle_verify_sampled(ga, err, family):
+def test_mq_31b_eagle_verify_sampled(ga, err, family, kv):
     """31B-shaped batch, S = 4 (3 speculative tokens + the accepted one), the
-    planner's plan, sampled rows against the oracle."""
+    planner's plan, sampled rows against the oracle; also on E4M3 pools with
+    a plan made for them ("Gemma 4 31B on vLLM -- operating-point reference",
+    LIGHT recipe: an fp8 KV cache with EAGLE3 verify)."""
     wl = W.config(3)
     fam = wl.local if family == "local" else wl.global_
+    fam = dataclasses.replace(fam, kv_dtype=kv)
     S = 4
     alloc = dataclasses.replace(fam, window=fam.window + S - 1 if fam.window else 0)
     wl2 = W.Workload(wl.name, wl.seq_lens, wl.page_size, alloc, alloc)
     fi, q = _inputs(wl.seq_lens, fam, S, seed=0, poison=False, wl=wl2)
-    out = _decode(ga, fi, q, fam, _plan(ga, wl.seq_lens, fam, S), err)
+    flags = ga.GA_PLAN_KV_E4M3 if kv else 0
+    out = _decode(ga, fi, q, fam, _plan(ga, wl.seq_lens, fam, S, flags=flags), err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     rows = W.sample_rows(wl.batch, 4)
     ref = _oracle(fi, q, fam, rows=rows)
-    assert_close(out[rows].float().cpu().numpy(), ref, what=f"31B S=4 {family}")
+    assert_close(out[rows].float().cpu().numpy(), ref, kv_dtype=kv, what=f"31B S=4 {family}")
     del fi
     torch.cuda.empty_cache()
 

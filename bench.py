@@ -45,32 +45,35 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-# The sources a bf16 decode launch's DRAM traffic depends on: the kernel, the
-# headers it includes, and the host code that encodes its tensor maps and
-# makes its plan.
-DECODE_SOURCES = ("ga_api.cu", "ga_decode.cu", "ga_decode_common.cuh", "ga_device.cuh",
-                  "ga_geometry.h")
+# The sources a one-query decode launch's DRAM traffic depends on: both
+# decode kernels (mma.sync and tcgen05), the headers they include, and the
+# host code that encodes their tensor maps and makes their plans.
+_CSRC = "paged_split_kv_gqa_gb300/csrc/"
+DECODE_SOURCES = ("include/ga.h", _CSRC + "ga_api.cu", _CSRC + "ga_decode.cu",
+                  _CSRC + "ga_decode_tc.cu", _CSRC + "ga_decode_common.cuh",
+                  _CSRC + "ga_device.cuh", _CSRC + "ga_geometry.h", _CSRC + "ga_internal.h")
 
 
 def kernel_source_hash(files=DECODE_SOURCES):
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_split_kv_gqa_gb300", "csrc")
     for fn in sorted(files):
-        with open(os.path.join(csrc, fn), "rb") as fh:
+        with open(os.path.join(ROOT, fn), "rb") as fh:
             h.update(fn.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    sources are unchanged since it was taken; else None."""
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel in
+    this workload's default step, if the decode sources are unchanged since
+    it was taken; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh).get(kernel)
     except Exception:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if (not rec or rec.get("workload") != workload
+            or rec.get("source_hash") != kernel_source_hash()):
         return None
     return rec.get("bytes_per_launch")
 
@@ -667,10 +670,15 @@ def run_ga(args):
     peak, peak_kind = measured_peak_gbs()
     dom_ach = families[dominant]["decode_gbs"]
     kname = "decode_global_hd512" if dominant == "global" else "decode_local_hd256"
-    # the committed counters cover the default 31B step (planner's splits, two pools)
-    default_step = (args.workload == "31b" and not args.rows and not args.splits
-                    and not args.kv_alias and args.q_len == 1 and args.fp8 == "none")
-    traffic = committed_traffic(kname) if default_step else None
+    if families[dominant]["kv_dtype"] == "e4m3":
+        kname += "_e4m3"
+    # the committed counters cover a workload's default step: the planner's
+    # plans and deal, the workload's own KV dtypes, the append fused
+    default_step = (not args.rows and not args.splits and not args.kv_alias
+                    and args.q_len == 1 and args.fp8 == "none" and args.deal == "auto"
+                    and not args.fp8_units and not args.separate_append
+                    and (args.workload != "ragged" or args.pools == 4))
+    traffic = committed_traffic(kname, args.workload) if default_step else None
 
     # ---- end to end through host buffers: H2D inputs, the C-ABI calls, D2H outputs
     e2e = None

@@ -287,11 +287,13 @@ int ga_plan_splits_mq(const int32_t* seq_lens_host, int32_t batch, int32_t num_q
     const int32_t cols = num_q_heads / num_kv_heads * q_len;
     const bool tc = (flags & GA_PLAN_TENSOR_CORE_UNITS) ||
                     (!(flags & GA_PLAN_COLUMN_PARALLEL_UNITS) && cols >= tc_min_cols(head_dim));
-    // (E4M3 pools run units of 8 columns whatever the tile: a plan made for
-    // them is costed with the units its kernels run)
-    const int32_t tw = (cols <= kHeadTile || (flags & GA_PLAN_KV_E4M3)) ? kHeadTile
-                       : tc                                           ? kTcColTile
-                                                                      : 4 * kHeadTile;
+    // (E4M3 pools run the tcgen05 E4M3 kernel, whose units hold 8 columns,
+    // or 16 for a kv head with more than 8: a plan made for them is costed
+    // with those units, and asks the kernel for 16-column ones)
+    const int32_t tw = (flags & GA_PLAN_KV_E4M3) ? (cols > kHeadTile ? 2 * kHeadTile : kHeadTile)
+                       : cols <= kHeadTile       ? kHeadTile
+                       : tc                      ? kTcColTile
+                                                 : 4 * kHeadTile;
     // A unit's fixed cost: the page-parallel kernels' merge and pipeline
     // refill (~3.5K cycles, about 4 pages of stream time); the tcgen05 E4M3
     // kernels' unit start and drain (q preparation, the first superstage's
@@ -419,8 +421,10 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
     if (plan->batch != batch || plan->num_q_heads != num_q_heads ||
         plan->num_kv_heads != num_kv_heads || plan->head_dim != head_dim ||
         plan->window != window || plan->page_size != page_size || plan->q_len < 1 ||
-        plan->q_len > kMaxQLen || (plan->col_tile != kHeadTile && plan->col_tile != 4 * kHeadTile &&
-         plan->col_tile != kTcColTile))
+        plan->q_len > kMaxQLen ||
+        (plan->col_tile != kHeadTile && plan->col_tile != 4 * kHeadTile &&
+         plan->col_tile != kTcColTile &&
+         (plan->col_tile != 2 * kHeadTile || kv_dtype != GA_KV_E4M3)))
         return GA_ERR_INVALID_ARG;
     if (batch == 0) return GA_OK;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return GA_ERR_INVALID_ARG;
@@ -445,7 +449,10 @@ static int decode_entry(const void* q, const void* k_pool, const void* v_pool, i
                  batch, num_q_heads, num_kv_heads, head_dim, window, num_pages, scale, plan,
                  workspace, out, err_word, reinterpret_cast<cudaStream_t>(stream)};
     if (append) {
-        if (num_q_heads / num_kv_heads <= kHeadTile && plan->col_tile != kTcColTile) {
+        // (the E4M3 kernel's 16-column units hold a kv head of up to 16 query heads)
+        const int32_t unit_cols =
+            kv_dtype == GA_KV_E4M3 && plan->col_tile == 2 * kHeadTile ? 2 * kHeadTile : kHeadTile;
+        if (num_q_heads / num_kv_heads <= unit_cols && plan->col_tile != kTcColTile) {
             // every kv head of a row chunk is one unit of a kernel that
             // appends: the decode appends
             a.k_new = k_new;

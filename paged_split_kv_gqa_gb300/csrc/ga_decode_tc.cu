@@ -28,15 +28,15 @@
 // block is fetched once into a V slot that serves both products, and all six
 // slots are V slots.
 //
-// Products (N = 16, K = 32 per instruction, fp32 accumulate):
-//   S   [keys x 16]  = K [keys x dims]  . Qs^T   (A K-major, B K-major; M = keys
-//                                                 of a superstage, 128 or 64)
-//   O^T [dims x 16] += V^T [dims x keys] . Ps^T  (A MN-major, B K-major; M = 128
-//                                                 dims, one product per region)
-// The 16 columns are 8 (query, head) columns twice: q scaled per column by
-// 448 / amax and split into E4M3 hi and lo parts (columns f and 8 + f), and
-// likewise P (scaled by 2^6) into hi and lo; a column's result is the sum of
-// its two halves.  S sits in TMEM lanes = keys (M = 64: key r in lane
+// Products (N = 2 NC, K = 32 per instruction, fp32 accumulate):
+//   S   [keys x 2NC]  = K [keys x dims]  . Qs^T   (A K-major, B K-major; M = keys
+//                                                  of a superstage, 128 or 64)
+//   O^T [dims x 2NC] += V^T [dims x keys] . Ps^T  (A MN-major, B K-major; M = 128
+//                                                  dims, one product per region)
+// The 2 NC columns are a unit's NC (query, head) columns (8, or 16 when a kv
+// head has more than 8) twice: q scaled per column by 448 / amax and split
+// into E4M3 hi and lo parts (columns f and NC + f), and likewise P (scaled by
+// 2^6) into hi and lo; a column's result is the sum of its two halves.  S sits in TMEM lanes = keys (M = 64: key r in lane
 // 32 (r / 16) + r % 16), O^T in lanes = dims, so a softmax thread owns one key
 // of a superstage and dim t of each 128-dim region.
 //
@@ -65,13 +65,11 @@ namespace tc {
 #endif
 constexpr int NKS = GA_TC_NKS;                    // K slots (freed by the QK product)
 constexpr int NVS = GA_TC_NVS;                    // V slots (freed by the PV product)
-constexpr int PBUF_BYTES = 16 * 128;              // [16 rows][up to 128 keys]
 constexpr int NPB = 4;                            // P buffers: the PV of a superstage
                                                   // completes well after the next one's P
 constexpr int NSW = 4;                            // softmax warps
 constexpr int MMA_WARP = 4, PROD_WARP = 5, Q_WARP = 6, PV_WARP = 7;
 constexpr int NTHREADS = 256;
-constexpr int TM_S = 0, TM_O = 32;               // S: 2 x 16 columns, then 2 O buffers
 constexpr float PSCALE = 64.0f;                   // P scale: with slack 2^2, P <= 256 < 448
 constexpr float MAX_SLACK = 2.0f;
 
@@ -91,6 +89,13 @@ static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
 // are one pool; each block is fetched once into a V slot that serves both
 // products, and the K ring's memory becomes V slots too.
 //
+// NC (query, head) columns per unit: 8, or 16 for a kv head with more than 8
+// (several queries per row, or a GQA group above 8), so that its pages are
+// streamed once for 16 columns.  Every product is then N = 2 NC wide (hi and
+// lo parts), S takes two buffers of 2 NC TMEM columns, and the q and P
+// operands 2 NC rows; a 16-column unit gives one V slot back to make room
+// for them.
+//
 // HP > 1 (head_dim 256, two pools): a unit spans HP kv heads (its 8 columns
 // are their query heads).  A superstage is 8 / HP pages of all HP heads, and
 // page i fills rows 16 HP i .. 16 HP i + 16 HP - 1 of each region as
@@ -100,12 +105,14 @@ static_assert(NKS >= 2 && NVS >= 2 && NVS <= 32 && NKS <= 32, "ring depth");
 // the PV product runs per head (its own accumulator, K = 32 keys per
 // instruction at a group stride of 1 KB x HP), so a NaN in one head's V never
 // meets another head's P.
-template <int D_, bool ALIAS_ = false, int HP_ = 1>
+template <int D_, bool ALIAS_ = false, int HP_ = 1, int NC_ = kHeadTile>
 struct Geo {
     static constexpr int D = D_;
     static constexpr bool ALIAS = ALIAS_;
     static constexpr int HP = HP_;                        // kv heads per unit
-    static constexpr int NVE = ALIAS ? NKS + NVS : NVS;   // V slots in use
+    static constexpr int NC = NC_;                        // (query, head) columns per unit
+    static constexpr int NVG = NC > kHeadTile ? NVS - 1 : NVS;   // V slots, two pools
+    static constexpr int NVE = ALIAS ? NKS + NVG : NVG;   // V slots in use
     static constexpr int NCH = D / 128;                  // 128-dim regions (128 B of E4M3)
     static constexpr int SSP = HP > 1 ? 8 / HP : (D == 256 ? 8 : 4);   // pages per superstage
     static constexpr int PAGE_ROWS = kPageSize * HP;      // rows a page adds to a region tile
@@ -113,14 +120,18 @@ struct Geo {
     static constexpr int CHUNK_BYTES = MQ * 128;          // one region: [MQ rows][128 B]
     static constexpr int SLOT_BYTES = NCH * CHUNK_BYTES;  // K or V of a superstage
     static constexpr int BLOCK_BYTES = kPageSize * D;     // K or V of one page-head block
-    static constexpr int QBUF_BYTES = NCH * 16 * 128;     // [region][16 rows][128 B]
-    static constexpr int O_HEAD = 16 * NCH;               // TMEM columns of one head's O
+    static constexpr int QREG_BYTES = 2 * NC * 128;       // one region: [2 NC rows][128 B]
+    static constexpr int QBUF_BYTES = NCH * QREG_BYTES;   // [region][2 NC rows][128 B]
+    static constexpr int PBUF_BYTES = 2 * NC * 128;       // [2 NC rows][up to 128 keys]
+    static constexpr int TM_S = 0, TM_O = 4 * NC;         // S: 2 x 2 NC columns, then 2 O
+    static constexpr int O_HEAD = 2 * NC * NCH;           // TMEM columns of one head's O
     static constexpr int O_COLS = HP * O_HEAD;            // TMEM columns of one O buffer
     static constexpr int TMEM_COLS = TM_O + 2 * O_COLS <= 128   ? 128
                                      : TM_O + 2 * O_COLS <= 256 ? 256
                                                                 : 512;
     static constexpr int PV_STEPS = HP > 1 ? 4 / HP : 0;  // K = 32 products per head and region
     static_assert(HP == 1 || (D == 256 && !ALIAS && (HP == 2 || HP == 4)), "heads per unit");
+    static_assert(NC == kHeadTile || (NC == 2 * kHeadTile && HP == 1), "columns per unit");
     // HP == 1: a page-head block arrives as one box over all its regions and
     // lands as [key / 8][region][key % 8] rows, page i at BLOCK_BYTES i: each
     // region's 8-key groups then sit 1 KB x NCH apart, in key order, starting
@@ -140,11 +151,11 @@ struct Geo {
     }
     static constexpr int OFF_RING = 0;                    // K slots, then V slots
     static constexpr int OFF_VRING = ALIAS ? OFF_RING : OFF_RING + NKS * SLOT_BYTES;
-    static constexpr int OFF_Q = OFF_RING + (NKS + NVS) * SLOT_BYTES;
+    static constexpr int OFF_Q = OFF_RING + (NKS + NVG) * SLOT_BYTES;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF_BYTES;
-    static constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;              // [2][4 warps][8]
-    static constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * kHeadTile * 4); // [2][8] q scales
-    static constexpr int OFF_PREFIX = al(OFF_QSC + 2 * kHeadTile * 4);
+    static constexpr int OFF_RED = OFF_P + NPB * PBUF_BYTES;              // [2][4 warps][NC]
+    static constexpr int OFF_QSC = al(OFF_RED + 2 * NSW * NC * 4);        // [2][NC] q scales
+    static constexpr int OFF_PREFIX = al(OFF_QSC + 2 * NC * 4);
     static constexpr int OFF_FLAGS = al(OFF_PREFIX + (kMaxBatch + 1) * 4);
     static constexpr int OFF_BARS = al(OFF_FLAGS + NVMAX * 4);
     static constexpr int SMEM_USED = al(OFF_BARS + NBARS * 8);
@@ -227,7 +238,7 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
         };
         if (has_next) {               // the next unit's q rows into L2 for the q warp
             constexpr int LPR = G::D * 2 / 128;           // 128-byte lines per q row
-            for (int l = lane; l < kHeadTile * LPR; l += 32) {
+            for (int l = lane; l < G::NC * LPR; l += 32) {
                 const int64_t r = (int64_t)unit_q_row(p, cur.nl) + l / LPR;
                 if ((r + 1) * G::D <= p.out_elems)
                     prefetch_l2(reinterpret_cast<const char*>(p.q + r * G::D) + 128 * (l % LPR));
@@ -342,7 +353,7 @@ __device__ void producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const C
 template <class G>
 __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
                           uint32_t qbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
-    constexpr uint32_t IQK = idesc_e4m3(G::MQ, 16, false, false);
+    constexpr uint32_t IQK = idesc_e4m3(G::MQ, 2 * G::NC, false, false);
     uint32_t m = 0, k = 0;                        // superstages, active units so far
     bool stop = false;
     UnitCursor cur(p, pre, U);
@@ -369,10 +380,10 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
             for (int c = 0; c < G::NCH; ++c)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_e4m3(tmem + TM_S + 16 * sb,
+                    tc_mma_e4m3(tmem + G::TM_S + 2 * G::NC * sb,
                                 smem_desc_sw128(ka + c * G::REGION_OFF + 32 * kk, 16,
                                                 G::GROUP_STRIDE),
-                                smem_desc_sw128(qa + c * 2048 + 32 * kk, 16, 1024), IQK,
+                                smem_desc_sw128(qa + c * G::QREG_BYTES + 32 * kk, 16, 1024), IQK,
                                 (c | kk) != 0 ? 1u : 0u);
             tc_commit(bar(bars, B_SFULL + (int)sb));
             if (!G::ALIAS) tc_commit(bar(bars, B_KEMPTY + (int)slot));  // the K slot may be refilled
@@ -388,7 +399,7 @@ __device__ void qk_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
 template <class G>
 __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, uint32_t ring,
                           uint32_t pbuf, uint32_t bars, uint32_t tmem, volatile int* abort_flag) {
-    constexpr uint32_t IPV = idesc_e4m3(128, 16, true, false);
+    constexpr uint32_t IPV = idesc_e4m3(128, 2 * G::NC, true, false);
     uint32_t m = 0, k = 0;
     bool stop = false;
     UnitCursor cur(p, pre, U);
@@ -418,21 +429,22 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                         ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::CHUNK_BYTES;
 #pragma unroll
                     for (int h = 0; h < G::HP; ++h) {
-                        const uint32_t d = tmem + TM_O + G::O_COLS * ob + G::O_HEAD * h + 16 * c;
+                        const uint32_t d =
+                            tmem + G::TM_O + G::O_COLS * ob + G::O_HEAD * h + 2 * G::NC * c;
                         for (int j = 0; j < G::PV_STEPS && j < nks; ++j)
                             tc_mma_e4m3(
                                 d,
                                 smem_desc_sw128(va + 1024 * h + j * 4 * (1024 * G::HP),
                                                 G::CHUNK_BYTES, 1024 * G::HP),
-                                smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * (h * G::PV_STEPS + j),
-                                                16, 1024),
+                                smem_desc_sw128(
+                                    pbuf + pb * G::PBUF_BYTES + 32 * (h * G::PV_STEPS + j), 16, 1024),
                                 IPV, (s == 0 && j == 0) ? 0u : 1u);
                     }
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < G::NCH; ++c) {
-                    const uint32_t d = tmem + TM_O + G::O_COLS * ob + 16 * c;
+                    const uint32_t d = tmem + G::TM_O + G::O_COLS * ob + 2 * G::NC * c;
                     const uint32_t va =
                         ring + (uint32_t)G::OFF_VRING + slot * G::SLOT_BYTES + c * G::REGION_OFF;
                     // 32 keys per product: 4 groups of 8, GROUP_STRIDE apart
@@ -440,7 +452,7 @@ __device__ void pv_issuer(const DecodeParams& p, const int32_t* pre, int64_t U, 
                         tc_mma_e4m3(d,
                                     smem_desc_sw128(va + 4 * G::GROUP_STRIDE * ks, G::CHUNK_BYTES,
                                                     G::GROUP_STRIDE),
-                                    smem_desc_sw128(pbuf + pb * PBUF_BYTES + 32 * ks, 16, 1024),
+                                    smem_desc_sw128(pbuf + pb * G::PBUF_BYTES + 32 * ks, 16, 1024),
                                     IPV, (s == 0 && ks == 0) ? 0u : 1u);
                 }
             }
@@ -490,65 +502,79 @@ __device__ void append_tokens(const DecodeParams& p, const int32_t* pre, int64_t
 
 // One unit's q rows into a q buffer (the layout q_warp describes) and their
 // scales, by the 32 lanes of the q warp: LPC lanes per column, each taking
-// D / LPC consecutive dims.  LPC = 4 covers all 8 columns (rows of columns
-// past the unit's valid ones written as zeros); LPC = 16 covers columns 0
-// and 1 only, for units of at most 2 valid columns whose other rows are
-// already zero.
+// D / LPC consecutive dims.  LPC x NC = 32 covers all NC columns (rows of
+// columns past the unit's valid ones written as zeros); LPC = 16 covers
+// columns 0 and 1 only, for units of at most 2 valid columns whose other
+// rows are already zero.  A lane holds at most 16 of its 16-byte pieces at
+// once: with more (16-column units at hd512) it reads them twice, once for
+// the column's amax and once to convert them.
 template <class G, int LPC>
 __device__ __forceinline__ void prep_q(const DecodeParams& p, const UnitInfo& y, uint8_t* qb_buf,
                                        float* qsc_b) {
     constexpr int DPL = G::D / LPC;                // dims per lane
     constexpr int NW = DPL / 8;                    // 16-byte loads per lane (8 dims each)
-    static_assert(NW % 2 == 0, "16-dim pieces");
+    constexpr int PW = NW < 16 ? NW : 16;          // loads held at once
+    constexpr int NBLK = NW / PW;
+    constexpr bool all_cols = LPC * G::NC == 32;
+    static_assert(PW % 2 == 0 && NBLK * PW == NW, "16-dim pieces");
     const int lane = threadIdx.x & 31;
     const int f = lane / LPC, part = lane % LPC, d0 = DPL * part;
-    uint4 wv[NW];
-#pragma unroll
-    for (int i = 0; i < NW; ++i) wv[i] = make_uint4(0u, 0u, 0u, 0u);
     const int64_t row = (int64_t)y.b * p.Hq + y.h0 + f;
+    bool have = false;
     if (f < y.nvalid) {
-        if (GA_CHK((row + 1) * G::D <= p.out_elems)) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + row * G::D + d0);
-#pragma unroll
-            for (int i = 0; i < NW; ++i) wv[i] = __ldg(src + i);
-        } else {
-            report(p.err_word, kErrSelfCheck);
-        }
+        have = GA_CHK((row + 1) * G::D <= p.out_elems);
+        if (!have) report(p.err_word, kErrSelfCheck);
     }
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + (have ? row * G::D + d0 : 0));
+    uint4 wv[PW];
+    auto load = [&](int blk) {
+#pragma unroll
+        for (int i = 0; i < PW; ++i)
+            wv[i] = have ? __ldg(src + PW * blk + i) : make_uint4(0u, 0u, 0u, 0u);
+    };
     float am = 0.f;
 #pragma unroll
-    for (int i = 0; i < NW; ++i) {
-        const uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+    for (int blk = 0; blk < NBLK; ++blk) {
+        load(blk);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            am = fmaxf(am, fmaxf(fabsf(bf16_lo(e[j])), fabsf(bf16_hi(e[j]))));
+        for (int i = 0; i < PW; ++i) {
+            const uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                am = fmaxf(am, fmaxf(fabsf(bf16_lo(e[j])), fabsf(bf16_hi(e[j]))));
+        }
     }
 #pragma unroll
     for (int off = 1; off < LPC; off <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
     if (part == 0 && f < y.nvalid && !(am < CUDART_INF_F)) report(p.err_word, kErrQRange);
     const float sc = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
     const float inv = 1.0f / sc;
-    if (LPC == 4 || f < y.nvalid) {
+    if (all_cols || f < y.nvalid) {
 #pragma unroll
-        for (int i = 0; i < NW; i += 2) {         // 16 dims: elements of wv[i], wv[i + 1]
-            const uint32_t e[8] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w,
-                                   wv[i + 1].x, wv[i + 1].y, wv[i + 1].z, wv[i + 1].w};
-            uint32_t hw[4], lw[4];
+        for (int blk = 0; blk < NBLK; ++blk) {
+            if (NBLK > 1) load(blk);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t h01, l01, h23, l23;
-                split_e4m3x2(bf16_lo(e[2 * j]) * inv, bf16_hi(e[2 * j]) * inv, h01, l01);
-                split_e4m3x2(bf16_lo(e[2 * j + 1]) * inv, bf16_hi(e[2 * j + 1]) * inv, h23, l23);
-                hw[j] = h01 | (h23 << 16);
-                lw[j] = l01 | (l23 << 16);
+            for (int i = 0; i < PW; i += 2) {     // 16 dims: elements of wv[i], wv[i + 1]
+                const uint32_t e[8] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w,
+                                       wv[i + 1].x, wv[i + 1].y, wv[i + 1].z, wv[i + 1].w};
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t h01, l01, h23, l23;
+                    split_e4m3x2(bf16_lo(e[2 * j]) * inv, bf16_hi(e[2 * j]) * inv, h01, l01);
+                    split_e4m3x2(bf16_lo(e[2 * j + 1]) * inv, bf16_hi(e[2 * j + 1]) * inv, h23,
+                                 l23);
+                    hw[j] = h01 | (h23 << 16);
+                    lw[j] = l01 | (l23 << 16);
+                }
+                const int dd = d0 + 8 * (PW * blk + i);          // first dim of the piece
+                const int jj = (dd & 127) >> 4;                  // 16-byte chunk of the 128-byte row
+                uint8_t* region = qb_buf + (dd >> 7) * G::QREG_BYTES;
+                *reinterpret_cast<uint4*>(region + f * 128 + ((jj ^ (f & 7)) << 4)) =
+                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(region + (G::NC + f) * 128 + ((jj ^ (f & 7)) << 4)) =
+                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
-            const int dd = d0 + 8 * i;                       // first dim of the piece
-            const int jj = (dd & 127) >> 4;                  // 16-byte chunk of the 128-byte row
-            uint8_t* half = qb_buf + (dd >> 7) * 2048;
-            *reinterpret_cast<uint4*>(half + f * 128 + ((jj ^ (f & 7)) << 4)) =
-                make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(half + (8 + f) * 128 + ((jj ^ (f & 7)) << 4)) =
-                make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         if (part == 0) qsc_b[f] = sc;
     }
@@ -556,16 +582,17 @@ __device__ __forceinline__ void prep_q(const DecodeParams& p, const UnitInfo& y,
 
 // Warp 6.  For each active unit (one with pages), in the order the MMA issuer
 // takes them: the unit's q rows as the QK operand in buffer k % 2 -- column f
-// scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row 8 + f
-// of each 128-dim region ([16 rows][128 B], 128-byte swizzle); rows of
-// columns past the unit's valid ones are zero.  Lane l takes column l / 4,
-// dims D/4 (l % 4) .. +D/4-1.  Buffer k % 2 is rewritten once the softmax
-// warps are done with active unit k - 2 (its scales read, all its S consumed).
+// scaled by 448 / amax_f, its E4M3 hi part in row f and lo part in row NC + f
+// of each 128-dim region ([2 NC rows][128 B], 128-byte swizzle); rows of
+// columns past the unit's valid ones are zero.  Lane l takes column l / LPC,
+// dims D/LPC (l % LPC) .. +D/LPC-1 (LPC = 32 / NC).  Buffer k % 2 is
+// rewritten once the softmax warps are done with active unit k - 2 (its
+// scales read, all its S consumed).
 template <class G, int NV>
 __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                        uint32_t bars, volatile int* abort_flag) {
     const int lane = threadIdx.x & 31;
-    float* qsc = reinterpret_cast<float*>(smem + G::OFF_QSC);  // [2][8]
+    float* qsc = reinterpret_cast<float*>(smem + G::OFF_QSC);  // [2][NC]
     uint8_t* qbuf = smem + G::OFF_Q;
     // At most 2 valid columns per unit (NV = 2: one kv head of GQA group 1 or
     // 2, the same for every unit of a launch): 16 lanes per column, and the
@@ -574,7 +601,7 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
     if constexpr (narrow) {
         for (int i = lane; i < 2 * G::QBUF_BYTES / 16; i += 32)
             reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (lane < 2 * kHeadTile) qsc[lane] = 1.0f;
+        if (lane < 2 * G::NC) qsc[lane] = 1.0f;
     }
     UnitCursor cur(p, pre, U);
     uint32_t k = 0;
@@ -596,7 +623,7 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
             }
             break;
         }
-        prep_q<G, narrow ? 16 : 4>(p, y, qbuf + qb * G::QBUF_BYTES, qsc + qb * kHeadTile);
+        prep_q<G, narrow ? 16 : 32 / G::NC>(p, y, qbuf + qb * G::QBUF_BYTES, qsc + qb * G::NC);
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bars, B_QFULL + (int)qb));
@@ -607,6 +634,22 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
 
 // ------------------------------------------------------------------ softmax warps
 
+// N consecutive TMEM columns of this warp's 32 lanes, 16 at a time.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N % 16 == 0, "whole 16-column loads");
+#pragma unroll
+    for (int i = 0; i < N / 16; ++i)
+        tmem_ld16(taddr + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * i));
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N % 16 == 0, "whole 16-column stores");
+#pragma unroll
+    for (int i = 0; i < N / 16; ++i)
+        tmem_st16(taddr + 16 * i, *reinterpret_cast<const uint32_t(*)[16]>(r + 16 * i));
+}
+
 // Warps 0-3.  Thread t owns one key of every superstage (M = 128: key t;
 // M = 64: key 16 w + lane for lanes 0..15 of warp w, the TMEM lanes the
 // product writes) and dim t of each 128-dim region of O.  Per superstage:
@@ -615,8 +658,9 @@ __device__ void q_warp(const DecodeParams& p, const int32_t* pre, int64_t U, uin
 // by more than MAX_SLACK; then O is rescaled in TMEM), write P's hi / lo
 // E4M3 parts as the PV operand, zero V rows the PV reads but no query
 // attends.  At the end of a unit: read O and write the output (or a split
-// partial and its LSE).  NV (2, 4 or 8) bounds the valid (query, head)
-// columns of every unit; columns NV.. of P stay zero.
+// partial and its LSE).  NV (2, 4, 8, or 16 for 16-column units) bounds the
+// valid (query, head) columns of every unit; columns NV.. of P stay zero.
+// Column f's hi part is TMEM / operand column f, its lo part NC + f.
 template <class G, int NV>
 __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t U, uint8_t* smem,
                               uint32_t bars, uint32_t tmem, volatile uint32_t* flags,
@@ -625,7 +669,8 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
     const uint32_t tl = tmem + ((uint32_t)(32 * w) << 16);     // this warp's TMEM lanes
-    float* red = reinterpret_cast<float*>(smem + G::OFF_RED);  // [max | sum][4 warps][8]
+    constexpr int NC = G::NC;
+    float* red = reinterpret_cast<float*>(smem + G::OFF_RED);  // [max | sum][4 warps][NC]
     const float* qsc = reinterpret_cast<const float*>(smem + G::OFF_QSC);
     uint8_t* pbuf = smem + G::OFF_P;
     uint8_t* ring = smem + G::OFF_RING;
@@ -635,7 +680,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
     bool stop = false;
 
     // P columns past NV are never written: zero them once.
-    for (int i = tid; i < NPB * PBUF_BYTES / 16; i += 128)
+    for (int i = tid; i < NPB * G::PBUF_BYTES / 16; i += 128)
         reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
 
     // A wait polled by one lane per warp, with one outcome for all 128 threads
@@ -714,16 +759,16 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         int32_t clo[NV], chi[NV];
 #pragma unroll
         for (int f = 0; f < NV; ++f) {
-            kf[f] = p.scale_log2 * ksc[f / GQ] * qsc[qb * kHeadTile + f];
+            kf[f] = p.scale_log2 * ksc[f / GQ] * qsc[qb * NC + f];
             // query i = column % S sits at position L - S + i: keys [clo, chi)
-            const int32_t pos = x.g.len - p.S + (x.hg * kHeadTile + f) % p.S;
+            const int32_t pos = x.g.len - p.S + (x.hg * NC + f) % p.S;
             chi[f] = f < x.nvalid ? pos + 1 : 0;
             clo[f] = f < x.nvalid ? (p.mask_window > 0 ? max(0, pos - p.mask_window + 1) : 0) : 0;
             m[f] = -CUDART_INF_F;
             l[f] = 0.f;
         }
         const uint32_t ob = k & 1;
-        const uint32_t to = tl + TM_O + G::O_COLS * ob;   // this unit's O^T columns
+        const uint32_t to = tl + G::TM_O + G::O_COLS * ob;   // this unit's O^T columns
         for (int s = 0; s < nss; ++s) {
             const uint32_t ms = n + (uint32_t)s, slot = ms % G::NVE, sb = ms & 1, pbi = ms % NPB;
             // S of this superstage, the stage's V copies (they carry the
@@ -737,8 +782,8 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                                                 ((ms - NPB) / NPB) & 1, abort_flag));
             if (!settle(__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0)) break;
             tc_fence_after();
-            uint32_t sr[16];
-            tmem_ld16(tl + TM_S + 16 * sb, sr);
+            uint32_t sr[2 * NC];
+            tmem_ld_cols(tl + G::TM_S + 2 * NC * sb, sr);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -759,7 +804,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             for (int f = 0; f < NV; ++f) {
                 const bool valid =
                     present && (G::HP == 1 || f / GQ == hrow) && kj >= clo[f] && kj < chi[f];
-                sc[f] = valid ? (__uint_as_float(sr[f]) + __uint_as_float(sr[8 + f])) * kf[f]
+                sc[f] = valid ? (__uint_as_float(sr[f]) + __uint_as_float(sr[NC + f])) * kf[f]
                               : -CUDART_INF_F;
                 grow |= sc[f] > m[f] + MAX_SLACK;
             }
@@ -771,14 +816,14 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1)
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    if (lane == 0) red[w * kHeadTile + f] = mx;
+                    if (lane == 0) red[w * NC + f] = mx;
                 }
                 named_barrier(1, 128);
 #pragma unroll
                 for (int f = 0; f < NV; ++f) {
                     const float M =
-                        fmaxf(m[f], fmaxf(fmaxf(red[f], red[kHeadTile + f]),
-                                          fmaxf(red[2 * kHeadTile + f], red[3 * kHeadTile + f])));
+                        fmaxf(m[f], fmaxf(fmaxf(red[f], red[NC + f]),
+                                          fmaxf(red[2 * NC + f], red[3 * NC + f])));
                     alpha[f] = (m[f] == -CUDART_INF_F) ? 0.f : exp2f(m[f] - M);
                     l[f] *= alpha[f];
                     m[f] = M;
@@ -794,21 +839,21 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                     for (int h = 0; h < G::HP; ++h)
 #pragma unroll
                     for (int c = 0; c < G::NCH; ++c) {
-                        uint32_t o[16];
-                        tmem_ld16(to + G::O_HEAD * h + 16 * c, o);
+                        uint32_t o[2 * NC];
+                        tmem_ld_cols(to + G::O_HEAD * h + 2 * NC * c, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int f = 0; f < NV; ++f) {
                             o[f] = __float_as_uint(__uint_as_float(o[f]) * alpha[f]);
-                            o[8 + f] = __float_as_uint(__uint_as_float(o[8 + f]) * alpha[f]);
+                            o[NC + f] = __float_as_uint(__uint_as_float(o[NC + f]) * alpha[f]);
                         }
-                        tmem_st16(to + G::O_HEAD * h + 16 * c, o);
+                        tmem_st_cols(to + G::O_HEAD * h + 2 * NC * c, o);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                 }
             }
-            // P = 2^(s - m) x 2^6 as E4M3 hi (row f) and lo (row 8 + f)
+            // P = 2^(s - m) x 2^6 as E4M3 hi (row f) and lo (row NC + f)
             uint32_t hb[NV / 2], lb[NV / 2];      // two columns' bytes each
 #pragma unroll
             for (int f = 0; f < NV; f += 2) {
@@ -819,7 +864,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 l[f + 1] += p1;
                 split_e4m3x2(p0 * PSCALE, p1 * PSCALE, hb[f / 2], lb[f / 2]);
             }
-            uint8_t* pb = pbuf + pbi * PBUF_BYTES;
+            uint8_t* pb = pbuf + pbi * G::PBUF_BYTES;
             // P^T position of this key: its head's keys together, in the
             // order the head's PV product reads them (HP > 1)
             const int kpos =
@@ -830,7 +875,7 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 for (int f = 0; f < NV; ++f) {
                     const int sh = 8 * (f & 1);
                     pb[f * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(hb[f / 2] >> sh);
-                    pb[(8 + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[f / 2] >> sh);
+                    pb[(NC + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[f / 2] >> sh);
                 }
             }
             // V rows inside the PV's 32-key steps that no query of the row
@@ -860,16 +905,15 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             float v = l[f];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red[NSW * kHeadTile + w * kHeadTile + f] = v;
+            if (lane == 0) red[NSW * NC + w * NC + f] = v;
         }
         const uint32_t ml = n + (uint32_t)nss - 1;
         if (!wait_all(B_PVDONE + (int)(ml % NPB), (ml / NPB) & 1)) break;   // also publishes red
         float Lt[NV];
 #pragma unroll
         for (int f = 0; f < NV; ++f) {
-            const float* r = red + NSW * kHeadTile + f;
-            Lt[f] = f < x.nvalid ? ((r[0] + r[kHeadTile]) + (r[2 * kHeadTile] + r[3 * kHeadTile]))
-                                 : 0.f;
+            const float* r = red + NSW * NC + f;
+            Lt[f] = f < x.nvalid ? ((r[0] + r[NC]) + (r[2 * NC] + r[3 * NC])) : 0.f;
         }
         // only an exactly empty sum means "no keys"; NaN in attended K / V
         // reaches the output as in the definition
@@ -884,15 +928,15 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         for (int h = 0; h < G::HP; ++h)         // HP > 1: head h's columns from its accumulator
 #pragma unroll
         for (int c = 0; c < G::NCH; ++c) {
-            uint32_t o[16];
-            tmem_ld16(to + G::O_HEAD * h + 16 * c, o);
+            uint32_t o[2 * NC];
+            tmem_ld_cols(to + G::O_HEAD * h + 2 * NC * c, o);
             tmem_ld_wait();
 #pragma unroll
             for (int f = 0; f < NV; ++f) {
                 if (f >= x.nvalid || f / GQ != h) continue;
                 const float v = (Lt[f] == 0.f)
                                     ? 0.f
-                                    : (__uint_as_float(o[f]) + __uint_as_float(o[8 + f])) * fac[f];
+                                    : (__uint_as_float(o[f]) + __uint_as_float(o[NC + f])) * fac[f];
                 if (single) {
                     if (GA_CHK((r0 + f + 1) * D <= p.out_elems))
                         p.out[(r0 + f) * D + 128 * c + tid] = __float2bfloat16_rn(v);
@@ -938,7 +982,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __shared__ uint32_t tmem_slot;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    using G = Geo<D, ALIAS, HP>;
+    using G = Geo<D, ALIAS, HP, (NV > kHeadTile ? 2 * kHeadTile : kHeadTile)>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t* pre = reinterpret_cast<int32_t*>(smem + G::OFF_PREFIX);
     volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_FLAGS);
@@ -1021,10 +1065,13 @@ template <int D, bool ALIAS, int HP = 1>
 static int run_tc(const DecodeArgs& a) {
     const ga_plan& pl = *a.plan;
     const int32_t S = pl.q_len;
-    // (query, head) columns of a kv head, at most 8 per unit; HP > 1: the
-    // unit's 8 columns are the query heads of HP kv heads
+    // (query, head) columns of a kv head: units of 16 when the plan was made
+    // for them (more than 8 columns), else of at most 8; HP > 1: the unit's 8
+    // columns are the query heads of HP kv heads
     const int32_t cols = a.num_q_heads / a.num_kv_heads * S;
-    const int nv = HP > 1 ? 8 : cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
+    const bool wide = HP == 1 && pl.col_tile == 2 * kHeadTile;
+    const int tw = wide ? 2 * kHeadTile : kHeadTile;
+    const int nv = HP > 1 ? 8 : wide ? 16 : cols <= 2 ? 2 : cols <= 4 ? 4 : 8;
     auto pick = [nv]() {
         if constexpr (HP > 1) {
             (void)nv;
@@ -1032,14 +1079,19 @@ static int run_tc(const DecodeArgs& a) {
         } else {
             return nv == 2   ? &tc::decode_tc_kernel<D, 2, ALIAS, 1>
                    : nv == 4 ? &tc::decode_tc_kernel<D, 4, ALIAS, 1>
-                             : &tc::decode_tc_kernel<D, 8, ALIAS, 1>;
+                   : nv == 8 ? &tc::decode_tc_kernel<D, 8, ALIAS, 1>
+                             : &tc::decode_tc_kernel<D, 16, ALIAS, 1>;
         }
     };
     auto kern = pick();
-    constexpr int kSmem = tc::Geo<D, ALIAS, HP>::SMEM_BYTES;
-    // attribute slots 8..19: (head dim, alias, column count); 22, 23: HP = 2, 4
-    int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmem,
+    int smem = tc::Geo<D, ALIAS, HP>::SMEM_BYTES;
+    if constexpr (HP == 1)
+        if (wide) smem = tc::Geo<D, ALIAS, 1, 2 * kHeadTile>::SMEM_BYTES;
+    // attribute slots 8..19: (head dim, alias, column count); 22, 23: HP = 2,
+    // 4; 24..27: (head dim, alias) of 16-column units
+    int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem,
                               HP > 1 ? (HP == 2 ? 22 : 23)
+                              : wide ? 24 + (D == 256 ? 0 : 2) + (ALIAS ? 1 : 0)
                                      : 8 + (D == 256 ? 0 : 6) + (ALIAS ? 3 : 0) +
                                            (nv == 2 ? 0 : nv == 4 ? 1 : 2));
     if (rc != GA_OK) return rc;
@@ -1093,8 +1145,8 @@ static int run_tc(const DecodeArgs& a) {
     // units over groups of HP kv heads (columns: their query heads)
     p.Hkv = a.num_kv_heads / HP;
     p.group = a.num_q_heads / a.num_kv_heads * S * HP;
-    p.TW = kHeadTile;
-    p.HG = (p.group + kHeadTile - 1) / kHeadTile;
+    p.TW = tw;
+    p.HG = (p.group + tw - 1) / tw;
     p.window = effective_window(a.window, S);
     p.S = S;
     p.mask_window = a.window;
@@ -1108,7 +1160,7 @@ static int run_tc(const DecodeArgs& a) {
     p.pool_rows = rows;
     p.out_elems = (int64_t)a.batch * a.num_q_heads * S * a.head_dim;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, tc::NTHREADS, kSmem, a.stream>>>(tmK, tmV, tmK1, tmV1, p);
+    kern<<<grid, tc::NTHREADS, smem, a.stream>>>(tmK, tmV, tmK1, tmV1, p);
     if (cudaGetLastError() != cudaSuccess) return GA_ERR_CUDA;
     if (split && !(pl.flags & GA_PLAN_EXTERNAL_COMBINE))
         return launch_combine(p.partial_o, p.partial_lse, a.plan, a.seq_lens, a.out, a.err_word,

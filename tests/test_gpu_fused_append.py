@@ -4,9 +4,9 @@ reads a row's last page first writes the row's new token into it.  The pools
 after the call and its outputs must be bit-identical to ga_kv_append (at
 positions seq_lens - 1) followed by the plain decode, for every decode kernel
 (bf16 page-parallel at both head dims, K == V, E4M3 on tcgen05 with one and
-with four kv heads per unit, the E4M3 global family), split or not, with empty
-rows; more than 8 query heads per kv head takes the two-launch path, same
-bits; K == V pools (one pool: the value token is the one that stays, as with
+with four kv heads per unit, the E4M3 global family, its 16-column units at a
+GQA group of 16), split or not, with empty rows; more than 8 query heads per
+kv head on bf16 pools takes the two-launch path, same bits; K == V pools (one pool: the value token is the one that stays, as with
 ga_kv_append); an invalid page at the token's slot is reported as by
 ga_kv_append.
 ("[Model] Gemma 4 M1 12B", Description: paged decode, the step's token
@@ -33,6 +33,7 @@ CASES = {
     "local_e4m3_4_heads": (W.Family("local", 16, 8, 256, 1024, 1), {"heads": 4}),
     "global_e4m3": (W.Family("global", 16, 2, 512, 0, 1), {}),
     "global_bf16_group16": (W.Family("global", 32, 2, 512, 0), {}),   # two-launch path
+    "global_e4m3_group16": (W.Family("global", 32, 2, 512, 0, 1), {}),  # 16-column units
     "local_e4m3_2_heads": (W.Family("local", 16, 4, 256, 1024, 1), {"heads": 2}),
     "local_e4m3_kv_alias": (W.Family("local", 16, 8, 256, 1024, 1), {"alias": True}),
     "global_e4m3_kv_alias": (W.Family("global", 16, 2, 512, 0, 1), {"alias": True}),

@@ -233,3 +233,28 @@ def test_e4m3_unit_cost(ga):
     assert ga.ga_plan_splits(lens[:4], flags=ga.GA_PLAN_KV_E4M3, **kw).mode == ga.GA_SPLIT_NONE
     assert ga.ga_plan_splits(lens[:4], **kw).mode == ga.GA_SPLIT_CHUNK
     assert ga.ga_plan_splits(lens[:1], flags=ga.GA_PLAN_KV_E4M3, **kw).mode == ga.GA_SPLIT_CHUNK
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,W_,S,tile", [
+    (16, 2, 512, 0, 1, 8),        # 8 columns per kv head
+    (16, 2, 512, 0, 2, 16),       # 16
+    (16, 2, 512, 0, 3, 16),       # 24: two units, the second half full
+    (16, 2, 512, 0, 4, 16),       # 32
+    (32, 2, 512, 0, 1, 16),       # a GQA group of 16 at one query
+    (8, 4, 256, 1024, 4, 8),      # 8
+    (8, 4, 256, 1024, 8, 16),     # 16
+    (8, 2, 256, 32, 3, 16),       # 12: one unit with 4 idle columns
+])
+def test_e4m3_plans_ask_for_16_column_units(ga, Hq, Hkv, D, W_, S, tile):
+    """A plan made with GA_PLAN_KV_E4M3 for more than 8 (query, head) columns
+    per kv head asks the E4M3 kernel for units of 16 columns and counts its
+    units so; the same shape without the flag keeps the bf16 tiles."""
+    lens = [0, 1, 17, 300, 2049, 40]
+    kw = dict(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, window=W_, num_sms=152,
+              requested_splits=2)
+    p = ga.ga_plan_splits(lens, flags=ga.GA_PLAN_KV_E4M3, q_len=S, **kw)
+    cols = Hq // Hkv * S
+    assert p.col_tile == tile and p.kv_heads_per_unit == 1
+    assert p.units == p.row_chunks * Hkv * -(-cols // tile)
+    plain = ga.ga_plan_splits(lens, q_len=S, **kw)
+    assert plain.col_tile != 16 and plain.row_chunks == p.row_chunks

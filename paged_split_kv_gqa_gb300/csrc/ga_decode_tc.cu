@@ -674,8 +674,19 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
     const float* qsc = reinterpret_cast<const float*>(smem + G::OFF_QSC);
     uint8_t* pbuf = smem + G::OFF_P;
     uint8_t* ring = smem + G::OFF_RING;
-    // this thread's key within a superstage, and whether it has one
-    const bool key_lane = G::MQ == 128 || lane < 16;
+    // This thread's key within a superstage.  M = 128: key t of thread t.
+    // M = 64: the product writes key 16 w + r to lane r < 16 of warp w's TMEM
+    // lanes, so lanes r and 16 + r share that key and split its columns
+    // (SPLIT): lane r takes columns 0 .. CW - 1 of the unit, lane 16 + r
+    // columns CW .. 2 CW - 1, its S values passed over by shuffles.  Every
+    // thread still holds the running maxima of all columns (O^T's rescale
+    // needs them); the V rows of unattended keys are zeroed by lanes < 16.
+    constexpr bool SPLIT = G::MQ == 64;
+    constexpr int CW = SPLIT ? NV / 2 : NV;         // columns of this thread
+    static_assert(!SPLIT || (G::HP == 1 && NV % 2 == 0), "column split");
+    const bool upper = SPLIT && lane >= 16;
+    const int cb = upper ? CW : 0;                  // this thread's first column
+    const bool zero_lane = G::MQ == 128 || lane < 16;
     const int kss = G::MQ == 128 ? tid : 16 * w + (lane & 15);
     bool stop = false;
 
@@ -755,18 +766,22 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         }
         const uint32_t qb = k & 1;
         if (!wait_all(B_QFULL + (int)qb, (k >> 1) & 1)) break;     // this unit's q scales
-        float kf[NV], m[NV], l[NV];
-        int32_t clo[NV], chi[NV];
+        float kf[CW], l[CW], m[NV];             // m: every column's running max
+        int32_t clo[CW], chi[CW];
 #pragma unroll
-        for (int f = 0; f < NV; ++f) {
-            kf[f] = p.scale_log2 * ksc[f / GQ] * qsc[qb * NC + f];
+        for (int j = 0; j < CW; ++j) {
+            const int f = cb + j;
+            kf[j] = p.scale_log2 * ksc[SPLIT ? 0 : j / GQ] * qsc[qb * NC + f];
             // query i = column % S sits at position L - S + i: keys [clo, chi)
             const int32_t pos = x.g.len - p.S + (x.hg * NC + f) % p.S;
-            chi[f] = f < x.nvalid ? pos + 1 : 0;
-            clo[f] = f < x.nvalid ? (p.mask_window > 0 ? max(0, pos - p.mask_window + 1) : 0) : 0;
-            m[f] = -CUDART_INF_F;
-            l[f] = 0.f;
+            chi[j] = f < x.nvalid ? pos + 1 : 0;
+            clo[j] = f < x.nvalid ? (p.mask_window > 0 ? max(0, pos - p.mask_window + 1) : 0) : 0;
+            l[j] = 0.f;
         }
+#pragma unroll
+        for (int f = 0; f < NV; ++f) m[f] = -CUDART_INF_F;
+        // this thread's column j's running max (compile-time indexes only)
+        auto mcol = [&](int j) -> float { return upper ? m[CW + j] : m[j]; };
         const uint32_t ob = k & 1;
         const uint32_t to = tl + G::TM_O + G::O_COLS * ob;   // this unit's O^T columns
         for (int s = 0; s < nss; ++s) {
@@ -796,27 +811,43 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             const int key = G::HP > 1 ? 8 * khi + (kss & 7) : (kss & 15);
             const int hrow = G::HP > 1 ? (rr >> 3) % G::HP : 0;
             const int npg = min(G::SSP, x.np - G::SSP * s);
-            const bool present = key_lane && pg < npg && !((flags[slot] >> pg) & 1u);
+            const bool present = pg < npg && !((flags[slot] >> pg) & 1u);
             const int32_t kj = (x.p0 + G::SSP * s + pg) * kPageSize + key;
-            float sc[NV];
+            // this thread's columns: hi and lo parts of their scores
+            float shi[CW], slo[CW];
+#pragma unroll
+            for (int j = 0; j < CW; ++j) {
+                if constexpr (SPLIT) {
+                    const uint32_t a = __shfl_sync(0xffffffffu, sr[CW + j], lane & 15);
+                    const uint32_t b = __shfl_sync(0xffffffffu, sr[NC + CW + j], lane & 15);
+                    shi[j] = __uint_as_float(upper ? a : sr[j]);
+                    slo[j] = __uint_as_float(upper ? b : sr[NC + j]);
+                } else {
+                    shi[j] = __uint_as_float(sr[j]);
+                    slo[j] = __uint_as_float(sr[NC + j]);
+                }
+            }
+            float sc[CW];
             bool grow = false;
 #pragma unroll
-            for (int f = 0; f < NV; ++f) {
+            for (int j = 0; j < CW; ++j) {
                 const bool valid =
-                    present && (G::HP == 1 || f / GQ == hrow) && kj >= clo[f] && kj < chi[f];
-                sc[f] = valid ? (__uint_as_float(sr[f]) + __uint_as_float(sr[NC + f])) * kf[f]
-                              : -CUDART_INF_F;
-                grow |= sc[f] > m[f] + MAX_SLACK;
+                    present && (G::HP == 1 || j / GQ == hrow) && kj >= clo[j] && kj < chi[j];
+                sc[j] = valid ? (shi[j] + slo[j]) * kf[j] : -CUDART_INF_F;
+                grow |= sc[j] > mcol(j) + MAX_SLACK;
             }
+            // lanes holding one column's scores of a warp: 16 (SPLIT) or 32
+            constexpr int XOR0 = SPLIT ? 8 : 16;
+            const bool col_writer = (lane & (2 * XOR0 - 1)) == 0;
             if (named_barrier_or(1, 128, grow)) {
                 float alpha[NV];
 #pragma unroll
-                for (int f = 0; f < NV; ++f) {
-                    float mx = sc[f];
+                for (int j = 0; j < CW; ++j) {
+                    float mx = sc[j];
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
+                    for (int off = XOR0; off > 0; off >>= 1)
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    if (lane == 0) red[w * NC + f] = mx;
+                    if (col_writer) red[w * NC + cb + j] = mx;
                 }
                 named_barrier(1, 128);
 #pragma unroll
@@ -825,9 +856,10 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                         fmaxf(m[f], fmaxf(fmaxf(red[f], red[NC + f]),
                                           fmaxf(red[2 * NC + f], red[3 * NC + f])));
                     alpha[f] = (m[f] == -CUDART_INF_F) ? 0.f : exp2f(m[f] - M);
-                    l[f] *= alpha[f];
                     m[f] = M;
                 }
+#pragma unroll
+                for (int j = 0; j < CW; ++j) l[j] *= upper ? alpha[CW + j] : alpha[j];
                 named_barrier(1, 128);          // maxima read before anyone rewrites them
                 if (s > 0) {                    // O holds this unit's earlier superstages
                     const uint32_t mp = ms - 1;
@@ -854,15 +886,21 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
                 }
             }
             // P = 2^(s - m) x 2^6 as E4M3 hi (row f) and lo (row NC + f)
-            uint32_t hb[NV / 2], lb[NV / 2];      // two columns' bytes each
+            uint32_t hb[(CW + 1) / 2], lb[(CW + 1) / 2];   // two columns' bytes each
 #pragma unroll
-            for (int f = 0; f < NV; f += 2) {
-                const float m0 = (m[f] == -CUDART_INF_F) ? 0.f : m[f];
-                const float m1 = (m[f + 1] == -CUDART_INF_F) ? 0.f : m[f + 1];
-                const float p0 = exp2f(sc[f] - m0), p1 = exp2f(sc[f + 1] - m1);
-                l[f] += p0;
-                l[f + 1] += p1;
-                split_e4m3x2(p0 * PSCALE, p1 * PSCALE, hb[f / 2], lb[f / 2]);
+            for (int j = 0; j < CW; j += 2) {
+                const float mj0 = mcol(j);
+                const float m0 = (mj0 == -CUDART_INF_F) ? 0.f : mj0;
+                const float p0 = exp2f(sc[j] - m0);
+                l[j] += p0;
+                float p1 = 0.f;
+                if (j + 1 < CW) {
+                    const float mj1 = mcol(j + 1);
+                    const float m1 = (mj1 == -CUDART_INF_F) ? 0.f : mj1;
+                    p1 = exp2f(sc[j + 1] - m1);
+                    l[j + 1] += p1;
+                }
+                split_e4m3x2(p0 * PSCALE, p1 * PSCALE, hb[j / 2], lb[j / 2]);
             }
             uint8_t* pb = pbuf + pbi * G::PBUF_BYTES;
             // P^T position of this key: its head's keys together, in the
@@ -870,19 +908,17 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
             const int kpos =
                 G::HP > 1 ? (128 / G::HP) * hrow + 8 * (2 * pg + khi) + (kss & 7) : kss;
             const int kc = kpos >> 4, kb = kpos & 15;
-            if (key_lane) {
 #pragma unroll
-                for (int f = 0; f < NV; ++f) {
-                    const int sh = 8 * (f & 1);
-                    pb[f * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(hb[f / 2] >> sh);
-                    pb[(NC + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[f / 2] >> sh);
-                }
+            for (int j = 0; j < CW; ++j) {
+                const int f = cb + j, sh = 8 * (j & 1);
+                pb[f * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(hb[j / 2] >> sh);
+                pb[(NC + f) * 128 + (((kc ^ (f & 7)) << 4) | kb)] = (uint8_t)(lb[j / 2] >> sh);
             }
             // V rows inside the PV's 32-key steps that no query of the row
             // attends (window edges, a flagged page, the page after an odd
             // last one) may hold anything, NaN included: zero them
             const int nks = (npg + 1) / 2;
-            if (key_lane && pg < 2 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
+            if (zero_lane && pg < 2 * nks && !(present && kj >= x.g.lo && kj < x.g.len)) {
 #pragma unroll
                 for (int c = 0; c < G::NCH; ++c) {
                     uint4* vr = reinterpret_cast<uint4*>(ring + G::OFF_VRING + slot * G::SLOT_BYTES +
@@ -900,12 +936,15 @@ __device__ void softmax_warps(const DecodeParams& p, const int32_t* pre, int64_t
         if (lane == 0) mbar_arrive(bar(bars, B_QFREE + (int)qb));
 
         // ---- epilogue: column sums, then O^T from TMEM
+        {
+            constexpr int XOR0 = SPLIT ? 8 : 16;
 #pragma unroll
-        for (int f = 0; f < NV; ++f) {
-            float v = l[f];
+            for (int j = 0; j < CW; ++j) {
+                float v = l[j];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red[NSW * NC + w * NC + f] = v;
+                for (int off = XOR0; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if ((lane & (2 * XOR0 - 1)) == 0) red[NSW * NC + w * NC + cb + j] = v;
+            }
         }
         const uint32_t ml = n + (uint32_t)nss - 1;
         if (!wait_all(B_PVDONE + (int)(ml % NPB), (ml / NPB) & 1)) break;   // also publishes red

@@ -115,9 +115,13 @@ enum {
                                       128-dim region for all of them: it does so when the
                                       one-head plan needs no split and the wider units alone
                                       fill at least four rounds of the SMs (fewer, larger units
-                                      measured slower below that).  Results do not depend on
-                                      it; a plan made without it also serves E4M3 pools, and
-                                      bf16 pools ignore it. */
+                                      measured slower below that).  With more than 8 (query,
+                                      head) columns per kv head it gives units of 16 columns
+                                      (col_tile 16), each streaming a kv head's pages once
+                                      for all 16; such a plan is for E4M3 pools only.  Results
+                                      stay within the E4M3 tolerance either way; a plan made
+                                      without it also serves E4M3 pools (8-column units), and
+                                      bf16 pools ignore the flag otherwise. */
 };
 
 /*
@@ -141,7 +145,9 @@ typedef struct ga_plan {
     int32_t col_tile;        /* (query, head) columns per work unit: 8; when a kv head has
                                 more than 8, 32 (column-parallel mma.sync units) or 64
                                 (tcgen05 units; bf16 pools with K and V apart, other
-                                pools run 8-column units) */
+                                pools run 8-column units), or, in a plan made with
+                                GA_PLAN_KV_E4M3, 16: units of 16 columns of the E4M3
+                                decode (accepted with E4M3 pools only) */
     int64_t row_chunks;      /* (row, chunk) pairs the workspace holds */
     int64_t units;           /* work units (row-chunk x kv head x head group) planned */
     int64_t workspace_bytes; /* device workspace the decode call needs (0 if none) */

@@ -569,6 +569,83 @@ def one_page_rows_ms(ga, layer, err, device, reps=21):
     return sorted(ts)[len(ts) // 2]
 
 
+def run_unit_cost(args):
+    """Profiling only (no bench line): the fixed and per-unit cost of each
+    decode kernel on the 31B shapes.  Rows of 1, 4, 16 or 64 pages, one kv
+    head per unit, no split, 2 to 16 units per CTA; each launch timed alone
+    with CUDA events (median of 15), and a least-squares line through the
+    times: intercept = the launch's fixed part, slope = one unit's time.
+    The stream time of a unit at the measured copy bandwidth's per-SM share
+    is printed beside it."""
+    import torch
+    from paged_split_kv_gqa_gb300 import _build
+    _build.build()
+    from paged_split_kv_gqa_gb300 import ga
+    from paged_split_kv_gqa_gb300 import workloads as W
+    device = "cuda"
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    sms = ga.num_sms()
+    peak, _ = measured_peak_gbs()
+    wl31 = W.config(3)
+    for fam0 in (wl31.local, wl31.global_):
+        for kv in (W.KV_BF16, W.KV_E4M3):
+            fam = W.Family(fam0.name, fam0.num_q_heads, fam0.num_kv_heads, fam0.head_dim,
+                           fam0.window, kv)
+            for npg in (1, 4, 16, 64):
+                pts = []
+                for upc in (2, 4, 8, 16):
+                    B = max(1, upc * sms // fam.num_kv_heads)
+                    lens = np.full(B, 16 * npg, dtype=np.int32)
+                    wl = W.Workload("unit-cost", lens, 16, fam, fam)
+                    fi = W.make_family_inputs(wl, fam, device=device, seed=args.seed + 1)
+                    plan = ga.ga_plan_splits(
+                        lens, num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
+                        head_dim=fam.head_dim, window=fam.window, requested_splits=1,
+                        flags=ga.GA_PLAN_KV_E4M3 if kv == W.KV_E4M3 else 0)
+                    plan.kv_heads_per_unit = 1
+                    ws = ga.workspace_for(plan, device)
+                    kw = dict(scale=1.0 / math.sqrt(fam.head_dim), plan=plan, workspace=ws,
+                              out=torch.empty_like(fi.q), k_scale=fi.k_scale,
+                              v_scale=fi.v_scale, err_word=err)
+
+                    def call():
+                        if fam.window > 0:
+                            ga.ga_decode_local_hd256(fi.q, fi.k_pool, fi.v_pool, fi.page_table,
+                                                     fi.seq_lens, window=fam.window, **kw)
+                        else:
+                            ga.ga_decode_global_hd512(fi.q, fi.k_pool, fi.v_pool, fi.page_table,
+                                                      fi.seq_lens, **kw)
+                    for _ in range(3):
+                        call()
+                    ts = []
+                    for _ in range(15):
+                        if hasattr(torch.cuda, "_sleep"):
+                            torch.cuda._sleep(1_000_000)
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        call()
+                        b.record()
+                        torch.cuda.synchronize()
+                        ts.append(a.elapsed_time(b))
+                    pts.append((B * fam.num_kv_heads / sms, sorted(ts)[len(ts) // 2] * 1e3))
+                    del fi, ws, kw
+                    torch.cuda.empty_cache()
+                slope, icpt = np.polyfit([x for x, _ in pts], [y for _, y in pts], 1)
+                esz = 1 if kv == W.KV_E4M3 else 2
+                unit_bytes = 2 * npg * 16 * fam.head_dim * esz
+                print(json.dumps({
+                    "family": fam.name, "kv_dtype": "e4m3" if kv == W.KV_E4M3 else "bf16",
+                    "pages_per_unit": npg, "units_per_cta_us": [[round(x, 2), round(y, 2)]
+                                                                 for x, y in pts],
+                    "fixed_us": round(float(icpt), 2), "us_per_unit": round(float(slope), 2),
+                    "unit_stream_us_at_peak_share": round(unit_bytes / (peak * 1e3 / sms), 2)}),
+                    flush=True)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+
+
 def run_ga(args):
     import torch
     from paged_split_kv_gqa_gb300 import ga
@@ -936,8 +1013,13 @@ def main():
                     help="multi-query units for more than 8 (query, head) columns per kv head: "
                          "the planner's choice, tcgen05 units of 64 columns, or column-parallel "
                          "mma.sync units of 32")
+    ap.add_argument("--unit-cost", action="store_true",
+                    help="profiling only: fixed and per-unit cost of each decode kernel on the "
+                         "31B shapes (one JSON line per kernel and unit length, no bench line)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.unit_cost:
+        return run_unit_cost(args)
     world = dist_env()[2]
     if "WORLD_SIZE" in os.environ and args.gpus != world:
         ap.error(f"--gpus {args.gpus} but {world} ranks were launched")

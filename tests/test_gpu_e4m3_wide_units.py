@@ -4,7 +4,8 @@ with GA_PLAN_KV_E4M3 asks the tcgen05 E4M3 decode for units of 16 columns
 for 16 columns instead of once per 8).  Checked against the oracle over edge
 lengths, every split mode, both head dims, K == V pools, more than one
 16-column unit per kv head, a ragged last unit, a GQA group of 16 at one
-query per row, and a 31B-shaped batch at S = 2 ("Gemma 4 31B on vLLM --
+query per row, a page id flagged invalid mid-superstage, scale 1.0 (a peaked
+softmax), and a 31B-shaped batch at S = 2 ("Gemma 4 31B on vLLM --
 operating-point reference", LIGHT recipe: an fp8 KV cache under EAGLE3
 verify; "[Model] Gemma 4 M3 31B", Acceptance Criteria: windows of 1024)."""
 import dataclasses
@@ -125,3 +126,45 @@ def test_wide_units_31b_s2_sampled(ga, err):
                  kv_dtype=fam.kv_dtype, what="31B global S=2 E4M3")
     del fi
     torch.cuda.empty_cache()
+
+
+def test_wide_units_flagged_page(ga):
+    """A page id outside the pool in the middle of a superstage, in a
+    16-column unit at head_dim 512 (both half-warps at work): reported, not
+    read; the other rows within tolerance and nothing turns NaN."""
+    from tests.helpers import oracle_decode, run_decode
+    fam = W.Family("global", 32, 2, 512, 0, W.KV_E4M3)          # group 16, one query
+    lens = [20 * 16, 300, 13 * 16 + 4]
+    wl = W.Workload("wide-flag", np.asarray(lens, dtype=np.int32), 16, fam, fam)
+    fi = W.make_family_inputs(wl, fam, device=DEV, seed=77, poison=True)
+    fi.page_table[0, 6] = 1 << 30                 # logical page 6: superstage 1, page 2
+    plan = ga.ga_plan_splits(lens, num_q_heads=32, num_kv_heads=2, head_dim=512, window=0,
+                             flags=ga.GA_PLAN_KV_E4M3)
+    assert plan.col_tile == 16
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_decode(ga, fi, plan, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ga.GA_DEVERR_PAGE_ID
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert_close(got[1:], oracle_decode(fi, rows=[1, 2]), kv_dtype=fam.kv_dtype,
+                 what="unflagged rows")
+
+
+@pytest.mark.parametrize("shape", ["global_g8_S2", "local_g2_S8"])
+def test_wide_units_scale_one(ga, err, shape):
+    """Scale 1.0 (the Gemma convention): a peaked softmax whose running maxima
+    are raised, and O^T rescaled in tensor memory, many times per unit."""
+    import math
+    fam, S = SHAPES[shape]
+    lens = [3, 40, 333, 1030, 2049]
+    fi, q = _inputs(lens, fam, S, seed=55)
+    plan = _plan(ga, lens, fam, S, requested_splits=2)
+    assert plan.col_tile == 16
+    out = _decode(ga, fi, q, fam, plan, err, scale=1.0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = _oracle(fi, q, fam, scale=1.0)
+    extra = 0.5 * 2.0 ** (math.floor(math.log2(max(np.abs(ref).max(), 1e-30))) - 7)
+    assert_close(out.float().cpu().numpy(), ref, kv_dtype=fam.kv_dtype,
+                 what=f"{shape} scale 1.0", extra_abs=extra)

@@ -50,18 +50,23 @@ def _plan(ga, fi, **kw):
 
 
 @pytest.mark.parametrize("window", [1 << 20, 1024, 40])
-@pytest.mark.parametrize("g", [1, 2, 3, 5, 8, 12])
+@pytest.mark.parametrize("g", [1, 2, 3, 5, 8, 12, "12-e4m3-plan"])
 def test_superstage_edges(ga, window, g):
     """Every page count around a superstage, every column-count variant
-    (1..2 -> 2 columns, 3..4 -> 4, more -> 8; 12 -> two head groups), three
-    split modes; unattended slots hold NaN."""
+    (1..2 -> 2 columns, 3..4 -> 4, more -> 8; 12 -> two head groups, or one
+    16-column unit with a plan made with GA_PLAN_KV_E4M3), three split modes;
+    unattended slots hold NaN."""
+    flags = ga.GA_PLAN_KV_E4M3 if g == "12-e4m3-plan" else 0
+    g = 12 if flags else g
     Hkv = 2
     fi = _inputs(EDGE_LENS, g * Hkv, Hkv, window, seed=300 + g)
     ref = oracle_decode(fi)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     for split in (dict(requested_splits=1), dict(fixed_chunk_tokens=3 * P),
                   dict(requested_splits=3)):
-        out = run_decode(ga, fi, _plan(ga, fi, **split), err=err)
+        plan = _plan(ga, fi, flags=flags, **split)
+        assert (plan.col_tile == 16) == bool(flags)
+        out = run_decode(ga, fi, plan, err=err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         assert_close(out.float().cpu().numpy(), ref, kv_dtype=1,

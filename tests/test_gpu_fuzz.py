@@ -1,4 +1,5 @@
-"""Randomised parity: many seeded shapes against the oracle, plus the
+"""Randomised parity: many seeded shapes against the oracle (E4M3 pools
+twice: with a plain plan and with one made for E4M3 pools), plus the
 call-level options (external combine, side streams, no error word)."""
 import math
 
@@ -48,16 +49,22 @@ def test_random_shapes(ga, seed):
     wl = W.Workload("fuzz", lens, 16, fam, fam)
     fi = W.make_family_inputs(wl, fam, device=DEV, seed=seed, poison=True,
                               release_old=bool(fam.window) and seed % 2 == 0)
-    plan = ga.ga_plan_splits(lens, num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
-                             head_dim=fam.head_dim, window=fam.window, **split)
-    err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out = run_decode(ga, fi, plan, scale=scale, err=err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    what = f"seed {seed}: D={fam.head_dim} kv={fam.kv_dtype} g={fam.num_q_heads // fam.num_kv_heads} " \
-           f"Hkv={fam.num_kv_heads} W={fam.window} B={len(lens)} {split}"
-    got = out.float().cpu().numpy()
-    assert_close(got, oracle_decode(fi, scale=scale), kv_dtype=fam.kv_dtype, what=what)
+    ref = oracle_decode(fi, scale=scale)
+    # E4M3 pools: a plain plan and one made for them (16-column units above 8
+    # query heads per kv head, several kv heads per sliding unit when they fill)
+    for flags in ((0, ga.GA_PLAN_KV_E4M3) if fam.kv_dtype else (0,)):
+        plan = ga.ga_plan_splits(lens, num_q_heads=fam.num_q_heads,
+                                 num_kv_heads=fam.num_kv_heads, head_dim=fam.head_dim,
+                                 window=fam.window, flags=flags, **split)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = run_decode(ga, fi, plan, scale=scale, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        what = f"seed {seed}: D={fam.head_dim} kv={fam.kv_dtype} " \
+               f"g={fam.num_q_heads // fam.num_kv_heads} Hkv={fam.num_kv_heads} " \
+               f"W={fam.window} B={len(lens)} {split} flags={flags} col_tile={plan.col_tile}"
+        got = out.float().cpu().numpy()
+        assert_close(got, ref, kv_dtype=fam.kv_dtype, what=what)
     assert np.all(got[lens == 0] == 0)
 
 

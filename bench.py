@@ -186,7 +186,7 @@ def make_layer(device, wl, fam, seed, layer, kv_alias=False, splits=0, q_len=1, 
                              (getattr(ga, unit_flag) if unit_flag else 0), q_len=S)
     if fp8_units and fam.kv_dtype == W.KV_E4M3 and fam.window > 0:
         plan.kv_heads_per_unit = fp8_units        # A/B: force the E4M3 unit width
-    if deal != "auto" and plan.mode == ga.GA_SPLIT_NONE and S == 1:
+    if deal != "auto" and plan.mode in (ga.GA_SPLIT_NONE, ga.GA_SPLIT_CHUNK) and S == 1:
         plan.schedule = DEALS[deal]               # A/B: force how units are dealt to CTAs
     ws = ga.workspace_for(plan, device)
     po, plse, _ = ga.workspace_views(plan, ws) if ws is not None else (None, None, None)
@@ -411,7 +411,7 @@ def workload_text(args):
     if args.separate_append:
         text += "; append kernel launched before each decode (not fused)"
     if args.deal != "auto":
-        text += f"; one-chunk plans deal units {args.deal}"
+        text += f"; unsplit and chunked plans deal units {args.deal}"
     if args.mq_units != "auto":
         text += {"tc": "; tcgen05 units of 64 columns forced",
                  "cp": "; column-parallel mma.sync units forced"}[args.mq_units]
@@ -1004,7 +1004,8 @@ def main():
                     help="one-query steps launch the append kernel before the decode instead "
                          "of the decode call with the append fused (A/B)")
     ap.add_argument("--deal", default="auto", choices=["auto"] + sorted(DEALS),
-                    help="how one-chunk one-query plans deal work units to the CTAs: the "
+                    help="how one-query plans (unsplit, or in fixed-size chunks) deal work "
+                         "units to the CTAs: the "
                          "planner's choice, or forced (A/B)")
     ap.add_argument("--fp8-units", type=int, default=0,
                     help="kv heads per unit of the E4M3 sliding-family decode (1, or 8 / group): "

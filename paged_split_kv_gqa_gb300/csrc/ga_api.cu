@@ -160,14 +160,19 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     const int64_t per_rc = (int64_t)(in.Hkv / in.HP) * HG;
     std::vector<int32_t> rc_pages;
     rc_pages.reserve(in.B * 4);
+    // chunked plans, the rows-by-size deal's order of row-chunks: the full
+    // chunks in row order, then the shorter last chunks, longest first
+    std::vector<int64_t> full_rc, last_rc;
     int64_t split_rows_rc = 0;
     for (int32_t b = 0; b < in.B; ++b) {
         const RowGeom g = row_geometry(in.lens[b], in.W, INT64_MAX / 64, cand.mode, cand.splits,
                                        cand.chunk_pages);
         cand.max_cp = std::max(cand.max_cp, std::min(g.cp, std::max(g.npages, 1)));
+        const int32_t nfull = full_chunks(g);
         for (int32_t j = 0; j < g.chunks; ++j) {
             int32_t p0, np;
             chunk_pages_of(g, j, &p0, &np);
+            (j < nfull ? full_rc : last_rc).push_back((int64_t)rc_pages.size());
             rc_pages.push_back(np);
         }
         if (g.chunks > 1) split_rows_rc += g.chunks;
@@ -190,22 +195,34 @@ void evaluate(const PlanInput& in, Candidate& cand) {
     }
     double makespan = 0;
     for (double v : load) makespan = std::max(makespan, v);
-    // One chunk per row: the rows-by-size deal (longest rows first, every
-    // other pass reversed) when it evens the CTA loads out by more than 3 %
-    // (the ragged 256-row sliding family: 213 against 238 superstages on the
-    // busiest CTA).  It is simulated here exactly as the kernels deal it.
+    // The rows-by-size deal (longest first, every other pass over the CTAs
+    // reversed) when it evens the CTA loads out by more than 3 %: one chunk
+    // per row (the ragged 256-row sliding family: 213 against 238
+    // superstages on the busiest CTA), or fixed-size chunks with the rows'
+    // shorter last chunks sorted after the full ones (the 31B global family
+    // on E4M3 pools, 256-page chunks: 2123 against 2304 pages).  Simulated
+    // here exactly as the kernels deal it.
     cand.schedule = kScheduleRoundRobin;
-    if (cand.mode == kSplitNone && in.S == 1 && sorted_schedule_fits(in.B) && cand.units > G) {
-        std::vector<int32_t> order((size_t)in.B);
-        for (int32_t b = 0; b < in.B; ++b) order[(size_t)b] = b;
-        std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
-            return row_sort_key(rc_pages[(size_t)a]) < row_sort_key(rc_pages[(size_t)b]);
-        });
+    const bool sortable = cand.mode == kSplitNone ? sorted_schedule_fits(in.B)
+                          : cand.mode == kSplitChunk && sorted_chunk_schedule_fits(in.B);
+    if (sortable && in.S == 1 && cand.units > G) {
+        std::vector<int64_t> order;           // row-chunks in the deal's order
+        if (cand.mode == kSplitNone) {
+            for (int32_t b = 0; b < in.B; ++b) order.push_back(b);
+        } else {
+            order = full_rc;
+            order.insert(order.end(), last_rc.begin(), last_rc.end());
+        }
+        std::stable_sort(order.begin() + (cand.mode == kSplitNone ? 0 : (int64_t)full_rc.size()),
+                         order.end(), [&](int64_t a, int64_t b) {
+                             return row_sort_key(rc_pages[(size_t)a]) <
+                                    row_sort_key(rc_pages[(size_t)b]);
+                         });
         std::vector<double> sorted_load((size_t)G, 0.0);
         for (int64_t u = 0; u < cand.units; ++u) {
             const uint32_t pos = snake_position((uint32_t)u, (uint32_t)G, (uint32_t)cand.units);
-            const int32_t b = order[(size_t)(pos / per_rc)];
-            sorted_load[(size_t)(u % G)] += rc_pages[(size_t)b] * in.HP * in.page_weight + unit_ovh;
+            const int64_t rc = order[(size_t)(pos / per_rc)];
+            sorted_load[(size_t)(u % G)] += rc_pages[(size_t)rc] * in.HP * in.page_weight + unit_ovh;
         }
         double sorted_span = 0;
         for (double v : sorted_load) sorted_span = std::max(sorted_span, v);

@@ -1001,7 +1001,7 @@ static int run(const DecodeArgs& a, int slot) {
     p.mode = pl.mode;
     p.splits = pl.splits;
     p.chunk_pages = pl.chunk_pages;
-    p.schedule = pl.schedule;
+    p.schedule = kernel_schedule(pl.schedule, pl.mode);
     p.touch_stride = pl.touch_stride;
     p.test_wait_timeout = (pl.flags & GA_PLAN_TEST_WAIT_TIMEOUT) ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -1056,11 +1056,13 @@ using CfgGlobalBf16Col = DecodeCfg<512, GA_KV_BF16, 4, GA_CG_NS, false, true>;
 using CfgGlobalE4m3Alias = DecodeCfg<512, GA_KV_E4M3, GA_GE_NCW, 2 * GA_GE_NS, true>;
 
 int launch_decode(const DecodeArgs& a) {
-    // the rows-by-size schedule: one-chunk one-query plans whose row order
-    // and counters fit after the row prefix
+    // the rows-by-size schedule: one-query plans, unsplit or in fixed-size
+    // chunks, whose sorted arrays and counters fit after the row prefix
     if (a.plan->schedule != kScheduleRoundRobin &&
-        (a.plan->schedule != kScheduleSorted || a.plan->mode != kSplitNone ||
-         a.plan->q_len != 1 || !sorted_schedule_fits(a.batch)))
+        (a.plan->schedule != kScheduleSorted || a.plan->q_len != 1 ||
+         !(a.plan->mode == kSplitNone    ? sorted_schedule_fits(a.batch)
+           : a.plan->mode == kSplitChunk ? sorted_chunk_schedule_fits(a.batch)
+                                         : false)))
         return GA_ERR_INVALID_ARG;
     // many (query, head) columns per kv head (multi-query decode) and a plan
     // made for 64-column units: the tensor-core kernel

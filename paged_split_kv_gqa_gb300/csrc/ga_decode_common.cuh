@@ -38,7 +38,8 @@ struct DecodeParams {
     int32_t B, Hq, Hkv, group, HG, window, mode, splits, chunk_pages, touch_stride;
     int32_t S, mask_window;
     int32_t TW;                   // columns per work unit (8, or 8 x warps column-parallel)
-    int32_t schedule;             // kScheduleRoundRobin, or kScheduleSorted (pre = row order)
+    int32_t schedule;             // kScheduleRoundRobin, kScheduleSorted (pre = row order) or
+                                  // kScheduleSortedChunks (sorted arrays after the prefix)
     int32_t test_wait_timeout;    // test hook: CTA 0's producer issues nothing
     float scale_log2;             // softmax scale * log2(e)
     int64_t out_elems;            // B * Hq * D
@@ -76,10 +77,11 @@ struct UnitLoc {
     int32_t b, c, hg;
 };
 
-// The rows-by-size deal: slot u -> position in the sorted order -> (row, kv
-// head, head group); one chunk per row, so the row-chunk is the row.  Kept
-// out of line: the decode kernels' hot loops are sensitive to the size of
-// the code inlined into them (their instruction fetch).
+// The rows-by-size deal of an unsplit plan: slot u -> position in the sorted
+// order -> (row, kv head, head group); one chunk per row, so the row-chunk
+// is the row, and pre[] holds the rows longest first.  Kept out of line: the
+// decode kernels' hot loops are sensitive to the size of the code inlined
+// into them (their instruction fetch).
 static __device__ __noinline__ UnitLoc locate_sorted(const DecodeParams& p, const int32_t* pre,
                                                      int64_t u) {
     UnitLoc l;
@@ -94,9 +96,37 @@ static __device__ __noinline__ UnitLoc locate_sorted(const DecodeParams& p, cons
     return l;
 }
 
+// The rows-by-size deal of a plan in fixed-size chunks: the full chunks
+// first (row order), then the rows' shorter last chunks longest first.  pre[]
+// keeps the row prefix; after it, fpre[0 .. B] (full chunks before each row)
+// and the rows with a shorter last chunk in that order (build_chunk_order).
+static __device__ __noinline__ UnitLoc locate_sorted_chunks(const DecodeParams& p,
+                                                            const int32_t* pre, int64_t u) {
+    UnitLoc l;
+    const uint32_t upr = (uint32_t)p.Hkv * (uint32_t)p.HG;
+    const uint32_t pos = snake_position((uint32_t)u, gridDim.x, (uint32_t)pre[p.B] * upr);
+    const uint32_t r = pos / upr, rem = pos - r * upr;
+    const uint32_t hg = (p.HG == 1) ? 0u : rem % (uint32_t)p.HG;
+    l.hg = (int32_t)hg;
+    l.c = (int32_t)((rem - hg) / (uint32_t)p.HG);
+    const int32_t* fpre = pre + p.B + 1;           // full chunks before each row
+    const int32_t* rrow = fpre + p.B + 1;          // rows with a shorter last chunk
+    const int32_t F = fpre[p.B];
+    if ((int32_t)r < F) {
+        l.b = find_row(fpre, p.B, r);
+        l.rc = pre[l.b] + ((int32_t)r - fpre[l.b]);
+    } else {
+        l.b = rrow[(int32_t)r - F];
+        l.rc = pre[l.b + 1] - 1;
+    }
+    return l;
+}
+
 __device__ __forceinline__ UnitLoc locate_unit(const DecodeParams& p, const int32_t* pre,
                                                int64_t u) {
-    if (p.schedule == kScheduleSorted) return locate_sorted(p, pre, u);
+    if (p.schedule != kScheduleRoundRobin)
+        return p.schedule == kScheduleSorted ? locate_sorted(p, pre, u)
+                                             : locate_sorted_chunks(p, pre, u);
     UnitLoc l;
     if (u < (int64_t(1) << 31)) {      // unit_coords in 32 bits (64-bit division is slow)
         const uint32_t v = (uint32_t)u, hg = (uint32_t)p.HG, hkv = (uint32_t)p.Hkv;
@@ -195,6 +225,94 @@ static __device__ __noinline__ void build_row_order(const DecodeParams& p, int32
     __syncthreads();
 }
 
+// The same for a plan in fixed-size chunks (pre[] stays the row prefix):
+// fpre[0 .. B] after it (full chunks before each row, a prefix by warp 0),
+// then the rows that end in a shorter chunk in descending order of its
+// pages (ties in row order), then the kSortKeys counters.
+static __device__ __noinline__ void build_chunk_order(const DecodeParams& p, int32_t* pre,
+                                                      int nthreads) {
+    int32_t* fpre = pre + p.B + 1;
+    int32_t* rrow = fpre + p.B + 1;
+    int32_t* cnt = rrow + p.B;
+    // a row's sort key (descending pages of its last chunk), or -1 if its
+    // chunks are all full
+    auto key_of = [&](int32_t b) -> int32_t {
+        const RowGeom g = row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride, p.mode,
+                                       p.splits, p.chunk_pages);
+        const int32_t full = full_chunks(g);
+        return full < g.chunks ? row_sort_key(g.npages - full * g.cp) : -1;
+    };
+    for (int b = threadIdx.x; b < p.B; b += nthreads)
+        fpre[b + 1] = full_chunks(row_geometry(__ldg(p.seq_lens + b), p.window, p.pt_stride,
+                                               p.mode, p.splits, p.chunk_pages));
+    for (int i = threadIdx.x; i < kSortKeys; i += nthreads) cnt[i] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < p.B; b += nthreads) {
+        const int32_t key = key_of(b);
+        if (key >= 0) atomicAdd(&cnt[key], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        // fpre: inclusive prefix of the full-chunk counts
+        {
+            const int seg = (p.B + 31) / 32;
+            const int lo = min(p.B, lane * seg), hi = min(p.B, lo + seg);
+            int run = 0;
+            for (int b = lo; b < hi; ++b) {
+                run += fpre[b + 1];
+                fpre[b + 1] = run;
+            }
+            int incl = run;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const int excl = incl - run;
+            for (int b = lo; b < hi; ++b) fpre[b + 1] += excl;
+            if (lane == 0) fpre[0] = 0;
+        }
+        // counting sort of the rows with a shorter last chunk into rrow
+        constexpr int PER = (kSortKeys + 31) / 32;        // buckets per lane
+        int v[PER], run = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int k = lane * PER + i;
+            v[i] = k < kSortKeys ? cnt[k] : 0;
+            run += v[i];
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+        }
+        int start = incl - run;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int k = lane * PER + i;
+            if (k < kSortKeys) cnt[k] = start;
+            start += v[i];
+        }
+        __syncwarp();
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            const int k0 = b < p.B ? key_of(b) : -1;
+            const bool live = k0 >= 0;
+            const int key = live ? k0 : kSortKeys + lane;   // dead lanes match none
+            const uint32_t peers = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int pos = live ? cnt[key] + rank : 0;
+            __syncwarp();
+            if (live && rank == __popc(peers) - 1) cnt[key] += __popc(peers);
+            __syncwarp();
+            if (live) rrow[pos] = b;
+        }
+    }
+    __syncthreads();
+}
+
 // Every thread of the block: chunk count of every row, then an inclusive
 // prefix pre[b+1] = sum_{b' <= b} in shared memory.  Reports invalid lengths
 // (block 0) and returns false (the whole block must then exit) when a split
@@ -232,6 +350,7 @@ __device__ __forceinline__ bool build_row_prefix(const DecodeParams& p, int32_t*
     if (bad && blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrSeqLen);
     *total_rc = pre[p.B];
     if (p.schedule == kScheduleSorted) build_row_order(p, pre, nthreads);
+    else if (p.schedule == kScheduleSortedChunks) build_chunk_order(p, pre, nthreads);
     if (p.mode != kSplitNone && *total_rc > p.rc_capacity) {
         if (blockIdx.x == 0 && threadIdx.x == 0) report(p.err_word, kErrCapacity);
         return false;

@@ -1192,7 +1192,7 @@ static int run_tc(const DecodeArgs& a) {
     p.mode = pl.mode;
     p.splits = pl.splits;
     p.chunk_pages = pl.chunk_pages;
-    p.schedule = pl.schedule;
+    p.schedule = kernel_schedule(pl.schedule, pl.mode);
     p.touch_stride = pl.touch_stride;
     p.test_wait_timeout = (pl.flags & GA_PLAN_TEST_WAIT_TIMEOUT) ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;

@@ -54,6 +54,14 @@ enum { kSplitNone = 0, kSplitCount = 1, kSplitChunk = 2 };
 // backwards, so the CTA that took the largest unit of one pass takes the
 // smallest of the next (a longest-first, snake-order deal of unequal units).
 enum { kScheduleRoundRobin = 0, kScheduleSorted = 1 };
+// The kernels' own id for the rows-by-size deal of a chunked plan (the plan
+// says kScheduleSorted; the unit lookup and the chunk index then differ).
+constexpr int kScheduleSortedChunks = 2;
+
+GA_HD int32_t kernel_schedule(int32_t plan_schedule, int32_t mode) {
+    return plan_schedule == kScheduleSorted && mode != kSplitNone ? kScheduleSortedChunks
+                                                                  : plan_schedule;
+}
 constexpr int kSortKeys = 257;    // sort key = 256 - min(attended pages, 256)
 
 GA_HD int32_t row_sort_key(int32_t npages) {
@@ -124,6 +132,22 @@ GA_HD void chunk_pages_of(const RowGeom& g, int32_t j, int32_t* p0, int32_t* np)
     if (a > b) a = b;
     *p0 = g.first_page + a;
     *np = b - a;
+}
+
+// A row of a chunked plan: its chunks of cp pages ("full"), then, unless its
+// pages divide evenly, one shorter last chunk (an empty row: one empty last
+// chunk and no full one).
+GA_HD int32_t full_chunks(const RowGeom& g) {
+    return (g.npages > 0 && g.npages % g.cp == 0) ? g.chunks : g.chunks - 1;
+}
+
+// The rows-by-size deal of a chunked plan (fixed chunk_pages) keeps three
+// arrays after the row prefix in shared memory -- each row's full chunks
+// before it (B + 1), the rows with a shorter last chunk in descending order
+// of its pages (B), and kSortKeys counters: batches up to
+// (kMaxBatch - kSortKeys - 1) / 3 rows.
+GA_HD bool sorted_chunk_schedule_fits(int32_t batch) {
+    return 3 * batch + kSortKeys + 1 <= kMaxBatch;
 }
 
 // Head groups of kHeadTile query heads per kv head.

@@ -1,6 +1,8 @@
 """The rows-by-size deal of work units (GA_SCHEDULE_ROWS_BY_SIZE: rows in
-descending order of attended pages, every other pass over the CTAs
-reversed) changes which CTA takes a unit, never what a unit computes: every
+descending order of attended pages, or for a plan in fixed-size chunks the
+full chunks first and the rows' shorter last chunks longest first; every
+other pass over the CTAs reversed) changes which CTA takes a unit, never
+what a unit computes: every
 decode kernel's outputs are bit-identical to the round-robin deal, the page
 sets read are the same, the fused append writes the same pools, and sampled
 rows match the oracle.  Batches with more units than CTAs (the plan made
@@ -30,6 +32,10 @@ CASES = {
     "local_e4m3_kv_alias": (W.Family("local", 16, 8, 256, 1024, 1), {"alias": True}),
     "global_bf16_unsplit": (W.Family("global", 16, 2, 512, 0), {}),
     "global_e4m3_unsplit": (W.Family("global", 16, 2, 512, 0, 1), {}),
+    "global_bf16_chunked": (W.Family("global", 16, 2, 512, 0), {"chunk": 128}),
+    "global_e4m3_chunked": (W.Family("global", 16, 2, 512, 0, 1), {"chunk": 256}),
+    "local_bf16_chunked": (W.Family("local", 16, 8, 256, 1024), {"chunk": 208}),
+    "global_e4m3_chunked_16_columns": (W.Family("global", 32, 2, 512, 0, 1), {"chunk": 96}),
 }
 
 
@@ -53,8 +59,12 @@ def _setup(case):
 
 def _plans(ga, fam, opt, flags=0):
     kw = dict(num_q_heads=fam.num_q_heads, num_kv_heads=fam.num_kv_heads,
-              head_dim=fam.head_dim, window=fam.window, requested_splits=1, num_sms=40,
+              head_dim=fam.head_dim, window=fam.window, num_sms=40,
               flags=flags | (ga.GA_PLAN_KV_E4M3 if fam.kv_dtype == W.KV_E4M3 else 0))
+    if "chunk" in opt:
+        kw["fixed_chunk_tokens"] = opt["chunk"]
+    else:
+        kw["requested_splits"] = 1
     out = []
     for sched in (ga.GA_SCHEDULE_ROUND_ROBIN, ga.GA_SCHEDULE_ROWS_BY_SIZE):
         plan = ga.ga_plan_splits(LENS, **kw)
@@ -85,10 +95,11 @@ def test_deal_changes_no_bit(ga, case):
                  kv_dtype=fam.kv_dtype, what=case)
 
 
-@pytest.mark.parametrize("case", ["local_bf16", "local_e4m3_4_heads"])
+@pytest.mark.parametrize("case", ["local_bf16", "local_e4m3_4_heads", "local_bf16_chunked"])
 def test_deal_reads_the_same_pages(ga, case):
-    """Touch log (one row-chunk per row in an unsplit plan): the same physical
-    pages per row under both deals, equal to the oracle's window pages."""
+    """Touch log (one entry list per row-chunk): the same physical pages per
+    row-chunk under both deals, and per row (its chunks in order) equal to
+    the oracle's window pages."""
     fam, opt, fi = _setup(case)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     logs = []
@@ -104,13 +115,18 @@ def test_deal_reads_the_same_pages(ga, case):
     assert int(err.item()) == 0
     assert np.array_equal(logs[0], logs[1])
     table = fi.page_table.cpu().numpy()
+    cp = opt.get("chunk", 0) // 16
+    rc = 0
     for b, L in enumerate(LENS):
         first, n = O.logical_pages(L, fam.window, 16)
-        assert [int(x) for x in logs[1][b] if x >= 0] == \
-            [int(table[b, p]) for p in range(first, first + n)], (b, L)
+        chunks = max(1, -(-n // cp)) if cp else 1
+        got = [int(x) for r in range(rc, rc + chunks) for x in logs[1][r] if x >= 0]
+        rc += chunks
+        assert got == [int(table[b, p]) for p in range(first, first + n)], (b, L)
 
 
-@pytest.mark.parametrize("case", ["local_bf16", "local_e4m3", "local_e4m3_4_heads"])
+@pytest.mark.parametrize("case", ["local_bf16", "local_e4m3", "local_e4m3_4_heads",
+                                  "local_bf16_chunked"])
 def test_deal_with_fused_append(ga, case):
     """The decode call with the append fused in: same pools and outputs under
     both deals (the unit that holds a row's last page writes its token)."""
@@ -188,4 +204,45 @@ def test_deal_at_the_batch_limit(ga):
     plan.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE
     with pytest.raises(ga.GAError) as exc:
         run_decode(ga, fi2, plan, err=err)
+    assert exc.value.status == ga.GA_ERR_INVALID_ARG
+
+
+def test_chunked_deal_limits(ga):
+    """A chunked plan takes the deal up to 596 rows (its three sorted arrays
+    and counters fill the row-prefix array); 597 rows, or a plan split into a
+    fixed number of chunks per row, with the deal forced are refused before
+    any launch."""
+    fam = W.Family("global", 2, 1, 512, 0)
+    rng = np.random.default_rng(8)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for n, ok in ((596, True), (597, False)):
+        lens = [int(x) for x in rng.integers(0, 300, n)]
+        wl = W.Workload("climit", np.asarray(lens, dtype=np.int32), 16, fam, fam)
+        fi = W.make_family_inputs(wl, fam, device=DEV, seed=4)
+        outs = []
+        for sched in (ga.GA_SCHEDULE_ROUND_ROBIN, ga.GA_SCHEDULE_ROWS_BY_SIZE):
+            plan = ga.ga_plan_splits(lens, num_q_heads=2, num_kv_heads=1, head_dim=512,
+                                     window=0, fixed_chunk_tokens=64, num_sms=40)
+            plan.schedule = sched
+            if sched == ga.GA_SCHEDULE_ROWS_BY_SIZE and not ok:
+                with pytest.raises(ga.GAError) as exc:
+                    run_decode(ga, fi, plan, err=err)
+                assert exc.value.status == ga.GA_ERR_INVALID_ARG
+                continue
+            outs.append(run_decode(ga, fi, plan, err=err))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        if ok:
+            assert torch.equal(_bits(outs[0]), _bits(outs[1]))
+            rows = W.sample_rows(n, 6, seed=1)
+            assert_close(outs[1][rows].float().cpu().numpy(),
+                         oracle_decode_rows_gathered(fi, rows), what="596 rows, chunked deal")
+    lens = [40, 300, 900, 17]
+    wl = W.Workload("count", np.asarray(lens, dtype=np.int32), 16, fam, fam)
+    fi = W.make_family_inputs(wl, fam, device=DEV, seed=4)
+    plan = ga.ga_plan_splits(lens, num_q_heads=2, num_kv_heads=1, head_dim=512, window=0,
+                             requested_splits=3)
+    plan.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE
+    with pytest.raises(ga.GAError) as exc:
+        run_decode(ga, fi, plan, err=err)
     assert exc.value.status == ga.GA_ERR_INVALID_ARG

@@ -258,3 +258,45 @@ def test_e4m3_plans_ask_for_16_column_units(ga, Hq, Hkv, D, W_, S, tile):
     assert p.units == p.row_chunks * Hkv * -(-cols // tile)
     plain = ga.ga_plan_splits(lens, q_len=S, **kw)
     assert plain.col_tile != 16 and plain.row_chunks == p.row_chunks
+
+
+def _chunk_deal_load(lens, cp, Hkv, G, sort):
+    """Pages per CTA of a chunked plan under round robin or the rows-by-size
+    deal as the header documents it: the full chunks in row order, then the
+    rows' shorter last chunks longest first (ties in row order), dealt in
+    snake order."""
+    rc_sizes = []                                  # row-chunks in row order
+    for L in lens:
+        n = _pages(int(L), 0)
+        rc_sizes += [min(cp, n - j * cp) for j in range(-(-n // cp))] if n else [0]
+    full = [s for s in rc_sizes if s == cp]
+    last = sorted((s for s in rc_sizes if s != cp), key=lambda s: -min(s, 256))
+    order = full + last if sort else rc_sizes
+    U = len(order) * Hkv
+    load = np.zeros(G)
+    for s in range(U):
+        load[s % G] += order[(_snake(s, G, U) if sort else s) // Hkv]
+    return load
+
+
+def test_rows_by_size_deal_of_chunked_plans(ga):
+    """Plans in fixed-size chunks take the rows-by-size deal too (full chunks
+    first, then the shorter last chunks longest first) when it evens the CTA
+    loads out: the 31B global family's chunked plans (bf16 and E4M3 pools)
+    and the ragged batch's; the busiest CTA's pages drop as simulated here.
+    Split-count plans and batches above 596 rows keep round robin."""
+    for idx, flags in ((3, 0), (3, "e4m3"), (5, 0)):
+        wl = W.config(idx)
+        fam = wl.global_
+        p = ga.ga_plan_splits(wl.seq_lens, num_q_heads=fam.num_q_heads,
+                              num_kv_heads=fam.num_kv_heads, head_dim=512, window=0,
+                              num_sms=152, flags=ga.GA_PLAN_KV_E4M3 if flags else 0)
+        assert p.mode == ga.GA_SPLIT_CHUNK and p.schedule == ga.GA_SCHEDULE_ROWS_BY_SIZE
+        rr = _chunk_deal_load(wl.seq_lens, p.chunk_pages, fam.num_kv_heads, p.grid, False)
+        sn = _chunk_deal_load(wl.seq_lens, p.chunk_pages, fam.num_kv_heads, p.grid, True)
+        assert rr.sum() == sn.sum() and sn.max() < 0.97 * rr.max(), (idx, flags)
+    lens = W.config(3).seq_lens
+    kw = dict(num_q_heads=32, num_kv_heads=4, head_dim=512, window=0, num_sms=152)
+    assert ga.ga_plan_splits(lens, requested_splits=4, **kw).schedule == 0
+    big = np.random.default_rng(1).integers(8000, 30000, 597)
+    assert ga.ga_plan_splits(big, fixed_chunk_tokens=2048, **kw).schedule == 0

@@ -160,11 +160,13 @@ typedef struct ga_plan {
                                     may set it to 1 or to that value; other kernels ignore it. */
     int32_t schedule;            /* how the persistent CTAs deal out the units:
                                     GA_SCHEDULE_ROUND_ROBIN (unit i to CTA i mod grid), or
-                                    GA_SCHEDULE_ROWS_BY_SIZE (one-chunk one-query plans of at
-                                    most 1791 rows: rows in descending order of attended
-                                    pages, every other pass over the CTAs reversed).  The
-                                    planner picks the second when it evens out CTA loads of
-                                    unequal rows.  Results do not depend on it.  The decode
+                                    GA_SCHEDULE_ROWS_BY_SIZE, for one-query plans: unsplit
+                                    ones of at most 1791 rows (rows in descending order of
+                                    attended pages) or ones in fixed-size chunks of at most
+                                    596 rows (the full chunks in row order, then the rows'
+                                    shorter last chunks longest first); every other pass
+                                    over the CTAs reversed.  The planner picks the second
+                                    when it evens out the CTA loads.  Results do not depend on it.  The decode
                                     calls refuse any other value, and the second on other
                                     plans, with GA_ERR_INVALID_ARG before any launch. */
 } ga_plan;

@@ -177,8 +177,14 @@ def test_decode_rejects_before_launch(ga):
     bad.col_tile = 16
     assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
     bad = _plan(ga, requested_splits=2)
-    bad.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE                              # split plan
+    bad.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE                              # split-count plan
     assert _decode_local(ga, bad, ws=FAKE, wsb=bad.workspace_bytes) == ga.GA_ERR_INVALID_ARG
+    big = ga.ga_plan_splits([40] * 597, num_q_heads=4, num_kv_heads=2, head_dim=256, window=32,
+                            num_sms=8, fixed_chunk_tokens=16)
+    assert big.mode == ga.GA_SPLIT_CHUNK
+    big.schedule = ga.GA_SCHEDULE_ROWS_BY_SIZE                   # chunked plan above 596 rows
+    assert _decode_local(ga, big, B=597, ws=FAKE, wsb=big.workspace_bytes) == \
+        ga.GA_ERR_INVALID_ARG
     bad = _plan(ga)
     bad.schedule = 2                                                        # unknown
     assert _decode_local(ga, bad) == ga.GA_ERR_INVALID_ARG
